@@ -1,0 +1,123 @@
+/*
+ * kda_decode.h -- C ABI of the GB300 (sm_103a) fused KDA decode step.
+ *
+ * One call runs, for every (token row n, value head h) of a decode batch, the
+ * three stages that the page "[ROCm][Perf] Kimi-K3 Fused kernel for KDA
+ * decode" (vLLM PR #50654 report; cited below as P1) fuses into one launch
+ * (P1, section 功能与动机 "motivation" and 实现拆解 "implementation
+ * breakdown" item 1):
+ *
+ *   1. causal conv1d state advance (width 4) + SiLU on the q, k, v channels;
+ *   2. gated delta-rule recurrence on the [128, 128] fp32 state:
+ *        q^ = q_scale * q / sqrt(|q|^2 + 1e-6),  k^ = k / sqrt(|k|^2 + 1e-6)
+ *        S' = (I - beta k^ k^T) Diag(exp(g)) S + beta k^ v^T,  o = S'^T q^
+ *   3. gated RMSNorm: out = o / sqrt(mean(o^2) + eps) * norm_weight * sigmoid(gate),
+ *      or out = o when KDA_OUT_NORM is not set.
+ *
+ * P1 does not print the equations; the standard KDA definition above is the
+ * one adopted.  Rows whose slot index is <= 0 are CUDA-graph padding: their
+ * output is zero and no state is read or written (P1 实现拆解 item 1 and the
+ * kernel excerpt under 关键源码片段 "code excerpts").
+ *
+ * Memory: every pointer is DEVICE memory owned by the caller, on the device
+ * current when kda_decode is called.  The library never allocates, frees,
+ * synchronises or reads device memory from the host, so a call may be
+ * captured into a CUDA graph (after one eager call on that device, which
+ * performs the once-per-device kernel attribute set-up).
+ */
+#ifndef KDA_DECODE_H
+#define KDA_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_DECODE_ABI_VERSION 1
+
+/* Fixed problem geometry (P1 实现拆解 item 3: head_dim 128, conv width 4). */
+#define KDA_HEAD_DIM 128
+#define KDA_CONV_WIDTH 4
+
+/* flags */
+#define KDA_OUT_NORM          1u /* apply the gated RMSNorm epilogue */
+#define KDA_UPDATE_CONV_STATE 2u /* write the advanced conv state back */
+
+/* return codes of kda_decode */
+#define KDA_OK            0
+#define KDA_ERR_NULLPTR  -1 /* a required pointer is NULL */
+#define KDA_ERR_SHAPE    -2 /* head_dim != 128, conv_width != 4, N < 0, H < 1,
+                               num_slots < 1, a stride too small, or N*H too large */
+#define KDA_ERR_ALIGN    -3 /* a pointer or row stride breaks the 16-byte rule */
+#define KDA_ERR_FLAGS    -4 /* unknown flag bits */
+#define KDA_ERR_LAUNCH   -5 /* the CUDA launch failed; see kda_last_error() */
+#define KDA_ERR_ABI      -6 /* args->struct_size does not match this library */
+
+/* bits OR-ed into *err_flag by the kernel (never a trap) */
+#define KDA_DEVERR_SLOT_RANGE 1 /* a row had slot >= num_slots; its output was zeroed */
+
+/*
+ * Arguments.  Shapes use N = rows (tokens), H = heads, D = H * 128,
+ * C = 3 * D (q | k | v channel blocks, each head-major).  bf16 tensors are
+ * passed as their 16-bit patterns (uint16_t).
+ *
+ * Alignment: every pointer except beta, slot_idx and err_flag must be
+ * 16-byte aligned, and every row stride must be a multiple of 8 elements.
+ */
+typedef struct KdaDecodeArgs {
+  uint32_t struct_size;        /* = sizeof(KdaDecodeArgs) */
+  int32_t N;                   /* rows; 0 is a no-op */
+  int32_t H;                   /* value heads (= key heads) */
+  int32_t num_slots;           /* state-pool entries; slot 0 is the padding slot */
+  int32_t head_dim;            /* must be 128 */
+  int32_t conv_width;          /* must be 4 */
+
+  const uint16_t* qkv;         /* bf16 [N][qkv_row_stride], channels [0, C) used */
+  int64_t qkv_row_stride;      /* elements, >= C */
+  const float* conv_weight;    /* fp32 [3][4][D], width-major, channel contiguous
+                                  (P1 实现拆解 item 3) */
+  const float* conv_bias;      /* fp32 [C] or NULL */
+  uint16_t* conv_state;        /* bf16 [num_slots][C][3], oldest tap first;
+                                  read, and rewritten in place if KDA_UPDATE_CONV_STATE */
+  float* state;                /* fp32 [num_slots][H][128][128], S[key][value],
+                                  value index contiguous; read and rewritten in place */
+  const float* g;              /* fp32 [N][H][128] log-decay, alpha = exp(g) */
+  const uint16_t* beta;        /* bf16 [N][H] write strength, already activated */
+  const uint16_t* gate;        /* bf16 [N][gate_row_stride], D used; KDA_OUT_NORM only */
+  int64_t gate_row_stride;     /* elements, >= D (ignored without KDA_OUT_NORM) */
+  const float* norm_weight;    /* fp32 [128], shared by all heads; KDA_OUT_NORM only */
+  const int32_t* slot_idx;     /* int32 [N]; <= 0 marks a padding row.  Positive
+                                  slots must be distinct within one call. */
+  uint16_t* out;               /* bf16 [N][out_row_stride], D written per row */
+  int64_t out_row_stride;      /* elements, >= D */
+  float eps;                   /* RMSNorm epsilon (e.g. 1e-6) */
+  float q_scale;               /* 0 => 1/sqrt(128) */
+  uint32_t flags;              /* KDA_OUT_NORM | KDA_UPDATE_CONV_STATE */
+  int32_t* err_flag;           /* device int32 or NULL; KDA_DEVERR_* bits are OR-ed in */
+} KdaDecodeArgs;
+
+/*
+ * Enqueue one fused decode step on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream).  Returns KDA_OK or a negative KDA_ERR_* code; on an
+ * argument error nothing is launched.  Asynchronous: results are visible
+ * after the stream reaches this point.  Rows with slot >= num_slots are
+ * treated as padding and raise KDA_DEVERR_SLOT_RANGE in *err_flag.
+ * Duplicate positive slots within one call give undefined state.
+ */
+int kda_decode(const KdaDecodeArgs* args, void* stream);
+
+/* Static text for a KDA_* return code. */
+const char* kda_status_string(int status);
+
+/* Detail of the last failing call on the calling host thread ("" if none). */
+const char* kda_last_error(void);
+
+/* KDA_DECODE_ABI_VERSION of the loaded library. */
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_DECODE_H */

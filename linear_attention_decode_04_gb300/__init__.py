@@ -1,0 +1,17 @@
+"""GB300-native fused KDA (Kimi Delta Attention) single-token decode step.
+
+The compute lives in one hand-written CUDA library (``csrc/``) behind a C ABI
+(``include/kda_decode.h``); ``kda_decode`` here only marshals torch tensors
+into that call.  The library is loaded on first use and a missing or stale
+build raises instead of falling back to anything else.
+"""
+from .binding import (  # noqa: F401
+    KDA_OUT_NORM,
+    KDA_UPDATE_CONV_STATE,
+    KdaDecodeCall,
+    KdaError,
+    kda_decode,
+    kda_status_string,
+    library_path,
+    load_library,
+)

@@ -1,0 +1,209 @@
+"""Python binding of the C ABI in ``include/kda_decode.h``.
+
+Argument marshalling only: tensors are checked for device, dtype and layout,
+their pointers are packed into ``KdaDecodeArgs`` and ``kda_decode`` in
+``lib/libkda_decode.so`` runs every step of the decode on the GPU.  There is
+no other code path: a missing library, a CPU tensor or a failing call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HEAD_DIM = 128
+CONV_WIDTH = 4
+KDA_OUT_NORM = 1
+KDA_UPDATE_CONV_STATE = 2
+KDA_DEVERR_SLOT_RANGE = 1
+ABI_VERSION = 1
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG_DIR, "lib", "libkda_decode.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"kda_decode failed with status {status}: {detail}")
+        self.status = status
+
+
+class KdaDecodeArgs(ctypes.Structure):
+    """Mirror of ``struct KdaDecodeArgs`` (field order and types must match)."""
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("N", ctypes.c_int32), ("H", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("conv_width", ctypes.c_int32),
+        ("qkv", ctypes.c_void_p), ("qkv_row_stride", ctypes.c_int64),
+        ("conv_weight", ctypes.c_void_p), ("conv_bias", ctypes.c_void_p),
+        ("conv_state", ctypes.c_void_p), ("state", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("gate", ctypes.c_void_p), ("gate_row_stride", ctypes.c_int64),
+        ("norm_weight", ctypes.c_void_p), ("slot_idx", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("out_row_stride", ctypes.c_int64),
+        ("eps", ctypes.c_float), ("q_scale", ctypes.c_float),
+        ("flags", ctypes.c_uint32), ("err_flag", ctypes.c_void_p),
+    ]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the CUDA library once; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise FileNotFoundError(
+                    f"{_LIB_PATH} is missing: build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(_LIB_PATH)
+            L.kda_decode.argtypes = [ctypes.POINTER(KdaDecodeArgs), ctypes.c_void_p]
+            L.kda_decode.restype = ctypes.c_int
+            L.kda_status_string.argtypes = [ctypes.c_int]
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_last_error.argtypes = []
+            L.kda_last_error.restype = ctypes.c_char_p
+            L.kda_abi_version.argtypes = []
+            L.kda_abi_version.restype = ctypes.c_int
+            if L.kda_abi_version() != ABI_VERSION:
+                raise RuntimeError(f"{_LIB_PATH}: ABI version {L.kda_abi_version()} != {ABI_VERSION}")
+            _lib = L
+    return _lib
+
+
+def kda_status_string(status: int) -> str:
+    return load_library().kda_status_string(int(status)).decode()
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device | None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _dense(t: torch.Tensor, name: str):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _rows(t: torch.Tensor, name: str, N: int, width: int) -> int:
+    """Row-strided 2-D view [N, >= width] with unit inner stride; returns the row stride."""
+    if t.dim() != 2 or t.shape[0] != N or t.shape[1] < width:
+        raise ValueError(f"{name} must be [N={N}, >={width}] (got {tuple(t.shape)})")
+    if t.stride(1) != 1:
+        raise ValueError(f"{name} needs a unit inner stride")
+    return t.stride(0) if N > 1 else max(t.stride(0), width)
+
+
+class KdaDecodeCall:
+    """A prepared ``kda_decode`` call: validates and packs the arguments once;
+    each ``__call__`` is one C call (cheap enough for eager loops and CUDA
+    graph capture).  Keeps references to the tensors it points at."""
+
+    def __init__(self, qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
+                 gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
+                 q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
+                 err_flag=None):
+        self._lib = load_library()
+        dev = state.device
+        _check(state, "state", torch.float32, None)
+        if state.dim() != 4 or state.shape[2:] != (HEAD_DIM, HEAD_DIM):
+            raise ValueError(f"state must be [slots, H, 128, 128] (got {tuple(state.shape)})")
+        _dense(state, "state")
+        num_slots, H = int(state.shape[0]), int(state.shape[1])
+        D = H * HEAD_DIM
+        C = 3 * D
+        _check(qkv, "qkv", torch.bfloat16, dev)
+        N = int(qkv.shape[0])
+        qkv_stride = _rows(qkv, "qkv", N, C)
+        _check(conv_weight, "conv_weight", torch.float32, dev)
+        if tuple(conv_weight.shape) != (3, CONV_WIDTH, D):
+            raise ValueError(f"conv_weight must be [3, 4, {D}] (got {tuple(conv_weight.shape)})")
+        _dense(conv_weight, "conv_weight")
+        _check(conv_state, "conv_state", torch.bfloat16, dev)
+        if tuple(conv_state.shape) != (num_slots, C, CONV_WIDTH - 1):
+            raise ValueError(f"conv_state must be [{num_slots}, {C}, 3] (got {tuple(conv_state.shape)})")
+        _dense(conv_state, "conv_state")
+        _check(g, "g", torch.float32, dev)
+        if tuple(g.shape) != (N, H, HEAD_DIM):
+            raise ValueError(f"g must be [{N}, {H}, 128] (got {tuple(g.shape)})")
+        _dense(g, "g")
+        _check(beta, "beta", torch.bfloat16, dev)
+        if tuple(beta.shape) != (N, H):
+            raise ValueError(f"beta must be [{N}, {H}] (got {tuple(beta.shape)})")
+        _dense(beta, "beta")
+        _check(slot_idx, "slot_idx", torch.int32, dev)
+        if tuple(slot_idx.shape) != (N,):
+            raise ValueError(f"slot_idx must be [{N}] (got {tuple(slot_idx.shape)})")
+        _dense(slot_idx, "slot_idx")
+        _check(out, "out", torch.bfloat16, dev)
+        out_stride = _rows(out, "out", N, D)
+        flags = (KDA_OUT_NORM if out_norm else 0) | (KDA_UPDATE_CONV_STATE if update_conv_state else 0)
+        gate_ptr = nw_ptr = None
+        gate_stride = 0
+        if out_norm:
+            if gate is None or norm_weight is None:
+                raise ValueError("out_norm needs gate and norm_weight")
+            _check(gate, "gate", torch.bfloat16, dev)
+            gate_stride = _rows(gate, "gate", N, D)
+            _check(norm_weight, "norm_weight", torch.float32, dev)
+            if tuple(norm_weight.shape) != (HEAD_DIM,):
+                raise ValueError("norm_weight must be [128]")
+            gate_ptr, nw_ptr = gate.data_ptr(), norm_weight.data_ptr()
+        bias_ptr = None
+        if conv_bias is not None:
+            _check(conv_bias, "conv_bias", torch.float32, dev)
+            if tuple(conv_bias.shape) != (C,):
+                raise ValueError(f"conv_bias must be [{C}]")
+            bias_ptr = conv_bias.data_ptr()
+        err_ptr = None
+        if err_flag is not None:
+            _check(err_flag, "err_flag", torch.int32, dev)
+            err_ptr = err_flag.data_ptr()
+        self.device = dev
+        self.N, self.H, self.num_slots = N, H, num_slots
+        self._keep = (qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate,
+                      norm_weight, conv_bias, err_flag)
+        self.args = KdaDecodeArgs(
+            struct_size=ctypes.sizeof(KdaDecodeArgs), N=N, H=H, num_slots=num_slots,
+            head_dim=HEAD_DIM, conv_width=CONV_WIDTH,
+            qkv=qkv.data_ptr(), qkv_row_stride=qkv_stride,
+            conv_weight=conv_weight.data_ptr(), conv_bias=bias_ptr,
+            conv_state=conv_state.data_ptr(), state=state.data_ptr(),
+            g=g.data_ptr(), beta=beta.data_ptr(), gate=gate_ptr, gate_row_stride=gate_stride,
+            norm_weight=nw_ptr, slot_idx=slot_idx.data_ptr(),
+            out=out.data_ptr(), out_row_stride=out_stride,
+            eps=float(eps), q_scale=float(q_scale), flags=flags, err_flag=err_ptr)
+        self._argp = ctypes.byref(self.args)
+
+    def __call__(self, stream: torch.cuda.Stream | None = None) -> None:
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        rc = self._lib.kda_decode(self._argp, ctypes.c_void_p(stream.cuda_stream))
+        if rc != 0:
+            raise KdaError(rc, f"{kda_status_string(rc)}: {self._lib.kda_last_error().decode()}")
+
+
+def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
+               gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
+               q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
+               err_flag=None, stream: torch.cuda.Stream | None = None) -> None:
+    """One fused decode step (see ``include/kda_decode.h``).  ``conv_state``,
+    ``state`` and ``out`` are written in place on ``stream`` (default: the
+    current stream of the state's device)."""
+    KdaDecodeCall(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate=gate,
+                  norm_weight=norm_weight, conv_bias=conv_bias, eps=eps, q_scale=q_scale,
+                  out_norm=out_norm, update_conv_state=update_conv_state,
+                  err_flag=err_flag)(stream)

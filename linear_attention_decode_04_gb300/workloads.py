@@ -1,0 +1,216 @@
+"""Seeded synthetic inputs for the fused KDA decode step.
+
+This module only draws random numbers and lays them out in the storage
+dtypes and shapes of the decode step; it holds none of the step's arithmetic.
+Both the CUDA path (through the tests and the benchmark) and the fp64 oracle
+consume the same arrays it returns.
+
+bf16 tensors are returned as numpy ``uint16`` bit patterns (round-to-nearest-
+even from the fp32 draw).  Every tensor has its own seed stream
+``SeedSequence([seed, tag, ...])``; the recurrent and conv state pools are
+drawn slot by slot (``SeedSequence([seed, tag, slot])``), so any slot can be
+regenerated on its own and large pools can be drawn by several threads.
+
+Value distributions (sigma is the standard deviation):
+  mixed qkv      bf16  N(0, 1)                      [N, 3*H*128]
+  conv weight    fp32  N(0, 0.5)                    [3, 4, H*128] width-major
+  conv state     bf16  N(0, 1)                      [slots, 3*H*128, 3]
+  state          fp32  N(0, 0.02)                   [slots, H, 128, 128]
+  g (log-decay)  fp32  -softplus(N(0, 1))           [N, H, 128]
+                  or   -5 * (1 - U[0,1))  (decays in [exp(-5), 1))
+  beta           bf16  sigmoid(N(0, 1))             [N, H]
+  output gate    bf16  N(0, 1)                      [N, H*128]
+  norm weight    fp32  1 + N(0, 0.1)                [128]
+  slot indices   int32 distinct draws from 1..slots-1, padding rows 0
+"""
+from __future__ import annotations
+
+import concurrent.futures as _cf
+import os
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+
+HEAD_DIM = 128
+CONV_WIDTH = 4
+
+# seed-stream tags, one per tensor
+_T_QKV, _T_CW, _T_CS, _T_STATE, _T_G, _T_BETA, _T_GATE, _T_NW, _T_SLOT, _T_BIAS = range(1, 11)
+
+
+def _rng(*key: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(list(key))))
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round-to-nearest-even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclass(frozen=True)
+class Spec:
+    """One synthetic decode-step problem."""
+    name: str
+    N: int
+    H: int
+    num_slots: int
+    seed: int
+    out_norm: bool = True
+    update_conv_state: bool = True
+    pad_tail: int = 0                 # last rows set to slot 0
+    slots: tuple | None = None        # explicit slot list overrides the draw
+    g_mode: str = "softplus"          # "softplus" | "uniform5"
+    eps: float = 1e-6
+    with_bias: bool = False
+    qkv_row_pad: int = 0              # extra bf16 elements per qkv row
+
+
+# The workloads the decode step is measured and checked on.
+PR1_REF = Spec("n4_h12_pool8", N=4, H=12, num_slots=8, seed=0, slots=(1, 3, 5, 7))
+PAD_TAIL = Spec("n32_h24_pool64_pad8", N=32, H=24, num_slots=64, seed=1, pad_tail=8)
+NORM_OFF = Spec("n128_h48_pool512_normoff", N=128, H=48, num_slots=512, seed=2,
+                out_norm=False, g_mode="uniform5")
+ROOFLINE = Spec("n256_h96_pool1024", N=256, H=96, num_slots=1024, seed=3)
+# 69 independent layers, each its own weights and state pool.
+STACK_LAYERS = 69
+STACK_LAYER = Spec("stack69_n64_h48_pool96_pad4", N=64, H=48, num_slots=96, seed=4000, pad_tail=4)
+
+SPECS = {s.name: s for s in (PR1_REF, PAD_TAIL, NORM_OFF, ROOFLINE)}
+
+
+def stack_layer_spec(layer: int) -> Spec:
+    return replace(STACK_LAYER, seed=STACK_LAYER.seed + layer)
+
+
+@dataclass
+class Inputs:
+    """Host arrays of one problem (bf16 as uint16 bits)."""
+    spec: Spec
+    qkv: np.ndarray
+    conv_weight: np.ndarray
+    conv_bias: np.ndarray | None
+    conv_state: np.ndarray
+    state: np.ndarray
+    g: np.ndarray
+    beta: np.ndarray
+    gate: np.ndarray
+    norm_weight: np.ndarray
+    slot_idx: np.ndarray
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def N(self) -> int: return self.spec.N
+
+    @property
+    def H(self) -> int: return self.spec.H
+
+    @property
+    def C(self) -> int: return 3 * self.spec.H * HEAD_DIM
+
+    def active_rows(self) -> np.ndarray:
+        s = self.slot_idx
+        return np.nonzero((s > 0) & (s < self.spec.num_slots))[0]
+
+
+def draw_slots(spec: Spec) -> np.ndarray:
+    if spec.slots is not None:
+        s = np.asarray(spec.slots, dtype=np.int32)
+        assert s.size == spec.N
+        return s
+    n_act = spec.N - spec.pad_tail
+    assert 0 <= n_act <= spec.num_slots - 1, "not enough distinct slots"
+    perm = _rng(spec.seed, _T_SLOT).permutation(np.arange(1, spec.num_slots, dtype=np.int32))
+    s = np.zeros(spec.N, dtype=np.int32)
+    s[:n_act] = perm[:n_act]
+    return s
+
+
+def _fill_pool(shape_per_slot, num_slots, seed, tag, sigma, dtype_out, threads):
+    """Draw a [num_slots, *shape_per_slot] pool slot by slot (one seed stream per slot)."""
+    out_dtype = np.float32 if dtype_out == "f32" else np.uint16
+    pool = np.empty((num_slots,) + tuple(shape_per_slot), dtype=out_dtype)
+
+    def one(slot):
+        x = _rng(seed, tag, slot).standard_normal(shape_per_slot, dtype=np.float32)
+        if sigma != 1.0:
+            x *= np.float32(sigma)
+        pool[slot] = x if dtype_out == "f32" else f32_to_bf16_bits(x)
+
+    if threads <= 1 or num_slots < 8:
+        for s in range(num_slots):
+            one(s)
+    else:
+        with _cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(num_slots)))
+    return pool
+
+
+def draw_step_inputs(spec: Spec, variant: int = 0) -> dict:
+    """Per-token inputs (qkv, g, beta, gate) of one step; ``variant`` selects
+    another independent draw with the same distributions."""
+    N, H, D = spec.N, spec.H, spec.H * HEAD_DIM
+    key = (spec.seed,) if variant == 0 else (spec.seed, 1000 + variant)
+    qkv = f32_to_bf16_bits(_rng(*key, _T_QKV).standard_normal((N, 3 * D + spec.qkv_row_pad),
+                                                               dtype=np.float32))
+    if spec.g_mode == "softplus":
+        z = _rng(*key, _T_G).standard_normal((N, H, HEAD_DIM))
+        g = (-np.logaddexp(0.0, z)).astype(np.float32)
+    elif spec.g_mode == "uniform5":
+        u = _rng(*key, _T_G).random((N, H, HEAD_DIM))
+        g = (-5.0 * (1.0 - u)).astype(np.float32)
+    else:
+        raise ValueError(spec.g_mode)
+    zb = _rng(*key, _T_BETA).standard_normal((N, H))
+    beta = f32_to_bf16_bits((1.0 / (1.0 + np.exp(-zb))).astype(np.float32))
+    gate = f32_to_bf16_bits(_rng(*key, _T_GATE).standard_normal((N, D), dtype=np.float32))
+    return dict(qkv=qkv, g=g, beta=beta, gate=gate)
+
+
+def make_inputs(spec: Spec, threads: int | None = None) -> Inputs:
+    """Draw every tensor of ``spec``."""
+    if threads is None:
+        threads = min(16, os.cpu_count() or 1)
+    H, D = spec.H, spec.H * HEAD_DIM
+    C = 3 * D
+    step = draw_step_inputs(spec, 0)
+    cw = _rng(spec.seed, _T_CW).standard_normal((3, CONV_WIDTH, D), dtype=np.float32)
+    cw *= np.float32(0.5)
+    bias = None
+    if spec.with_bias:
+        bias = _rng(spec.seed, _T_BIAS).standard_normal(C, dtype=np.float32) * np.float32(0.1)
+    cs = _fill_pool((C, CONV_WIDTH - 1), spec.num_slots, spec.seed, _T_CS, 1.0, "bf16", threads)
+    st = _fill_pool((H, HEAD_DIM, HEAD_DIM), spec.num_slots, spec.seed, _T_STATE, 0.02, "f32",
+                    threads)
+    nw = (1.0 + 0.1 * _rng(spec.seed, _T_NW).standard_normal(HEAD_DIM)).astype(np.float32)
+    return Inputs(spec=spec, qkv=step["qkv"], conv_weight=cw, conv_bias=bias, conv_state=cs,
+                  state=st, g=step["g"], beta=step["beta"], gate=step["gate"],
+                  norm_weight=nw, slot_idx=draw_slots(spec))
+
+
+def algorithmic_bytes(N: int, H: int, n_active_rows: int, out_norm: bool = True) -> int:
+    """Bytes one decode launch must move at minimum (DRAM or L2), counting
+    each tensor once: per active (row, head) the fp32 state read and write
+    (2 * 64 KiB), its q/k/v inputs, conv-state read and write, g, beta, gate
+    and output; per padding (row, head) its zeroed output; per launch the conv
+    weight, norm weight and slot indices."""
+    K = V = HEAD_DIM
+    per_active = (2 * K * V * 4          # state read + write
+                  + 3 * K * 2            # qkv slice
+                  + 2 * 3 * K * 3 * 2    # conv state read + write
+                  + K * 4                # g
+                  + 2                    # beta
+                  + V * 2)               # out
+    if out_norm:
+        per_active += V * 2              # gate
+    per_pad = V * 2
+    fixed = 3 * CONV_WIDTH * H * K * 4 + 4 * N
+    if out_norm:
+        fixed += V * 4
+    n_pad = N - n_active_rows
+    return H * (n_active_rows * per_active + n_pad * per_pad) + fixed

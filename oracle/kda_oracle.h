@@ -1,0 +1,148 @@
+/*
+ * kda_oracle.h -- plain, slow fp64 CPU oracle for the single-token fused KDA
+ * (Kimi Delta Attention) decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The product path (the
+ * CUDA library and its Python binding) never calls it and shares no code,
+ * header, table or helper with it.
+ *
+ * Source cited throughout as "P1": the web page "[ROCm][Perf] Kimi-K3 Fused
+ * kernel for KDA decode" (vLLM PR #50654 report).  Section names are the
+ * page's own: 功能与动机 (motivation), 实现拆解 (implementation breakdown),
+ * 关键源码片段 (code excerpts), 风险与影响 (risks and impact).
+ *
+ * ---------------------------------------------------------------------------
+ * FORMULATION ADOPTED
+ *
+ * P1 (功能与动机) names the three stages a decode step runs for every
+ * (sequence, value head): causal conv1d state advance, gated delta-rule
+ * recurrence, gated RMSNorm.  P1 never writes the equations; the oracle
+ * adopts the standard KDA definition, stated here in full.  Notation:
+ * K = key head dim, V = value head dim, W = conv width, H = heads,
+ * D_q = D_k = H*K, D_v = H*V, C = D_q + D_k + D_v channels.
+ *
+ * For each row n in [0,N) and head h in [0,H), with s = slot_idx[n]:
+ *
+ *  0. Padding.  If s <= 0 the row is CUDA-graph padding (P1 实现拆解 #1 and
+ *     the kernel excerpt in 关键源码片段): out[n, h*V + j] = 0 for all j and
+ *     nothing else is read or written.  If s >= num_slots the oracle does the
+ *     same and counts the row as out of range (library contract, not P1).
+ *
+ *  1. Conv + SiLU.  For block c in {q, k, v} and channel j of head h, global
+ *     channel ch = off_c + h*dim_c + j (blocks laid out q | k | v, each
+ *     head-major; off_q = 0, off_k = D_q, off_v = D_q + D_k):
+ *        x_t = conv_state[s, ch, t]     t = 0 .. W-2   (oldest .. newest)
+ *        x_{W-1} = qkv[n, ch]           (the current token)
+ *        y = sum_t Wc_c[t, h*dim_c + j] * x_t  (+ bias[ch] if given)
+ *        a = y * sigmoid(y)  (SiLU)
+ *     If update_conv_state: conv_state[s, ch, :] <- (x_1, ..., x_{W-1}),
+ *     the same bf16 bit patterns (a pure shift, never rounded).
+ *
+ *  2. L2 norm.  q^ = q_scale * q~ / sqrt(|q~|^2 + l2_eps),
+ *               k^ = k~ / sqrt(|k~|^2 + l2_eps),
+ *     q_scale = 1/sqrt(K) unless given, l2_eps = 1e-6.  v~ is used as is.
+ *
+ *  3. Gated delta rule on S = state[s, h] (K x V, S[i][j], i = key channel,
+ *     j = value channel, j contiguous):
+ *        alpha_i = exp(g[n, h, i])
+ *        S' = (I - beta k^ k^T) Diag(alpha) S + beta k^ v~^T
+ *     beta = beta[n, h] (bf16, already activated), g already activated.
+ *
+ *  4. Readout.  o = S'^T q^ (length V).
+ *
+ *  5. Output.  out_norm on:  out_j = o_j / sqrt(mean_j(o_j^2) + eps)
+ *                                     * norm_weight[j] * sigmoid(gate[n, h*V + j])
+ *              out_norm off: out_j = o_j
+ *
+ *  6. Rounding.  Every stored input is widened exactly to fp64; all
+ *     arithmetic is fp64; out is rounded to bf16 and S' to fp32, both
+ *     round-to-nearest-even, and S' is written back to slot s.
+ *
+ * The choices P1 leaves open (q scale, the two epsilons' placement, the
+ * conv-state tap order, the state's index order, norm weight shared across
+ * heads, the gate activation, norm-off output) are taken as above.
+ * Parity unpinned by the pages: the q scale (1/sqrt(K)) and the L2-norm
+ * epsilon's placement have no passage behind them; both sides follow the
+ * formulation written here.
+ * ---------------------------------------------------------------------------
+ */
+#ifndef KDA_ORACLE_H
+#define KDA_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Whole-step problem.  All pointers are host memory owned by the caller.
+ * bf16 tensors are passed as their raw 16-bit patterns. */
+typedef struct {
+  int32_t N, H, K, V, W, num_slots;
+  const uint16_t* qkv;        /* [N][qkv_row_stride], first C used */
+  int64_t qkv_row_stride;     /* elements; >= C */
+  const float* conv_weight;   /* q block [W][H*K], k block [W][H*K], v block [W][H*V] */
+  const float* conv_bias;     /* [C] or NULL */
+  uint16_t* conv_state;       /* [num_slots][C][W-1] */
+  float* state;               /* [num_slots][H][K][V] */
+  const float* g;             /* [N][H][K] log-decay */
+  const uint16_t* beta;       /* [N][H] */
+  const uint16_t* gate;       /* [N][H*V]; ignored when out_norm == 0 */
+  const float* norm_weight;   /* [V]; ignored when out_norm == 0 */
+  const int32_t* slot_idx;    /* [N] */
+  uint16_t* out;              /* [N][H*V] */
+  double* out_f64;            /* optional [N][H*V]: out before bf16 rounding */
+  double eps;                 /* RMSNorm epsilon */
+  double l2_eps;              /* L2-norm epsilon */
+  double q_scale;             /* 0 => 1/sqrt(K) */
+  int32_t out_norm;           /* 1: gated RMSNorm epilogue, 0: raw o */
+  int32_t update_conv_state;  /* 1: write the shifted conv state */
+} kda_oracle_problem;
+
+/* Runs one decode step over every (row, head).  num_threads <= 0 uses the
+ * OpenMP default.  Returns the number of rows whose slot was >= num_slots
+ * (they are zeroed like padding), or -1 on a bad argument. */
+int kda_oracle_decode(const kda_oracle_problem* p, int num_threads);
+
+/* Size of kda_oracle_problem, so a foreign-function caller can check that its
+ * mirror of the struct matches. */
+int kda_oracle_problem_size(void);
+
+/* ---- the individual steps, fp64, exposed for the fact tests ---- */
+
+/* sigmoid(x) = 1 / (1 + exp(-x)). */
+double kda_oracle_sigmoid(double x);
+
+/* Step 1: y = sum_t w[t] * x[t] + bias over a window x[0..W-1], oldest first,
+ * x[W-1] the current input; returns y (before SiLU). */
+double kda_oracle_causal_conv(const double* x, const double* w, int W, double bias);
+
+/* SiLU(y) = y * sigmoid(y). */
+double kda_oracle_silu(double y);
+
+/* Step 2: y = scale * x / sqrt(sum x^2 + eps), length n. */
+void kda_oracle_l2norm(const double* x, int n, double eps, double scale, double* y);
+
+/* Step 3: S (K x V, row-major, in place) <- (I - beta k k^T) Diag(alpha) S + beta k v^T. */
+void kda_oracle_gated_delta_update(int K, int V, double* S, const double* alpha,
+                                   double beta, const double* k, const double* v);
+
+/* Step 4: o = S^T q, S K x V row-major. */
+void kda_oracle_readout(int K, int V, const double* S, const double* q, double* o);
+
+/* Step 5: y_j = o_j / sqrt(mean(o^2) + eps) * w_j * sigmoid(gate_j). */
+void kda_oracle_gated_rmsnorm(int V, const double* o, const double* w,
+                              const double* gate, double eps, double* y);
+
+/* Round to bf16, nearest-even, directly from fp64; returns the bit pattern. */
+uint16_t kda_oracle_round_bf16(double x);
+
+/* Exact widening of a bf16 bit pattern. */
+double kda_oracle_bf16_to_f64(uint16_t b);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_ORACLE_H */

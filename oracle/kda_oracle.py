@@ -1,0 +1,216 @@
+"""ctypes wrapper of the C oracle (``kda_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  ``build()`` compiles the C source with the host's
+gcc into ``oracle/_build/`` (plain C, OpenMP, ``-ffp-contract=off`` so x86 and
+Arm produce the same bits).  Arrays are numpy; bf16 tensors travel as their
+uint16 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_HDR = os.path.join(_HERE, "kda_oracle.h")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_OUT_DIR, "libkda_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle library if it is missing or older than its source."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    newest_src = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= newest_src:
+        return _SO
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int32), ("H", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("V", ctypes.c_int32), ("W", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+        ("qkv", ctypes.c_void_p), ("qkv_row_stride", ctypes.c_int64),
+        ("conv_weight", ctypes.c_void_p), ("conv_bias", ctypes.c_void_p),
+        ("conv_state", ctypes.c_void_p), ("state", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("gate", ctypes.c_void_p),
+        ("norm_weight", ctypes.c_void_p), ("slot_idx", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("out_f64", ctypes.c_void_p),
+        ("eps", ctypes.c_double), ("l2_eps", ctypes.c_double), ("q_scale", ctypes.c_double),
+        ("out_norm", ctypes.c_int32), ("update_conv_state", ctypes.c_int32),
+    ]
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            # KDA_ORACLE_SO points the pins at another build of the oracle
+            # (the planted-mistake tests use it); normally unset.
+            so = os.environ.get("KDA_ORACLE_SO") or build()
+            L = ctypes.CDLL(so)
+            dp = ctypes.POINTER(ctypes.c_double)
+            L.kda_oracle_decode.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int]
+            L.kda_oracle_decode.restype = ctypes.c_int
+            L.kda_oracle_problem_size.restype = ctypes.c_int
+            L.kda_oracle_sigmoid.argtypes = [ctypes.c_double]
+            L.kda_oracle_sigmoid.restype = ctypes.c_double
+            L.kda_oracle_silu.argtypes = [ctypes.c_double]
+            L.kda_oracle_silu.restype = ctypes.c_double
+            L.kda_oracle_causal_conv.argtypes = [dp, dp, ctypes.c_int, ctypes.c_double]
+            L.kda_oracle_causal_conv.restype = ctypes.c_double
+            L.kda_oracle_l2norm.argtypes = [dp, ctypes.c_int, ctypes.c_double, ctypes.c_double, dp]
+            L.kda_oracle_gated_delta_update.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp,
+                                                        ctypes.c_double, dp, dp]
+            L.kda_oracle_readout.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp, dp]
+            L.kda_oracle_gated_rmsnorm.argtypes = [ctypes.c_int, dp, dp, dp, ctypes.c_double, dp]
+            L.kda_oracle_round_bf16.argtypes = [ctypes.c_double]
+            L.kda_oracle_round_bf16.restype = ctypes.c_uint16
+            L.kda_oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            L.kda_oracle_bf16_to_f64.restype = ctypes.c_double
+            if L.kda_oracle_problem_size() != ctypes.sizeof(_Problem):
+                raise RuntimeError("oracle struct layout mismatch")
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _dp(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+# ------------------------------------------------------------ step functions
+
+def sigmoid(x: float) -> float:
+    return lib().kda_oracle_sigmoid(float(x))
+
+
+def silu(y: float) -> float:
+    return lib().kda_oracle_silu(float(y))
+
+
+def causal_conv(x, w, bias: float = 0.0) -> float:
+    x, w = _f64(x), _f64(w)
+    assert x.shape == w.shape and x.ndim == 1
+    return lib().kda_oracle_causal_conv(_dp(x), _dp(w), x.size, float(bias))
+
+
+def l2norm(x, eps: float = 1e-6, scale: float = 1.0) -> np.ndarray:
+    x = _f64(x)
+    y = np.empty_like(x)
+    lib().kda_oracle_l2norm(_dp(x), x.size, float(eps), float(scale), _dp(y))
+    return y
+
+
+def gated_delta_update(S, alpha, beta: float, k, v) -> np.ndarray:
+    S = _f64(S).copy()
+    K, V = S.shape
+    alpha, k, v = _f64(alpha), _f64(k), _f64(v)
+    assert alpha.shape == (K,) and k.shape == (K,) and v.shape == (V,)
+    lib().kda_oracle_gated_delta_update(K, V, _dp(S), _dp(alpha), float(beta), _dp(k), _dp(v))
+    return S
+
+
+def readout(S, q) -> np.ndarray:
+    S, q = _f64(S), _f64(q)
+    K, V = S.shape
+    o = np.empty(V)
+    lib().kda_oracle_readout(K, V, _dp(S), _dp(q), _dp(o))
+    return o
+
+
+def gated_rmsnorm(o, w, gate, eps: float = 1e-6) -> np.ndarray:
+    o, w, gate = _f64(o), _f64(w), _f64(gate)
+    y = np.empty_like(o)
+    lib().kda_oracle_gated_rmsnorm(o.size, _dp(o), _dp(w), _dp(gate), float(eps), _dp(y))
+    return y
+
+
+def round_bf16(x: float) -> int:
+    return int(lib().kda_oracle_round_bf16(float(x)))
+
+
+def bf16_to_f64(b: int) -> float:
+    return lib().kda_oracle_bf16_to_f64(int(b))
+
+
+# ------------------------------------------------------------ whole step
+
+@dataclass
+class OracleResult:
+    out: np.ndarray            # uint16 bf16 bits [N, H*V]
+    out_f64: np.ndarray | None  # fp64 [N, H*V] before rounding
+    conv_state: np.ndarray     # uint16 [slots, C, W-1] after the step
+    state: np.ndarray          # float32 [slots, H, K, V] after the step
+    n_out_of_range: int
+
+
+def decode(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, H: int,
+           K: int = 128, V: int = 128, W: int = 4, gate=None, norm_weight=None,
+           conv_bias=None, eps: float = 1e-6, l2_eps: float = 1e-6, q_scale: float = 0.0,
+           out_norm: bool = True, update_conv_state: bool = True, threads: int = 0,
+           want_f64: bool = True, in_place: bool = False) -> OracleResult:
+    """One decode step over all rows.  ``conv_state``/``state`` are copied
+    unless ``in_place``; the updated arrays come back in the result."""
+    qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
+    N = qkv.shape[0]
+    C = 2 * H * K + H * V
+    conv_weight = np.ascontiguousarray(conv_weight, dtype=np.float32)
+    assert conv_weight.size == W * C, conv_weight.shape
+    if in_place:
+        assert conv_state.dtype == np.uint16 and conv_state.flags.c_contiguous
+        assert state.dtype == np.float32 and state.flags.c_contiguous
+        cs, st = conv_state, state
+    else:
+        cs = np.array(conv_state, dtype=np.uint16, order="C", copy=True)
+        st = np.array(state, dtype=np.float32, order="C", copy=True)
+    num_slots = st.shape[0]
+    assert st.size == num_slots * H * K * V
+    assert cs.size == num_slots * C * max(W - 1, 0) or W == 1
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    beta = np.ascontiguousarray(beta, dtype=np.uint16)
+    slot_idx = np.ascontiguousarray(slot_idx, dtype=np.int32)
+    assert g.size == N * H * K and beta.size == N * H and slot_idx.size == N
+    if out_norm:
+        gate = np.ascontiguousarray(gate, dtype=np.uint16)
+        norm_weight = np.ascontiguousarray(norm_weight, dtype=np.float32)
+        assert gate.size == N * H * V and norm_weight.size == V
+    else:
+        gate = norm_weight = None
+    if conv_bias is not None:
+        conv_bias = np.ascontiguousarray(conv_bias, dtype=np.float32)
+        assert conv_bias.size == C
+    out = np.zeros((N, H * V), dtype=np.uint16)
+    out64 = np.zeros((N, H * V), dtype=np.float64) if want_f64 else None
+    p = _Problem(N=N, H=H, K=K, V=V, W=W, num_slots=num_slots,
+                 qkv=_ptr(qkv), qkv_row_stride=qkv.shape[1] if qkv.ndim == 2 else C,
+                 conv_weight=_ptr(conv_weight), conv_bias=_ptr(conv_bias),
+                 conv_state=_ptr(cs), state=_ptr(st), g=_ptr(g), beta=_ptr(beta),
+                 gate=_ptr(gate), norm_weight=_ptr(norm_weight), slot_idx=_ptr(slot_idx),
+                 out=_ptr(out), out_f64=_ptr(out64), eps=eps, l2_eps=l2_eps,
+                 q_scale=q_scale, out_norm=int(bool(out_norm)),
+                 update_conv_state=int(bool(update_conv_state)))
+    rc = lib().kda_oracle_decode(ctypes.byref(p), int(threads))
+    if rc < 0:
+        raise ValueError("kda_oracle_decode rejected its arguments")
+    return OracleResult(out=out, out_f64=out64, conv_state=cs, state=st, n_out_of_range=rc)

@@ -1,0 +1,59 @@
+"""Planted mistakes: each copy of the oracle below carries one plausible
+error (a dropped term, a wrong sign or index, reversed taps, a misplaced
+epsilon, ...).  The pin suite, run against that copy in a child process,
+must fail.  Mistakes are planted in a temporary copy of the C source on the
+CPU; the real oracle is never modified."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "kda_oracle.c")
+
+MUTANTS = {
+    "dropped_beta_k_v_term": (
+        "- beta * k[i] * u[j] + beta * k[i] * v[j];", "- beta * k[i] * u[j];"),
+    "wrong_sign_on_erase": (
+        "- beta * k[i] * u[j] + beta * k[i] * v[j];", "+ beta * k[i] * u[j] + beta * k[i] * v[j];"),
+    "decay_on_value_index": (
+        "S[(size_t)i * V + j] *= alpha[i];", "S[(size_t)i * V + j] *= alpha[j % K];"),
+    "l2_eps_outside_sqrt": (
+        "double inv = 1.0 / sqrt(ss + eps);", "double inv = 1.0 / (sqrt(ss) + eps);"),
+    "rms_eps_outside_sqrt": (
+        "double r = 1.0 / sqrt(ss / (double)V + eps);", "double r = 1.0 / (sqrt(ss / (double)V) + eps);"),
+    "reversed_conv_taps": (
+        "wt[t] = (double)wc[(int64_t)t * D_c", "wt[t] = (double)wc[(int64_t)(W - 1 - t) * D_c"),
+    "conv_state_shift_wrong_end": ("cs[W - 2] = xin;", "cs[0] = xin;"),
+    "gate_silu_not_sigmoid": (
+        "* w[j] * kda_oracle_sigmoid(gate[j]);", "* w[j] * kda_oracle_silu(gate[j]);"),
+    "q_scale_from_value_dim": (
+        "1.0 / sqrt((double)K);", "1.0 / sqrt((double)V);"),
+    "slot_zero_not_padding": ("if (s <= 0 || s >= p->num_slots) {", "if (s < 0 || s >= p->num_slots) {"),
+    "bf16_ties_away": (
+        "if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;",
+        "if (rem >= 0.5) fl += 1.0;"),
+    "readout_skips_last_key": (
+        "for (int i = 0; i < K; ++i) acc += S[(size_t)i * V + j] * q[i];",
+        "for (int i = 0; i < K - 1; ++i) acc += S[(size_t)i * V + j] * q[i];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    (tmp_path / "kda_oracle.c").write_text(src.replace(old, new))
+    hdr = os.path.join(ROOT, "oracle", "kda_oracle.h")
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                    "-I", os.path.dirname(hdr), str(tmp_path / "kda_oracle.c"), "-o", str(so), "-lm"],
+                   check=True)
+    env = dict(os.environ, KDA_ORACLE_SO=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    # exit code 1 = some test failed (not a crash, not a collection error)
+    assert r.returncode == 1, f"mutant {name} survived or crashed:\n{r.stdout[-2000:]}\n{r.stderr[-2000:]}"
