@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused KDA decode step on GB300.
+
+One step = one decode token through a stack of 69 independent KDA layers
+(H=48 heads of 128, a 96-slot state pool per layer, N=64 rows of which the
+last 4 are slot-0 padding), all 69 launches captured in one CUDA graph and
+replayed.  The metric is (sequence, head) state updates per second; the
+roofline object reports the algorithmic HBM bytes of one launch over its
+measured duration against the measured copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (under torchrun) every rank runs its own stack on its own GPU
+with no data exchange (weak scaling); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused KDA decode: seq·head updates/s and achieved HBM GB/s vs GB300 peak"
+UNIT = "updates/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "kda_decode_stack69_traffic.md")
+KERNEL_SRC = os.path.join(ROOT, "linear_attention_decode_04_gb300", "csrc", "kda_decode.cu")
+
+
+# ----------------------------------------------------------------- host logic
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def aggregate(ms_local: float, units_local: int, world: int, device=None) -> tuple[float, int]:
+    """Max step time and total units over ranks (identity at world 1)."""
+    if world == 1:
+        return ms_local, units_local
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item())
+
+
+def measured_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic() -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        text = open(TRAFFIC_NOTE).read()
+    except OSError:
+        return None
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not h or not b or h.group(1) != kernel_source_hash():
+        return None
+    return float(b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self) -> dict:
+        try:
+            rows = [r.split(",") for r in open(self.file.name).read().strip().splitlines() if r.strip()]
+        finally:
+            os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- oracle leg
+
+def oracle_rate(host_layers, budget_s: float) -> dict:
+    """Time the fp64 oracle (as it stands) on the given layers' inputs,
+    repeating passes until ``budget_s`` of wall time; returns units/s."""
+    import oracle
+    threads = os.cpu_count() or 1
+    units = done = 0
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        for x in host_layers:
+            r = oracle.decode(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state,
+                              state=x.state, g=x.g, beta=x.beta, slot_idx=x.slot_idx, H=x.H,
+                              gate=x.gate, norm_weight=x.norm_weight, eps=x.spec.eps,
+                              out_norm=x.spec.out_norm, update_conv_state=x.spec.update_conv_state,
+                              threads=threads, want_f64=False, in_place=True)
+            assert r.n_out_of_range == 0
+            units += len(x.active_rows()) * x.H
+        passes += 1
+        done = time.perf_counter() - t0
+        if done >= budget_s:
+            break
+    return {"units": units, "seconds": done, "value": units / done, "threads": threads, "passes": passes}
+
+
+# ----------------------------------------------------------------- main
+
+def build_stack(device, n_layers: int, keep_host: int):
+    import torch
+
+    from linear_attention_decode_04_gb300 import workloads as W
+    layers, host = [], []
+    for ell in range(n_layers):
+        x = W.make_inputs(W.stack_layer_spec(ell))
+        L = dict(
+            qkv=torch.from_numpy(x.qkv.view(np.int16)).view(torch.bfloat16).to(device),
+            conv_weight=torch.from_numpy(x.conv_weight).to(device),
+            conv_state=torch.from_numpy(x.conv_state.view(np.int16)).view(torch.bfloat16).to(device),
+            state=torch.from_numpy(x.state).to(device),
+            g=torch.from_numpy(x.g).to(device),
+            beta=torch.from_numpy(x.beta.view(np.int16)).view(torch.bfloat16).to(device),
+            gate=torch.from_numpy(x.gate.view(np.int16)).view(torch.bfloat16).to(device),
+            norm_weight=torch.from_numpy(x.norm_weight).to(device),
+            slot_idx=torch.from_numpy(x.slot_idx).to(device),
+            out=torch.empty(x.N, x.H * W.HEAD_DIM, dtype=torch.bfloat16, device=device),
+            err_flag=torch.zeros(1, dtype=torch.int32, device=device),
+        )
+        layers.append(L)
+        if ell < keep_host:
+            host.append(x)
+        n_active = len(x.active_rows())
+    return layers, host, x.spec, n_active
+
+
+def run_ours(args) -> dict | None:
+    import torch
+
+    from linear_attention_decode_04_gb300 import workloads as W
+    from linear_attention_decode_04_gb300.stack import STEP_INPUTS, DecodeStack
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    n_layers = W.STACK_LAYERS
+    keep_host = 2 if (rank == 0 and not args.no_cpu_baseline) else 0
+    layers, host, spec, n_active = build_stack(device, n_layers, keep_host)
+    stack = DecodeStack(layers, eps=spec.eps, out_norm=spec.out_norm,
+                        update_conv_state=spec.update_conv_state)
+    stream = torch.cuda.Stream(device)
+    stack.capture(stream)
+
+    units_step = n_layers * n_active * spec.H
+    launch_bytes = W.algorithmic_bytes(spec.N, spec.H, n_active, spec.out_norm)
+    state_bytes = n_layers * spec.num_slots * spec.H * 128 * 128 * 4
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- device-resident timing (graph replay)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            stack.replay()
+    torch.cuda.synchronize(device)
+    barrier()
+    torch.cuda.synchronize(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                stack.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(device)
+    barrier()
+    torch.cuda.synchronize(device)
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms_step, units_total = aggregate(ms_local, units_step, world, device)
+    clocks = clk.summary()
+
+    # ---- end to end: pinned host inputs -> device, graph, output -> host
+    host_in = [{k: torch.empty_like(L[k], device="cpu").pin_memory() for k in STEP_INPUTS}
+               for L in layers]
+    for L, hin in zip(layers, host_in):
+        for k in STEP_INPUTS:
+            hin[k].copy_(L[k])
+    host_out = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in layers]
+    h2d = sum(t.numel() * t.element_size() for hin in host_in for t in hin.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(3, args.steps // 4)
+
+    def e2e_step():
+        for L, hin in zip(layers, host_in):
+            for k in STEP_INPUTS:
+                L[k].copy_(hin[k], non_blocking=True)
+        stack.replay()
+        for L, ho in zip(layers, host_out):
+            ho.copy_(L["out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+    torch.cuda.synchronize(device)
+    barrier()
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    e2e_ms, _ = aggregate(ev0.elapsed_time(ev1) / e2e_steps, units_step, world, device)
+
+    errs = sum(int(L["err_flag"].item()) for L in layers)
+    if errs:
+        raise SystemExit(f"device error flag raised ({errs})")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        r = oracle_rate(host, args.cpu_budget)
+        cpu = {"value": r["value"], "unit": UNIT, "cores": r["threads"], "kind": "oracle",
+               "sample": (f"fp64 C oracle, OpenMP {r['threads']} threads, {len(host)} of the 69 layers "
+                          f"({r['units']} (row, head) updates over {r['passes']} passes, "
+                          f"{r['seconds']:.1f} s)")}
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    peak, peak_kind = measured_peak()
+    per_launch_s = ms_step / 1e3 / stack.launches_per_step
+    achieved = launch_bytes / per_launch_s / 1e9
+    traffic = recorded_traffic()
+    return {
+        "metric": METRIC, "value": units_total / (ms_step / 1e3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; distributions of the decode-step workload)",
+        "config": {"workload": W.STACK_LAYER.name, "layers": n_layers, "N": spec.N, "H": spec.H,
+                   "head_dim": 128, "pool_slots": spec.num_slots, "pad_rows": spec.pad_tail,
+                   "active_units_per_step": units_step, "graph": "one CUDA graph per step",
+                   "l2": f"inputs larger than L2: {state_bytes / 1e9:.1f} GB state pools",
+                   "parallelism": f"replicas x{world} (no exchange)"},
+        "achieved_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": launch_bytes},
+        "e2e": {"value": units_total / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": stack.launches_per_step * args.steps,
+        "impl": "ours",
+    }
+
+
+def run_reference(args) -> dict | None:
+    """The oracle as it stands, timed on the host cores on a bounded sample
+    of the same workload (rank 0 only)."""
+    from linear_attention_decode_04_gb300 import workloads as W
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    host = [W.make_inputs(W.stack_layer_spec(ell)) for ell in range(args.ref_layers)]
+    n_active = len(host[0].active_rows())
+    units = n_active * host[0].H * len(host)
+    import oracle
+    threads = os.cpu_count() or 1
+
+    def step():
+        for x in host:
+            oracle.decode(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state,
+                          g=x.g, beta=x.beta, slot_idx=x.slot_idx, H=x.H, gate=x.gate,
+                          norm_weight=x.norm_weight, eps=x.spec.eps, threads=threads,
+                          want_f64=False, in_place=True)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = units / dt
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": W.STACK_LAYER.name, "layers_sampled": len(host), "N": 64, "H": 48},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{len(host)} of 69 layers per step ({units} updates)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
+    ap.add_argument("--ref-layers", type=int, default=2, help="layers per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

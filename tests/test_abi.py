@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads without a GPU and exports every function
+``include/*.h`` declares; its host-side argument checks answer with the right
+codes before any CUDA call (fake, never-dereferenced pointers)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from linear_attention_decode_04_gb300 import binding
+from linear_attention_decode_04_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(kda_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    assert {"kda_decode", "kda_status_string", "kda_last_error", "kda_abi_version"} <= set(declared_functions())
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(binding.library_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared but not exported"
+
+
+def test_struct_layout_matches_header(lib):
+    # every field of the C struct, in order, in the Python mirror
+    text = open(os.path.join(ROOT, "include", "kda_decode.h")).read()
+    body = text[text.index("typedef struct KdaDecodeArgs {"):text.index("} KdaDecodeArgs;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"(\w+)\s*;", body)
+    assert fields == [f for f, _ in binding.KdaDecodeArgs._fields_]
+
+
+def _args(**kw):
+    a = binding.KdaDecodeArgs(struct_size=ctypes.sizeof(binding.KdaDecodeArgs), N=4, H=12,
+                              num_slots=8, head_dim=128, conv_width=4, eps=1e-6, flags=3)
+    fake = 0x10000
+    for f in ("qkv", "conv_weight", "conv_state", "state", "g", "beta", "gate", "norm_weight",
+              "slot_idx", "out"):
+        setattr(a, f, fake)
+        fake += 0x100000
+    a.qkv_row_stride = 3 * 12 * 128
+    a.gate_row_stride = a.out_row_stride = 12 * 128
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _call(lib, a):
+    return lib.kda_decode(ctypes.byref(a), None)
+
+
+def test_host_validation_codes(lib):
+    assert lib.kda_decode(None, None) == -1
+    assert _call(lib, _args(struct_size=8)) == -6
+    assert _call(lib, _args(head_dim=64)) == -2
+    assert _call(lib, _args(conv_width=3)) == -2
+    assert _call(lib, _args(H=0)) == -2
+    assert _call(lib, _args(N=-1)) == -2
+    assert _call(lib, _args(flags=8)) == -4
+    assert _call(lib, _args(N=0)) == 0          # no-op, no launch
+    assert _call(lib, _args(qkv=None)) == -1
+    assert _call(lib, _args(gate=None)) == -1    # norm on needs the gate
+    assert _call(lib, _args(qkv_row_stride=100)) == -2
+    assert _call(lib, _args(qkv_row_stride=3 * 12 * 128 + 4)) == -3
+    assert _call(lib, _args(state=0x10004)) == -3
+    assert b"aligned" in lib.kda_last_error()
+    assert lib.kda_status_string(-3).decode().startswith("pointer")
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(FileNotFoundError):
+        binding.load_library()
+
+
+def test_oracle_builds():
+    import oracle
+    assert os.path.exists(oracle.build())

@@ -1,0 +1,144 @@
+"""CUDA path vs the fp64 oracle on the same seeded inputs, through the C ABI.
+
+Tolerances: conv state and untouched slots bit-exact; recurrent state
+|d| <= 1e-4 + 1e-4|ref|; bf16 output |d| <= 3e-2 and, tighter, within one
+bf16 ulp of the exact output."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import kda_testlib as T
+from linear_attention_decode_04_gb300 import KdaError, kda_decode
+from linear_attention_decode_04_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(x, dev, **kw):
+    d = T.to_device(x, dev)
+    T.run_gpu(x, d, **kw)
+    torch.cuda.synchronize()
+    ref = T.run_oracle(x, **kw)
+    res = T.compare_all(x, d, ref, init_state=x.state, init_conv=x.conv_state)
+    assert int(d["err_flag"].item()) == 0
+    return res
+
+
+@pytest.mark.parametrize("name", list(W.SPECS))
+def test_workload_parity(name, cuda_device):
+    """The four seeded workloads of the decode step, compared element by element."""
+    x = W.make_inputs(W.SPECS[name])
+    res = _check(x, cuda_device)
+    print(name, res)
+
+
+@pytest.mark.parametrize("out_norm", [True, False])
+@pytest.mark.parametrize("update_conv_state", [True, False])
+def test_flag_combinations(out_norm, update_conv_state, cuda_device):
+    x = W.make_inputs(W.Spec("flags_n9_h12_pool16", N=9, H=12, num_slots=16, seed=21, pad_tail=2))
+    _check(x, cuda_device, out_norm=out_norm, update_conv_state=update_conv_state)
+
+
+@pytest.mark.parametrize("H", [12, 24, 48, 96, 5])
+@pytest.mark.parametrize("N", [1, 7])
+def test_heads_and_rows(H, N, cuda_device):
+    """Every supported head count (12/24/48/96 = 96 heads over TP 8/4/2/1),
+    an unusual one, and the odd row count 7."""
+    x = W.make_inputs(W.Spec(f"h{H}_n{N}", N=N, H=H, num_slots=N + 3, seed=100 + H + N))
+    _check(x, cuda_device)
+
+
+def test_negative_and_zero_slots_are_padding(cuda_device):
+    spec = W.Spec("pad_mix_n6_h12", N=6, H=12, num_slots=8, seed=31, slots=(0, 4, -3, 7, 0, 2))
+    x = W.make_inputs(spec)
+    res = _check(x, cuda_device)
+    assert res["out_max_abs"] <= T.OUT_ATOL
+
+
+def test_all_padding_batch(cuda_device):
+    x = W.make_inputs(W.Spec("all_pad_n5_h24", N=5, H=24, num_slots=4, seed=32, slots=(0, 0, -1, 0, 0)))
+    d = T.to_device(x, cuda_device)
+    T.run_gpu(x, d)
+    torch.cuda.synchronize()
+    assert not torch.any(d["out"].float() != 0)
+    assert np.array_equal(d["state"].cpu().numpy(), x.state)
+    assert np.array_equal(T.bf16_bits(d["conv_state"]), x.conv_state)
+
+
+def test_out_of_range_slot_sets_flag_without_trap(cuda_device):
+    x = W.make_inputs(W.Spec("oob_n4_h12", N=4, H=12, num_slots=6, seed=33, slots=(1, 6, 3, 1000)))
+    d = T.to_device(x, cuda_device)
+    T.run_gpu(x, d)
+    torch.cuda.synchronize()
+    assert int(d["err_flag"].item()) == 1
+    ref = T.run_oracle(x)
+    assert ref.n_out_of_range == 2
+    T.compare_all(x, d, ref, init_state=x.state, init_conv=x.conv_state)
+
+
+def test_bias_and_row_strides(cuda_device):
+    """Conv bias, a qkv row longer than 3*H*128, and row-strided gate/out
+    views; the padding columns of out stay unwritten."""
+    spec = W.Spec("strided_n5_h12", N=5, H=12, num_slots=9, seed=34, with_bias=True, qkv_row_pad=24,
+                  pad_tail=1)
+    x = W.make_inputs(spec)
+    d = T.to_device(x, cuda_device, out_row_pad=16, gate_row_pad=8)
+    T.run_gpu(x, d)
+    torch.cuda.synchronize()
+    ref = T.run_oracle(x)
+    T.compare_all(x, d, ref, init_state=x.state, init_conv=x.conv_state)
+    assert torch.isnan(d["out_full"][:, x.H * 128:].float()).all()
+
+
+def test_q_scale_argument(cuda_device):
+    x = W.make_inputs(replace(W.NORM_OFF, name="qscale_n16_h12", N=16, H=12, num_slots=20))
+    _check(x, cuda_device, q_scale=1.0)
+
+
+def test_deterministic_repeat(cuda_device):
+    x = W.make_inputs(W.PAD_TAIL)
+    outs = []
+    for _ in range(2):
+        d = T.to_device(x, cuda_device)
+        T.run_gpu(x, d)
+        torch.cuda.synchronize()
+        outs.append((T.bf16_bits(d["out"]), d["state"].cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_pool_guard_regions_untouched(cuda_device):
+    """Allocate the pools with guard slots on both sides (sentinel-filled) and
+    pass the middle: nothing outside the passed pool is written."""
+    x = W.make_inputs(W.Spec("guard_n8_h12", N=8, H=12, num_slots=10, seed=35, pad_tail=1))
+    d = T.to_device(x, cuda_device)
+    S, H, C = x.spec.num_slots, x.H, x.C
+    big = torch.full((S + 2, H, 128, 128), 7.25, dtype=torch.float32, device=cuda_device)
+    big[1:S + 1] = d["state"]
+    bigcs = torch.full((S + 2, C, 3), -2.0, dtype=torch.bfloat16, device=cuda_device)
+    bigcs[1:S + 1] = d["conv_state"]
+    d["state"], d["conv_state"] = big[1:S + 1], bigcs[1:S + 1]
+    T.run_gpu(x, d)
+    torch.cuda.synchronize()
+    assert torch.all(big[0] == 7.25) and torch.all(big[S + 1] == 7.25)
+    assert torch.all(bigcs[0] == -2.0) and torch.all(bigcs[S + 1] == -2.0)
+    T.compare_all(x, d, T.run_oracle(x))
+
+
+def test_binding_rejects_cpu_and_bad_shapes(cuda_device):
+    x = W.make_inputs(W.PR1_REF)
+    d = T.to_device(x, cuda_device)
+    with pytest.raises(ValueError):
+        kda_decode(d["qkv"].cpu(), d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
+                   d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"])
+    with pytest.raises(ValueError):
+        kda_decode(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"][:, :5], d["beta"],
+                   d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"])
+    # misaligned qkv (offset by one element) is refused by the C ABI itself
+    raw = torch.empty(x.N * x.C + 8, dtype=torch.bfloat16, device=cuda_device)
+    mis = raw[1:1 + x.N * x.C].view(x.N, x.C)
+    with pytest.raises(KdaError) as ei:
+        kda_decode(mis, d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
+                   d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"])
+    assert ei.value.status == -3
