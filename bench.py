@@ -174,12 +174,17 @@ def oracle_rate(host_layers, budget_s: float) -> dict:
 # ----------------------------------------------------------------- main
 
 def build_stack(device, n_layers: int, keep_host: int):
+    from linear_attention_decode_04_gb300 import workloads as W
+    return build_stack_specs(device, [W.stack_layer_spec(ell) for ell in range(n_layers)], keep_host)
+
+
+def build_stack_specs(device, specs, keep_host: int = 0):
     import torch
 
     from linear_attention_decode_04_gb300 import workloads as W
     layers, host = [], []
-    for ell in range(n_layers):
-        x = W.make_inputs(W.stack_layer_spec(ell))
+    for ell, sp in enumerate(specs):
+        x = W.make_inputs(sp)
         L = dict(
             qkv=torch.from_numpy(x.qkv.view(np.int16)).view(torch.bfloat16).to(device),
             conv_weight=torch.from_numpy(x.conv_weight).to(device),
@@ -333,6 +338,48 @@ def run_ours(args) -> dict | None:
     }
 
 
+def run_case(args) -> dict | None:
+    """Timing of one launch configuration on its own (also the small case
+    for ncu captures): ``layer`` = one layer of the stack, launched eagerly;
+    ``roofline`` = N=256, H=96, pool 1024 as one launch replayed from a CUDA
+    graph.  Prints a line with ``mode`` set; not the headline line."""
+    import torch
+
+    from linear_attention_decode_04_gb300 import workloads as W
+    from linear_attention_decode_04_gb300.stack import DecodeStack
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    spec = W.stack_layer_spec(0) if args.case == "layer" else W.ROOFLINE
+    layers, _, spec, n_active = build_stack_specs(device, [spec])
+    stack = DecodeStack(layers, eps=spec.eps, out_norm=spec.out_norm,
+                        update_conv_state=spec.update_conv_state)
+    stream = torch.cuda.Stream(device)
+    graph = args.case != "layer"
+    if graph:
+        stack.capture(stream)
+    step = stack.replay if graph else (lambda: stack.run_eager(stream))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                step()
+            ev1.record(stream)
+        torch.cuda.synchronize(device)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    nbytes = W.algorithmic_bytes(spec.N, spec.H, n_active, spec.out_norm)
+    peak, kind = measured_peak()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"mode": args.case, "workload": spec.name, "graph": graph, "ms_per_launch": ms,
+            "updates_per_s": n_active * spec.H / (ms / 1e3), "achieved_gbs": gbs, "peak_gbs": peak,
+            "frac": gbs / peak, "peak_source": kind, "algorithmic_bytes_per_launch": nbytes,
+            "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup}
+
+
 def run_reference(args) -> dict | None:
     """The oracle as it stands, timed on the host cores on a bounded sample
     of the same workload (rank 0 only)."""
@@ -381,10 +428,18 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--ref-layers", type=int, default=2, help="layers per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=("stack69", "layer", "roofline"), default="stack69",
+                    help="stack69: the headline 69-layer graph step; layer / roofline: one "
+                         "launch configuration timed on its own (profiling aid)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.impl == "reference":
+        res = run_reference(args)
+    elif args.case != "stack69":
+        res = run_case(args)
+    else:
+        res = run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 
