@@ -56,6 +56,8 @@ extern "C" {
 
 /* bits OR-ed into *err_flag by the kernel (never a trap) */
 #define KDA_DEVERR_SLOT_RANGE 1 /* a row had slot >= num_slots; its output was zeroed */
+#define KDA_DEVERR_TIMEOUT    2 /* an internal pipeline wait gave up after 2 s; the launch
+                                   stopped early and its results are incomplete */
 
 /*
  * Arguments.  Shapes use N = rows (tokens), H = heads, D = H * 128,

@@ -18,17 +18,24 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <mutex>
+
 #include "kda_decode.h"
 
 namespace {
 
-constexpr int kDim = 128;              // key = value head dim
-constexpr int kWidth = 4;              // conv taps
-constexpr int kThreads = 256;          // 8 warps
-constexpr int kWarps = kThreads / 32;
-constexpr int kRowsPerWarp = kDim / kWarps;   // 16 key rows per warp
-constexpr int kCsU4 = kDim * (kWidth - 1) * 2 / 16;  // 48 uint4 per block slice of conv state
-constexpr int kXU4 = kDim * 2 / 16;                  // 16 uint4 per block slice of qkv
+constexpr int kDim = 128;                      // key = value head dim
+constexpr int kWidth = 4;                      // conv taps
+constexpr int kStages = 3;                     // state tiles in flight per CTA
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;  // 256 math threads
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
+constexpr int kRowsPerWarp = kDim / kConsumerWarps;  // 16 key rows per consumer warp
+constexpr uint32_t kTileBytes = kDim * kDim * 4;           // 64 KiB fp32 state tile
+constexpr uint32_t kCsSliceBytes = kDim * (kWidth - 1) * 2;  // 768 B conv state per block
+constexpr uint32_t kXSliceBytes = kDim * 2;                  // 256 B qkv per block
+constexpr int kCsU4 = kCsSliceBytes / 16;                    // 48
+constexpr uint64_t kWaitLimitNs = 2000000000ull;             // bounded waits: 2 s
 
 struct Params {
   const uint16_t* qkv;
@@ -46,8 +53,27 @@ struct Params {
   uint16_t* out;
   int64_t out_stride;
   int N, H, num_slots;
+  int total_units;  // N * H
   float eps, q_scale;
   int32_t* err;
+};
+
+// Dynamic shared memory of one CTA (about 214 KB): the staged tiles and the
+// per-unit inputs for kStages units, plus the consumers' scratch.
+struct __align__(128) Smem {
+  float tile[kStages][kDim * kDim];
+  uint16_t cs[kStages][3][kDim * (kWidth - 1)];
+  uint16_t x[kStages][3][kDim];
+  float g[kStages][kDim];
+  uint16_t gate[kStages][kDim];
+  float q[kDim], k[kDim], v[kDim], alpha[kDim];
+  float red[2][kConsumerWarps][kDim];
+  float delta[kDim];
+  float sum[4][4];
+  int info[kStages][4];           // slot, n, h of the unit in each stage
+  unsigned long long full[kStages];
+  unsigned long long done[kStages];
+  volatile int abort;
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
@@ -64,176 +90,390 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One CTA per (row n, head h).  Thread (warp w, lane l) owns value columns
-// 4l..4l+3 of key rows 16w..16w+15: 64 fp32 of the tile, loaded with
-// streaming 128-bit loads before anything else (the whole-state prefetch of
-// P1 实现拆解 item 1) and kept in registers until the write.
+// ---- PTX wrappers: mbarrier, bulk async copies (TMA engine), barriers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Shared -> global bulk copy tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+               "r"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier 1 among the consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// Consumer-wide OR of a predicate (also a barrier).
+__device__ __forceinline__ int consumer_any(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 2, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "n"(kConsumers)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ void flag_error(const Params& p, int bits) {
+  if (p.err) atomicOr(p.err, bits);
+}
+
+// Persistent kernel: one CTA per SM walks units u = blockIdx.x + k*gridDim.x
+// (unit u = row u / H, head u % H).  Warp 8 is the producer: it reads each
+// unit's slot, streams the 64 KiB state tile and the unit's small inputs
+// into a stage of the shared-memory ring with bulk copies, and streams the
+// updated tile back out once the consumers release it.  Warps 0-7 compute.
+// Two tiles are in flight per SM while the consumers work on a third.
 template <bool kOutNorm, bool kUpdateConv>
-__global__ void __launch_bounds__(kThreads, 2) kda_decode_tile_kernel(const Params p) {
-  __shared__ __align__(16) uint16_t s_cs[3][kDim * (kWidth - 1)];  // old conv state, q|k|v
-  __shared__ __align__(16) uint16_t s_x[3][kDim];                   // this token's q|k|v
-  __shared__ __align__(16) float s_q[kDim], s_k[kDim], s_v[kDim], s_alpha[kDim];
-  __shared__ __align__(16) float s_red[2][kWarps][kDim];
-  __shared__ __align__(16) float s_delta[kDim];
-  __shared__ float s_sum[4][4];
-
+__global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.x / p.H;
-  const int h = blockIdx.x - n * p.H;
+  const int G = gridDim.x;
   const int64_t D = static_cast<int64_t>(p.H) * kDim;
-  uint16_t* out_row = p.out + n * p.out_stride + static_cast<int64_t>(h) * kDim;
 
-  // Padding rows (slot <= 0) write zeros and touch no state (P1 实现拆解
-  // item 1; kernel excerpt in 关键源码片段).  The slot is uniform over the
-  // CTA, so the early return keeps every later barrier paired.
-  const int slot = __ldg(p.slot_idx + n);
-  if (slot <= 0 || slot >= p.num_slots) {
-    if (slot >= p.num_slots && tid == 0 && p.err) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
-    if (tid < kDim * 2 / 16) reinterpret_cast<uint4*>(out_row)[tid] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&S.full[s]), 1);
+      mbar_init(smem_addr(&S.done[s]), kConsumerWarps);
+    }
+    S.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint64_t policy = l2_evict_first_policy();
+    const uint32_t in_bytes = kTileBytes + 3 * kCsSliceBytes + 3 * kXSliceBytes + kDim * 4 +
+                              (kOutNorm ? kXSliceBytes : 0);
+    int it = 0;
+    int next_slot = 0;
+    int unit = blockIdx.x;
+    if (unit < p.total_units) next_slot = __ldg(p.slot_idx + unit / p.H);
+    for (; unit < p.total_units; unit += G, ++it) {
+      const int stage = it % kStages;
+      const int n = unit / p.H, h = unit - n * p.H;
+      const int slot = next_slot;
+      if (unit + G < p.total_units) next_slot = __ldg(p.slot_idx + (unit + G) / p.H);
+      if (it >= kStages) {
+        // Stage reuse: the consumers must have released the previous unit
+        // in this stage; write its tile back, and let the copy engine finish
+        // reading it before the stage is refilled.
+        if (!mbar_wait_bounded(smem_addr(&S.done[stage]), ((it / kStages) - 1) & 1)) {
+          flag_error(p, KDA_DEVERR_TIMEOUT);
+          S.abort = 1;
+          break;
+        }
+        const int* prev = S.info[stage];
+        if (prev[0] > 0 && prev[0] < p.num_slots) {
+          float* dst = p.state + (static_cast<int64_t>(prev[0]) * p.H + prev[2]) * (kDim * kDim);
+          bulk_store(dst, smem_addr(S.tile[stage]), kTileBytes, policy);
+          bulk_commit();
+        }
+        bulk_wait_read_all();
+      }
+      S.info[stage][0] = slot;
+      S.info[stage][1] = n;
+      S.info[stage][2] = h;
+      const uint32_t full = smem_addr(&S.full[stage]);
+      if (slot > 0 && slot < p.num_slots) {
+        mbar_arrive_expect_tx(full, in_bytes);
+        bulk_load(smem_addr(S.tile[stage]),
+                  p.state + (static_cast<int64_t>(slot) * p.H + h) * (kDim * kDim), kTileBytes, full, policy);
+        for (int c = 0; c < 3; ++c) {
+          bulk_load(smem_addr(S.cs[stage][c]),
+                    p.conv_state +
+                        (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1),
+                    kCsSliceBytes, full, policy);
+          bulk_load(smem_addr(S.x[stage][c]), p.qkv + n * p.qkv_stride + c * D + static_cast<int64_t>(h) * kDim,
+                    kXSliceBytes, full, policy);
+        }
+        bulk_load(smem_addr(S.g[stage]), p.g + (static_cast<int64_t>(n) * p.H + h) * kDim, kDim * 4, full, policy);
+        if (kOutNorm)
+          bulk_load(smem_addr(S.gate[stage]), p.gate + n * p.gate_stride + static_cast<int64_t>(h) * kDim,
+                    kXSliceBytes, full, policy);
+      } else {
+        mbar_arrive(full);  // padding or out-of-range row: nothing to stream
+      }
+    }
+    // Drain: write back the units still held in the ring.
+    const int first = it > kStages ? it - kStages : 0;
+    for (int j = first; j < it && !S.abort; ++j) {
+      const int stage = j % kStages;
+      if (!mbar_wait_bounded(smem_addr(&S.done[stage]), (j / kStages) & 1)) {
+        flag_error(p, KDA_DEVERR_TIMEOUT);
+        break;
+      }
+      const int* prev = S.info[stage];
+      if (prev[0] > 0 && prev[0] < p.num_slots) {
+        float* dst = p.state + (static_cast<int64_t>(prev[0]) * p.H + prev[2]) * (kDim * kDim);
+        bulk_store(dst, smem_addr(S.tile[stage]), kTileBytes, policy);
+        bulk_commit();
+      }
+    }
+    // Before the CTA's shared memory goes away: every load this thread armed
+    // has landed (normally long since) and every store has completed.
+    for (int j = it > kStages ? it - kStages : 0; j < it; ++j) {
+      const int stage = j % kStages;
+      if (!mbar_wait_bounded(smem_addr(&S.full[stage]), (j / kStages) & 1)) flag_error(p, KDA_DEVERR_TIMEOUT);
+    }
+    bulk_wait_all();
     return;
   }
 
-  // 1. Stream the state tile in (evict-first: it is read exactly once).
-  float* tile = p.state + (static_cast<int64_t>(slot) * p.H + h) * (kDim * kDim);
-  const float4* tile4 = reinterpret_cast<const float4*>(tile);
-  float4 a[kRowsPerWarp];
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) a[r] = __ldcs(tile4 + (warp * kRowsPerWarp + r) * 32 + lane);
-
-  // 2. Conv inputs: the three 768-byte conv-state slices and 256-byte qkv slices.
-  if (tid < 3 * kCsU4) {
-    const int c = tid / kCsU4, e = tid - c * kCsU4;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.conv_state + (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1));
-    reinterpret_cast<uint4*>(s_cs[c])[e] = __ldg(src + e);
-  } else if (tid < 3 * kCsU4 + 3 * kXU4) {
-    const int t = tid - 3 * kCsU4, c = t / kXU4, e = t - c * kXU4;
-    const uint4* src = reinterpret_cast<const uint4*>(p.qkv + n * p.qkv_stride + c * D +
-                                                      static_cast<int64_t>(h) * kDim);
-    reinterpret_cast<uint4*>(s_x[c])[e] = __ldg(src + e);
-  }
-  __syncthreads();
-
-  // Conv-state advance: each channel's window drops its oldest tap and takes
-  // the new input -- a pure move of bf16 bit patterns.
-  if (kUpdateConv && tid < 3 * kCsU4) {
-    const int c = tid / kCsU4, e = tid - c * kCsU4;
-    uint16_t v[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int pos = e * 8 + t, j = pos / 3, k = pos - 3 * j;
-      v[t] = (k < kWidth - 2) ? s_cs[c][3 * j + k + 1] : s_x[c][j];
-    }
-    uint4 w;
-    w.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-    w.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
-    w.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
-    w.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
-    uint4* dst = reinterpret_cast<uint4*>(
-        p.conv_state + (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1));
-    dst[e] = w;
-  }
-
-  // Conv (4 taps, width-major fp32 weights) + SiLU for the 384 channels, and
-  // the per-key-channel decay alpha = exp(g).
-  for (int idx = tid; idx < 4 * kDim; idx += kThreads) {
-    if (idx < 3 * kDim) {
-      const int c = idx >> 7, j = idx & (kDim - 1);
-      const int64_t ch = c * D + static_cast<int64_t>(h) * kDim + j;
-      const float* w = p.conv_w + c * kWidth * D + static_cast<int64_t>(h) * kDim + j;
-      float y = p.conv_b ? __ldg(p.conv_b + ch) : 0.0f;
-      y = fmaf(__ldg(w + 0 * D), bf16_to_f32(s_cs[c][3 * j + 0]), y);
-      y = fmaf(__ldg(w + 1 * D), bf16_to_f32(s_cs[c][3 * j + 1]), y);
-      y = fmaf(__ldg(w + 2 * D), bf16_to_f32(s_cs[c][3 * j + 2]), y);
-      y = fmaf(__ldg(w + 3 * D), bf16_to_f32(s_x[c][j]), y);
-      const float act = y / (1.0f + expf(-y));
-      (c == 0 ? s_q : c == 1 ? s_k : s_v)[j] = act;
-    } else {
-      const int i = idx - 3 * kDim;
-      s_alpha[i] = expf(__ldg(p.g + (static_cast<int64_t>(n) * p.H + h) * kDim + i));
-    }
-  }
-  __syncthreads();
-
-  // |q|^2, |k|^2 and q.k in one pass (three block sums).
-  if (tid < kDim) {
-    const float q = s_q[tid], k = s_k[tid];
-    const float sq = warp_sum(q * q), sk = warp_sum(k * k), sqk = warp_sum(q * k);
-    if (lane == 0) {
-      s_sum[warp][0] = sq;
-      s_sum[warp][1] = sk;
-      s_sum[warp][2] = sqk;
-    }
-  }
-  __syncthreads();
-  const float ssq = (s_sum[0][0] + s_sum[1][0]) + (s_sum[2][0] + s_sum[3][0]);
-  const float ssk = (s_sum[0][1] + s_sum[1][1]) + (s_sum[2][1] + s_sum[3][1]);
-  const float sqk = (s_sum[0][2] + s_sum[1][2]) + (s_sum[2][2] + s_sum[3][2]);
+  // -------------------------------------------------------------- consumers
   const float scale = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
-  const float rq = scale / sqrtf(ssq + 1e-6f);
-  const float rk = 1.0f / sqrtf(ssk + 1e-6f);
-  const float qk = sqk * rq * rk;  // q^ . k^
+  const float nw = (kOutNorm && tid < kDim) ? __ldg(p.norm_w + tid) : 0.0f;
+  int it = 0;
+  for (int unit = blockIdx.x; unit < p.total_units; unit += G, ++it) {
+    const int stage = it % kStages;
+    const int n = unit / p.H, h = unit - n * p.H;
 
-  // 3. Decay the tile in registers and form the partial column sums
-  //    u = (Diag(alpha) S)^T k^ and w = (Diag(alpha) S)^T q^ over this warp's rows.
-  float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
+    // Per-unit inputs that do not depend on the slot: read while the tile streams.
+    float wq[kWidth], wv[kWidth];
+    float bq = 0.0f, bv = 0.0f;
+    {
+      const int c = tid >> 7, j = tid & (kDim - 1);  // channel tid: q (tid<128) or k
+      const float* w = p.conv_w + c * kWidth * D + static_cast<int64_t>(h) * kDim + j;
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int i = warp * kRowsPerWarp + r;
-    const float al = s_alpha[i], kh = s_k[i] * rk, qh = s_q[i] * rq;
-    a[r].x *= al; a[r].y *= al; a[r].z *= al; a[r].w *= al;
-    u.x = fmaf(kh, a[r].x, u.x); u.y = fmaf(kh, a[r].y, u.y);
-    u.z = fmaf(kh, a[r].z, u.z); u.w = fmaf(kh, a[r].w, u.w);
-    w.x = fmaf(qh, a[r].x, w.x); w.y = fmaf(qh, a[r].y, w.y);
-    w.z = fmaf(qh, a[r].z, w.z); w.w = fmaf(qh, a[r].w, w.w);
-  }
-  reinterpret_cast<float4*>(s_red[0][warp])[lane] = u;
-  reinterpret_cast<float4*>(s_red[1][warp])[lane] = w;
-  __syncthreads();
-
-  // 4. delta_j = beta (v_j - u_j); the readout of the updated state
-  //    o = S'^T q^ = w + (q^ . k^) delta needs no second pass over S'.
-  float o = 0.0f;
-  if (tid < kDim) {
-    float uj = 0.0f, wj = 0.0f;
+      for (int t = 0; t < kWidth; ++t) wq[t] = __ldg(w + t * D);
+      if (p.conv_b) bq = __ldg(p.conv_b + c * D + static_cast<int64_t>(h) * kDim + j);
+      if (tid < kDim) {  // second channel: v block
+        const float* w2 = p.conv_w + 2 * kWidth * D + static_cast<int64_t>(h) * kDim + j;
 #pragma unroll
-    for (int r = 0; r < kWarps; ++r) {
-      uj += s_red[0][r][tid];
-      wj += s_red[1][r][tid];
+        for (int t = 0; t < kWidth; ++t) wv[t] = __ldg(w2 + t * D);
+        if (p.conv_b) bv = __ldg(p.conv_b + 2 * D + static_cast<int64_t>(h) * kDim + j);
+      }
     }
-    const float beta = bf16_to_f32(__ldg(p.beta + static_cast<int64_t>(n) * p.H + h));
-    const float dj = beta * (s_v[tid] - uj);
-    s_delta[tid] = dj;
-    o = fmaf(qk, dj, wj);
-    if (kOutNorm) {
-      const float ss = warp_sum(o * o);
-      if (lane == 0) s_sum[warp][3] = ss;
-    }
-  }
-  __syncthreads();
+    const float beta = (tid < kDim) ? bf16_to_f32(__ldg(p.beta + static_cast<int64_t>(n) * p.H + h)) : 0.0f;
 
-  // 5. S' = Diag(alpha) S + k^ delta^T, streamed out (evict-first).
-  const float4 d = reinterpret_cast<const float4*>(s_delta)[lane];
-  float4* tile4w = reinterpret_cast<float4*>(tile);
+    const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), (it / kStages) & 1);
+    // All consumers agree (this is also the barrier that guards the scratch).
+    if (consumer_any(!ok || S.abort)) {
+      if (tid == 0) {
+        flag_error(p, KDA_DEVERR_TIMEOUT);
+        S.abort = 1;
+      }
+      break;
+    }
+    const int slot = S.info[stage][0];
+    uint16_t* out_row = p.out + n * p.out_stride + static_cast<int64_t>(h) * kDim;
+
+    // Padding rows (slot <= 0) write zeros and touch no state (P1 实现拆解
+    // item 1; kernel excerpt in 关键源码片段).
+    if (slot <= 0 || slot >= p.num_slots) {
+      if (tid < kDim * 2 / 16) reinterpret_cast<uint4*>(out_row)[tid] = make_uint4(0, 0, 0, 0);
+      if (slot >= p.num_slots && tid == 0) flag_error(p, KDA_DEVERR_SLOT_RANGE);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&S.done[stage]));
+      continue;
+    }
+
+    // Conv-state advance: drop the oldest tap, append the new input (a pure
+    // move of bf16 bit patterns).
+    if (kUpdateConv && tid < 3 * kCsU4) {
+      const int c = tid / kCsU4, e = tid - c * kCsU4;
+      uint16_t v8[8];
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int i = warp * kRowsPerWarp + r;
-    const float kh = s_k[i] * rk;
-    a[r].x = fmaf(kh, d.x, a[r].x); a[r].y = fmaf(kh, d.y, a[r].y);
-    a[r].z = fmaf(kh, d.z, a[r].z); a[r].w = fmaf(kh, d.w, a[r].w);
-    __stcs(tile4w + i * 32 + lane, a[r]);
-  }
-
-  // 6. Gated RMSNorm epilogue (or the raw readout) to bf16.
-  if (tid < kDim) {
-    float y = o;
-    if (kOutNorm) {
-      const float ss = (s_sum[0][3] + s_sum[1][3]) + (s_sum[2][3] + s_sum[3][3]);
-      const float rr = 1.0f / sqrtf(ss * (1.0f / kDim) + p.eps);
-      const float gt = bf16_to_f32(__ldg(p.gate + n * p.gate_stride + static_cast<int64_t>(h) * kDim + tid));
-      y = o * rr * __ldg(p.norm_w + tid) * (1.0f / (1.0f + expf(-gt)));
+      for (int t = 0; t < 8; ++t) {
+        const int pos = e * 8 + t, j = pos / 3, k = pos - 3 * j;
+        v8[t] = (k < kWidth - 2) ? S.cs[stage][c][3 * j + k + 1] : S.x[stage][c][j];
+      }
+      uint4 w4;
+      w4.x = v8[0] | (static_cast<uint32_t>(v8[1]) << 16);
+      w4.y = v8[2] | (static_cast<uint32_t>(v8[3]) << 16);
+      w4.z = v8[4] | (static_cast<uint32_t>(v8[5]) << 16);
+      w4.w = v8[6] | (static_cast<uint32_t>(v8[7]) << 16);
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.conv_state + (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1));
+      dst[e] = w4;
     }
-    out_row[tid] = f32_to_bf16(y);
+
+    // Conv (4 taps) + SiLU on the 384 q|k|v channels; decay alpha = exp(g).
+    {
+      const int c = tid >> 7, j = tid & (kDim - 1);
+      const uint16_t* cs = S.cs[stage][c] + 3 * j;
+      float y = bq;
+      y = fmaf(wq[0], bf16_to_f32(cs[0]), y);
+      y = fmaf(wq[1], bf16_to_f32(cs[1]), y);
+      y = fmaf(wq[2], bf16_to_f32(cs[2]), y);
+      y = fmaf(wq[3], bf16_to_f32(S.x[stage][c][j]), y);
+      (c == 0 ? S.q : S.k)[j] = y / (1.0f + expf(-y));
+      if (tid < kDim) {
+        const uint16_t* csv = S.cs[stage][2] + 3 * j;
+        float yv = bv;
+        yv = fmaf(wv[0], bf16_to_f32(csv[0]), yv);
+        yv = fmaf(wv[1], bf16_to_f32(csv[1]), yv);
+        yv = fmaf(wv[2], bf16_to_f32(csv[2]), yv);
+        yv = fmaf(wv[3], bf16_to_f32(S.x[stage][2][j]), yv);
+        S.v[j] = yv / (1.0f + expf(-yv));
+      } else {
+        S.alpha[j] = expf(S.g[stage][j]);
+      }
+    }
+    const float gate_j = (kOutNorm && tid < kDim) ? bf16_to_f32(S.gate[stage][tid]) : 0.0f;
+    consumer_sync();
+
+    // |q|^2, |k|^2, q.k in one pass.
+    if (tid < kDim) {
+      const float qv = S.q[tid], kv = S.k[tid];
+      const float sq = warp_sum(qv * qv), sk = warp_sum(kv * kv), sqk = warp_sum(qv * kv);
+      if (lane == 0) {
+        S.sum[warp][0] = sq;
+        S.sum[warp][1] = sk;
+        S.sum[warp][2] = sqk;
+      }
+    }
+    consumer_sync();
+    const float ssq = (S.sum[0][0] + S.sum[1][0]) + (S.sum[2][0] + S.sum[3][0]);
+    const float ssk = (S.sum[0][1] + S.sum[1][1]) + (S.sum[2][1] + S.sum[3][1]);
+    const float sqk = (S.sum[0][2] + S.sum[1][2]) + (S.sum[2][2] + S.sum[3][2]);
+    const float rq = scale / sqrtf(ssq + 1e-6f);
+    const float rk = 1.0f / sqrtf(ssk + 1e-6f);
+    const float qk = sqk * rq * rk;  // q^ . k^
+
+    // Decay the staged tile and form partial u = A^T k^, w = A^T q^ over this
+    // warp's 16 key rows (A = Diag(alpha) S, kept in registers).
+    const float4* tile4 = reinterpret_cast<const float4*>(S.tile[stage]);
+    float4 a[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int i = warp * kRowsPerWarp + r;
+      const float al = S.alpha[i], kh = S.k[i] * rk, qh = S.q[i] * rq;
+      a[r].x *= al; a[r].y *= al; a[r].z *= al; a[r].w *= al;
+      u.x = fmaf(kh, a[r].x, u.x); u.y = fmaf(kh, a[r].y, u.y);
+      u.z = fmaf(kh, a[r].z, u.z); u.w = fmaf(kh, a[r].w, u.w);
+      w.x = fmaf(qh, a[r].x, w.x); w.y = fmaf(qh, a[r].y, w.y);
+      w.z = fmaf(qh, a[r].z, w.z); w.w = fmaf(qh, a[r].w, w.w);
+    }
+    reinterpret_cast<float4*>(S.red[0][warp])[lane] = u;
+    reinterpret_cast<float4*>(S.red[1][warp])[lane] = w;
+    consumer_sync();
+
+    // delta_j = beta (v_j - u_j); readout of the updated state
+    // o = S'^T q^ = w + (q^ . k^) delta, with no second pass over S'.
+    float o = 0.0f;
+    if (tid < kDim) {
+      float uj = 0.0f, wj = 0.0f;
+#pragma unroll
+      for (int r = 0; r < kConsumerWarps; ++r) {
+        uj += S.red[0][r][tid];
+        wj += S.red[1][r][tid];
+      }
+      const float dj = beta * (S.v[tid] - uj);
+      S.delta[tid] = dj;
+      o = fmaf(qk, dj, wj);
+      if (kOutNorm) {
+        const float ss = warp_sum(o * o);
+        if (lane == 0) S.sum[warp][3] = ss;
+      }
+    }
+    consumer_sync();
+
+    // S' = A + k^ delta^T written back into the stage, then handed to the
+    // producer for the bulk store.
+    const float4 d = reinterpret_cast<const float4*>(S.delta)[lane];
+    float4* tile4w = reinterpret_cast<float4*>(S.tile[stage]);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int i = warp * kRowsPerWarp + r;
+      const float kh = S.k[i] * rk;
+      a[r].x = fmaf(kh, d.x, a[r].x); a[r].y = fmaf(kh, d.y, a[r].y);
+      a[r].z = fmaf(kh, d.z, a[r].z); a[r].w = fmaf(kh, d.w, a[r].w);
+      tile4w[i * 32 + lane] = a[r];
+    }
+    fence_proxy_async_smem();  // generic-proxy writes before the async-proxy store
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&S.done[stage]));
+
+    // Gated RMSNorm epilogue (or the raw readout) to bf16.
+    if (tid < kDim) {
+      float y = o;
+      if (kOutNorm) {
+        const float ss = (S.sum[0][3] + S.sum[1][3]) + (S.sum[2][3] + S.sum[3][3]);
+        const float rr = 1.0f / sqrtf(ss * (1.0f / kDim) + p.eps);
+        y = o * rr * nw * (1.0f / (1.0f + expf(-gate_j)));
+      }
+      out_row[tid] = f32_to_bf16(y);
+    }
   }
 }
 
@@ -249,10 +489,46 @@ int fail(int code, const char* fmt, ...) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+struct DeviceInfo {
+  int sms = 0;
+  bool attrs_set = false;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
 template <bool kOutNorm, bool kUpdateConv>
-cudaError_t launch(const Params& p, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>(p.N) * static_cast<unsigned>(p.H);
-  kda_decode_tile_kernel<kOutNorm, kUpdateConv><<<grid, kThreads, 0, stream>>>(p);
+cudaError_t set_attrs() {
+  return cudaFuncSetAttribute(kda_decode_persistent_kernel<kOutNorm, kUpdateConv>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(Smem)));
+}
+
+// Once per device: SM count and the large dynamic shared-memory opt-in for
+// every kernel variant.  Not a stream operation, but it should run before
+// any stream capture (the first call on a device does it).
+cudaError_t device_setup(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.attrs_set) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = set_attrs<true, true>()) != cudaSuccess) return e;
+    if ((e = set_attrs<true, false>()) != cudaSuccess) return e;
+    if ((e = set_attrs<false, true>()) != cudaSuccess) return e;
+    if ((e = set_attrs<false, false>()) != cudaSuccess) return e;
+    d.attrs_set = true;
+  }
+  *sms = d.sms;
+  return cudaSuccess;
+}
+
+template <bool kOutNorm, bool kUpdateConv>
+cudaError_t launch(const Params& p, int sms, cudaStream_t stream) {
+  const int grid = p.total_units < sms ? p.total_units : sms;
+  kda_decode_persistent_kernel<kOutNorm, kUpdateConv><<<grid, kThreads, sizeof(Smem), stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -294,7 +570,7 @@ extern "C" int kda_decode(const KdaDecodeArgs* a, void* stream) {
   if (norm && (!a->gate || !a->norm_weight))
     return fail(KDA_ERR_NULLPTR, "KDA_OUT_NORM needs gate and norm_weight");
   const int64_t D = static_cast<int64_t>(a->H) * KDA_HEAD_DIM;
-  if (static_cast<int64_t>(a->N) * a->H > 0x7fffffffLL)
+  if (static_cast<int64_t>(a->N) * a->H > (1LL << 30))
     return fail(KDA_ERR_SHAPE, "N*H = %lld exceeds the grid limit", static_cast<long long>(a->N) * a->H);
   if (a->qkv_row_stride < 3 * D || a->out_row_stride < D || (norm && a->gate_row_stride < D))
     return fail(KDA_ERR_SHAPE, "row stride below the row width");
@@ -327,11 +603,15 @@ extern "C" int kda_decode(const KdaDecodeArgs* a, void* stream) {
   p.eps = a->eps;
   p.q_scale = a->q_scale;
   p.err = a->err_flag;
+  p.total_units = a->N * a->H;
 
+  int sms = 0;
+  cudaError_t es = device_setup(&sms);
+  if (es != cudaSuccess) return fail(KDA_ERR_LAUNCH, "device set-up: %s", cudaGetErrorString(es));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool conv = (a->flags & KDA_UPDATE_CONV_STATE) != 0;
-  cudaError_t e = norm ? (conv ? launch<true, true>(p, s) : launch<true, false>(p, s))
-                       : (conv ? launch<false, true>(p, s) : launch<false, false>(p, s));
+  cudaError_t e = norm ? (conv ? launch<true, true>(p, sms, s) : launch<true, false>(p, sms, s))
+                       : (conv ? launch<false, true>(p, sms, s) : launch<false, false>(p, sms, s));
   if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "%s", cudaGetErrorString(e));
   return KDA_OK;
 }
