@@ -43,6 +43,13 @@ extern "C" {
 /* flags */
 #define KDA_OUT_NORM          1u /* apply the gated RMSNorm epilogue */
 #define KDA_UPDATE_CONV_STATE 2u /* write the advanced conv state back */
+/* The caller guarantees that the kernel enqueued immediately before this call
+ * on the stream writes none of slot_idx, state or conv_state (for example the
+ * previous layer's decode, with its own pools).  The call may then start
+ * streaming state and conv state while that kernel is still running; all
+ * per-token inputs (qkv, g, beta, gate) are still read only after it has
+ * completed.  Without this flag nothing is read before it completes. */
+#define KDA_EARLY_PREFETCH    4u
 
 /* return codes of kda_decode */
 #define KDA_OK            0
@@ -95,19 +102,35 @@ typedef struct KdaDecodeArgs {
   int64_t out_row_stride;      /* elements, >= D */
   float eps;                   /* RMSNorm epsilon (e.g. 1e-6) */
   float q_scale;               /* 0 => 1/sqrt(128) */
-  uint32_t flags;              /* KDA_OUT_NORM | KDA_UPDATE_CONV_STATE */
+  uint32_t flags;              /* KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH */
   int32_t* err_flag;           /* device int32 or NULL; KDA_DEVERR_* bits are OR-ed in */
 } KdaDecodeArgs;
 
 /*
  * Enqueue one fused decode step on `stream` (a cudaStream_t; NULL = the
- * legacy default stream).  Returns KDA_OK or a negative KDA_ERR_* code; on an
+ * legacy default stream).  The launch is a programmatic dependent launch:
+ * it may become resident while the previous kernel on the stream drains and
+ * waits for that kernel's completion before reading anything it could have
+ * written (see KDA_EARLY_PREFETCH for the one exception the caller can allow).  Returns KDA_OK or a negative KDA_ERR_* code; on an
  * argument error nothing is launched.  Asynchronous: results are visible
  * after the stream reaches this point.  Rows with slot >= num_slots are
  * treated as padding and raise KDA_DEVERR_SLOT_RANGE in *err_flag.
  * Duplicate positive slots within one call give undefined state.
  */
 int kda_decode(const KdaDecodeArgs* args, void* stream);
+
+/*
+ * Test hook for the bounded-wait path (no counterpart on the page; it exists
+ * so that the failure handling can be exercised without faulting a GPU).
+ * Same as kda_decode, except that every internal pipeline wait gives up after
+ * `wait_limit_ns` (> 0) instead of 2 s, and the inputs of unit
+ * `withhold_unit` (= row * H + head; -1 for none) are never signalled as
+ * loaded, so the waits that depend on them run out.  The kernel then sets
+ * KDA_DEVERR_TIMEOUT in *err_flag, stops early and returns; the context stays
+ * usable.  Results of such a launch are incomplete.
+ */
+int kda_decode_wait_test(const KdaDecodeArgs* args, void* stream, uint64_t wait_limit_ns,
+                         int32_t withhold_unit);
 
 /* Static text for a KDA_* return code. */
 const char* kda_status_string(int status);

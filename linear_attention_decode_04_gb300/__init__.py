@@ -6,6 +6,7 @@ into that call.  The library is loaded on first use and a missing or stale
 build raises instead of falling back to anything else.
 """
 from .binding import (  # noqa: F401
+    KDA_EARLY_PREFETCH,
     KDA_OUT_NORM,
     KDA_UPDATE_CONV_STATE,
     KdaDecodeCall,

@@ -17,7 +17,9 @@ HEAD_DIM = 128
 CONV_WIDTH = 4
 KDA_OUT_NORM = 1
 KDA_UPDATE_CONV_STATE = 2
+KDA_EARLY_PREFETCH = 4
 KDA_DEVERR_SLOT_RANGE = 1
+KDA_DEVERR_TIMEOUT = 2
 ABI_VERSION = 1
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +72,9 @@ def load_library() -> ctypes.CDLL:
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_last_error.argtypes = []
             L.kda_last_error.restype = ctypes.c_char_p
+            L.kda_decode_wait_test.argtypes = [ctypes.POINTER(KdaDecodeArgs), ctypes.c_void_p,
+                                               ctypes.c_uint64, ctypes.c_int32]
+            L.kda_decode_wait_test.restype = ctypes.c_int
             L.kda_abi_version.argtypes = []
             L.kda_abi_version.restype = ctypes.c_int
             if L.kda_abi_version() != ABI_VERSION:
@@ -115,7 +120,7 @@ class KdaDecodeCall:
     def __init__(self, qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                  gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
-                 err_flag=None):
+                 err_flag=None, early_prefetch: bool = False):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -150,7 +155,8 @@ class KdaDecodeCall:
         _dense(slot_idx, "slot_idx")
         _check(out, "out", torch.bfloat16, dev)
         out_stride = _rows(out, "out", N, D)
-        flags = (KDA_OUT_NORM if out_norm else 0) | (KDA_UPDATE_CONV_STATE if update_conv_state else 0)
+        flags = ((KDA_OUT_NORM if out_norm else 0) | (KDA_UPDATE_CONV_STATE if update_conv_state else 0)
+                 | (KDA_EARLY_PREFETCH if early_prefetch else 0))
         gate_ptr = nw_ptr = None
         gate_stride = 0
         if out_norm:
@@ -195,15 +201,28 @@ class KdaDecodeCall:
         if rc != 0:
             raise KdaError(rc, f"{kda_status_string(rc)}: {self._lib.kda_last_error().decode()}")
 
+    def wait_test(self, wait_limit_ns: int, withhold_unit: int,
+                  stream: torch.cuda.Stream | None = None) -> None:
+        """``kda_decode_wait_test``: exercise the bounded-wait failure path."""
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        rc = self._lib.kda_decode_wait_test(self._argp, ctypes.c_void_p(stream.cuda_stream),
+                                            int(wait_limit_ns), int(withhold_unit))
+        if rc != 0:
+            raise KdaError(rc, f"{kda_status_string(rc)}: {self._lib.kda_last_error().decode()}")
+
 
 def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
-               err_flag=None, stream: torch.cuda.Stream | None = None) -> None:
+               err_flag=None, early_prefetch: bool = False,
+               stream: torch.cuda.Stream | None = None) -> None:
     """One fused decode step (see ``include/kda_decode.h``).  ``conv_state``,
     ``state`` and ``out`` are written in place on ``stream`` (default: the
-    current stream of the state's device)."""
+    current stream of the state's device).  ``early_prefetch`` sets
+    KDA_EARLY_PREFETCH: only when the kernel enqueued just before on the
+    stream writes none of slot_idx, state and conv_state."""
     KdaDecodeCall(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate=gate,
                   norm_weight=norm_weight, conv_bias=conv_bias, eps=eps, q_scale=q_scale,
                   out_norm=out_norm, update_conv_state=update_conv_state,
-                  err_flag=err_flag)(stream)
+                  err_flag=err_flag, early_prefetch=early_prefetch)(stream)

@@ -35,7 +35,7 @@ constexpr uint32_t kTileBytes = kDim * kDim * 4;           // 64 KiB fp32 state 
 constexpr uint32_t kCsSliceBytes = kDim * (kWidth - 1) * 2;  // 768 B conv state per block
 constexpr uint32_t kXSliceBytes = kDim * 2;                  // 256 B qkv per block
 constexpr int kCsU4 = kCsSliceBytes / 16;                    // 48
-constexpr uint64_t kWaitLimitNs = 2000000000ull;             // bounded waits: 2 s
+constexpr uint64_t kWaitLimitNs = 2000000000ull;             // bounded waits: 2 s by default
 
 struct Params {
   const uint16_t* qkv;
@@ -54,6 +54,9 @@ struct Params {
   int64_t out_stride;
   int N, H, num_slots;
   int total_units;  // N * H
+  int early_prefetch;  // KDA_EARLY_PREFETCH
+  int withhold_unit;   // wait-path test: this unit's load is never signalled (-1: none)
+  uint64_t wait_limit_ns;
   float eps, q_scale;
   int32_t* err;
 };
@@ -126,12 +129,12 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -186,6 +189,14 @@ __device__ __forceinline__ int consumer_any(int pred) {
   return r;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream be
+// scheduled now, and wait for the previous one to complete (with its memory
+// visible) before touching anything it may have written.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void flag_error(const Params& p, int bits) {
   if (p.err) atomicOr(p.err, bits);
 }
@@ -214,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     fence_proxy_async_smem();
   }
   __syncthreads();
+  griddep_launch_dependents();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -221,10 +233,60 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     const uint64_t policy = l2_evict_first_policy();
     const uint32_t in_bytes = kTileBytes + 3 * kCsSliceBytes + 3 * kXSliceBytes + kDim * 4 +
                               (kOutNorm ? kXSliceBytes : 0);
+    // Slot-indexed inputs of a unit: its state tile and conv-state slices.
+    auto load_slot_parts = [&](int stage, int h, int slot) {
+      const uint32_t full = smem_addr(&S.full[stage]);
+      bulk_load(smem_addr(S.tile[stage]), p.state + (static_cast<int64_t>(slot) * p.H + h) * (kDim * kDim),
+                kTileBytes, full, policy);
+      for (int c = 0; c < 3; ++c)
+        bulk_load(smem_addr(S.cs[stage][c]),
+                  p.conv_state +
+                      (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1),
+                  kCsSliceBytes, full, policy);
+    };
+    // Per-token inputs of a unit: qkv slices, g row, gate row.
+    auto load_token_parts = [&](int stage, int n, int h) {
+      const uint32_t full = smem_addr(&S.full[stage]);
+      for (int c = 0; c < 3; ++c)
+        bulk_load(smem_addr(S.x[stage][c]), p.qkv + n * p.qkv_stride + c * D + static_cast<int64_t>(h) * kDim,
+                  kXSliceBytes, full, policy);
+      bulk_load(smem_addr(S.g[stage]), p.g + (static_cast<int64_t>(n) * p.H + h) * kDim, kDim * 4, full, policy);
+      if (kOutNorm)
+        bulk_load(smem_addr(S.gate[stage]), p.gate + n * p.gate_stride + static_cast<int64_t>(h) * kDim,
+                  kXSliceBytes, full, policy);
+    };
+
     int it = 0;
-    int next_slot = 0;
     int unit = blockIdx.x;
-    if (unit < p.total_units) next_slot = __ldg(p.slot_idx + unit / p.H);
+    // With KDA_EARLY_PREFETCH the first ring's worth of state streams in
+    // before the previous kernel in the stream has finished (the caller
+    // guarantees that kernel does not write the slot indices, the state or
+    // the conv state); everything per-token waits for it.
+    if (p.early_prefetch) {
+      for (; unit < p.total_units && it < kStages; unit += G, ++it) {
+        const int n = unit / p.H, h = unit - n * p.H;
+        const int slot = __ldg(p.slot_idx + n);
+        S.info[it][0] = slot;
+        S.info[it][1] = n;
+        S.info[it][2] = h;
+        S.info[it][3] = (unit == p.withhold_unit);
+        if (slot > 0 && slot < p.num_slots && !S.info[it][3]) {
+          mbar_arrive_expect_tx(smem_addr(&S.full[it]), in_bytes);
+          load_slot_parts(it, h, slot);
+        }
+      }
+    }
+    griddep_wait();
+    for (int j = 0; j < it; ++j) {
+      const int slot = S.info[j][0];
+      if (S.info[j][3]) continue;  // withheld (wait-path test)
+      if (slot > 0 && slot < p.num_slots)
+        load_token_parts(j, S.info[j][1], S.info[j][2]);
+      else
+        mbar_arrive(smem_addr(&S.full[j]));  // padding row: nothing to stream
+    }
+
+    int next_slot = (unit < p.total_units) ? __ldg(p.slot_idx + unit / p.H) : 0;
     for (; unit < p.total_units; unit += G, ++it) {
       const int stage = it % kStages;
       const int n = unit / p.H, h = unit - n * p.H;
@@ -234,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         // Stage reuse: the consumers must have released the previous unit
         // in this stage; write its tile back, and let the copy engine finish
         // reading it before the stage is refilled.
-        if (!mbar_wait_bounded(smem_addr(&S.done[stage]), ((it / kStages) - 1) & 1)) {
+        if (!mbar_wait_bounded(smem_addr(&S.done[stage]), ((it / kStages) - 1) & 1, p.wait_limit_ns)) {
           flag_error(p, KDA_DEVERR_TIMEOUT);
           S.abort = 1;
           break;
@@ -250,32 +312,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       S.info[stage][0] = slot;
       S.info[stage][1] = n;
       S.info[stage][2] = h;
-      const uint32_t full = smem_addr(&S.full[stage]);
+      S.info[stage][3] = 0;
+      if (unit == p.withhold_unit) continue;  // wait-path test: never signalled
       if (slot > 0 && slot < p.num_slots) {
-        mbar_arrive_expect_tx(full, in_bytes);
-        bulk_load(smem_addr(S.tile[stage]),
-                  p.state + (static_cast<int64_t>(slot) * p.H + h) * (kDim * kDim), kTileBytes, full, policy);
-        for (int c = 0; c < 3; ++c) {
-          bulk_load(smem_addr(S.cs[stage][c]),
-                    p.conv_state +
-                        (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1),
-                    kCsSliceBytes, full, policy);
-          bulk_load(smem_addr(S.x[stage][c]), p.qkv + n * p.qkv_stride + c * D + static_cast<int64_t>(h) * kDim,
-                    kXSliceBytes, full, policy);
-        }
-        bulk_load(smem_addr(S.g[stage]), p.g + (static_cast<int64_t>(n) * p.H + h) * kDim, kDim * 4, full, policy);
-        if (kOutNorm)
-          bulk_load(smem_addr(S.gate[stage]), p.gate + n * p.gate_stride + static_cast<int64_t>(h) * kDim,
-                    kXSliceBytes, full, policy);
+        mbar_arrive_expect_tx(smem_addr(&S.full[stage]), in_bytes);
+        load_slot_parts(stage, h, slot);
+        load_token_parts(stage, n, h);
       } else {
-        mbar_arrive(full);  // padding or out-of-range row: nothing to stream
+        mbar_arrive(smem_addr(&S.full[stage]));  // padding or out-of-range row: nothing to stream
       }
     }
     // Drain: write back the units still held in the ring.
     const int first = it > kStages ? it - kStages : 0;
     for (int j = first; j < it && !S.abort; ++j) {
       const int stage = j % kStages;
-      if (!mbar_wait_bounded(smem_addr(&S.done[stage]), (j / kStages) & 1)) {
+      if (!mbar_wait_bounded(smem_addr(&S.done[stage]), (j / kStages) & 1, p.wait_limit_ns)) {
         flag_error(p, KDA_DEVERR_TIMEOUT);
         break;
       }
@@ -290,13 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     // has landed (normally long since) and every store has completed.
     for (int j = it > kStages ? it - kStages : 0; j < it; ++j) {
       const int stage = j % kStages;
-      if (!mbar_wait_bounded(smem_addr(&S.full[stage]), (j / kStages) & 1)) flag_error(p, KDA_DEVERR_TIMEOUT);
+      if (!mbar_wait_bounded(smem_addr(&S.full[stage]), (j / kStages) & 1, p.wait_limit_ns)) flag_error(p, KDA_DEVERR_TIMEOUT);
     }
     bulk_wait_all();
     return;
   }
 
   // -------------------------------------------------------------- consumers
+  griddep_wait();
   const float scale = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
   const float nw = (kOutNorm && tid < kDim) ? __ldg(p.norm_w + tid) : 0.0f;
   int it = 0;
@@ -322,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     }
     const float beta = (tid < kDim) ? bf16_to_f32(__ldg(p.beta + static_cast<int64_t>(n) * p.H + h)) : 0.0f;
 
-    const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), (it / kStages) & 1);
+    const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), (it / kStages) & 1, p.wait_limit_ns);
     // All consumers agree (this is also the barrier that guards the scratch).
     if (consumer_any(!ok || S.abort)) {
       if (tid == 0) {
@@ -527,9 +579,21 @@ cudaError_t device_setup(int* sms) {
 
 template <bool kOutNorm, bool kUpdateConv>
 cudaError_t launch(const Params& p, int sms, cudaStream_t stream) {
-  const int grid = p.total_units < sms ? p.total_units : sms;
-  kda_decode_persistent_kernel<kOutNorm, kUpdateConv><<<grid, kThreads, sizeof(Smem), stream>>>(p);
-  return cudaGetLastError();
+  // Every launch is a programmatic dependent launch: the CTAs may become
+  // resident while the previous kernel in the stream drains, and wait for
+  // it (griddepcontrol.wait) before touching its results.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.total_units < sms ? p.total_units : sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kda_decode_persistent_kernel<kOutNorm, kUpdateConv>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -551,7 +615,22 @@ extern "C" const char* kda_status_string(int status) {
   }
 }
 
+namespace {
+int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, int32_t withhold_unit);
+}  // namespace
+
 extern "C" int kda_decode(const KdaDecodeArgs* a, void* stream) {
+  return decode_impl(a, stream, kWaitLimitNs, -1);
+}
+
+extern "C" int kda_decode_wait_test(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns,
+                                    int32_t withhold_unit) {
+  if (wait_limit_ns == 0) return fail(KDA_ERR_SHAPE, "wait_limit_ns must be > 0");
+  return decode_impl(a, stream, wait_limit_ns, withhold_unit);
+}
+
+namespace {
+int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, int32_t withhold_unit) {
   g_last_error[0] = '\0';
   // Validation touches no CUDA API and no device memory.
   if (!a) return fail(KDA_ERR_NULLPTR, "args is NULL");
@@ -561,7 +640,8 @@ extern "C" int kda_decode(const KdaDecodeArgs* a, void* stream) {
     return fail(KDA_ERR_SHAPE, "head_dim %d / conv_width %d (need 128 / 4)", a->head_dim, a->conv_width);
   if (a->N < 0 || a->H < 1 || a->num_slots < 1)
     return fail(KDA_ERR_SHAPE, "N=%d H=%d num_slots=%d", a->N, a->H, a->num_slots);
-  if (a->flags & ~(KDA_OUT_NORM | KDA_UPDATE_CONV_STATE)) return fail(KDA_ERR_FLAGS, "flags 0x%x", a->flags);
+  if (a->flags & ~(KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH))
+    return fail(KDA_ERR_FLAGS, "flags 0x%x", a->flags);
   if (a->N == 0) return KDA_OK;
   const bool norm = (a->flags & KDA_OUT_NORM) != 0;
   if (!a->qkv || !a->conv_weight || !a->conv_state || !a->state || !a->g || !a->beta || !a->slot_idx ||
@@ -604,6 +684,9 @@ extern "C" int kda_decode(const KdaDecodeArgs* a, void* stream) {
   p.q_scale = a->q_scale;
   p.err = a->err_flag;
   p.total_units = a->N * a->H;
+  p.early_prefetch = (a->flags & KDA_EARLY_PREFETCH) != 0;
+  p.withhold_unit = withhold_unit;
+  p.wait_limit_ns = wait_limit_ns;
 
   int sms = 0;
   cudaError_t es = device_setup(&sms);
@@ -615,3 +698,4 @@ extern "C" int kda_decode(const KdaDecodeArgs* a, void* stream) {
   if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "%s", cudaGetErrorString(e));
   return KDA_OK;
 }
+}  // namespace

@@ -18,4 +18,6 @@ from .kda_oracle import (  # noqa: F401
     gated_delta_update,
     readout,
     gated_rmsnorm,
+    softplus,
+    kda_gate,
 )

@@ -122,6 +122,18 @@ void kda_oracle_gated_rmsnorm(int V, const double* o, const double* w,
   for (int j = 0; j < V; ++j) y[j] = o[j] * r * w[j] * kda_oracle_sigmoid(gate[j]);
 }
 
+/* Gate activation ahead of the recurrence when the kernel fuses it (P1
+ * 实现拆解 item 1 "safe gate"; formula is the standard KDA gate, not on P1). */
+double kda_oracle_softplus(double z) {
+  /* log(1 + e^z), written so that neither branch overflows */
+  return (z > 0.0) ? z + log1p(exp(-z)) : log1p(exp(z));
+}
+
+double kda_oracle_kda_gate(double z, double A_log, double lower_bound) {
+  if (lower_bound < 0.0) return lower_bound * kda_oracle_sigmoid(exp(A_log) * z);
+  return -exp(A_log) * kda_oracle_softplus(z);
+}
+
 /* ---------------------------------------------------------------- step */
 
 /* One (row n, head h).  Returns 1 if the slot was out of range. */
@@ -187,8 +199,19 @@ static int decode_unit(const kda_oracle_problem* p, int n, int h, double* work) 
   /* 3. Gated delta rule on the slot's state. */
   float* Sg = p->state + (((int64_t)s * H + h) * K) * V;
   for (int64_t e = 0; e < (int64_t)K * V; ++e) S[e] = (double)Sg[e];
-  for (int i = 0; i < K; ++i) alpha[i] = exp((double)p->g[((int64_t)n * H + h) * K + i]);
-  const double beta = kda_oracle_bf16_to_f64(p->beta[(int64_t)n * H + h]);
+  double beta = kda_oracle_bf16_to_f64(p->beta[(int64_t)n * H + h]);
+  if (p->fused_gate) {
+    /* the gate activation replaces the pre-activated g and beta */
+    const double a_log = (double)p->A_log[h];
+    for (int i = 0; i < K; ++i) {
+      double z = (double)p->g[((int64_t)n * H + h) * K + i];
+      if (p->dt_bias) z += (double)p->dt_bias[(int64_t)h * K + i];
+      alpha[i] = exp(kda_oracle_kda_gate(z, a_log, p->lower_bound));
+    }
+    beta = kda_oracle_sigmoid(beta);
+  } else {
+    for (int i = 0; i < K; ++i) alpha[i] = exp((double)p->g[((int64_t)n * H + h) * K + i]);
+  }
   kda_oracle_gated_delta_update(K, V, S, alpha, beta, kh, vt);
 
   /* 4. Readout from the updated state. */
@@ -221,6 +244,7 @@ int kda_oracle_decode(const kda_oracle_problem* p, int num_threads) {
       !p->slot_idx || !p->out)
     return -1;
   if (p->out_norm && (!p->gate || !p->norm_weight)) return -1;
+  if (p->fused_gate && !p->A_log) return -1;
   const int64_t C = 2 * (int64_t)p->H * p->K + (int64_t)p->H * p->V;
   if (p->qkv_row_stride < C) return -1;
 

@@ -55,6 +55,16 @@
  *                                     * norm_weight[j] * sigmoid(gate[n, h*V + j])
  *              out_norm off: out_j = o_j
  *
+ *  Fused gate (fused_gate = 1; P1 实现拆解 item 1 "safe gate" template flag and
+ *  the op's raw_g / raw_beta / A_log / dt_bias / lower_bound arguments in
+ *  关键源码片段; P1 does not print the formula, the standard KDA gate is
+ *  adopted, parity unpinned by the pages):
+ *        z_i = raw_g[n, h, i] + dt_bias[h*K + i]        (dt_bias may be absent)
+ *        lower_bound < 0:  g_i = lower_bound * sigmoid(exp(A_log[h]) * z_i)
+ *        otherwise:        g_i = -exp(A_log[h]) * softplus(z_i)
+ *        beta = sigmoid(raw_beta[n, h])
+ *     softplus(z) = log(1 + exp(z)).  These replace the activated g and beta.
+ *
  *  6. Rounding.  Every stored input is widened exactly to fp64; all
  *     arithmetic is fp64; out is rounded to bf16 and S' to fp32, both
  *     round-to-nearest-even, and S' is written back to slot s.
@@ -98,6 +108,10 @@ typedef struct {
   double q_scale;             /* 0 => 1/sqrt(K) */
   int32_t out_norm;           /* 1: gated RMSNorm epilogue, 0: raw o */
   int32_t update_conv_state;  /* 1: write the shifted conv state */
+  int32_t fused_gate;         /* 1: g and beta hold raw logits (see "Fused gate") */
+  const float* A_log;         /* [H]; fused_gate only */
+  const float* dt_bias;       /* [H*K] or NULL; fused_gate only */
+  double lower_bound;         /* < 0: bounded ("safe") gate; fused_gate only */
 } kda_oracle_problem;
 
 /* Runs one decode step over every (row, head).  num_threads <= 0 uses the
@@ -134,6 +148,12 @@ void kda_oracle_readout(int K, int V, const double* S, const double* q, double* 
 /* Step 5: y_j = o_j / sqrt(mean(o^2) + eps) * w_j * sigmoid(gate_j). */
 void kda_oracle_gated_rmsnorm(int V, const double* o, const double* w,
                               const double* gate, double eps, double* y);
+
+/* softplus(z) = log(1 + exp(z)). */
+double kda_oracle_softplus(double z);
+
+/* Fused gate: g from z = raw + bias (see "Fused gate" above). */
+double kda_oracle_kda_gate(double z, double A_log, double lower_bound);
 
 /* Round to bf16, nearest-even, directly from fp64; returns the bit pattern. */
 uint16_t kda_oracle_round_bf16(double x);

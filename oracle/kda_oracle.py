@@ -51,6 +51,8 @@ class _Problem(ctypes.Structure):
         ("out", ctypes.c_void_p), ("out_f64", ctypes.c_void_p),
         ("eps", ctypes.c_double), ("l2_eps", ctypes.c_double), ("q_scale", ctypes.c_double),
         ("out_norm", ctypes.c_int32), ("update_conv_state", ctypes.c_int32),
+        ("fused_gate", ctypes.c_int32), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("lower_bound", ctypes.c_double),
     ]
 
 
@@ -77,6 +79,10 @@ def lib() -> ctypes.CDLL:
                                                         ctypes.c_double, dp, dp]
             L.kda_oracle_readout.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp, dp]
             L.kda_oracle_gated_rmsnorm.argtypes = [ctypes.c_int, dp, dp, dp, ctypes.c_double, dp]
+            L.kda_oracle_softplus.argtypes = [ctypes.c_double]
+            L.kda_oracle_softplus.restype = ctypes.c_double
+            L.kda_oracle_kda_gate.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double]
+            L.kda_oracle_kda_gate.restype = ctypes.c_double
             L.kda_oracle_round_bf16.argtypes = [ctypes.c_double]
             L.kda_oracle_round_bf16.restype = ctypes.c_uint16
             L.kda_oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
@@ -146,6 +152,14 @@ def gated_rmsnorm(o, w, gate, eps: float = 1e-6) -> np.ndarray:
     return y
 
 
+def softplus(z: float) -> float:
+    return lib().kda_oracle_softplus(float(z))
+
+
+def kda_gate(z: float, A_log: float, lower_bound: float = 0.0) -> float:
+    return lib().kda_oracle_kda_gate(float(z), float(A_log), float(lower_bound))
+
+
 def round_bf16(x: float) -> int:
     return int(lib().kda_oracle_round_bf16(float(x)))
 
@@ -169,9 +183,12 @@ def decode(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, H: int,
            K: int = 128, V: int = 128, W: int = 4, gate=None, norm_weight=None,
            conv_bias=None, eps: float = 1e-6, l2_eps: float = 1e-6, q_scale: float = 0.0,
            out_norm: bool = True, update_conv_state: bool = True, threads: int = 0,
-           want_f64: bool = True, in_place: bool = False) -> OracleResult:
+           want_f64: bool = True, in_place: bool = False, fused_gate: bool = False,
+           A_log=None, dt_bias=None, lower_bound: float = 0.0) -> OracleResult:
     """One decode step over all rows.  ``conv_state``/``state`` are copied
-    unless ``in_place``; the updated arrays come back in the result."""
+    unless ``in_place``; the updated arrays come back in the result.  With
+    ``fused_gate``, ``g`` and ``beta`` hold raw logits and are activated with
+    ``A_log``, ``dt_bias`` and ``lower_bound``."""
     qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
     N = qkv.shape[0]
     C = 2 * H * K + H * V
@@ -200,6 +217,14 @@ def decode(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, H: int,
     if conv_bias is not None:
         conv_bias = np.ascontiguousarray(conv_bias, dtype=np.float32)
         assert conv_bias.size == C
+    if fused_gate:
+        A_log = np.ascontiguousarray(A_log, dtype=np.float32)
+        assert A_log.size == H
+        if dt_bias is not None:
+            dt_bias = np.ascontiguousarray(dt_bias, dtype=np.float32)
+            assert dt_bias.size == H * K
+    else:
+        A_log = dt_bias = None
     out = np.zeros((N, H * V), dtype=np.uint16)
     out64 = np.zeros((N, H * V), dtype=np.float64) if want_f64 else None
     p = _Problem(N=N, H=H, K=K, V=V, W=W, num_slots=num_slots,
@@ -209,7 +234,8 @@ def decode(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, H: int,
                  gate=_ptr(gate), norm_weight=_ptr(norm_weight), slot_idx=_ptr(slot_idx),
                  out=_ptr(out), out_f64=_ptr(out64), eps=eps, l2_eps=l2_eps,
                  q_scale=q_scale, out_norm=int(bool(out_norm)),
-                 update_conv_state=int(bool(update_conv_state)))
+                 update_conv_state=int(bool(update_conv_state)), fused_gate=int(bool(fused_gate)),
+                 A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), lower_bound=float(lower_bound))
     rc = lib().kda_oracle_decode(ctypes.byref(p), int(threads))
     if rc < 0:
         raise ValueError("kda_oracle_decode rejected its arguments")

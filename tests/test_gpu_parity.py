@@ -16,9 +16,9 @@ from linear_attention_decode_04_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _check(x, dev, **kw):
+def _check(x, dev, early_prefetch=False, **kw):
     d = T.to_device(x, dev)
-    T.run_gpu(x, d, **kw)
+    T.run_gpu(x, d, early_prefetch=early_prefetch, **kw)
     torch.cuda.synchronize()
     ref = T.run_oracle(x, **kw)
     res = T.compare_all(x, d, ref, init_state=x.state, init_conv=x.conv_state)
@@ -39,6 +39,54 @@ def test_workload_parity(name, cuda_device):
 def test_flag_combinations(out_norm, update_conv_state, cuda_device):
     x = W.make_inputs(W.Spec("flags_n9_h12_pool16", N=9, H=12, num_slots=16, seed=21, pad_tail=2))
     _check(x, cuda_device, out_norm=out_norm, update_conv_state=update_conv_state)
+
+
+@pytest.mark.parametrize("name", list(W.SPECS))
+def test_workload_parity_early_prefetch(name, cuda_device):
+    """Same results with KDA_EARLY_PREFETCH (state streamed before the
+    previous kernel on the stream completes; nothing before it writes the
+    pools here)."""
+    _check(W.make_inputs(W.SPECS[name]), cuda_device, early_prefetch=True)
+
+
+def test_back_to_back_same_pool_in_one_graph(cuda_device):
+    """Three decode steps on the SAME pools, captured in one CUDA graph
+    (programmatic dependent launches, no early prefetch): each step must see
+    the previous step's state and conv state, as three oracle steps do."""
+    from linear_attention_decode_04_gb300.stack import warm_up
+    from linear_attention_decode_04_gb300 import KdaDecodeCall
+    spec = W.Spec("chain_n24_h24_pool32", N=24, H=24, num_slots=32, seed=41, pad_tail=3)
+    x = W.make_inputs(spec)
+    d = T.to_device(x, cuda_device)
+    steps = [W.draw_step_inputs(spec, v) for v in range(3)]
+    dev_steps, calls = [], []
+    for st in steps:
+        ds = dict(qkv=T.bf16_tensor(st["qkv"], cuda_device), g=torch.from_numpy(st["g"]).to(cuda_device),
+                  beta=T.bf16_tensor(st["beta"], cuda_device), gate=T.bf16_tensor(st["gate"], cuda_device),
+                  out=torch.empty(x.N, x.H * 128, dtype=torch.bfloat16, device=cuda_device))
+        dev_steps.append(ds)
+        calls.append(KdaDecodeCall(ds["qkv"], d["conv_weight"], d["conv_state"], d["state"], ds["g"],
+                                   ds["beta"], d["slot_idx"], ds["out"], gate=ds["gate"],
+                                   norm_weight=d["norm_weight"], eps=spec.eps, err_flag=d["err_flag"]))
+    warm_up(cuda_device)
+    s = torch.cuda.Stream(cuda_device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    cs, stt = x.conv_state.copy(), x.state.copy()
+    import oracle
+    for st, ds in zip(steps, dev_steps):
+        ref = oracle.decode(qkv=st["qkv"], conv_weight=x.conv_weight, conv_state=cs, state=stt, g=st["g"],
+                            beta=st["beta"], slot_idx=x.slot_idx, H=x.H, gate=st["gate"],
+                            norm_weight=x.norm_weight, eps=spec.eps, in_place=True)
+        T.check_out(T.bf16_bits(ds["out"]), ref, "chained step")
+    assert np.array_equal(T.bf16_bits(d["conv_state"]), cs)
+    for sl in range(spec.num_slots):
+        T.check_state_slot(d["state"][sl].cpu().numpy(), stt[sl], f"slot {sl}")
+    assert int(d["err_flag"].item()) == 0
 
 
 @pytest.mark.parametrize("H", [12, 24, 48, 96, 5])
@@ -142,3 +190,23 @@ def test_binding_rejects_cpu_and_bad_shapes(cuda_device):
         kda_decode(mis, d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
                    d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"])
     assert ei.value.status == -3
+
+
+@pytest.mark.parametrize("early_prefetch", [False, True])
+def test_bounded_wait_runs_out_and_reports(early_prefetch, cuda_device):
+    """Failure path without a GPU fault: one unit's load is never signalled
+    and the waits are limited to 20 ms.  The launch must return (no hang, no
+    trap) with KDA_DEVERR_TIMEOUT set, and the context must stay usable: a
+    normal call afterwards still matches the oracle."""
+    from linear_attention_decode_04_gb300 import KdaDecodeCall
+    from linear_attention_decode_04_gb300.binding import KDA_DEVERR_TIMEOUT
+    x = W.make_inputs(W.Spec("waittest_n40_h24_pool48", N=40, H=24, num_slots=48, seed=51, pad_tail=2))
+    d = T.to_device(x, cuda_device)
+    call = KdaDecodeCall(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
+                         d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"],
+                         eps=x.spec.eps, err_flag=d["err_flag"], early_prefetch=early_prefetch)
+    call.wait_test(20_000_000, withhold_unit=0)
+    torch.cuda.synchronize()
+    assert int(d["err_flag"].item()) & KDA_DEVERR_TIMEOUT
+    # the context is intact: a fresh problem decodes correctly
+    _check(W.make_inputs(W.PAD_TAIL), cuda_device)

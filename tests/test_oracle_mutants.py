@@ -34,6 +34,11 @@ MUTANTS = {
     "bf16_ties_away": (
         "if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;",
         "if (rem >= 0.5) fl += 1.0;"),
+    "gate_drops_dt_bias": (
+        "if (p->dt_bias) z += (double)p->dt_bias[(int64_t)h * K + i];", "(void)0;"),
+    "gate_uses_A_log_not_exp": (
+        "if (lower_bound < 0.0) return lower_bound * kda_oracle_sigmoid(exp(A_log) * z);",
+        "if (lower_bound < 0.0) return lower_bound * kda_oracle_sigmoid(A_log * z);"),
     "readout_skips_last_key": (
         "for (int i = 0; i < K; ++i) acc += S[(size_t)i * V + j] * q[i];",
         "for (int i = 0; i < K - 1; ++i) acc += S[(size_t)i * V + j] * q[i];"),

@@ -435,3 +435,110 @@ def test_threads_do_not_change_bits():
     p = tiny_problem(seed=20, N=6, H=4, num_slots=9)
     a, b = run(p, threads=1), run(p, threads=4)
     assert np.array_equal(a.out, b.out) and np.array_equal(a.state, b.state)
+
+
+# ----------------------------------------------------------------- fused gate
+
+
+def test_softplus_library_and_stability():
+    for z in (-700.0, -30.0, -1.5, 0.0, 0.25, 3.0, 30.0, 700.0):
+        want = F.softplus(torch.tensor(z, dtype=torch.float64), threshold=1e9).item()
+        got = oracle.softplus(z)
+        assert math.isfinite(got)
+        assert abs(got - want) <= 1e-15 * max(1.0, abs(want)), (z, got, want)
+    assert oracle.softplus(0.0) == math.log(2.0)
+
+
+def test_kda_gate_closed_forms():
+    """Bounded gate: z=0 gives lower_bound/2, the range is (lower_bound, 0),
+    decreasing in z, slope lower_bound*e^A/4 at 0.  Unbounded gate:
+    -e^A log 2 at z=0 and -e^A softplus(z) in general (torch softplus)."""
+    lb, A = -5.0, 0.3
+    assert oracle.kda_gate(0.0, A, lb) == lb / 2
+    assert abs(oracle.kda_gate(60.0, A, lb) - lb) < 1e-12 and abs(oracle.kda_gate(-60.0, A, lb)) < 1e-12
+    zs = np.linspace(-6, 6, 41)
+    gs = [oracle.kda_gate(z, A, lb) for z in zs]
+    assert all(lb < g < 0 for g in gs) and all(a > b for a, b in zip(gs, gs[1:]))
+    h = 1e-6
+    slope = (oracle.kda_gate(h, A, lb) - oracle.kda_gate(-h, A, lb)) / (2 * h)
+    assert abs(slope - lb * math.exp(A) / 4) < 1e-6
+    assert abs(oracle.kda_gate(0.0, A, 0.0) + math.exp(A) * math.log(2)) < 1e-15
+    for z in (-3.0, 0.7, 9.0):
+        want = -math.exp(A) * F.softplus(torch.tensor(z, dtype=torch.float64), threshold=1e9).item()
+        assert abs(oracle.kda_gate(z, A, 0.0) - want) < 1e-14
+
+
+def _gate_problem(seed, lower_bound, with_bias=True):
+    p = tiny_problem(seed=seed, N=4, H=3, K=3, V=5, num_slots=8, slots=[3, 0, 7, 1])
+    rng = np.random.default_rng(seed + 1000)
+    p["g"] = rng.standard_normal(p["g"].shape).astype(np.float32)             # raw logits
+    p["beta"] = bf16_bits(rng.standard_normal(p["beta"].shape))               # raw logits
+    p.update(fused_gate=True, A_log=rng.standard_normal(3).astype(np.float32) * 0.5,
+             dt_bias=(rng.standard_normal(3 * 3).astype(np.float32) if with_bias else None),
+             lower_bound=lower_bound)
+    return p
+
+
+@pytest.mark.parametrize("lower_bound", [-5.0, 0.0])
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_fused_gate_whole_step_equals_preactivated(lower_bound, with_bias):
+    """The fused-gate step equals the plain step fed with g and beta that
+    torch activates from the same raw logits (library softplus / sigmoid)."""
+    p = _gate_problem(71, lower_bound, with_bias)
+    r = run(p)
+    H, K = p["H"], p["K"]
+    z = torch.from_numpy(p["g"].astype(np.float64))
+    if with_bias:
+        z = z + torch.from_numpy(p["dt_bias"].astype(np.float64)).view(H, K)
+    A = torch.from_numpy(p["A_log"].astype(np.float64)).view(1, H, 1).exp()
+    if lower_bound < 0:
+        g = lower_bound * torch.sigmoid(A * z)
+    else:
+        g = -A * F.softplus(z, threshold=1e9)
+    beta = torch.sigmoid(torch.from_numpy(widen(p["beta"])))
+    # Feed the activated values through the float64 library composition.
+    q = dict(p)
+    q["g"], q["beta"] = g.numpy(), beta.numpy()
+    ref_out, ref_state = _torch_reference_f64_gate(q)
+    assert np.allclose(r.out_f64, ref_out, rtol=0, atol=1e-12)
+    for (s, h), Sn in ref_state.items():
+        assert np.array_equal(r.state[s, h], Sn.astype(np.float32))
+
+
+def _torch_reference_f64_gate(p):
+    """torch_reference with g and beta given as float64 activated values."""
+    q = dict(p)
+    g64, b64 = q.pop("g"), q.pop("beta")
+    q["g"] = np.zeros(g64.shape, np.float32)
+    q["beta"] = np.zeros(b64.shape, np.uint16)
+    # re-run the composition with exact activated values
+    H, K, V, W = q["H"], q["K"], q["V"], q["W"]
+    Dq, Dv = H * K, H * V
+    C = 2 * Dq + Dv
+    qkv = torch.from_numpy(widen(q["qkv"]))[:, :C]
+    wts = torch.from_numpy(channel_weights(q)).unsqueeze(1)
+    cs = torch.from_numpy(widen(q["conv_state"]))
+    S_all = torch.from_numpy(q["state"].astype(np.float64))
+    gate = torch.from_numpy(widen(q["gate"]))
+    nw = torch.from_numpy(q["norm_weight"].astype(np.float64))
+    out = torch.zeros(qkv.shape[0], Dv, dtype=torch.float64)
+    new_state = {}
+    for n in range(qkv.shape[0]):
+        s = int(q["slot_idx"][n])
+        if s <= 0:
+            continue
+        window = torch.cat([cs[s], qkv[n].unsqueeze(1)], dim=1)
+        a = F.silu(F.conv1d(window.unsqueeze(0), wts, groups=C)[0, :, 0])
+        for h in range(H):
+            qt, kt = a[h * K:(h + 1) * K], a[Dq + h * K: Dq + (h + 1) * K]
+            vt = a[2 * Dq + h * V: 2 * Dq + (h + 1) * V]
+            qh = qt / torch.sqrt((qt * qt).sum() + 1e-6) / math.sqrt(K)
+            kh = kt / torch.sqrt((kt * kt).sum() + 1e-6)
+            b = float(b64[n, h])
+            M = torch.eye(K, dtype=torch.float64) - b * torch.outer(kh, kh)
+            Sn = M @ torch.diag(torch.exp(torch.from_numpy(np.asarray(g64[n, h])))) @ S_all[s, h] \
+                + b * torch.outer(kh, vt)
+            o = F.rms_norm(Sn.T @ qh, (V,), weight=nw, eps=1e-6) * torch.sigmoid(gate[n, h * V:(h + 1) * V])
+            out[n, h * V:(h + 1) * V] = o
+            new_state[(s, h)] = Sn.numpy()
+    return out.numpy(), new_state
