@@ -50,6 +50,9 @@ extern "C" {
  * per-token inputs (qkv, g, beta, gate) are still read only after it has
  * completed.  Without this flag nothing is read before it completes. */
 #define KDA_EARLY_PREFETCH    4u
+/* g and beta hold raw logits and the kernel activates them (the page's
+ * "safe gate" variant; formula below, in KdaDecodeArgs.lower_bound). */
+#define KDA_FUSED_GATE        8u
 
 /* return codes of kda_decode */
 #define KDA_OK            0
@@ -71,7 +74,7 @@ extern "C" {
  * C = 3 * D (q | k | v channel blocks, each head-major).  bf16 tensors are
  * passed as their 16-bit patterns (uint16_t).
  *
- * Alignment: every pointer except beta, slot_idx and err_flag must be
+ * Alignment: every pointer except beta, slot_idx, err_flag, A_log and dt_bias must be
  * 16-byte aligned, and every row stride must be a multiple of 8 elements.
  */
 typedef struct KdaDecodeArgs {
@@ -102,8 +105,20 @@ typedef struct KdaDecodeArgs {
   int64_t out_row_stride;      /* elements, >= D */
   float eps;                   /* RMSNorm epsilon (e.g. 1e-6) */
   float q_scale;               /* 0 => 1/sqrt(128) */
-  uint32_t flags;              /* KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH */
+  uint32_t flags;              /* KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH |
+                                  KDA_FUSED_GATE */
   int32_t* err_flag;           /* device int32 or NULL; KDA_DEVERR_* bits are OR-ed in */
+
+  /* KDA_FUSED_GATE only (P1 关键源码片段: the op's A_log, dt_bias, lower_bound;
+   * the formula is the standard KDA gate, not printed on P1).  With
+   * z = g[n][h][i] + dt_bias[h*128 + i] (raw logits plus bias):
+   *   lower_bound < 0:  g' = lower_bound * sigmoid(exp(A_log[h]) * z)
+   *   otherwise:        g' = -exp(A_log[h]) * softplus(z)
+   * and beta' = sigmoid(beta[n][h]); alpha = exp(g').  Scalar loads only, so
+   * these two pointers need 4-byte alignment. */
+  const float* A_log;          /* fp32 [H] */
+  const float* dt_bias;        /* fp32 [H*128] or NULL */
+  float lower_bound;
 } KdaDecodeArgs;
 
 /*

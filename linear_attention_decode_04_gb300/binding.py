@@ -18,6 +18,7 @@ CONV_WIDTH = 4
 KDA_OUT_NORM = 1
 KDA_UPDATE_CONV_STATE = 2
 KDA_EARLY_PREFETCH = 4
+KDA_FUSED_GATE = 8
 KDA_DEVERR_SLOT_RANGE = 1
 KDA_DEVERR_TIMEOUT = 2
 ABI_VERSION = 1
@@ -49,6 +50,7 @@ class KdaDecodeArgs(ctypes.Structure):
         ("out", ctypes.c_void_p), ("out_row_stride", ctypes.c_int64),
         ("eps", ctypes.c_float), ("q_scale", ctypes.c_float),
         ("flags", ctypes.c_uint32), ("err_flag", ctypes.c_void_p),
+        ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("lower_bound", ctypes.c_float),
     ]
 
 
@@ -120,7 +122,8 @@ class KdaDecodeCall:
     def __init__(self, qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                  gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
-                 err_flag=None, early_prefetch: bool = False):
+                 err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
+                 lower_bound: float = 0.0):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -155,8 +158,21 @@ class KdaDecodeCall:
         _dense(slot_idx, "slot_idx")
         _check(out, "out", torch.bfloat16, dev)
         out_stride = _rows(out, "out", N, D)
+        fused_gate = A_log is not None
         flags = ((KDA_OUT_NORM if out_norm else 0) | (KDA_UPDATE_CONV_STATE if update_conv_state else 0)
-                 | (KDA_EARLY_PREFETCH if early_prefetch else 0))
+                 | (KDA_EARLY_PREFETCH if early_prefetch else 0) | (KDA_FUSED_GATE if fused_gate else 0))
+        alog_ptr = dtb_ptr = None
+        if fused_gate:
+            _check(A_log, "A_log", torch.float32, dev)
+            if tuple(A_log.shape) != (H,):
+                raise ValueError(f"A_log must be [{H}]")
+            alog_ptr = A_log.data_ptr()
+            if dt_bias is not None:
+                _check(dt_bias, "dt_bias", torch.float32, dev)
+                if tuple(dt_bias.shape) != (H * HEAD_DIM,):
+                    raise ValueError(f"dt_bias must be [{H * HEAD_DIM}]")
+                _dense(dt_bias, "dt_bias")
+                dtb_ptr = dt_bias.data_ptr()
         gate_ptr = nw_ptr = None
         gate_stride = 0
         if out_norm:
@@ -181,7 +197,7 @@ class KdaDecodeCall:
         self.device = dev
         self.N, self.H, self.num_slots = N, H, num_slots
         self._keep = (qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate,
-                      norm_weight, conv_bias, err_flag)
+                      norm_weight, conv_bias, err_flag, A_log, dt_bias)
         self.args = KdaDecodeArgs(
             struct_size=ctypes.sizeof(KdaDecodeArgs), N=N, H=H, num_slots=num_slots,
             head_dim=HEAD_DIM, conv_width=CONV_WIDTH,
@@ -191,7 +207,8 @@ class KdaDecodeCall:
             g=g.data_ptr(), beta=beta.data_ptr(), gate=gate_ptr, gate_row_stride=gate_stride,
             norm_weight=nw_ptr, slot_idx=slot_idx.data_ptr(),
             out=out.data_ptr(), out_row_stride=out_stride,
-            eps=float(eps), q_scale=float(q_scale), flags=flags, err_flag=err_ptr)
+            eps=float(eps), q_scale=float(q_scale), flags=flags, err_flag=err_ptr,
+            A_log=alog_ptr, dt_bias=dtb_ptr, lower_bound=float(lower_bound))
         self._argp = ctypes.byref(self.args)
 
     def __call__(self, stream: torch.cuda.Stream | None = None) -> None:
@@ -215,14 +232,16 @@ class KdaDecodeCall:
 def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
-               err_flag=None, early_prefetch: bool = False,
-               stream: torch.cuda.Stream | None = None) -> None:
+               err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
+               lower_bound: float = 0.0, stream: torch.cuda.Stream | None = None) -> None:
     """One fused decode step (see ``include/kda_decode.h``).  ``conv_state``,
     ``state`` and ``out`` are written in place on ``stream`` (default: the
     current stream of the state's device).  ``early_prefetch`` sets
     KDA_EARLY_PREFETCH: only when the kernel enqueued just before on the
-    stream writes none of slot_idx, state and conv_state."""
+    stream writes none of slot_idx, state and conv_state.  Passing ``A_log``
+    sets KDA_FUSED_GATE: ``g`` and ``beta`` are then raw logits."""
     KdaDecodeCall(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate=gate,
                   norm_weight=norm_weight, conv_bias=conv_bias, eps=eps, q_scale=q_scale,
                   out_norm=out_norm, update_conv_state=update_conv_state,
-                  err_flag=err_flag, early_prefetch=early_prefetch)(stream)
+                  err_flag=err_flag, early_prefetch=early_prefetch, A_log=A_log, dt_bias=dt_bias,
+                  lower_bound=lower_bound)(stream)

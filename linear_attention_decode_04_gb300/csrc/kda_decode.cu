@@ -55,6 +55,10 @@ struct Params {
   int N, H, num_slots;
   int total_units;  // N * H
   int early_prefetch;  // KDA_EARLY_PREFETCH
+  int fused_gate;      // KDA_FUSED_GATE: g / beta are raw logits
+  const float* A_log;
+  const float* dt_bias;
+  float lower_bound;
   int withhold_unit;   // wait-path test: this unit's load is never signalled (-1: none)
   uint64_t wait_limit_ns;
   float eps, q_scale;
@@ -372,7 +376,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         if (p.conv_b) bv = __ldg(p.conv_b + 2 * D + static_cast<int64_t>(h) * kDim + j);
       }
     }
-    const float beta = (tid < kDim) ? bf16_to_f32(__ldg(p.beta + static_cast<int64_t>(n) * p.H + h)) : 0.0f;
+    float beta = (tid < kDim) ? bf16_to_f32(__ldg(p.beta + static_cast<int64_t>(n) * p.H + h)) : 0.0f;
+    float gate_a = 0.0f, gate_bias = 0.0f;  // exp(A_log[h]) and dt_bias for key channel tid-128
+    if (p.fused_gate) {
+      if (tid < kDim) {
+        beta = 1.0f / (1.0f + expf(-beta));
+      } else {
+        gate_a = expf(__ldg(p.A_log + h));
+        if (p.dt_bias) gate_bias = __ldg(p.dt_bias + static_cast<int64_t>(h) * kDim + (tid - kDim));
+      }
+    }
 
     const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), (it / kStages) & 1, p.wait_limit_ns);
     // All consumers agree (this is also the barrier that guards the scratch).
@@ -435,7 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         yv = fmaf(wv[3], bf16_to_f32(S.x[stage][2][j]), yv);
         S.v[j] = yv / (1.0f + expf(-yv));
       } else {
-        S.alpha[j] = expf(S.g[stage][j]);
+        float g = S.g[stage][j];
+        if (p.fused_gate) {
+          // Gate activation (the page's safe-gate variant; standard KDA form).
+          const float z = g + gate_bias;
+          if (p.lower_bound < 0.0f) {
+            g = p.lower_bound / (1.0f + expf(-gate_a * z));
+          } else {
+            const float sp = (z > 0.0f) ? z + log1pf(expf(-z)) : log1pf(expf(z));
+            g = -gate_a * sp;
+          }
+        }
+        S.alpha[j] = expf(g);
       }
     }
     const float gate_j = (kOutNorm && tid < kDim) ? bf16_to_f32(S.gate[stage][tid]) : 0.0f;
@@ -640,7 +664,7 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
     return fail(KDA_ERR_SHAPE, "head_dim %d / conv_width %d (need 128 / 4)", a->head_dim, a->conv_width);
   if (a->N < 0 || a->H < 1 || a->num_slots < 1)
     return fail(KDA_ERR_SHAPE, "N=%d H=%d num_slots=%d", a->N, a->H, a->num_slots);
-  if (a->flags & ~(KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH))
+  if (a->flags & ~(KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH | KDA_FUSED_GATE))
     return fail(KDA_ERR_FLAGS, "flags 0x%x", a->flags);
   if (a->N == 0) return KDA_OK;
   const bool norm = (a->flags & KDA_OUT_NORM) != 0;
@@ -649,6 +673,11 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
     return fail(KDA_ERR_NULLPTR, "a required tensor pointer is NULL");
   if (norm && (!a->gate || !a->norm_weight))
     return fail(KDA_ERR_NULLPTR, "KDA_OUT_NORM needs gate and norm_weight");
+  const bool fused_gate = (a->flags & KDA_FUSED_GATE) != 0;
+  if (fused_gate && !a->A_log) return fail(KDA_ERR_NULLPTR, "KDA_FUSED_GATE needs A_log");
+  if (fused_gate && ((reinterpret_cast<uintptr_t>(a->A_log) & 3u) ||
+                     (reinterpret_cast<uintptr_t>(a->dt_bias) & 3u)))
+    return fail(KDA_ERR_ALIGN, "A_log and dt_bias must be 4-byte aligned");
   const int64_t D = static_cast<int64_t>(a->H) * KDA_HEAD_DIM;
   if (static_cast<int64_t>(a->N) * a->H > (1LL << 30))
     return fail(KDA_ERR_SHAPE, "N*H = %lld exceeds the grid limit", static_cast<long long>(a->N) * a->H);
@@ -685,6 +714,10 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
   p.err = a->err_flag;
   p.total_units = a->N * a->H;
   p.early_prefetch = (a->flags & KDA_EARLY_PREFETCH) != 0;
+  p.fused_gate = fused_gate;
+  p.A_log = fused_gate ? a->A_log : nullptr;
+  p.dt_bias = fused_gate ? a->dt_bias : nullptr;
+  p.lower_bound = a->lower_bound;
   p.withhold_unit = withhold_unit;
   p.wait_limit_ns = wait_limit_ns;
 

@@ -73,7 +73,9 @@ def test_host_validation_codes(lib):
     assert _call(lib, _args(conv_width=3)) == -2
     assert _call(lib, _args(H=0)) == -2
     assert _call(lib, _args(N=-1)) == -2
-    assert _call(lib, _args(flags=8)) == -4
+    assert _call(lib, _args(flags=16)) == -4
+    assert _call(lib, _args(flags=3 | 8)) == -1            # fused gate needs A_log
+    assert _call(lib, _args(flags=3 | 8, A_log=0x20002)) == -3
     assert _call(lib, _args(N=0)) == 0          # no-op, no launch
     assert _call(lib, _args(qkv=None)) == -1
     assert _call(lib, _args(gate=None)) == -1    # norm on needs the gate

@@ -210,3 +210,30 @@ def test_bounded_wait_runs_out_and_reports(early_prefetch, cuda_device):
     assert int(d["err_flag"].item()) & KDA_DEVERR_TIMEOUT
     # the context is intact: a fresh problem decodes correctly
     _check(W.make_inputs(W.PAD_TAIL), cuda_device)
+
+
+@pytest.mark.parametrize("lower_bound", [-5.0, 0.0])
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_fused_gate_parity(lower_bound, with_bias, cuda_device):
+    """KDA_FUSED_GATE: g and beta arrive as raw logits and are activated in
+    the kernel (bounded form with lower_bound < 0, softplus form otherwise)."""
+    import oracle
+    spec = W.Spec("gate_n20_h24_pool32", N=20, H=24, num_slots=32, seed=61, pad_tail=2)
+    x = W.make_inputs(spec)
+    rng = np.random.default_rng(62)
+    x.g = rng.standard_normal(x.g.shape).astype(np.float32)                    # raw gate logits
+    x.beta = W.f32_to_bf16_bits(rng.standard_normal(x.beta.shape).astype(np.float32))
+    A_log = (0.5 * rng.standard_normal(x.H)).astype(np.float32)
+    dt_bias = (0.5 * rng.standard_normal(x.H * 128)).astype(np.float32) if with_bias else None
+    d = T.to_device(x, cuda_device)
+    kda_decode(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"], d["slot_idx"],
+               d["out"], gate=d["gate"], norm_weight=d["norm_weight"], eps=spec.eps, err_flag=d["err_flag"],
+               A_log=torch.from_numpy(A_log).to(cuda_device),
+               dt_bias=None if dt_bias is None else torch.from_numpy(dt_bias).to(cuda_device),
+               lower_bound=lower_bound)
+    torch.cuda.synchronize()
+    ref = oracle.decode(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state, g=x.g,
+                        beta=x.beta, slot_idx=x.slot_idx, H=x.H, gate=x.gate, norm_weight=x.norm_weight,
+                        eps=spec.eps, fused_gate=True, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound)
+    T.compare_all(x, d, ref, init_state=x.state, init_conv=x.conv_state)
+    assert int(d["err_flag"].item()) == 0
