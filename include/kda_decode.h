@@ -119,6 +119,14 @@ typedef struct KdaDecodeArgs {
   const float* A_log;          /* fp32 [H] */
   const float* dt_bias;        /* fp32 [H*128] or NULL */
   float lower_bound;
+
+  /* Optional work queue: device int32[2], zero before the call; every call
+   * leaves it zero again.  With it, units beyond each CTA's first few are
+   * handed out dynamically so that all SMs finish together; NULL keeps a
+   * static round-robin schedule.  Calls that may overlap on the GPU (for
+   * example on different streams) need different queues; calls ordered on
+   * one stream may share one.  4-byte alignment. */
+  int32_t* work_queue;
 } KdaDecodeArgs;
 
 /*

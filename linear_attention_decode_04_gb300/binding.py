@@ -51,6 +51,7 @@ class KdaDecodeArgs(ctypes.Structure):
         ("eps", ctypes.c_float), ("q_scale", ctypes.c_float),
         ("flags", ctypes.c_uint32), ("err_flag", ctypes.c_void_p),
         ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("lower_bound", ctypes.c_float),
+        ("work_queue", ctypes.c_void_p),
     ]
 
 
@@ -123,7 +124,7 @@ class KdaDecodeCall:
                  gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
                  err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
-                 lower_bound: float = 0.0):
+                 lower_bound: float = 0.0, work_queue=None):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -190,6 +191,12 @@ class KdaDecodeCall:
             if tuple(conv_bias.shape) != (C,):
                 raise ValueError(f"conv_bias must be [{C}]")
             bias_ptr = conv_bias.data_ptr()
+        queue_ptr = None
+        if work_queue is not None:
+            _check(work_queue, "work_queue", torch.int32, dev)
+            if work_queue.numel() < 2:
+                raise ValueError("work_queue needs 2 int32")
+            queue_ptr = work_queue.data_ptr()
         err_ptr = None
         if err_flag is not None:
             _check(err_flag, "err_flag", torch.int32, dev)
@@ -197,7 +204,7 @@ class KdaDecodeCall:
         self.device = dev
         self.N, self.H, self.num_slots = N, H, num_slots
         self._keep = (qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate,
-                      norm_weight, conv_bias, err_flag, A_log, dt_bias)
+                      norm_weight, conv_bias, err_flag, A_log, dt_bias, work_queue)
         self.args = KdaDecodeArgs(
             struct_size=ctypes.sizeof(KdaDecodeArgs), N=N, H=H, num_slots=num_slots,
             head_dim=HEAD_DIM, conv_width=CONV_WIDTH,
@@ -208,7 +215,7 @@ class KdaDecodeCall:
             norm_weight=nw_ptr, slot_idx=slot_idx.data_ptr(),
             out=out.data_ptr(), out_row_stride=out_stride,
             eps=float(eps), q_scale=float(q_scale), flags=flags, err_flag=err_ptr,
-            A_log=alog_ptr, dt_bias=dtb_ptr, lower_bound=float(lower_bound))
+            A_log=alog_ptr, dt_bias=dtb_ptr, lower_bound=float(lower_bound), work_queue=queue_ptr)
         self._argp = ctypes.byref(self.args)
 
     def __call__(self, stream: torch.cuda.Stream | None = None) -> None:
@@ -233,15 +240,17 @@ def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
                err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
-               lower_bound: float = 0.0, stream: torch.cuda.Stream | None = None) -> None:
+               lower_bound: float = 0.0, work_queue=None,
+               stream: torch.cuda.Stream | None = None) -> None:
     """One fused decode step (see ``include/kda_decode.h``).  ``conv_state``,
     ``state`` and ``out`` are written in place on ``stream`` (default: the
     current stream of the state's device).  ``early_prefetch`` sets
     KDA_EARLY_PREFETCH: only when the kernel enqueued just before on the
     stream writes none of slot_idx, state and conv_state.  Passing ``A_log``
-    sets KDA_FUSED_GATE: ``g`` and ``beta`` are then raw logits."""
+    sets KDA_FUSED_GATE: ``g`` and ``beta`` are then raw logits.
+    ``work_queue`` (int32[2], zero) enables the dynamic schedule."""
     KdaDecodeCall(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate=gate,
                   norm_weight=norm_weight, conv_bias=conv_bias, eps=eps, q_scale=q_scale,
                   out_norm=out_norm, update_conv_state=update_conv_state,
                   err_flag=err_flag, early_prefetch=early_prefetch, A_log=A_log, dt_bias=dt_bias,
-                  lower_bound=lower_bound)(stream)
+                  lower_bound=lower_bound, work_queue=work_queue)(stream)

@@ -59,6 +59,7 @@ struct Params {
   const float* A_log;
   const float* dt_bias;
   float lower_bound;
+  int* queue;          // work queue int32[2] (next dynamic unit, finished CTAs) or null
   int withhold_unit;   // wait-path test: this unit's load is never signalled (-1: none)
   uint64_t wait_limit_ns;
   float eps, q_scale;
@@ -77,7 +78,8 @@ struct __align__(128) Smem {
   float red[2][kConsumerWarps][kDim];
   float delta[kDim];
   float sum[4][4];
-  int info[kStages][4];           // slot, n, h of the unit in each stage
+  int info[kStages][4];           // slot, n (-1: no more units), h, withheld
+  unsigned long long ready[kStages];  // info of the stage is written
   unsigned long long full[kStages];
   unsigned long long done[kStages];
   volatile int abort;
@@ -205,12 +207,17 @@ __device__ __forceinline__ void flag_error(const Params& p, int bits) {
   if (p.err) atomicOr(p.err, bits);
 }
 
-// Persistent kernel: one CTA per SM walks units u = blockIdx.x + k*gridDim.x
-// (unit u = row u / H, head u % H).  Warp 8 is the producer: it reads each
-// unit's slot, streams the 64 KiB state tile and the unit's small inputs
-// into a stage of the shared-memory ring with bulk copies, and streams the
-// updated tile back out once the consumers release it.  Warps 0-7 compute.
-// Two tiles are in flight per SM while the consumers work on a third.
+// Persistent kernel, one CTA per SM.  A unit is one (row n, head h) =
+// unit index n*H + h.  Each CTA takes its first kStages units statically
+// (blockIdx.x + k*gridDim.x, so they can be prefetched before the previous
+// kernel finishes); the rest come from the work queue when one is given
+// (an atomic counter: CTAs that run ahead take more units, so every CTA
+// finishes at nearly the same time), else continue the static stride.
+// Warp 8 is the producer: for each unit it publishes (slot, n, h) on the
+// stage's `ready` barrier, streams the 64 KiB state tile and the unit's small
+// inputs into the stage with bulk copies (`full` barrier), and once the
+// consumers release the stage (`done`) streams the updated tile back out.
+// Warps 0-7 compute.  Two tiles stream in while the consumers work on a third.
 template <bool kOutNorm, bool kUpdateConv>
 __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -221,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&S.ready[s]), 1);
       mbar_init(smem_addr(&S.full[s]), 1);
       mbar_init(smem_addr(&S.done[s]), kConsumerWarps);
     }
@@ -259,22 +267,45 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         bulk_load(smem_addr(S.gate[stage]), p.gate + n * p.gate_stride + static_cast<int64_t>(h) * kDim,
                   kXSliceBytes, full, policy);
     };
+    auto active = [&](int slot) { return slot > 0 && slot < p.num_slots; };
+    // Write the stage's tile back if it held an active unit.
+    auto store_stage = [&](int stage) {
+      const int* prev = S.info[stage];
+      if (active(prev[0])) {
+        float* dst = p.state + (static_cast<int64_t>(prev[0]) * p.H + prev[2]) * (kDim * kDim);
+        bulk_store(dst, smem_addr(S.tile[stage]), kTileBytes, policy);
+        bulk_commit();
+      }
+    };
+    int k_static = 0;  // static units taken so far
+    auto next_unit = [&]() -> int {
+      int u;
+      if (k_static < kStages || p.queue == nullptr)
+        u = blockIdx.x + (k_static++) * G;
+      else
+        u = kStages * G + atomicAdd(p.queue, 1);
+      return u < p.total_units ? u : -1;
+    };
 
+    // First ring: static units.  With KDA_EARLY_PREFETCH the first unit's
+    // state streams in before the previous kernel in the stream has finished
+    // (the caller guarantees that kernel does not write the slot indices,
+    // the state or the conv state); everything per-token waits for it.  The
+    // ring then fills one stage at a time (each stage once the one before
+    // it has landed), so that the first tile of every CTA arrives early
+    // instead of all CTAs' three tiles arriving together.
     int it = 0;
-    int unit = blockIdx.x;
-    // With KDA_EARLY_PREFETCH the first ring's worth of state streams in
-    // before the previous kernel in the stream has finished (the caller
-    // guarantees that kernel does not write the slot indices, the state or
-    // the conv state); everything per-token waits for it.
-    if (p.early_prefetch) {
-      for (; unit < p.total_units && it < kStages; unit += G, ++it) {
-        const int n = unit / p.H, h = unit - n * p.H;
+    for (; it < kStages; ++it) {
+      const int u = next_unit();
+      if (u < 0) break;
+      const int n = u / p.H, h = u - n * p.H;
+      S.info[it][1] = n;
+      S.info[it][2] = h;
+      S.info[it][3] = (u == p.withhold_unit);
+      if (p.early_prefetch && it == 0) {
         const int slot = __ldg(p.slot_idx + n);
         S.info[it][0] = slot;
-        S.info[it][1] = n;
-        S.info[it][2] = h;
-        S.info[it][3] = (unit == p.withhold_unit);
-        if (slot > 0 && slot < p.num_slots && !S.info[it][3]) {
+        if (active(slot) && !S.info[it][3]) {
           mbar_arrive_expect_tx(smem_addr(&S.full[it]), in_bytes);
           load_slot_parts(it, h, slot);
         }
@@ -282,72 +313,96 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     }
     griddep_wait();
     for (int j = 0; j < it; ++j) {
-      const int slot = S.info[j][0];
-      if (S.info[j][3]) continue;  // withheld (wait-path test)
-      if (slot > 0 && slot < p.num_slots)
-        load_token_parts(j, S.info[j][1], S.info[j][2]);
+      const int n = S.info[j][1], h = S.info[j][2];
+      if (j > 0 && !S.info[j - 1][3]) mbar_wait_bounded(smem_addr(&S.full[j - 1]), 0, p.wait_limit_ns);
+      if (!p.early_prefetch || j > 0) {
+        const int slot = __ldg(p.slot_idx + n);
+        S.info[j][0] = slot;
+        if (active(slot) && !S.info[j][3]) {
+          mbar_arrive_expect_tx(smem_addr(&S.full[j]), in_bytes);
+          load_slot_parts(j, h, slot);
+        }
+      }
+      mbar_arrive(smem_addr(&S.ready[j]));
+      if (S.info[j][3]) continue;  // withheld (wait-path test): never signalled
+      if (active(S.info[j][0]))
+        load_token_parts(j, n, h);
       else
         mbar_arrive(smem_addr(&S.full[j]));  // padding row: nothing to stream
     }
 
-    int next_slot = (unit < p.total_units) ? __ldg(p.slot_idx + unit / p.H) : 0;
-    for (; unit < p.total_units; unit += G, ++it) {
+    // Steady state: the next unit and its slot are fetched one step ahead.
+    int next = (it == kStages) ? next_unit() : -1;
+    int next_slot = next >= 0 ? __ldg(p.slot_idx + next / p.H) : 0;
+    bool ok = true;
+    for (; next >= 0; ++it) {
+      const int unit = next, slot = next_slot;
+      next = next_unit();
+      next_slot = next >= 0 ? __ldg(p.slot_idx + next / p.H) : 0;
       const int stage = it % kStages;
       const int n = unit / p.H, h = unit - n * p.H;
-      const int slot = next_slot;
-      if (unit + G < p.total_units) next_slot = __ldg(p.slot_idx + (unit + G) / p.H);
-      if (it >= kStages) {
-        // Stage reuse: the consumers must have released the previous unit
-        // in this stage; write its tile back, and let the copy engine finish
-        // reading it before the stage is refilled.
-        if (!mbar_wait_bounded(smem_addr(&S.done[stage]), ((it / kStages) - 1) & 1, p.wait_limit_ns)) {
-          flag_error(p, KDA_DEVERR_TIMEOUT);
-          S.abort = 1;
-          break;
-        }
-        const int* prev = S.info[stage];
-        if (prev[0] > 0 && prev[0] < p.num_slots) {
-          float* dst = p.state + (static_cast<int64_t>(prev[0]) * p.H + prev[2]) * (kDim * kDim);
-          bulk_store(dst, smem_addr(S.tile[stage]), kTileBytes, policy);
-          bulk_commit();
-        }
-        bulk_wait_read_all();
+      // Stage reuse: the consumers must have released the previous unit in
+      // this stage; write its tile back and let the copy engine finish
+      // reading it before the stage is refilled.
+      if (!mbar_wait_bounded(smem_addr(&S.done[stage]), ((it / kStages) - 1) & 1, p.wait_limit_ns)) {
+        ok = false;
+        break;
       }
+      store_stage(stage);
+      bulk_wait_read_all();
       S.info[stage][0] = slot;
       S.info[stage][1] = n;
       S.info[stage][2] = h;
-      S.info[stage][3] = 0;
-      if (unit == p.withhold_unit) continue;  // wait-path test: never signalled
-      if (slot > 0 && slot < p.num_slots) {
+      S.info[stage][3] = (unit == p.withhold_unit);
+      mbar_arrive(smem_addr(&S.ready[stage]));
+      if (S.info[stage][3]) continue;  // withheld (wait-path test): never signalled
+      if (active(slot)) {
         mbar_arrive_expect_tx(smem_addr(&S.full[stage]), in_bytes);
         load_slot_parts(stage, h, slot);
         load_token_parts(stage, n, h);
       } else {
-        mbar_arrive(smem_addr(&S.full[stage]));  // padding or out-of-range row: nothing to stream
+        mbar_arrive(smem_addr(&S.full[stage]));  // padding or out-of-range row
+      }
+    }
+    // End of work: the consumers find n = -1 in the next stage they read.
+    if (ok) {
+      const int stage = it % kStages;
+      if (it >= kStages) {
+        ok = mbar_wait_bounded(smem_addr(&S.done[stage]), ((it / kStages) - 1) & 1, p.wait_limit_ns);
+        if (ok) store_stage(stage);
+      }
+      if (ok) {
+        bulk_wait_read_all();
+        S.info[stage][1] = -1;
+        mbar_arrive(smem_addr(&S.ready[stage]));
       }
     }
     // Drain: write back the units still held in the ring.
-    const int first = it > kStages ? it - kStages : 0;
-    for (int j = first; j < it && !S.abort; ++j) {
+    for (int j = it > kStages - 1 ? it - kStages + 1 : 0; ok && j < it; ++j) {
       const int stage = j % kStages;
-      if (!mbar_wait_bounded(smem_addr(&S.done[stage]), (j / kStages) & 1, p.wait_limit_ns)) {
-        flag_error(p, KDA_DEVERR_TIMEOUT);
-        break;
-      }
-      const int* prev = S.info[stage];
-      if (prev[0] > 0 && prev[0] < p.num_slots) {
-        float* dst = p.state + (static_cast<int64_t>(prev[0]) * p.H + prev[2]) * (kDim * kDim);
-        bulk_store(dst, smem_addr(S.tile[stage]), kTileBytes, policy);
-        bulk_commit();
-      }
+      ok = mbar_wait_bounded(smem_addr(&S.done[stage]), (j / kStages) & 1, p.wait_limit_ns);
+      if (ok) store_stage(stage);
+    }
+    if (!ok) {
+      flag_error(p, KDA_DEVERR_TIMEOUT);
+      S.abort = 1;
     }
     // Before the CTA's shared memory goes away: every load this thread armed
     // has landed (normally long since) and every store has completed.
     for (int j = it > kStages ? it - kStages : 0; j < it; ++j) {
       const int stage = j % kStages;
-      if (!mbar_wait_bounded(smem_addr(&S.full[stage]), (j / kStages) & 1, p.wait_limit_ns)) flag_error(p, KDA_DEVERR_TIMEOUT);
+      if (!mbar_wait_bounded(smem_addr(&S.full[stage]), (j / kStages) & 1, p.wait_limit_ns))
+        flag_error(p, KDA_DEVERR_TIMEOUT);
     }
     bulk_wait_all();
+    // The last CTA to finish returns the work queue to zero for the next call.
+    if (p.queue != nullptr) {
+      __threadfence();
+      if (atomicAdd(p.queue + 1, 1) == G - 1) {
+        atomicExch(p.queue, 0);
+        atomicExch(p.queue + 1, 0);
+      }
+    }
     return;
   }
 
@@ -355,10 +410,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
   griddep_wait();
   const float scale = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
   const float nw = (kOutNorm && tid < kDim) ? __ldg(p.norm_w + tid) : 0.0f;
-  int it = 0;
-  for (int unit = blockIdx.x; unit < p.total_units; unit += G, ++it) {
+  for (int it = 0;; ++it) {
     const int stage = it % kStages;
-    const int n = unit / p.H, h = unit - n * p.H;
+    const uint32_t parity = (it / kStages) & 1;
+    // Which unit is next (all consumers agree; also the barrier that guards the scratch).
+    const bool have_info = mbar_wait_bounded(smem_addr(&S.ready[stage]), parity, p.wait_limit_ns);
+    if (consumer_any(!have_info || S.abort)) {
+      if (tid == 0) {
+        flag_error(p, KDA_DEVERR_TIMEOUT);
+        S.abort = 1;
+      }
+      break;
+    }
+    const int n = S.info[stage][1], h = S.info[stage][2];
+    if (n < 0) break;  // no more units
 
     // Per-unit inputs that do not depend on the slot: read while the tile streams.
     float wq[kWidth], wv[kWidth];
@@ -387,8 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       }
     }
 
-    const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), (it / kStages) & 1, p.wait_limit_ns);
-    // All consumers agree (this is also the barrier that guards the scratch).
+    const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), parity, p.wait_limit_ns);
     if (consumer_any(!ok || S.abort)) {
       if (tid == 0) {
         flag_error(p, KDA_DEVERR_TIMEOUT);
@@ -678,6 +742,7 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
   if (fused_gate && ((reinterpret_cast<uintptr_t>(a->A_log) & 3u) ||
                      (reinterpret_cast<uintptr_t>(a->dt_bias) & 3u)))
     return fail(KDA_ERR_ALIGN, "A_log and dt_bias must be 4-byte aligned");
+  if (reinterpret_cast<uintptr_t>(a->work_queue) & 3u) return fail(KDA_ERR_ALIGN, "work_queue must be 4-byte aligned");
   const int64_t D = static_cast<int64_t>(a->H) * KDA_HEAD_DIM;
   if (static_cast<int64_t>(a->N) * a->H > (1LL << 30))
     return fail(KDA_ERR_SHAPE, "N*H = %lld exceeds the grid limit", static_cast<long long>(a->N) * a->H);
@@ -718,6 +783,7 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
   p.A_log = fused_gate ? a->A_log : nullptr;
   p.dt_bias = fused_gate ? a->dt_bias : nullptr;
   p.lower_bound = a->lower_bound;
+  p.queue = a->work_queue;
   p.withhold_unit = withhold_unit;
   p.wait_limit_ns = wait_limit_ns;
 

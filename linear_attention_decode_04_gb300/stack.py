@@ -51,12 +51,24 @@ class DecodeStack:
         if len(set(ptrs)) != len(ptrs):
             raise ValueError("every layer needs its own state pool")
         early = len(layers) > 1
+        # The dynamic schedule (work queue) pays off for long launches, where
+        # per-SM bandwidth differences add up; for short ones the static
+        # schedule, whose first units stream in while the previous layer
+        # drains, is faster (measured on GB300: about 20 units per SM is
+        # short, about 160 long).  One queue serves every layer: the launches
+        # are ordered on one stream and each touches the queue only after the
+        # previous one ended.
+        dev = layers[0]["state"].device
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        units = max(int(L["qkv"].shape[0]) * int(L["state"].shape[1]) for L in layers)
+        self.queue = (torch.zeros(2, dtype=torch.int32, device=dev) if units >= 64 * sms else None)
         self.calls = [
             KdaDecodeCall(L["qkv"], L["conv_weight"], L["conv_state"], L["state"], L["g"], L["beta"],
                           L["slot_idx"], L["out"], gate=L.get("gate"),
                           norm_weight=L.get("norm_weight"), conv_bias=L.get("conv_bias"), eps=eps,
                           out_norm=out_norm, update_conv_state=update_conv_state,
-                          err_flag=L.get("err_flag"), early_prefetch=early)
+                          err_flag=L.get("err_flag"), early_prefetch=early,
+                          work_queue=self.queue)
             for L in layers
         ]
         self.graph: torch.cuda.CUDAGraph | None = None

@@ -55,13 +55,14 @@ def to_device(x: W.Inputs, device, out_row_pad: int = 0, gate_row_pad: int = 0) 
 
 
 def run_gpu(x: W.Inputs, d: dict, out_norm=None, update_conv_state=None, q_scale=0.0,
-            early_prefetch=False):
+            early_prefetch=False, work_queue=None):
     out_norm = x.spec.out_norm if out_norm is None else out_norm
     upd = x.spec.update_conv_state if update_conv_state is None else update_conv_state
     kda_decode(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
                d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"],
                conv_bias=d["conv_bias"], eps=x.spec.eps, q_scale=q_scale, out_norm=out_norm,
-               update_conv_state=upd, err_flag=d["err_flag"], early_prefetch=early_prefetch)
+               update_conv_state=upd, err_flag=d["err_flag"], early_prefetch=early_prefetch,
+               work_queue=work_queue)
 
 
 def run_oracle(x: W.Inputs, out_norm=None, update_conv_state=None, q_scale=0.0, in_place=False):

@@ -16,13 +16,16 @@ from linear_attention_decode_04_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _check(x, dev, early_prefetch=False, **kw):
+def _check(x, dev, early_prefetch=False, queue=False, **kw):
     d = T.to_device(x, dev)
-    T.run_gpu(x, d, early_prefetch=early_prefetch, **kw)
+    wq = torch.zeros(2, dtype=torch.int32, device=dev) if queue else None
+    T.run_gpu(x, d, early_prefetch=early_prefetch, work_queue=wq, **kw)
     torch.cuda.synchronize()
     ref = T.run_oracle(x, **kw)
     res = T.compare_all(x, d, ref, init_state=x.state, init_conv=x.conv_state)
     assert int(d["err_flag"].item()) == 0
+    if queue:
+        assert wq.tolist() == [0, 0], "work queue not returned to zero"
     return res
 
 
@@ -42,11 +45,18 @@ def test_flag_combinations(out_norm, update_conv_state, cuda_device):
 
 
 @pytest.mark.parametrize("name", list(W.SPECS))
-def test_workload_parity_early_prefetch(name, cuda_device):
+@pytest.mark.parametrize("queue", [False, True])
+def test_workload_parity_early_prefetch(name, queue, cuda_device):
     """Same results with KDA_EARLY_PREFETCH (state streamed before the
     previous kernel on the stream completes; nothing before it writes the
-    pools here)."""
-    _check(W.make_inputs(W.SPECS[name]), cuda_device, early_prefetch=True)
+    pools here), with the static and the work-queue schedule; the queue is
+    zero again afterwards."""
+    _check(W.make_inputs(W.SPECS[name]), cuda_device, early_prefetch=True, queue=queue)
+
+
+@pytest.mark.parametrize("name", list(W.SPECS))
+def test_workload_parity_work_queue(name, cuda_device):
+    _check(W.make_inputs(W.SPECS[name]), cuda_device, queue=True)
 
 
 def test_back_to_back_same_pool_in_one_graph(cuda_device):
@@ -60,6 +70,7 @@ def test_back_to_back_same_pool_in_one_graph(cuda_device):
     d = T.to_device(x, cuda_device)
     steps = [W.draw_step_inputs(spec, v) for v in range(3)]
     dev_steps, calls = [], []
+    queue = torch.zeros(2, dtype=torch.int32, device=cuda_device)
     for st in steps:
         ds = dict(qkv=T.bf16_tensor(st["qkv"], cuda_device), g=torch.from_numpy(st["g"]).to(cuda_device),
                   beta=T.bf16_tensor(st["beta"], cuda_device), gate=T.bf16_tensor(st["gate"], cuda_device),
@@ -67,7 +78,8 @@ def test_back_to_back_same_pool_in_one_graph(cuda_device):
         dev_steps.append(ds)
         calls.append(KdaDecodeCall(ds["qkv"], d["conv_weight"], d["conv_state"], d["state"], ds["g"],
                                    ds["beta"], d["slot_idx"], ds["out"], gate=ds["gate"],
-                                   norm_weight=d["norm_weight"], eps=spec.eps, err_flag=d["err_flag"]))
+                                   norm_weight=d["norm_weight"], eps=spec.eps, err_flag=d["err_flag"],
+                                   work_queue=queue))
     warm_up(cuda_device)
     s = torch.cuda.Stream(cuda_device)
     g = torch.cuda.CUDAGraph()
@@ -87,6 +99,7 @@ def test_back_to_back_same_pool_in_one_graph(cuda_device):
     for sl in range(spec.num_slots):
         T.check_state_slot(d["state"][sl].cpu().numpy(), stt[sl], f"slot {sl}")
     assert int(d["err_flag"].item()) == 0
+    assert queue.tolist() == [0, 0]
 
 
 @pytest.mark.parametrize("H", [12, 24, 48, 96, 5])
@@ -193,7 +206,8 @@ def test_binding_rejects_cpu_and_bad_shapes(cuda_device):
 
 
 @pytest.mark.parametrize("early_prefetch", [False, True])
-def test_bounded_wait_runs_out_and_reports(early_prefetch, cuda_device):
+@pytest.mark.parametrize("queue", [False, True])
+def test_bounded_wait_runs_out_and_reports(early_prefetch, queue, cuda_device):
     """Failure path without a GPU fault: one unit's load is never signalled
     and the waits are limited to 20 ms.  The launch must return (no hang, no
     trap) with KDA_DEVERR_TIMEOUT set, and the context must stay usable: a
@@ -202,12 +216,17 @@ def test_bounded_wait_runs_out_and_reports(early_prefetch, cuda_device):
     from linear_attention_decode_04_gb300.binding import KDA_DEVERR_TIMEOUT
     x = W.make_inputs(W.Spec("waittest_n40_h24_pool48", N=40, H=24, num_slots=48, seed=51, pad_tail=2))
     d = T.to_device(x, cuda_device)
+    wq = torch.zeros(2, dtype=torch.int32, device=cuda_device) if queue else None
     call = KdaDecodeCall(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
                          d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"],
-                         eps=x.spec.eps, err_flag=d["err_flag"], early_prefetch=early_prefetch)
-    call.wait_test(20_000_000, withhold_unit=0)
+                         eps=x.spec.eps, err_flag=d["err_flag"], early_prefetch=early_prefetch,
+                         work_queue=wq)
+    # withhold a static unit, or (with the queue) one handed out dynamically
+    call.wait_test(20_000_000, withhold_unit=0 if not queue else x.N * x.H - 5)
     torch.cuda.synchronize()
     assert int(d["err_flag"].item()) & KDA_DEVERR_TIMEOUT
+    if queue:
+        assert wq.tolist() == [0, 0], "work queue not reset after the aborted launch"
     # the context is intact: a fresh problem decodes correctly
     _check(W.make_inputs(W.PAD_TAIL), cuda_device)
 
