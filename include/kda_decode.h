@@ -155,6 +155,29 @@ int kda_decode(const KdaDecodeArgs* args, void* stream);
 int kda_decode_wait_test(const KdaDecodeArgs* args, void* stream, uint64_t wait_limit_ns,
                          int32_t withhold_unit);
 
+/*
+ * kda_decode_noalloc: the same decode step for callers that cannot allocate
+ * device memory (no counterpart on the page; it exists for integration).
+ * Code that enqueues work while a CUDA graph is being captured (cudaMalloc
+ * synchronises the device and is not a stream operation), plugin interfaces
+ * whose enqueue step must not allocate, and serving loops with a memory
+ * budget fixed at start-up cannot hand the kernel a work queue of their own.
+ * This entry point runs the dynamic schedule with the queue kept in a
+ * file-scope device array of 256 bytes inside the library (every GPU that
+ * loads the library holds it until the process exits; one call uses 8 bytes,
+ * a fixed need whatever N and H, and a larger need would be rejected with
+ * KDA_ERR_SHAPE).  args->work_queue is ignored.  The caller still passes all
+ * inputs and outputs.  It allocates nothing: it calls no cudaMalloc,
+ * cudaFree or allocating library routine.  Each call first clears the queue
+ * with an asynchronous memset on `stream`, then launches as kda_decode.
+ * Every call shares the one array: calls that overlap on the GPU (other
+ * streams, other host threads) race on it and give wrong results; calls
+ * ordered on one stream are safe.  The first call on a device looks up the
+ * array's device address (and does kda_decode's once-per-device set-up);
+ * make that first call before any stream capture on that device.
+ */
+int kda_decode_noalloc(const KdaDecodeArgs* args, void* stream);
+
 /* Static text for a KDA_* return code. */
 const char* kda_status_string(int status);
 

@@ -798,3 +798,60 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
   return KDA_OK;
 }
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot allocate device memory for the work queue: code that
+// enqueues work while a CUDA graph is being captured (cudaMalloc is not a
+// stream operation and synchronises the device), plugin interfaces whose
+// enqueue step must not allocate, and serving loops that fix their memory
+// budget at start-up.  kda_decode_noalloc serves them with the dynamic
+// schedule, keeping the queue in this file-scope device array instead of a
+// caller-provided buffer.  Every GPU that loads the library holds the array
+// until the process exits.
+namespace {
+constexpr size_t kNoAllocScratchBytes = 256;                    // stated maximum
+constexpr size_t kNoAllocQueueBytes = 2 * sizeof(int32_t);      // what one call uses
+}  // namespace
+
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
+
+namespace {
+int32_t* g_noalloc_ptr[64];  // device address of g_noalloc_scratch per device (guarded by g_dev_mutex)
+}  // namespace
+
+extern "C" int kda_decode_noalloc(const KdaDecodeArgs* a, void* stream) {
+  g_last_error[0] = '\0';
+  if (!a) return fail(KDA_ERR_NULLPTR, "args is NULL");
+  if (a->struct_size != sizeof(KdaDecodeArgs))
+    return fail(KDA_ERR_ABI, "struct_size %u, library expects %zu", a->struct_size, sizeof(KdaDecodeArgs));
+  if (kNoAllocQueueBytes > kNoAllocScratchBytes)
+    return fail(KDA_ERR_SHAPE, "needs %zu bytes of scratch, the static array holds %zu", kNoAllocQueueBytes,
+                kNoAllocScratchBytes);
+  if (a->N == 0) return decode_impl(a, stream, kWaitLimitNs, -1);
+  // Once per device, with that device current: the array's device address
+  // (in host code the array's name is only a stand-in, never a pointer the
+  // kernel can use).
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(KDA_ERR_LAUNCH, "device ordinal %d out of range", dev);
+  int32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_noalloc_ptr[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      g_noalloc_ptr[dev] = static_cast<int32_t*>(ptr);
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // The queue must start at zero; the array keeps whatever the last call left.
+  e = cudaMemsetAsync(scratch, 0, kNoAllocQueueBytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "clearing the scratch: %s", cudaGetErrorString(e));
+  KdaDecodeArgs b = *a;
+  b.work_queue = scratch;
+  return decode_impl(&b, stream, kWaitLimitNs, -1);
+}
