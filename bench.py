@@ -36,7 +36,7 @@ UNIT = "updates/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "kda_decode_stack69_traffic.md")
-KERNEL_SRC = os.path.join(ROOT, "linear_attention_decode_04_gb300", "csrc", "kda_decode.cu")
+KERNEL_SRC = os.path.join(ROOT, "linear_attention_decode_04_gb300", "csrc", "kda_decode_kernel.cuh")
 
 
 # ----------------------------------------------------------------- host logic

@@ -1,0 +1,607 @@
+// kda_decode_kernel.cuh -- device code of the fused KDA decode step
+// (sm_103a): constants, parameter block, PTX wrappers and the persistent
+// kernel.  Included once, by kda_decode.cu, which holds the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kda_decode.h"
+
+namespace {
+
+constexpr int kDim = 128;                      // key = value head dim
+constexpr int kWidth = 4;                      // conv taps
+constexpr int kStages = 3;                     // state tiles in flight per CTA
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;  // 256 math threads
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
+constexpr int kRowsPerWarp = kDim / kConsumerWarps;  // 16 key rows per consumer warp
+constexpr uint32_t kTileBytes = kDim * kDim * 4;           // 64 KiB fp32 state tile
+constexpr uint32_t kCsSliceBytes = kDim * (kWidth - 1) * 2;  // 768 B conv state per block
+constexpr uint32_t kXSliceBytes = kDim * 2;                  // 256 B qkv per block
+constexpr int kCsU4 = kCsSliceBytes / 16;                    // 48
+constexpr uint64_t kWaitLimitNs = 2000000000ull;             // bounded waits: 2 s by default
+
+struct Params {
+  const uint16_t* qkv;
+  int64_t qkv_stride;
+  const float* conv_w;
+  const float* conv_b;
+  uint16_t* conv_state;
+  float* state;
+  const float* g;
+  const uint16_t* beta;
+  const uint16_t* gate;
+  int64_t gate_stride;
+  const float* norm_w;
+  const int32_t* slot_idx;
+  uint16_t* out;
+  int64_t out_stride;
+  int N, H, num_slots;
+  int total_units;  // N * H
+  int early_prefetch;  // KDA_EARLY_PREFETCH
+  int fused_gate;      // KDA_FUSED_GATE: g / beta are raw logits
+  const float* A_log;
+  const float* dt_bias;
+  float lower_bound;
+  int* queue;          // work queue int32[2] (next dynamic unit, finished CTAs) or null
+  int withhold_unit;   // wait-path test: this unit's load is never signalled (-1: none)
+  uint64_t wait_limit_ns;
+  float eps, q_scale;
+  int32_t* err;
+};
+
+// Dynamic shared memory of one CTA (about 214 KB): the staged tiles and the
+// per-unit inputs for kStages units, plus the consumers' scratch.
+struct __align__(128) Smem {
+  float tile[kStages][kDim * kDim];
+  uint16_t cs[kStages][3][kDim * (kWidth - 1)];
+  uint16_t x[kStages][3][kDim];
+  float g[kStages][kDim];
+  uint16_t gate[kStages][kDim];
+  float q[kDim], k[kDim], v[kDim], alpha[kDim];
+  float red[2][kConsumerWarps][kDim];
+  float delta[kDim];
+  float sum[4][4];
+  int info[kStages][4];           // slot, n (-1: no more units), h, withheld
+  unsigned long long ready[kStages];  // info of the stage is written
+  unsigned long long full[kStages];
+  unsigned long long done[kStages];
+  volatile int abort;
+};
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---- PTX wrappers: mbarrier, bulk async copies (TMA engine), barriers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Shared -> global bulk copy tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+               "r"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier 1 among the consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// Consumer-wide OR of a predicate (also a barrier).
+__device__ __forceinline__ int consumer_any(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 2, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "n"(kConsumers)
+      : "memory");
+  return r;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream be
+// scheduled now, and wait for the previous one to complete (with its memory
+// visible) before touching anything it may have written.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void flag_error(const Params& p, int bits) {
+  if (p.err) atomicOr(p.err, bits);
+}
+
+// Persistent kernel, one CTA per SM.  A unit is one (row n, head h) =
+// unit index n*H + h.  Each CTA takes its first kStages units statically
+// (blockIdx.x + k*gridDim.x, so they can be prefetched before the previous
+// kernel finishes); the rest come from the work queue when one is given
+// (an atomic counter: CTAs that run ahead take more units, so every CTA
+// finishes at nearly the same time), else continue the static stride.
+// Warp 8 is the producer: for each unit it publishes (slot, n, h) on the
+// stage's `ready` barrier, streams the 64 KiB state tile and the unit's small
+// inputs into the stage with bulk copies (`full` barrier), and once the
+// consumers release the stage (`done`) streams the updated tile back out.
+// Warps 0-7 compute.  Two tiles stream in while the consumers work on a third.
+template <bool kOutNorm, bool kUpdateConv>
+__global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x;
+  const int64_t D = static_cast<int64_t>(p.H) * kDim;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&S.ready[s]), 1);
+      mbar_init(smem_addr(&S.full[s]), 1);
+      mbar_init(smem_addr(&S.done[s]), kConsumerWarps);
+    }
+    S.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  griddep_launch_dependents();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint64_t policy = l2_evict_first_policy();
+    const uint32_t in_bytes = kTileBytes + 3 * kCsSliceBytes + 3 * kXSliceBytes + kDim * 4 +
+                              (kOutNorm ? kXSliceBytes : 0);
+    // Slot-indexed inputs of a unit: its state tile and conv-state slices.
+    auto load_slot_parts = [&](int stage, int h, int slot) {
+      const uint32_t full = smem_addr(&S.full[stage]);
+      bulk_load(smem_addr(S.tile[stage]), p.state + (static_cast<int64_t>(slot) * p.H + h) * (kDim * kDim),
+                kTileBytes, full, policy);
+      for (int c = 0; c < 3; ++c)
+        bulk_load(smem_addr(S.cs[stage][c]),
+                  p.conv_state +
+                      (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1),
+                  kCsSliceBytes, full, policy);
+    };
+    // Per-token inputs of a unit: qkv slices, g row, gate row.
+    auto load_token_parts = [&](int stage, int n, int h) {
+      const uint32_t full = smem_addr(&S.full[stage]);
+      for (int c = 0; c < 3; ++c)
+        bulk_load(smem_addr(S.x[stage][c]), p.qkv + n * p.qkv_stride + c * D + static_cast<int64_t>(h) * kDim,
+                  kXSliceBytes, full, policy);
+      bulk_load(smem_addr(S.g[stage]), p.g + (static_cast<int64_t>(n) * p.H + h) * kDim, kDim * 4, full, policy);
+      if (kOutNorm)
+        bulk_load(smem_addr(S.gate[stage]), p.gate + n * p.gate_stride + static_cast<int64_t>(h) * kDim,
+                  kXSliceBytes, full, policy);
+    };
+    auto active = [&](int slot) { return slot > 0 && slot < p.num_slots; };
+    // Write the stage's tile back if it held an active unit.
+    auto store_stage = [&](int stage) {
+      const int* prev = S.info[stage];
+      if (active(prev[0])) {
+        float* dst = p.state + (static_cast<int64_t>(prev[0]) * p.H + prev[2]) * (kDim * kDim);
+        bulk_store(dst, smem_addr(S.tile[stage]), kTileBytes, policy);
+        bulk_commit();
+      }
+    };
+    int k_static = 0;  // static units taken so far
+    auto next_unit = [&]() -> int {
+      int u;
+      if (k_static < kStages || p.queue == nullptr)
+        u = blockIdx.x + (k_static++) * G;
+      else
+        u = kStages * G + atomicAdd(p.queue, 1);
+      return u < p.total_units ? u : -1;
+    };
+
+    // First ring: static units.  With KDA_EARLY_PREFETCH the first unit's
+    // state streams in before the previous kernel in the stream has finished
+    // (the caller guarantees that kernel does not write the slot indices,
+    // the state or the conv state); everything per-token waits for it.  The
+    // ring then fills one stage at a time (each stage once the one before
+    // it has landed), so that the first tile of every CTA arrives early
+    // instead of all CTAs' three tiles arriving together.
+    int it = 0;
+    for (; it < kStages; ++it) {
+      const int u = next_unit();
+      if (u < 0) break;
+      const int n = u / p.H, h = u - n * p.H;
+      S.info[it][1] = n;
+      S.info[it][2] = h;
+      S.info[it][3] = (u == p.withhold_unit);
+      if (p.early_prefetch && it == 0) {
+        const int slot = __ldg(p.slot_idx + n);
+        S.info[it][0] = slot;
+        if (active(slot) && !S.info[it][3]) {
+          mbar_arrive_expect_tx(smem_addr(&S.full[it]), in_bytes);
+          load_slot_parts(it, h, slot);
+        }
+      }
+    }
+    griddep_wait();
+    for (int j = 0; j < it; ++j) {
+      const int n = S.info[j][1], h = S.info[j][2];
+      if (j > 0 && !S.info[j - 1][3]) mbar_wait_bounded(smem_addr(&S.full[j - 1]), 0, p.wait_limit_ns);
+      if (!p.early_prefetch || j > 0) {
+        const int slot = __ldg(p.slot_idx + n);
+        S.info[j][0] = slot;
+        if (active(slot) && !S.info[j][3]) {
+          mbar_arrive_expect_tx(smem_addr(&S.full[j]), in_bytes);
+          load_slot_parts(j, h, slot);
+        }
+      }
+      mbar_arrive(smem_addr(&S.ready[j]));
+      if (S.info[j][3]) continue;  // withheld (wait-path test): never signalled
+      if (active(S.info[j][0]))
+        load_token_parts(j, n, h);
+      else
+        mbar_arrive(smem_addr(&S.full[j]));  // padding row: nothing to stream
+    }
+
+    // Steady state: the next unit and its slot are fetched one step ahead.
+    int next = (it == kStages) ? next_unit() : -1;
+    int next_slot = next >= 0 ? __ldg(p.slot_idx + next / p.H) : 0;
+    bool ok = true;
+    for (; next >= 0; ++it) {
+      const int unit = next, slot = next_slot;
+      next = next_unit();
+      next_slot = next >= 0 ? __ldg(p.slot_idx + next / p.H) : 0;
+      const int stage = it % kStages;
+      const int n = unit / p.H, h = unit - n * p.H;
+      // Stage reuse: the consumers must have released the previous unit in
+      // this stage; write its tile back and let the copy engine finish
+      // reading it before the stage is refilled.
+      if (!mbar_wait_bounded(smem_addr(&S.done[stage]), ((it / kStages) - 1) & 1, p.wait_limit_ns)) {
+        ok = false;
+        break;
+      }
+      store_stage(stage);
+      bulk_wait_read_all();
+      S.info[stage][0] = slot;
+      S.info[stage][1] = n;
+      S.info[stage][2] = h;
+      S.info[stage][3] = (unit == p.withhold_unit);
+      mbar_arrive(smem_addr(&S.ready[stage]));
+      if (S.info[stage][3]) continue;  // withheld (wait-path test): never signalled
+      if (active(slot)) {
+        mbar_arrive_expect_tx(smem_addr(&S.full[stage]), in_bytes);
+        load_slot_parts(stage, h, slot);
+        load_token_parts(stage, n, h);
+      } else {
+        mbar_arrive(smem_addr(&S.full[stage]));  // padding or out-of-range row
+      }
+    }
+    // End of work: the consumers find n = -1 in the next stage they read.
+    if (ok) {
+      const int stage = it % kStages;
+      if (it >= kStages) {
+        ok = mbar_wait_bounded(smem_addr(&S.done[stage]), ((it / kStages) - 1) & 1, p.wait_limit_ns);
+        if (ok) store_stage(stage);
+      }
+      if (ok) {
+        bulk_wait_read_all();
+        S.info[stage][1] = -1;
+        mbar_arrive(smem_addr(&S.ready[stage]));
+      }
+    }
+    // Drain: write back the units still held in the ring.
+    for (int j = it > kStages - 1 ? it - kStages + 1 : 0; ok && j < it; ++j) {
+      const int stage = j % kStages;
+      ok = mbar_wait_bounded(smem_addr(&S.done[stage]), (j / kStages) & 1, p.wait_limit_ns);
+      if (ok) store_stage(stage);
+    }
+    if (!ok) {
+      flag_error(p, KDA_DEVERR_TIMEOUT);
+      S.abort = 1;
+    }
+    // Before the CTA's shared memory goes away: every load this thread armed
+    // has landed (normally long since) and every store has completed.
+    for (int j = it > kStages ? it - kStages : 0; j < it; ++j) {
+      const int stage = j % kStages;
+      if (!mbar_wait_bounded(smem_addr(&S.full[stage]), (j / kStages) & 1, p.wait_limit_ns))
+        flag_error(p, KDA_DEVERR_TIMEOUT);
+    }
+    bulk_wait_all();
+    // The last CTA to finish returns the work queue to zero for the next call.
+    if (p.queue != nullptr) {
+      __threadfence();
+      if (atomicAdd(p.queue + 1, 1) == G - 1) {
+        atomicExch(p.queue, 0);
+        atomicExch(p.queue + 1, 0);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  griddep_wait();
+  const float scale = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
+  const float nw = (kOutNorm && tid < kDim) ? __ldg(p.norm_w + tid) : 0.0f;
+  for (int it = 0;; ++it) {
+    const int stage = it % kStages;
+    const uint32_t parity = (it / kStages) & 1;
+    // Which unit is next (all consumers agree; also the barrier that guards the scratch).
+    const bool have_info = mbar_wait_bounded(smem_addr(&S.ready[stage]), parity, p.wait_limit_ns);
+    if (consumer_any(!have_info || S.abort)) {
+      if (tid == 0) {
+        flag_error(p, KDA_DEVERR_TIMEOUT);
+        S.abort = 1;
+      }
+      break;
+    }
+    const int n = S.info[stage][1], h = S.info[stage][2];
+    if (n < 0) break;  // no more units
+
+    // Per-unit inputs that do not depend on the slot: read while the tile streams.
+    float wq[kWidth], wv[kWidth];
+    float bq = 0.0f, bv = 0.0f;
+    {
+      const int c = tid >> 7, j = tid & (kDim - 1);  // channel tid: q (tid<128) or k
+      const float* w = p.conv_w + c * kWidth * D + static_cast<int64_t>(h) * kDim + j;
+#pragma unroll
+      for (int t = 0; t < kWidth; ++t) wq[t] = __ldg(w + t * D);
+      if (p.conv_b) bq = __ldg(p.conv_b + c * D + static_cast<int64_t>(h) * kDim + j);
+      if (tid < kDim) {  // second channel: v block
+        const float* w2 = p.conv_w + 2 * kWidth * D + static_cast<int64_t>(h) * kDim + j;
+#pragma unroll
+        for (int t = 0; t < kWidth; ++t) wv[t] = __ldg(w2 + t * D);
+        if (p.conv_b) bv = __ldg(p.conv_b + 2 * D + static_cast<int64_t>(h) * kDim + j);
+      }
+    }
+    float beta = (tid < kDim) ? bf16_to_f32(__ldg(p.beta + static_cast<int64_t>(n) * p.H + h)) : 0.0f;
+    float gate_a = 0.0f, gate_bias = 0.0f;  // exp(A_log[h]) and dt_bias for key channel tid-128
+    if (p.fused_gate) {
+      if (tid < kDim) {
+        beta = 1.0f / (1.0f + expf(-beta));
+      } else {
+        gate_a = expf(__ldg(p.A_log + h));
+        if (p.dt_bias) gate_bias = __ldg(p.dt_bias + static_cast<int64_t>(h) * kDim + (tid - kDim));
+      }
+    }
+
+    const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), parity, p.wait_limit_ns);
+    if (consumer_any(!ok || S.abort)) {
+      if (tid == 0) {
+        flag_error(p, KDA_DEVERR_TIMEOUT);
+        S.abort = 1;
+      }
+      break;
+    }
+    const int slot = S.info[stage][0];
+    uint16_t* out_row = p.out + n * p.out_stride + static_cast<int64_t>(h) * kDim;
+
+    // Padding rows (slot <= 0) write zeros and touch no state (P1 实现拆解
+    // item 1; kernel excerpt in 关键源码片段).
+    if (slot <= 0 || slot >= p.num_slots) {
+      if (tid < kDim * 2 / 16) reinterpret_cast<uint4*>(out_row)[tid] = make_uint4(0, 0, 0, 0);
+      if (slot >= p.num_slots && tid == 0) flag_error(p, KDA_DEVERR_SLOT_RANGE);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&S.done[stage]));
+      continue;
+    }
+
+    // Conv-state advance: drop the oldest tap, append the new input (a pure
+    // move of bf16 bit patterns).
+    if (kUpdateConv && tid < 3 * kCsU4) {
+      const int c = tid / kCsU4, e = tid - c * kCsU4;
+      uint16_t v8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int pos = e * 8 + t, j = pos / 3, k = pos - 3 * j;
+        v8[t] = (k < kWidth - 2) ? S.cs[stage][c][3 * j + k + 1] : S.x[stage][c][j];
+      }
+      uint4 w4;
+      w4.x = v8[0] | (static_cast<uint32_t>(v8[1]) << 16);
+      w4.y = v8[2] | (static_cast<uint32_t>(v8[3]) << 16);
+      w4.z = v8[4] | (static_cast<uint32_t>(v8[5]) << 16);
+      w4.w = v8[6] | (static_cast<uint32_t>(v8[7]) << 16);
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.conv_state + (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1));
+      dst[e] = w4;
+    }
+
+    // Conv (4 taps) + SiLU on the 384 q|k|v channels; decay alpha = exp(g).
+    {
+      const int c = tid >> 7, j = tid & (kDim - 1);
+      const uint16_t* cs = S.cs[stage][c] + 3 * j;
+      float y = bq;
+      y = fmaf(wq[0], bf16_to_f32(cs[0]), y);
+      y = fmaf(wq[1], bf16_to_f32(cs[1]), y);
+      y = fmaf(wq[2], bf16_to_f32(cs[2]), y);
+      y = fmaf(wq[3], bf16_to_f32(S.x[stage][c][j]), y);
+      (c == 0 ? S.q : S.k)[j] = y / (1.0f + expf(-y));
+      if (tid < kDim) {
+        const uint16_t* csv = S.cs[stage][2] + 3 * j;
+        float yv = bv;
+        yv = fmaf(wv[0], bf16_to_f32(csv[0]), yv);
+        yv = fmaf(wv[1], bf16_to_f32(csv[1]), yv);
+        yv = fmaf(wv[2], bf16_to_f32(csv[2]), yv);
+        yv = fmaf(wv[3], bf16_to_f32(S.x[stage][2][j]), yv);
+        S.v[j] = yv / (1.0f + expf(-yv));
+      } else {
+        float g = S.g[stage][j];
+        if (p.fused_gate) {
+          // Gate activation (the page's safe-gate variant; standard KDA form).
+          const float z = g + gate_bias;
+          if (p.lower_bound < 0.0f) {
+            g = p.lower_bound / (1.0f + expf(-gate_a * z));
+          } else {
+            const float sp = (z > 0.0f) ? z + log1pf(expf(-z)) : log1pf(expf(z));
+            g = -gate_a * sp;
+          }
+        }
+        S.alpha[j] = expf(g);
+      }
+    }
+    const float gate_j = (kOutNorm && tid < kDim) ? bf16_to_f32(S.gate[stage][tid]) : 0.0f;
+    consumer_sync();
+
+    // |q|^2, |k|^2, q.k in one pass.
+    if (tid < kDim) {
+      const float qv = S.q[tid], kv = S.k[tid];
+      const float sq = warp_sum(qv * qv), sk = warp_sum(kv * kv), sqk = warp_sum(qv * kv);
+      if (lane == 0) {
+        S.sum[warp][0] = sq;
+        S.sum[warp][1] = sk;
+        S.sum[warp][2] = sqk;
+      }
+    }
+    consumer_sync();
+    const float ssq = (S.sum[0][0] + S.sum[1][0]) + (S.sum[2][0] + S.sum[3][0]);
+    const float ssk = (S.sum[0][1] + S.sum[1][1]) + (S.sum[2][1] + S.sum[3][1]);
+    const float sqk = (S.sum[0][2] + S.sum[1][2]) + (S.sum[2][2] + S.sum[3][2]);
+    const float rq = scale / sqrtf(ssq + 1e-6f);
+    const float rk = 1.0f / sqrtf(ssk + 1e-6f);
+    const float qk = sqk * rq * rk;  // q^ . k^
+
+    // Decay the staged tile and form partial u = A^T k^, w = A^T q^ over this
+    // warp's 16 key rows (A = Diag(alpha) S, kept in registers).
+    const float4* tile4 = reinterpret_cast<const float4*>(S.tile[stage]);
+    float4 a[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int i = warp * kRowsPerWarp + r;
+      const float al = S.alpha[i], kh = S.k[i] * rk, qh = S.q[i] * rq;
+      a[r].x *= al; a[r].y *= al; a[r].z *= al; a[r].w *= al;
+      u.x = fmaf(kh, a[r].x, u.x); u.y = fmaf(kh, a[r].y, u.y);
+      u.z = fmaf(kh, a[r].z, u.z); u.w = fmaf(kh, a[r].w, u.w);
+      w.x = fmaf(qh, a[r].x, w.x); w.y = fmaf(qh, a[r].y, w.y);
+      w.z = fmaf(qh, a[r].z, w.z); w.w = fmaf(qh, a[r].w, w.w);
+    }
+    reinterpret_cast<float4*>(S.red[0][warp])[lane] = u;
+    reinterpret_cast<float4*>(S.red[1][warp])[lane] = w;
+    consumer_sync();
+
+    // delta_j = beta (v_j - u_j); readout of the updated state
+    // o = S'^T q^ = w + (q^ . k^) delta, with no second pass over S'.
+    float o = 0.0f;
+    if (tid < kDim) {
+      float uj = 0.0f, wj = 0.0f;
+#pragma unroll
+      for (int r = 0; r < kConsumerWarps; ++r) {
+        uj += S.red[0][r][tid];
+        wj += S.red[1][r][tid];
+      }
+      const float dj = beta * (S.v[tid] - uj);
+      S.delta[tid] = dj;
+      o = fmaf(qk, dj, wj);
+      if (kOutNorm) {
+        const float ss = warp_sum(o * o);
+        if (lane == 0) S.sum[warp][3] = ss;
+      }
+    }
+    consumer_sync();
+
+    // S' = A + k^ delta^T written back into the stage, then handed to the
+    // producer for the bulk store.
+    const float4 d = reinterpret_cast<const float4*>(S.delta)[lane];
+    float4* tile4w = reinterpret_cast<float4*>(S.tile[stage]);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int i = warp * kRowsPerWarp + r;
+      const float kh = S.k[i] * rk;
+      a[r].x = fmaf(kh, d.x, a[r].x); a[r].y = fmaf(kh, d.y, a[r].y);
+      a[r].z = fmaf(kh, d.z, a[r].z); a[r].w = fmaf(kh, d.w, a[r].w);
+      tile4w[i * 32 + lane] = a[r];
+    }
+    fence_proxy_async_smem();  // generic-proxy writes before the async-proxy store
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&S.done[stage]));
+
+    // Gated RMSNorm epilogue (or the raw readout) to bf16.
+    if (tid < kDim) {
+      float y = o;
+      if (kOutNorm) {
+        const float ss = (S.sum[0][3] + S.sum[1][3]) + (S.sum[2][3] + S.sum[3][3]);
+        const float rr = 1.0f / sqrtf(ss * (1.0f / kDim) + p.eps);
+        y = o * rr * nw * (1.0f / (1.0f + expf(-gate_j)));
+      }
+      out_row[tid] = f32_to_bf16(y);
+    }
+  }
+}
+
+}  // namespace
