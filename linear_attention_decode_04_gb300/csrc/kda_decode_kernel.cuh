@@ -194,6 +194,41 @@ __device__ __forceinline__ void flag_error(const Params& p, int bits) {
   if (p.err) atomicOr(p.err, bits);
 }
 
+// Slot-independent inputs one consumer thread needs for a unit: its conv
+// taps (thread tid: q channel tid or k channel tid-128, plus v channel tid
+// for tid < 128), conv biases, beta, and the gate parameters of key channel
+// tid-128 when the gate is fused.
+struct UnitInputs {
+  float wq[kWidth], wv[kWidth];
+  float bq, bv, beta, gate_a, gate_bias;
+};
+
+__device__ __forceinline__ UnitInputs load_unit_inputs(const Params& p, int n, int h, int tid, int64_t D) {
+  UnitInputs u;
+  u.bq = u.bv = u.beta = u.gate_a = u.gate_bias = 0.0f;
+  const int c = tid >> 7, j = tid & (kDim - 1);
+  const float* w = p.conv_w + c * kWidth * D + static_cast<int64_t>(h) * kDim + j;
+#pragma unroll
+  for (int t = 0; t < kWidth; ++t) u.wq[t] = __ldg(w + t * D);
+  if (p.conv_b) u.bq = __ldg(p.conv_b + c * D + static_cast<int64_t>(h) * kDim + j);
+  if (tid < kDim) {
+    const float* w2 = p.conv_w + 2 * kWidth * D + static_cast<int64_t>(h) * kDim + j;
+#pragma unroll
+    for (int t = 0; t < kWidth; ++t) u.wv[t] = __ldg(w2 + t * D);
+    if (p.conv_b) u.bv = __ldg(p.conv_b + 2 * D + static_cast<int64_t>(h) * kDim + j);
+    const float b = bf16_to_f32(__ldg(p.beta + static_cast<int64_t>(n) * p.H + h));
+    u.beta = p.fused_gate ? 1.0f / (1.0f + expf(-b)) : b;
+  } else {
+#pragma unroll
+    for (int t = 0; t < kWidth; ++t) u.wv[t] = 0.0f;
+    if (p.fused_gate) {
+      u.gate_a = expf(__ldg(p.A_log + h));
+      if (p.dt_bias) u.gate_bias = __ldg(p.dt_bias + static_cast<int64_t>(h) * kDim + j);
+    }
+  }
+  return u;
+}
+
 // Persistent kernel, one CTA per SM.  A unit is one (row n, head h) =
 // unit index n*H + h.  Each CTA takes its first kStages units statically
 // (blockIdx.x + k*gridDim.x, so they can be prefetched before the previous
@@ -397,6 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
   griddep_wait();
   const float scale = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
   const float nw = (kOutNorm && tid < kDim) ? __ldg(p.norm_w + tid) : 0.0f;
+  UnitInputs cur, nxt;
+  bool have_next = false;  // nxt holds the inputs of the coming unit
   for (int it = 0;; ++it) {
     const int stage = it % kStages;
     const uint32_t parity = (it / kStages) & 1;
@@ -412,32 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     const int n = S.info[stage][1], h = S.info[stage][2];
     if (n < 0) break;  // no more units
 
-    // Per-unit inputs that do not depend on the slot: read while the tile streams.
-    float wq[kWidth], wv[kWidth];
-    float bq = 0.0f, bv = 0.0f;
-    {
-      const int c = tid >> 7, j = tid & (kDim - 1);  // channel tid: q (tid<128) or k
-      const float* w = p.conv_w + c * kWidth * D + static_cast<int64_t>(h) * kDim + j;
-#pragma unroll
-      for (int t = 0; t < kWidth; ++t) wq[t] = __ldg(w + t * D);
-      if (p.conv_b) bq = __ldg(p.conv_b + c * D + static_cast<int64_t>(h) * kDim + j);
-      if (tid < kDim) {  // second channel: v block
-        const float* w2 = p.conv_w + 2 * kWidth * D + static_cast<int64_t>(h) * kDim + j;
-#pragma unroll
-        for (int t = 0; t < kWidth; ++t) wv[t] = __ldg(w2 + t * D);
-        if (p.conv_b) bv = __ldg(p.conv_b + 2 * D + static_cast<int64_t>(h) * kDim + j);
-      }
+    // Per-unit inputs that do not depend on the slot (conv weights, beta,
+    // gate parameters): usually prefetched while the previous unit computed.
+    if (have_next) {
+      cur = nxt;
+    } else {
+      cur = load_unit_inputs(p, n, h, tid, D);
     }
-    float beta = (tid < kDim) ? bf16_to_f32(__ldg(p.beta + static_cast<int64_t>(n) * p.H + h)) : 0.0f;
-    float gate_a = 0.0f, gate_bias = 0.0f;  // exp(A_log[h]) and dt_bias for key channel tid-128
-    if (p.fused_gate) {
-      if (tid < kDim) {
-        beta = 1.0f / (1.0f + expf(-beta));
-      } else {
-        gate_a = expf(__ldg(p.A_log + h));
-        if (p.dt_bias) gate_bias = __ldg(p.dt_bias + static_cast<int64_t>(h) * kDim + (tid - kDim));
-      }
-    }
+    have_next = false;
 
     const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), parity, p.wait_limit_ns);
     if (consumer_any(!ok || S.abort)) {
@@ -447,6 +466,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       }
       break;
     }
+    // If the next unit is already published, start loading its inputs now;
+    // they arrive while this unit computes.
+    {
+      const int s2 = (it + 1) % kStages;
+      if (mbar_try_wait(smem_addr(&S.ready[s2]), ((it + 1) / kStages) & 1)) {
+        const int n2 = S.info[s2][1], h2 = S.info[s2][2];
+        if (n2 >= 0) {
+          nxt = load_unit_inputs(p, n2, h2, tid, D);
+          have_next = true;
+        }
+      }
+    }
+    const float* wq = cur.wq;
+    const float* wv = cur.wv;
+    const float bq = cur.bq, bv = cur.bv, beta = cur.beta, gate_a = cur.gate_a, gate_bias = cur.gate_bias;
     const int slot = S.info[stage][0];
     uint16_t* out_row = p.out + n * p.out_stride + static_cast<int64_t>(h) * kDim;
 
