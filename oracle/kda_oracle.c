@@ -177,17 +177,22 @@ static int decode_unit(const kda_oracle_problem* p, int n, int h, double* work) 
     double* dst = (c == 0) ? qt : (c == 1) ? kt : vt;
     for (int j = 0; j < dim_c; ++j) {
       const int64_t ch = off_c + (int64_t)h * dim_c + j;
-      uint16_t* cs = p->conv_state + ((int64_t)s * C + ch) * (W - 1);
+      /* element (s, ch, t) of the conv state, in either layout */
+      uint16_t* cs0 = p->conv_state + (int64_t)s * C * (W - 1);
+      const int64_t cs_ch = p->conv_state_sd ? 1 : (W - 1);
+      const int64_t cs_t = p->conv_state_sd ? C : 1;
+#define CS(t) cs0[ch * cs_ch + (int64_t)(t) * cs_t]
       const uint16_t xin = p->qkv[(int64_t)n * p->qkv_row_stride + ch];
-      for (int t = 0; t < W - 1; ++t) x[t] = kda_oracle_bf16_to_f64(cs[t]);
+      for (int t = 0; t < W - 1; ++t) x[t] = kda_oracle_bf16_to_f64(CS(t));
       x[W - 1] = kda_oracle_bf16_to_f64(xin);
       for (int t = 0; t < W; ++t) wt[t] = (double)wc[(int64_t)t * D_c + (int64_t)h * dim_c + j];
       const double bias = p->conv_bias ? (double)p->conv_bias[ch] : 0.0;
       dst[j] = kda_oracle_silu(kda_oracle_causal_conv(x, wt, W, bias));
       if (p->update_conv_state && W > 1) {
-        for (int t = 0; t < W - 2; ++t) cs[t] = cs[t + 1];
-        cs[W - 2] = xin;
+        for (int t = 0; t < W - 2; ++t) CS(t) = CS(t + 1);
+        CS(W - 2) = xin;
       }
+#undef CS
     }
   }
 

@@ -38,6 +38,12 @@
  *        a = y * sigmoid(y)  (SiLU)
  *     If update_conv_state: conv_state[s, ch, :] <- (x_1, ..., x_{W-1}),
  *     the same bf16 bit patterns (a pure shift, never rounded).
+ *     The conv state is stored dim-first ("DS", [slots][C][W-1], the kernel's
+ *     (..., dim, width-1) view) or, with conv_state_sd, tap-first ("SD",
+ *     [slots][W-1][C], channel contiguous), which P1's model layer otherwise
+ *     transposes into the dim-first view (关键源码片段, kda.py).  Element
+ *     conv_state[s, ch, t] is at s*C*(W-1) + ch*(W-1) + t (DS) or
+ *     s*C*(W-1) + t*C + ch (SD); the values are the same either way.
  *
  *  2. L2 norm.  q^ = q_scale * q~ / sqrt(|q~|^2 + l2_eps),
  *               k^ = k~ / sqrt(|k~|^2 + l2_eps),
@@ -94,7 +100,7 @@ typedef struct {
   int64_t qkv_row_stride;     /* elements; >= C */
   const float* conv_weight;   /* q block [W][H*K], k block [W][H*K], v block [W][H*V] */
   const float* conv_bias;     /* [C] or NULL */
-  uint16_t* conv_state;       /* [num_slots][C][W-1] */
+  uint16_t* conv_state;       /* [num_slots][C][W-1], or [num_slots][W-1][C] if conv_state_sd */
   float* state;               /* [num_slots][H][K][V] */
   const float* g;             /* [N][H][K] log-decay */
   const uint16_t* beta;       /* [N][H] */
@@ -112,6 +118,7 @@ typedef struct {
   const float* A_log;         /* [H]; fused_gate only */
   const float* dt_bias;       /* [H*K] or NULL; fused_gate only */
   double lower_bound;         /* < 0: bounded ("safe") gate; fused_gate only */
+  int32_t conv_state_sd;      /* 1: conv_state is [num_slots][W-1][C] (tap-first) */
 } kda_oracle_problem;
 
 /* Runs one decode step over every (row, head).  num_threads <= 0 uses the

@@ -52,7 +52,7 @@ class _Problem(ctypes.Structure):
         ("eps", ctypes.c_double), ("l2_eps", ctypes.c_double), ("q_scale", ctypes.c_double),
         ("out_norm", ctypes.c_int32), ("update_conv_state", ctypes.c_int32),
         ("fused_gate", ctypes.c_int32), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
-        ("lower_bound", ctypes.c_double),
+        ("lower_bound", ctypes.c_double), ("conv_state_sd", ctypes.c_int32),
     ]
 
 
@@ -184,11 +184,13 @@ def decode(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, H: int,
            conv_bias=None, eps: float = 1e-6, l2_eps: float = 1e-6, q_scale: float = 0.0,
            out_norm: bool = True, update_conv_state: bool = True, threads: int = 0,
            want_f64: bool = True, in_place: bool = False, fused_gate: bool = False,
-           A_log=None, dt_bias=None, lower_bound: float = 0.0) -> OracleResult:
+           A_log=None, dt_bias=None, lower_bound: float = 0.0,
+           conv_state_sd: bool = False) -> OracleResult:
     """One decode step over all rows.  ``conv_state``/``state`` are copied
     unless ``in_place``; the updated arrays come back in the result.  With
     ``fused_gate``, ``g`` and ``beta`` hold raw logits and are activated with
-    ``A_log``, ``dt_bias`` and ``lower_bound``."""
+    ``A_log``, ``dt_bias`` and ``lower_bound``.  ``conv_state_sd``: the conv
+    state is [slots, W-1, C] (tap-first) instead of [slots, C, W-1]."""
     qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
     N = qkv.shape[0]
     C = 2 * H * K + H * V
@@ -235,7 +237,8 @@ def decode(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, H: int,
                  out=_ptr(out), out_f64=_ptr(out64), eps=eps, l2_eps=l2_eps,
                  q_scale=q_scale, out_norm=int(bool(out_norm)),
                  update_conv_state=int(bool(update_conv_state)), fused_gate=int(bool(fused_gate)),
-                 A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), lower_bound=float(lower_bound))
+                 A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), lower_bound=float(lower_bound),
+                 conv_state_sd=int(bool(conv_state_sd)))
     rc = lib().kda_oracle_decode(ctypes.byref(p), int(threads))
     if rc < 0:
         raise ValueError("kda_oracle_decode rejected its arguments")

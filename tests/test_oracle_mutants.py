@@ -25,7 +25,7 @@ MUTANTS = {
         "double r = 1.0 / sqrt(ss / (double)V + eps);", "double r = 1.0 / (sqrt(ss / (double)V) + eps);"),
     "reversed_conv_taps": (
         "wt[t] = (double)wc[(int64_t)t * D_c", "wt[t] = (double)wc[(int64_t)(W - 1 - t) * D_c"),
-    "conv_state_shift_wrong_end": ("cs[W - 2] = xin;", "cs[0] = xin;"),
+    "conv_state_shift_wrong_end": ("CS(W - 2) = xin;", "CS(0) = xin;"),
     "gate_silu_not_sigmoid": (
         "* w[j] * kda_oracle_sigmoid(gate[j]);", "* w[j] * kda_oracle_silu(gate[j]);"),
     "q_scale_from_value_dim": (
@@ -39,6 +39,9 @@ MUTANTS = {
     "gate_uses_A_log_not_exp": (
         "if (lower_bound < 0.0) return lower_bound * kda_oracle_sigmoid(exp(A_log) * z);",
         "if (lower_bound < 0.0) return lower_bound * kda_oracle_sigmoid(A_log * z);"),
+    "sd_layout_taps_newest_first": (
+        "#define CS(t) cs0[ch * cs_ch + (int64_t)(t) * cs_t]",
+        "#define CS(t) cs0[ch * cs_ch + (int64_t)(p->conv_state_sd ? (W - 2 - (t)) : (t)) * cs_t]"),
     "readout_skips_last_key": (
         "for (int i = 0; i < K; ++i) acc += S[(size_t)i * V + j] * q[i];",
         "for (int i = 0; i < K - 1; ++i) acc += S[(size_t)i * V + j] * q[i];"),

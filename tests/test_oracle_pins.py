@@ -542,3 +542,29 @@ def _torch_reference_f64_gate(p):
             out[n, h * V:(h + 1) * V] = o
             new_state[(s, h)] = Sn.numpy()
     return out.numpy(), new_state
+
+
+# ----------------------------------------------------------------- SD layout
+
+
+@pytest.mark.parametrize("update", [True, False])
+def test_sd_conv_state_layout_is_a_transpose(update):
+    """The tap-first (SD) conv state gives the same step as the dim-first one
+    on the transposed array, and its update is the transpose of the DS
+    update (catches SD strides mixed up with DS ones)."""
+    p = tiny_problem(seed=81, N=4, H=3, K=3, V=5, num_slots=7, slots=[2, 0, 6, 3])
+    ds = run(p, update_conv_state=update)
+    q = dict(p)
+    q["conv_state"] = np.ascontiguousarray(p["conv_state"].transpose(0, 2, 1))  # [slots, W-1, C]
+    sd = run(q, update_conv_state=update, conv_state_sd=True)
+    assert np.array_equal(sd.out, ds.out) and np.array_equal(sd.out_f64, ds.out_f64)
+    assert np.array_equal(sd.state, ds.state)
+    assert np.array_equal(sd.conv_state, np.ascontiguousarray(ds.conv_state.transpose(0, 2, 1)))
+    # and the SD update is the shift, read in the SD layout
+    C = p["conv_state"].shape[1]
+    for n, s in enumerate(p["slot_idx"]):
+        if s <= 0 or not update:
+            continue
+        assert np.array_equal(sd.conv_state[s, 0], q["conv_state"][s, 1])
+        assert np.array_equal(sd.conv_state[s, 1], q["conv_state"][s, 2])
+        assert np.array_equal(sd.conv_state[s, 2], p["qkv"][n, :C])
