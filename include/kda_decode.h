@@ -53,6 +53,10 @@ extern "C" {
 /* g and beta hold raw logits and the kernel activates them (the page's
  * "safe gate" variant; formula below, in KdaDecodeArgs.lower_bound). */
 #define KDA_FUSED_GATE        8u
+/* conv_state is stored tap-first, [num_slots][3][C] with the channel index
+ * contiguous (P1 关键源码片段, kda.py: the "SD" layout its model layer would
+ * otherwise transpose into the kernel's dim-first view). */
+#define KDA_CONV_STATE_SD    16u
 
 /* return codes of kda_decode */
 #define KDA_OK            0
@@ -90,7 +94,8 @@ typedef struct KdaDecodeArgs {
   const float* conv_weight;    /* fp32 [3][4][D], width-major, channel contiguous
                                   (P1 实现拆解 item 3) */
   const float* conv_bias;      /* fp32 [C] or NULL */
-  uint16_t* conv_state;        /* bf16 [num_slots][C][3], oldest tap first;
+  uint16_t* conv_state;        /* bf16 [num_slots][C][3] (dim-first, oldest tap first),
+                                  or [num_slots][3][C] with KDA_CONV_STATE_SD;
                                   read, and rewritten in place if KDA_UPDATE_CONV_STATE */
   float* state;                /* fp32 [num_slots][H][128][128], S[key][value],
                                   value index contiguous; read and rewritten in place */
@@ -106,7 +111,7 @@ typedef struct KdaDecodeArgs {
   float eps;                   /* RMSNorm epsilon (e.g. 1e-6) */
   float q_scale;               /* 0 => 1/sqrt(128) */
   uint32_t flags;              /* KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH |
-                                  KDA_FUSED_GATE */
+                                  KDA_FUSED_GATE | KDA_CONV_STATE_SD */
   int32_t* err_flag;           /* device int32 or NULL; KDA_DEVERR_* bits are OR-ed in */
 
   /* KDA_FUSED_GATE only (P1 关键源码片段: the op's A_log, dt_bias, lower_bound;

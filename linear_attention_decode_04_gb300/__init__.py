@@ -8,6 +8,7 @@ build raises instead of falling back to anything else.
 from .binding import (  # noqa: F401
     KDA_EARLY_PREFETCH,
     KDA_FUSED_GATE,
+    KDA_CONV_STATE_SD,
     KDA_OUT_NORM,
     KDA_UPDATE_CONV_STATE,
     KdaDecodeCall,

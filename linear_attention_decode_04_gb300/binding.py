@@ -19,6 +19,7 @@ KDA_OUT_NORM = 1
 KDA_UPDATE_CONV_STATE = 2
 KDA_EARLY_PREFETCH = 4
 KDA_FUSED_GATE = 8
+KDA_CONV_STATE_SD = 16
 KDA_DEVERR_SLOT_RANGE = 1
 KDA_DEVERR_TIMEOUT = 2
 ABI_VERSION = 1
@@ -124,7 +125,7 @@ class KdaDecodeCall:
                  gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
                  err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
-                 lower_bound: float = 0.0, work_queue=None):
+                 lower_bound: float = 0.0, work_queue=None, conv_state_layout: str = "DS"):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -142,8 +143,11 @@ class KdaDecodeCall:
             raise ValueError(f"conv_weight must be [3, 4, {D}] (got {tuple(conv_weight.shape)})")
         _dense(conv_weight, "conv_weight")
         _check(conv_state, "conv_state", torch.bfloat16, dev)
-        if tuple(conv_state.shape) != (num_slots, C, CONV_WIDTH - 1):
-            raise ValueError(f"conv_state must be [{num_slots}, {C}, 3] (got {tuple(conv_state.shape)})")
+        if conv_state_layout not in ("DS", "SD"):
+            raise ValueError("conv_state_layout is 'DS' ([slots, C, 3]) or 'SD' ([slots, 3, C])")
+        want_cs = (num_slots, C, CONV_WIDTH - 1) if conv_state_layout == "DS" else (num_slots, CONV_WIDTH - 1, C)
+        if tuple(conv_state.shape) != want_cs:
+            raise ValueError(f"conv_state ({conv_state_layout}) must be {list(want_cs)} (got {tuple(conv_state.shape)})")
         _dense(conv_state, "conv_state")
         _check(g, "g", torch.float32, dev)
         if tuple(g.shape) != (N, H, HEAD_DIM):
@@ -161,7 +165,8 @@ class KdaDecodeCall:
         out_stride = _rows(out, "out", N, D)
         fused_gate = A_log is not None
         flags = ((KDA_OUT_NORM if out_norm else 0) | (KDA_UPDATE_CONV_STATE if update_conv_state else 0)
-                 | (KDA_EARLY_PREFETCH if early_prefetch else 0) | (KDA_FUSED_GATE if fused_gate else 0))
+                 | (KDA_EARLY_PREFETCH if early_prefetch else 0) | (KDA_FUSED_GATE if fused_gate else 0)
+                 | (KDA_CONV_STATE_SD if conv_state_layout == "SD" else 0))
         alog_ptr = dtb_ptr = None
         if fused_gate:
             _check(A_log, "A_log", torch.float32, dev)
@@ -240,7 +245,7 @@ def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
                err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
-               lower_bound: float = 0.0, work_queue=None,
+               lower_bound: float = 0.0, work_queue=None, conv_state_layout: str = "DS",
                stream: torch.cuda.Stream | None = None) -> None:
     """One fused decode step (see ``include/kda_decode.h``).  ``conv_state``,
     ``state`` and ``out`` are written in place on ``stream`` (default: the
@@ -248,9 +253,11 @@ def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
     KDA_EARLY_PREFETCH: only when the kernel enqueued just before on the
     stream writes none of slot_idx, state and conv_state.  Passing ``A_log``
     sets KDA_FUSED_GATE: ``g`` and ``beta`` are then raw logits.
-    ``work_queue`` (int32[2], zero) enables the dynamic schedule."""
+    ``work_queue`` (int32[2], zero) enables the dynamic schedule.
+    ``conv_state_layout`` is "DS" ([slots, C, 3]) or "SD" ([slots, 3, C])."""
     KdaDecodeCall(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate=gate,
                   norm_weight=norm_weight, conv_bias=conv_bias, eps=eps, q_scale=q_scale,
                   out_norm=out_norm, update_conv_state=update_conv_state,
                   err_flag=err_flag, early_prefetch=early_prefetch, A_log=A_log, dt_bias=dt_bias,
-                  lower_bound=lower_bound, work_queue=work_queue)(stream)
+                  lower_bound=lower_bound, work_queue=work_queue,
+                  conv_state_layout=conv_state_layout)(stream)

@@ -137,7 +137,8 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
     return fail(KDA_ERR_SHAPE, "head_dim %d / conv_width %d (need 128 / 4)", a->head_dim, a->conv_width);
   if (a->N < 0 || a->H < 1 || a->num_slots < 1)
     return fail(KDA_ERR_SHAPE, "N=%d H=%d num_slots=%d", a->N, a->H, a->num_slots);
-  if (a->flags & ~(KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH | KDA_FUSED_GATE))
+  if (a->flags &
+      ~(KDA_OUT_NORM | KDA_UPDATE_CONV_STATE | KDA_EARLY_PREFETCH | KDA_FUSED_GATE | KDA_CONV_STATE_SD))
     return fail(KDA_ERR_FLAGS, "flags 0x%x", a->flags);
   if (a->N == 0) return KDA_OK;
   const bool norm = (a->flags & KDA_OUT_NORM) != 0;
@@ -189,6 +190,7 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
   p.total_units = a->N * a->H;
   p.early_prefetch = (a->flags & KDA_EARLY_PREFETCH) != 0;
   p.fused_gate = fused_gate;
+  p.conv_sd = (a->flags & KDA_CONV_STATE_SD) != 0;
   p.A_log = fused_gate ? a->A_log : nullptr;
   p.dt_bias = fused_gate ? a->dt_bias : nullptr;
   p.lower_bound = a->lower_bound;

@@ -43,6 +43,7 @@ struct Params {
   int total_units;  // N * H
   int early_prefetch;  // KDA_EARLY_PREFETCH
   int fused_gate;      // KDA_FUSED_GATE: g / beta are raw logits
+  int conv_sd;         // KDA_CONV_STATE_SD: conv state [slots][3][C]
   const float* A_log;
   const float* dt_bias;
   float lower_bound;
@@ -57,7 +58,7 @@ struct Params {
 // per-unit inputs for kStages units, plus the consumers' scratch.
 struct __align__(128) Smem {
   float tile[kStages][kDim * kDim];
-  uint16_t cs[kStages][3][kDim * (kWidth - 1)];
+  uint16_t cs[kStages][3][kDim * (kWidth - 1)];  // per block: [128][3] (DS) or [3][128] (SD)
   uint16_t x[kStages][3][kDim];
   float g[kStages][kDim];
   uint16_t gate[kStages][kDim];
@@ -272,11 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       const uint32_t full = smem_addr(&S.full[stage]);
       bulk_load(smem_addr(S.tile[stage]), p.state + (static_cast<int64_t>(slot) * p.H + h) * (kDim * kDim),
                 kTileBytes, full, policy);
-      for (int c = 0; c < 3; ++c)
-        bulk_load(smem_addr(S.cs[stage][c]),
-                  p.conv_state +
-                      (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1),
-                  kCsSliceBytes, full, policy);
+      for (int c = 0; c < 3; ++c) {
+        if (!p.conv_sd) {  // dim-first: one contiguous 768-byte slice per block
+          bulk_load(smem_addr(S.cs[stage][c]),
+                    p.conv_state +
+                        (static_cast<int64_t>(slot) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1),
+                    kCsSliceBytes, full, policy);
+        } else {  // tap-first: one 256-byte channel run per tap
+          for (int t = 0; t < kWidth - 1; ++t)
+            bulk_load(smem_addr(S.cs[stage][c] + t * kDim),
+                      p.conv_state + (static_cast<int64_t>(slot) * (kWidth - 1) + t) * 3 * D + c * D +
+                          static_cast<int64_t>(h) * kDim,
+                      kXSliceBytes, full, policy);
+        }
+      }
     };
     // Per-token inputs of a unit: qkv slices, g row, gate row.
     auto load_token_parts = [&](int stage, int n, int h) {
@@ -496,7 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
 
     // Conv-state advance: drop the oldest tap, append the new input (a pure
     // move of bf16 bit patterns).
-    if (kUpdateConv && tid < 3 * kCsU4) {
+    if (kUpdateConv && tid < 3 * kCsU4 && p.conv_sd) {
+      // tap-first: taps 0, 1 take the old taps 1, 2; tap 2 takes the input
+      const int c = tid / kCsU4, e = tid - c * kCsU4, t = e >> 4, q = e & 15;
+      const uint4 v = (t < kWidth - 2) ? reinterpret_cast<const uint4*>(S.cs[stage][c] + (t + 1) * kDim)[q]
+                                       : reinterpret_cast<const uint4*>(S.x[stage][c])[q];
+      reinterpret_cast<uint4*>(p.conv_state + (static_cast<int64_t>(slot) * (kWidth - 1) + t) * 3 * D + c * D +
+                               static_cast<int64_t>(h) * kDim)[q] = v;
+    } else if (kUpdateConv && tid < 3 * kCsU4) {
       const int c = tid / kCsU4, e = tid - c * kCsU4;
       uint16_t v8[8];
 #pragma unroll
@@ -517,19 +534,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     // Conv (4 taps) + SiLU on the 384 q|k|v channels; decay alpha = exp(g).
     {
       const int c = tid >> 7, j = tid & (kDim - 1);
-      const uint16_t* cs = S.cs[stage][c] + 3 * j;
+      // tap t of channel j: [j][t] (dim-first) or [t][j] (tap-first)
+      const int cs_j = p.conv_sd ? 1 : kWidth - 1, cs_t = p.conv_sd ? kDim : 1;
+      const uint16_t* cs = S.cs[stage][c] + cs_j * j;
       float y = bq;
-      y = fmaf(wq[0], bf16_to_f32(cs[0]), y);
-      y = fmaf(wq[1], bf16_to_f32(cs[1]), y);
-      y = fmaf(wq[2], bf16_to_f32(cs[2]), y);
+      y = fmaf(wq[0], bf16_to_f32(cs[0 * cs_t]), y);
+      y = fmaf(wq[1], bf16_to_f32(cs[1 * cs_t]), y);
+      y = fmaf(wq[2], bf16_to_f32(cs[2 * cs_t]), y);
       y = fmaf(wq[3], bf16_to_f32(S.x[stage][c][j]), y);
       (c == 0 ? S.q : S.k)[j] = y / (1.0f + expf(-y));
       if (tid < kDim) {
-        const uint16_t* csv = S.cs[stage][2] + 3 * j;
+        const uint16_t* csv = S.cs[stage][2] + cs_j * j;
         float yv = bv;
-        yv = fmaf(wv[0], bf16_to_f32(csv[0]), yv);
-        yv = fmaf(wv[1], bf16_to_f32(csv[1]), yv);
-        yv = fmaf(wv[2], bf16_to_f32(csv[2]), yv);
+        yv = fmaf(wv[0], bf16_to_f32(csv[0 * cs_t]), yv);
+        yv = fmaf(wv[1], bf16_to_f32(csv[1 * cs_t]), yv);
+        yv = fmaf(wv[2], bf16_to_f32(csv[2 * cs_t]), yv);
         yv = fmaf(wv[3], bf16_to_f32(S.x[stage][2][j]), yv);
         S.v[j] = yv / (1.0f + expf(-yv));
       } else {

@@ -73,7 +73,7 @@ def test_host_validation_codes(lib):
     assert _call(lib, _args(conv_width=3)) == -2
     assert _call(lib, _args(H=0)) == -2
     assert _call(lib, _args(N=-1)) == -2
-    assert _call(lib, _args(flags=16)) == -4
+    assert _call(lib, _args(flags=32)) == -4
     assert _call(lib, _args(flags=3 | 8)) == -1            # fused gate needs A_log
     assert _call(lib, _args(flags=3 | 8, A_log=0x20002)) == -3
     assert _call(lib, _args(N=0)) == 0          # no-op, no launch

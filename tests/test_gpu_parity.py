@@ -256,3 +256,28 @@ def test_fused_gate_parity(lower_bound, with_bias, cuda_device):
                         eps=spec.eps, fused_gate=True, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound)
     T.compare_all(x, d, ref, init_state=x.state, init_conv=x.conv_state)
     assert int(d["err_flag"].item()) == 0
+
+
+@pytest.mark.parametrize("name", ["n4_h12_pool8", "n32_h24_pool64_pad8", "n128_h48_pool512_normoff"])
+@pytest.mark.parametrize("update_conv_state", [True, False])
+def test_sd_conv_state_layout(name, update_conv_state, cuda_device):
+    """KDA_CONV_STATE_SD: the conv state stored tap-first [slots, 3, C]; the
+    whole pool must match the oracle's SD-layout step bit for bit."""
+    import oracle
+    x = W.make_inputs(W.SPECS[name])
+    cs_sd = np.ascontiguousarray(x.conv_state.transpose(0, 2, 1))
+    d = T.to_device(x, cuda_device)
+    d["conv_state"] = T.bf16_tensor(cs_sd, cuda_device)
+    kda_decode(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"], d["slot_idx"],
+               d["out"], gate=d["gate"], norm_weight=d["norm_weight"], eps=x.spec.eps, err_flag=d["err_flag"],
+               out_norm=x.spec.out_norm, update_conv_state=update_conv_state, conv_state_layout="SD")
+    torch.cuda.synchronize()
+    ref = oracle.decode(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=cs_sd, state=x.state, g=x.g,
+                        beta=x.beta, slot_idx=x.slot_idx, H=x.H, gate=x.gate, norm_weight=x.norm_weight,
+                        eps=x.spec.eps, out_norm=x.spec.out_norm, update_conv_state=update_conv_state,
+                        conv_state_sd=True)
+    T.check_out(T.bf16_bits(d["out"]), ref)
+    assert np.array_equal(T.bf16_bits(d["conv_state"]), ref.conv_state), "SD conv state not bit-exact"
+    for s in range(x.spec.num_slots):
+        T.check_state_slot(d["state"][s].cpu().numpy(), ref.state[s], f"slot {s}")
+    assert int(d["err_flag"].item()) == 0
