@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     KDA_UPDATE_CONV_STATE,
     KdaDecodeCall,
     KdaError,
+    kda_chunk_metadata,
     kda_decode,
     kda_status_string,
     library_path,

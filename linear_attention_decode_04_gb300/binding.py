@@ -79,6 +79,10 @@ def load_library() -> ctypes.CDLL:
             L.kda_decode_wait_test.argtypes = [ctypes.POINTER(KdaDecodeArgs), ctypes.c_void_p,
                                                ctypes.c_uint64, ctypes.c_int32]
             L.kda_decode_wait_test.restype = ctypes.c_int
+            L.kda_chunk_metadata.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p]
+            L.kda_chunk_metadata.restype = ctypes.c_int
             L.kda_abi_version.argtypes = []
             L.kda_abi_version.restype = ctypes.c_int
             if L.kda_abi_version() != ABI_VERSION:
@@ -261,3 +265,33 @@ def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                   err_flag=err_flag, early_prefetch=early_prefetch, A_log=A_log, dt_bias=dt_bias,
                   lower_bound=lower_bound, work_queue=work_queue,
                   conv_state_layout=conv_state_layout)(stream)
+
+
+def kda_chunk_metadata(cu_seqlens: torch.Tensor, cu_seqlens_cpu: torch.Tensor, chunk_size: int,
+                       err_flag=None, stream: torch.cuda.Stream | None = None):
+    """Device-side chunk metadata for chunked prefill (``include/kda_chunk_metadata.h``):
+    returns ``(chunk_indices int32 [total, 2], chunk_offsets int64 [N + 1])``.
+    The output size comes from the host copy ``cu_seqlens_cpu``, so nothing
+    waits for the device; the values are computed by the GPU from
+    ``cu_seqlens`` (int32, on the GPU)."""
+    lib = load_library()
+    _check(cu_seqlens, "cu_seqlens", torch.int32, None)
+    _dense(cu_seqlens, "cu_seqlens")
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be [N + 1]")
+    n = cu_seqlens.numel() - 1
+    lens = (cu_seqlens_cpu[1:] - cu_seqlens_cpu[:-1]).to(torch.int64).clamp(min=0)
+    total = int(((lens + chunk_size - 1) // chunk_size).sum()) if n > 0 else 0
+    dev = cu_seqlens.device
+    idx = torch.empty(max(total, 1), 2, dtype=torch.int32, device=dev)
+    off = torch.empty(n + 1, dtype=torch.int64, device=dev)
+    if err_flag is not None:
+        _check(err_flag, "err_flag", torch.int32, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = lib.kda_chunk_metadata(cu_seqlens.data_ptr(), n, int(chunk_size), idx.data_ptr(), total,
+                                off.data_ptr(), None if err_flag is None else err_flag.data_ptr(),
+                                ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise KdaError(rc, kda_status_string(rc))
+    return idx[:total], off

@@ -96,3 +96,17 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 def test_oracle_builds():
     import oracle
     assert os.path.exists(oracle.build())
+
+
+def test_chunk_metadata_validation_codes(lib):
+    L = ctypes.CDLL(binding.library_path())
+    f = L.kda_chunk_metadata
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(None, 4, 64, 0x1000, 8, 0x2000, None, None) == -1      # no cu_seqlens
+    assert f(0x1000, 4, 64, None, 8, 0x2000, None, None) == -1      # rows wanted, no buffer
+    assert f(0x1000, 4, 0, 0x2000, 8, 0x3000, None, None) == -2     # chunk size 0
+    assert f(0x1000, -1, 64, 0x2000, 8, 0x3000, None, None) == -2   # negative count
+    assert f(0x1002, 4, 64, 0x2000, 8, 0x3000, None, None) == -3    # cu_seqlens misaligned
+    assert f(0x1000, 4, 64, 0x2004, 8, 0x3000, None, None) == -3    # indices not 8-byte aligned
