@@ -396,6 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         mbar_arrive(smem_addr(&S.full[stage]));  // padding or out-of-range row
       }
     }
+    // This CTA draws no more units: the last CTA to get here returns the
+    // work queue to zero for the next call.  Done now rather than at exit,
+    // so the atomic's round trip overlaps the units still in the ring.
+    if (p.queue != nullptr) {
+      __threadfence();
+      if (atomicAdd(p.queue + 1, 1) == G - 1) {
+        atomicExch(p.queue, 0);
+        atomicExch(p.queue + 1, 0);
+      }
+    }
     // End of work: the consumers find n = -1 in the next stage they read.
     if (ok) {
       const int stage = it % kStages;
@@ -427,14 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         flag_error(p, KDA_DEVERR_TIMEOUT);
     }
     bulk_wait_all();
-    // The last CTA to finish returns the work queue to zero for the next call.
-    if (p.queue != nullptr) {
-      __threadfence();
-      if (atomicAdd(p.queue + 1, 1) == G - 1) {
-        atomicExch(p.queue, 0);
-        atomicExch(p.queue + 1, 0);
-      }
-    }
     return;
   }
 
