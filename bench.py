@@ -376,6 +376,42 @@ def run_case(args) -> dict | None:
             "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup}
 
 
+def run_chunk_metadata(args) -> dict:
+    """Timing of the device-side chunk metadata build for a prefill batch
+    (256 sequences, lengths 1..8192 tokens, chunk size 64), replayed from a
+    CUDA graph: the latency a prefill step pays instead of a host round trip."""
+    import torch
+
+    from linear_attention_decode_04_gb300 import kda_chunk_metadata
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(7)
+    lens = rng.integers(1, 8193, 256)
+    cu_cpu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+    cu = cu_cpu.to(dev)
+    kda_chunk_metadata(cu, cu_cpu, 64)
+    s = torch.cuda.Stream(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        idx, off = kda_chunk_metadata(cu, cu_cpu, 64)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / args.steps * 1e3
+    total = int(off[-1].item())
+    return {"mode": "chunk_metadata", "sequences": 256, "tokens": int(lens.sum()), "chunk_size": 64,
+            "chunks": total, "us_per_call": us, "bound": "latency (one CTA, a scan then an expansion)",
+            "bytes": 257 * 4 + 257 * 8 + total * 8, "steps": args.steps, "warmup": args.warmup}
+
+
 def run_reference(args) -> dict | None:
     """The oracle as it stands, timed on the host cores on a bounded sample
     of the same workload (rank 0 only)."""
@@ -424,7 +460,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--ref-layers", type=int, default=2, help="layers per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=("stack69", "layer", "roofline"), default="stack69",
+    ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata"), default="stack69",
                     help="stack69: the headline 69-layer graph step; layer / roofline: one "
                          "launch configuration timed on its own (profiling aid)")
     args = ap.parse_args(argv)
@@ -432,6 +468,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         res = run_reference(args)
+    elif args.case == "chunk_metadata":
+        res = run_chunk_metadata(args)
     elif args.case != "stack69":
         res = run_case(args)
     else:
