@@ -3,8 +3,9 @@
 // KDA", 实现拆解 item 2; definition in include/kda_chunk_metadata.h).
 //
 // One CTA: a block-wide exclusive scan of the per-sequence chunk counts in
-// tiles of 1024 sequences writes chunk_offsets, then every thread expands
-// rows r = tid, tid + 1024, ... by a binary search of r in chunk_offsets.
+// tiles of 1024 sequences writes chunk_offsets (and, for up to 4096
+// sequences, a shared-memory copy), then every thread expands rows
+// r = tid, tid + 1024, ... by a binary search of r in the offsets.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -14,6 +15,7 @@
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kSharedOffsets = 4097;  // offsets kept on chip for up to 4096 sequences
 
 __global__ void __launch_bounds__(kThreads) chunk_metadata_kernel(const int32_t* __restrict__ cu, int n_seqs,
                                                                    int bt, int32_t* __restrict__ idx,
@@ -21,6 +23,8 @@ __global__ void __launch_bounds__(kThreads) chunk_metadata_kernel(const int32_t*
                                                                    int32_t* err) {
   __shared__ int64_t warp_tot[kThreads / 32];
   __shared__ int64_t carry_s;
+  __shared__ int64_t off_s[kSharedOffsets];
+  const bool on_chip = n_seqs < kSharedOffsets;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry_s = 0;
   __syncthreads();
@@ -54,16 +58,23 @@ __global__ void __launch_bounds__(kThreads) chunk_metadata_kernel(const int32_t*
     __syncthreads();
     const int64_t carry = carry_s;
     const int64_t excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - nt;
-    if (i < n_seqs) off[i] = excl;
+    if (i < n_seqs) {
+      off[i] = excl;
+      if (on_chip) off_s[i] = excl;
+    }
     __syncthreads();
     if (tid == 0) carry_s = carry + warp_tot[kThreads / 32 - 1];
     __syncthreads();
   }
   const int64_t total = carry_s;
-  if (tid == 0) off[n_seqs] = total;
+  if (tid == 0) {
+    off[n_seqs] = total;
+    if (on_chip) off_s[n_seqs] = total;
+  }
   if (bad && err) atomicOr(err, KDA_DEVERR_SEQLENS);
   if (tid == 0 && total > capacity && err) atomicOr(err, KDA_DEVERR_CAPACITY);
   __syncthreads();  // offsets written by this CTA are visible to it from here on
+  const int64_t* offs = on_chip ? off_s : off;
   const int64_t rows = total < capacity ? total : capacity;
   for (int64_t r = tid; r < rows; r += kThreads) {
     // last sequence whose offset is <= r: it owns chunk r (empty sequences
@@ -71,10 +82,10 @@ __global__ void __launch_bounds__(kThreads) chunk_metadata_kernel(const int32_t*
     int lo = 0, hi = n_seqs;  // answer in [0, n_seqs - 1]
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (off[mid] <= r) lo = mid; else hi = mid - 1;
+      if (offs[mid] <= r) lo = mid; else hi = mid - 1;
     }
     idx[2 * r] = lo;
-    idx[2 * r + 1] = static_cast<int32_t>(r - off[lo]);
+    idx[2 * r + 1] = static_cast<int32_t>(r - offs[lo]);
   }
 }
 
