@@ -4,8 +4,9 @@
 //
 // One CTA: a block-wide exclusive scan of the per-sequence chunk counts in
 // tiles of 1024 sequences writes chunk_offsets (and, for up to 4096
-// sequences, a shared-memory copy), then every thread expands rows
-// r = tid, tid + 1024, ... by a binary search of r in the offsets.
+// sequences, a shared-memory copy), then each warp takes sequences
+// i = warp, warp + 32, ... and its lanes write that sequence's rows
+// off[i] + c, c = lane, lane + 32, ... (coalesced 8-byte rows).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -75,17 +76,14 @@ __global__ void __launch_bounds__(kThreads) chunk_metadata_kernel(const int32_t*
   if (tid == 0 && total > capacity && err) atomicOr(err, KDA_DEVERR_CAPACITY);
   __syncthreads();  // offsets written by this CTA are visible to it from here on
   const int64_t* offs = on_chip ? off_s : off;
-  const int64_t rows = total < capacity ? total : capacity;
-  for (int64_t r = tid; r < rows; r += kThreads) {
-    // last sequence whose offset is <= r: it owns chunk r (empty sequences
-    // share their offset with the next one and are skipped)
-    int lo = 0, hi = n_seqs;  // answer in [0, n_seqs - 1]
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (offs[mid] <= r) lo = mid; else hi = mid - 1;
+  for (int i = warp; i < n_seqs; i += kThreads / 32) {
+    const int64_t first = offs[i], last = offs[i + 1] < capacity ? offs[i + 1] : capacity;
+    for (int64_t r = first + lane; r < last; r += 32) {
+      int2 row;
+      row.x = i;
+      row.y = static_cast<int32_t>(r - first);
+      reinterpret_cast<int2*>(idx)[r] = row;
     }
-    idx[2 * r] = lo;
-    idx[2 * r + 1] = static_cast<int32_t>(r - offs[lo]);
   }
 }
 
