@@ -65,7 +65,8 @@ struct __align__(128) Smem {
   float q[kDim], k[kDim], v[kDim], alpha[kDim];
   float red[2][kConsumerWarps][kDim];
   float delta[kDim];
-  float sum[4][4];
+  float nsum[kConsumerWarps];     // per-warp |q~|^2 (warps 0-3) and |k~|^2 (warps 4-7)
+  float sum[4][4];                // per-warp q~.k~, |w|^2, w.delta, |delta|^2
   int info[kStages][4];           // slot, n (-1: no more units), h, withheld
   unsigned long long ready[kStages];  // info of the stage is written
   unsigned long long full[kStages];
@@ -544,7 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       y = fmaf(wq[1], bf16_to_f32(cs[1 * cs_t]), y);
       y = fmaf(wq[2], bf16_to_f32(cs[2 * cs_t]), y);
       y = fmaf(wq[3], bf16_to_f32(S.x[stage][c][j]), y);
-      (c == 0 ? S.q : S.k)[j] = y / (1.0f + expf(-y));
+      const float act = y / (1.0f + expf(-y));
+      (c == 0 ? S.q : S.k)[j] = act;
+      // this warp's share of |q~|^2 (warps 0-3) or |k~|^2 (warps 4-7)
+      const float ss = warp_sum(act * act);
+      if (lane == 0) S.nsum[warp] = ss;
       if (tid < kDim) {
         const uint16_t* csv = S.cs[stage][2] + cs_j * j;
         float yv = bv;
@@ -571,26 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     const float gate_j = (kOutNorm && tid < kDim) ? bf16_to_f32(S.gate[stage][tid]) : 0.0f;
     consumer_sync();
 
-    // |q|^2, |k|^2, q.k in one pass.
-    if (tid < kDim) {
-      const float qv = S.q[tid], kv = S.k[tid];
-      const float sq = warp_sum(qv * qv), sk = warp_sum(kv * kv), sqk = warp_sum(qv * kv);
-      if (lane == 0) {
-        S.sum[warp][0] = sq;
-        S.sum[warp][1] = sk;
-        S.sum[warp][2] = sqk;
-      }
-    }
-    consumer_sync();
-    const float ssq = (S.sum[0][0] + S.sum[1][0]) + (S.sum[2][0] + S.sum[3][0]);
-    const float ssk = (S.sum[0][1] + S.sum[1][1]) + (S.sum[2][1] + S.sum[3][1]);
-    const float sqk = (S.sum[0][2] + S.sum[1][2]) + (S.sum[2][2] + S.sum[3][2]);
-    const float rq = scale / sqrtf(ssq + 1e-6f);
-    const float rk = 1.0f / sqrtf(ssk + 1e-6f);
-    const float qk = sqk * rq * rk;  // q^ . k^
-
-    // Decay the staged tile and form partial u = A^T k^, w = A^T q^ over this
-    // warp's 16 key rows (A = Diag(alpha) S, kept in registers).
+    // Decay the staged tile and form partial column sums over this warp's 16
+    // key rows with the unnormalised q~, k~ (the L2 norms are applied to the
+    // sums afterwards): u~ = A^T k~, w~ = A^T q~, A = Diag(alpha) S kept in
+    // registers.
     const float4* tile4 = reinterpret_cast<const float4*>(S.tile[stage]);
     float4 a[kRowsPerWarp];
 #pragma unroll
@@ -599,33 +588,46 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
       const int i = warp * kRowsPerWarp + r;
-      const float al = S.alpha[i], kh = S.k[i] * rk, qh = S.q[i] * rq;
+      const float al = S.alpha[i], kt = S.k[i], qt = S.q[i];
       a[r].x *= al; a[r].y *= al; a[r].z *= al; a[r].w *= al;
-      u.x = fmaf(kh, a[r].x, u.x); u.y = fmaf(kh, a[r].y, u.y);
-      u.z = fmaf(kh, a[r].z, u.z); u.w = fmaf(kh, a[r].w, u.w);
-      w.x = fmaf(qh, a[r].x, w.x); w.y = fmaf(qh, a[r].y, w.y);
-      w.z = fmaf(qh, a[r].z, w.z); w.w = fmaf(qh, a[r].w, w.w);
+      u.x = fmaf(kt, a[r].x, u.x); u.y = fmaf(kt, a[r].y, u.y);
+      u.z = fmaf(kt, a[r].z, u.z); u.w = fmaf(kt, a[r].w, u.w);
+      w.x = fmaf(qt, a[r].x, w.x); w.y = fmaf(qt, a[r].y, w.y);
+      w.z = fmaf(qt, a[r].z, w.z); w.w = fmaf(qt, a[r].w, w.w);
     }
     reinterpret_cast<float4*>(S.red[0][warp])[lane] = u;
     reinterpret_cast<float4*>(S.red[1][warp])[lane] = w;
     consumer_sync();
 
-    // delta_j = beta (v_j - u_j); readout of the updated state
+    // L2 norms: q^ = rq q~, k^ = rk k~.  u = rk u~, w = rq w~;
+    // delta_j = beta (v_j - u_j); the readout of the updated state is
     // o = S'^T q^ = w + (q^ . k^) delta, with no second pass over S'.
-    float o = 0.0f;
+    float rq = 0.0f, rk = 0.0f, wj = 0.0f, dj = 0.0f;
     if (tid < kDim) {
-      float uj = 0.0f, wj = 0.0f;
+      const float ssq = (S.nsum[0] + S.nsum[1]) + (S.nsum[2] + S.nsum[3]);
+      const float ssk = (S.nsum[4] + S.nsum[5]) + (S.nsum[6] + S.nsum[7]);
+      rq = scale / sqrtf(ssq + 1e-6f);
+      rk = 1.0f / sqrtf(ssk + 1e-6f);
+      float uj = 0.0f;
 #pragma unroll
       for (int r = 0; r < kConsumerWarps; ++r) {
         uj += S.red[0][r][tid];
         wj += S.red[1][r][tid];
       }
-      const float dj = beta * (S.v[tid] - uj);
-      S.delta[tid] = dj;
-      o = fmaf(qk, dj, wj);
+      uj *= rk;
+      wj *= rq;
+      dj = beta * (S.v[tid] - uj);
+      S.delta[tid] = rk * dj;  // pass 2 adds k~ (rk delta)^T = k^ delta^T
+      // q~.k~ for (q^ . k^), and the three sums that give sum_j o_j^2
+      const float sqk = warp_sum(S.q[tid] * S.k[tid]);
+      if (lane == 0) S.sum[warp][0] = sqk;
       if (kOutNorm) {
-        const float ss = warp_sum(o * o);
-        if (lane == 0) S.sum[warp][3] = ss;
+        const float sww = warp_sum(wj * wj), swd = warp_sum(wj * dj), sdd = warp_sum(dj * dj);
+        if (lane == 0) {
+          S.sum[warp][1] = sww;
+          S.sum[warp][2] = swd;
+          S.sum[warp][3] = sdd;
+        }
       }
     }
     consumer_sync();
@@ -637,9 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
       const int i = warp * kRowsPerWarp + r;
-      const float kh = S.k[i] * rk;
-      a[r].x = fmaf(kh, d.x, a[r].x); a[r].y = fmaf(kh, d.y, a[r].y);
-      a[r].z = fmaf(kh, d.z, a[r].z); a[r].w = fmaf(kh, d.w, a[r].w);
+      const float kt = S.k[i];
+      a[r].x = fmaf(kt, d.x, a[r].x); a[r].y = fmaf(kt, d.y, a[r].y);
+      a[r].z = fmaf(kt, d.z, a[r].z); a[r].w = fmaf(kt, d.w, a[r].w);
       tile4w[i * 32 + lane] = a[r];
     }
     fence_proxy_async_smem();  // generic-proxy writes before the async-proxy store
@@ -648,10 +650,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
 
     // Gated RMSNorm epilogue (or the raw readout) to bf16.
     if (tid < kDim) {
+      const float qk = ((S.sum[0][0] + S.sum[1][0]) + (S.sum[2][0] + S.sum[3][0])) * rq * rk;  // q^ . k^
+      const float o = fmaf(qk, dj, wj);
       float y = o;
       if (kOutNorm) {
-        const float ss = (S.sum[0][3] + S.sum[1][3]) + (S.sum[2][3] + S.sum[3][3]);
-        const float rr = 1.0f / sqrtf(ss * (1.0f / kDim) + p.eps);
+        // sum_j o_j^2 = sum w^2 + 2 qk sum w delta + qk^2 sum delta^2
+        const float sww = (S.sum[0][1] + S.sum[1][1]) + (S.sum[2][1] + S.sum[3][1]);
+        const float swd = (S.sum[0][2] + S.sum[1][2]) + (S.sum[2][2] + S.sum[3][2]);
+        const float sdd = (S.sum[0][3] + S.sum[1][3]) + (S.sum[2][3] + S.sum[3][3]);
+        const float ss = fmaf(qk, fmaf(qk, sdd, 2.0f * swd), sww);
+        const float rr = 1.0f / sqrtf(fmaxf(ss, 0.0f) * (1.0f / kDim) + p.eps);
         y = o * rr * nw * (1.0f / (1.0f + expf(-gate_j)));
       }
       out_row[tid] = f32_to_bf16(y);
