@@ -19,8 +19,11 @@
  * output is zero and no state is read or written (P1 实现拆解 item 1 and the
  * kernel excerpt under 关键源码片段 "code excerpts").
  *
- * Memory: every pointer is DEVICE memory owned by the caller, on the device
- * current when kda_decode is called.  The library never allocates, frees,
+ * Memory: every pointer is memory owned by the caller that the device current
+ * when kda_decode is called can address: device memory, or (for the
+ * per-token tensors qkv, g, beta, gate, slot_idx and out) pinned host memory
+ * mapped into the device's address space, which the kernel then reads and
+ * writes directly over the CPU-GPU link.  The library never allocates, frees,
  * synchronises or reads device memory from the host, so a call may be
  * captured into a CUDA graph (after one eager call on that device, which
  * performs the once-per-device kernel attribute set-up).

@@ -95,9 +95,18 @@ def kda_status_string(status: int) -> str:
     return load_library().kda_status_string(int(status)).decode()
 
 
-def _check(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device | None):
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device | None,
+           host_ok: bool = False):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
+    if host_ok and t.device.type == "cpu":
+        # pinned host memory is mapped into the GPU's address space: the
+        # kernel reads or writes it directly over the CPU-GPU link
+        if not t.is_pinned():
+            raise ValueError(f"{name} is a CPU tensor: it must be pinned (tensor.pin_memory())")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+        return
     if t.device.type != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
     if t.dtype != dtype:
@@ -123,13 +132,19 @@ def _rows(t: torch.Tensor, name: str, N: int, width: int) -> int:
 class KdaDecodeCall:
     """A prepared ``kda_decode`` call: validates and packs the arguments once;
     each ``__call__`` is one C call (cheap enough for eager loops and CUDA
-    graph capture).  Keeps references to the tensors it points at."""
+    graph capture).  Keeps references to the tensors it points at.
+
+    ``host_token_io=True`` lets the per-token tensors (qkv, g, beta, gate,
+    slot_idx, out) be pinned host tensors: the kernel then reads them and
+    writes the output straight over the CPU-GPU link, with no copy step.
+    The host must not rewrite them while a launch that uses them may run."""
 
     def __init__(self, qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                  gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
                  err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
-                 lower_bound: float = 0.0, work_queue=None, conv_state_layout: str = "DS"):
+                 lower_bound: float = 0.0, work_queue=None, conv_state_layout: str = "DS",
+                 host_token_io: bool = False):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -139,7 +154,7 @@ class KdaDecodeCall:
         num_slots, H = int(state.shape[0]), int(state.shape[1])
         D = H * HEAD_DIM
         C = 3 * D
-        _check(qkv, "qkv", torch.bfloat16, dev)
+        _check(qkv, "qkv", torch.bfloat16, dev, host_token_io)
         N = int(qkv.shape[0])
         qkv_stride = _rows(qkv, "qkv", N, C)
         _check(conv_weight, "conv_weight", torch.float32, dev)
@@ -153,19 +168,19 @@ class KdaDecodeCall:
         if tuple(conv_state.shape) != want_cs:
             raise ValueError(f"conv_state ({conv_state_layout}) must be {list(want_cs)} (got {tuple(conv_state.shape)})")
         _dense(conv_state, "conv_state")
-        _check(g, "g", torch.float32, dev)
+        _check(g, "g", torch.float32, dev, host_token_io)
         if tuple(g.shape) != (N, H, HEAD_DIM):
             raise ValueError(f"g must be [{N}, {H}, 128] (got {tuple(g.shape)})")
         _dense(g, "g")
-        _check(beta, "beta", torch.bfloat16, dev)
+        _check(beta, "beta", torch.bfloat16, dev, host_token_io)
         if tuple(beta.shape) != (N, H):
             raise ValueError(f"beta must be [{N}, {H}] (got {tuple(beta.shape)})")
         _dense(beta, "beta")
-        _check(slot_idx, "slot_idx", torch.int32, dev)
+        _check(slot_idx, "slot_idx", torch.int32, dev, host_token_io)
         if tuple(slot_idx.shape) != (N,):
             raise ValueError(f"slot_idx must be [{N}] (got {tuple(slot_idx.shape)})")
         _dense(slot_idx, "slot_idx")
-        _check(out, "out", torch.bfloat16, dev)
+        _check(out, "out", torch.bfloat16, dev, host_token_io)
         out_stride = _rows(out, "out", N, D)
         fused_gate = A_log is not None
         flags = ((KDA_OUT_NORM if out_norm else 0) | (KDA_UPDATE_CONV_STATE if update_conv_state else 0)
@@ -188,7 +203,7 @@ class KdaDecodeCall:
         if out_norm:
             if gate is None or norm_weight is None:
                 raise ValueError("out_norm needs gate and norm_weight")
-            _check(gate, "gate", torch.bfloat16, dev)
+            _check(gate, "gate", torch.bfloat16, dev, host_token_io)
             gate_stride = _rows(gate, "gate", N, D)
             _check(norm_weight, "norm_weight", torch.float32, dev)
             if tuple(norm_weight.shape) != (HEAD_DIM,):

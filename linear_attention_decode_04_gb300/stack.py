@@ -38,14 +38,17 @@ def warm_up(device: torch.device) -> None:
 class DecodeStack:
     """``layers`` is a list of dicts of device tensors with the keys of
     ``kda_decode`` (qkv, conv_weight, conv_state, state, g, beta, slot_idx,
-    out, gate, norm_weight, conv_bias, err_flag).  Each layer must own its
+    out, gate, norm_weight, conv_bias, err_flag).  With ``host_token_io`` the
+    per-token tensors (``STEP_INPUTS`` and out) may be pinned host tensors,
+    read and written by the kernels directly over the CPU-GPU link, so a step
+    needs no copies at all.  Each layer must own its
     state and conv-state pools.  With two or more layers, consecutive launches
     never share a pool (the last layer is followed by the first on the next
     replay), so every launch may stream its state while the previous layer's
     kernel drains (KDA_EARLY_PREFETCH)."""
 
     def __init__(self, layers: list[dict], eps: float = 1e-6, out_norm: bool = True,
-                 update_conv_state: bool = True):
+                 update_conv_state: bool = True, host_token_io: bool = False):
         self.layers = layers
         ptrs = [L["state"].data_ptr() for L in layers]
         if len(set(ptrs)) != len(ptrs):
@@ -68,7 +71,7 @@ class DecodeStack:
                           norm_weight=L.get("norm_weight"), conv_bias=L.get("conv_bias"), eps=eps,
                           out_norm=out_norm, update_conv_state=update_conv_state,
                           err_flag=L.get("err_flag"), early_prefetch=early,
-                          work_queue=self.queue)
+                          work_queue=self.queue, host_token_io=host_token_io)
             for L in layers
         ]
         self.graph: torch.cuda.CUDAGraph | None = None
@@ -95,45 +98,3 @@ class DecodeStack:
 
     def replay(self) -> None:
         self.graph.replay()
-
-    def capture_host_io(self, host_in: list[dict], host_out: list[torch.Tensor],
-                        stream: torch.cuda.Stream | None = None) -> torch.cuda.CUDAGraph:
-        """Capture a step that also moves data to and from the host: every
-        layer's per-token inputs (``STEP_INPUTS``) are copied from pinned host
-        tensors on a copy stream, each layer's kernel waits only for its own
-        inputs, and each output row block is copied back to pinned host memory
-        on a second copy stream as soon as its kernel is done.  Copies of later
-        layers overlap the kernels of earlier ones."""
-        dev = self.layers[0]["state"].device
-        warm_up(dev)
-        main = stream if stream is not None else torch.cuda.Stream(dev)
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=main):
-            fork = torch.cuda.Event()
-            fork.record(main)
-            s_in.wait_event(fork)
-            s_out.wait_event(fork)
-            ready = []
-            with torch.cuda.stream(s_in):
-                for L, hin in zip(self.layers, host_in):
-                    for k in STEP_INPUTS:
-                        L[k].copy_(hin[k], non_blocking=True)
-                    e = torch.cuda.Event()
-                    e.record(s_in)
-                    ready.append(e)
-            for c, L, e, hout in zip(self.calls, self.layers, ready, host_out):
-                main.wait_event(e)
-                c(main)
-                done = torch.cuda.Event()
-                done.record(main)
-                s_out.wait_event(done)
-                with torch.cuda.stream(s_out):
-                    hout.copy_(L["out"], non_blocking=True)
-            join_in, join_out = torch.cuda.Event(), torch.cuda.Event()
-            join_in.record(s_in)
-            join_out.record(s_out)
-            main.wait_event(join_in)
-            main.wait_event(join_out)
-        self.io_graph, self.io_stream = g, main
-        return g
