@@ -585,10 +585,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
     float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
+    // this warp's 16 rows of alpha, k~, q~ as float4 broadcasts
+    float al_r[kRowsPerWarp], kt_r[kRowsPerWarp], qt_r[kRowsPerWarp];
+#pragma unroll
+    for (int r4 = 0; r4 < kRowsPerWarp / 4; ++r4) {
+      const float4 al4 = reinterpret_cast<const float4*>(S.alpha + warp * kRowsPerWarp)[r4];
+      const float4 kt4 = reinterpret_cast<const float4*>(S.k + warp * kRowsPerWarp)[r4];
+      const float4 qt4 = reinterpret_cast<const float4*>(S.q + warp * kRowsPerWarp)[r4];
+      al_r[4 * r4] = al4.x; al_r[4 * r4 + 1] = al4.y; al_r[4 * r4 + 2] = al4.z; al_r[4 * r4 + 3] = al4.w;
+      kt_r[4 * r4] = kt4.x; kt_r[4 * r4 + 1] = kt4.y; kt_r[4 * r4 + 2] = kt4.z; kt_r[4 * r4 + 3] = kt4.w;
+      qt_r[4 * r4] = qt4.x; qt_r[4 * r4 + 1] = qt4.y; qt_r[4 * r4 + 2] = qt4.z; qt_r[4 * r4 + 3] = qt4.w;
+    }
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-      const int i = warp * kRowsPerWarp + r;
-      const float al = S.alpha[i], kt = S.k[i], qt = S.q[i];
+      const float al = al_r[r], kt = kt_r[r], qt = qt_r[r];
       a[r].x *= al; a[r].y *= al; a[r].z *= al; a[r].w *= al;
       u.x = fmaf(kt, a[r].x, u.x); u.y = fmaf(kt, a[r].y, u.y);
       u.z = fmaf(kt, a[r].z, u.z); u.w = fmaf(kt, a[r].w, u.w);
@@ -639,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
       const int i = warp * kRowsPerWarp + r;
-      const float kt = S.k[i];
+      const float kt = kt_r[r];
       a[r].x = fmaf(kt, d.x, a[r].x); a[r].y = fmaf(kt, d.y, a[r].y);
       a[r].z = fmaf(kt, d.z, a[r].z); a[r].w = fmaf(kt, d.w, a[r].w);
       tile4w[i * 32 + lane] = a[r];
