@@ -450,28 +450,28 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
   for (int it = 0;; ++it) {
     const int stage = it % kStages;
     const uint32_t parity = (it / kStages) & 1;
-    // Which unit is next (all consumers agree; also the barrier that guards the scratch).
+    // Which unit is next, then its staged data.  The per-unit inputs that do
+    // not depend on the slot (conv weights, beta, gate parameters) are
+    // usually prefetched while the previous unit computed.
     const bool have_info = mbar_wait_bounded(smem_addr(&S.ready[stage]), parity, p.wait_limit_ns);
-    if (consumer_any(!have_info || S.abort)) {
-      if (tid == 0) {
-        flag_error(p, KDA_DEVERR_TIMEOUT);
-        S.abort = 1;
+    int n = -1, h = 0;
+    bool ok = have_info;
+    if (have_info) {
+      n = S.info[stage][1];
+      h = S.info[stage][2];
+      if (n >= 0) {
+        if (have_next) {
+          cur = nxt;
+        } else {
+          cur = load_unit_inputs(p, n, h, tid, D);
+        }
+        have_next = false;
+        ok = mbar_wait_bounded(smem_addr(&S.full[stage]), parity, p.wait_limit_ns);
       }
-      break;
     }
-    const int n = S.info[stage][1], h = S.info[stage][2];
-    if (n < 0) break;  // no more units
-
-    // Per-unit inputs that do not depend on the slot (conv weights, beta,
-    // gate parameters): usually prefetched while the previous unit computed.
-    if (have_next) {
-      cur = nxt;
-    } else {
-      cur = load_unit_inputs(p, n, h, tid, D);
-    }
-    have_next = false;
-
-    const bool ok = mbar_wait_bounded(smem_addr(&S.full[stage]), parity, p.wait_limit_ns);
+    // All consumers agree on going on (one vote for both waits; also the
+    // barrier that guards the scratch).  Without a timeout every consumer
+    // has read the same info, so the end-of-work test below is uniform.
     if (consumer_any(!ok || S.abort)) {
       if (tid == 0) {
         flag_error(p, KDA_DEVERR_TIMEOUT);
@@ -479,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       }
       break;
     }
+    if (n < 0) break;  // no more units
     // If the next unit is already published, start loading its inputs now;
     // they arrive while this unit computes.
     {
