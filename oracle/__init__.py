@@ -1,4 +1,4 @@
-"""fp64 CPU oracle of the fused KDA decode step.
+"""fp64 CPU oracle of the fused KDA decode step and of the varlen prefill.
 
 TEST INFRASTRUCTURE ONLY: the test-suite, the smoke check and the benchmark's
 CPU-baseline leg load it; the product library never does, and the two share
@@ -8,6 +8,7 @@ from .kda_oracle import (  # noqa: F401
     OracleResult,
     build,
     decode,
+    prefill,
     lib,
     round_bf16,
     bf16_to_f64,

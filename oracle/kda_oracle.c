@@ -274,3 +274,148 @@ int kda_oracle_decode(const kda_oracle_problem* p, int num_threads) {
   }
   return oob;
 }
+
+/* ---------------------------------------------------------------- prefill */
+
+int kda_oracle_prefill_problem_size(void) { return (int)sizeof(kda_oracle_prefill_problem); }
+
+/* One (sequence b, head h) of the prefill: the decode steps token by token,
+ * the window and the state carried along (P2 实现拆解 #2-#3 for the varlen
+ * batch; steps as in the decode formulation).  Returns 1 if the slot was out
+ * of range. */
+static int prefill_unit(const kda_oracle_prefill_problem* p, int b, int h, double* work) {
+  const int H = p->H, K = p->K, V = p->V, W = p->W;
+  const int64_t Dq = (int64_t)H * K, Dv = (int64_t)H * V, C = 2 * Dq + Dv;
+  const int32_t r0 = p->cu_seqlens[b], r1 = p->cu_seqlens[b + 1];
+  const int32_t s = p->slot_idx[b];
+  if (r1 <= r0) return 0; /* empty sequence: nothing to do */
+
+  if (s < 1 || s >= p->num_slots) { /* padding or out of range */
+    for (int32_t r = r0; r < r1; ++r)
+      for (int j = 0; j < V; ++j) {
+        p->out[(int64_t)r * Dv + (int64_t)h * V + j] = 0;
+        if (p->out_f64) p->out_f64[(int64_t)r * Dv + (int64_t)h * V + j] = 0.0;
+      }
+    return s >= p->num_slots;
+  }
+
+  double* qt = work;            /* K */
+  double* kt = qt + K;          /* K */
+  double* vt = kt + K;          /* V */
+  double* qh = vt + V;          /* K */
+  double* kh = qh + K;          /* K */
+  double* alpha = kh + K;       /* K */
+  double* o = alpha + K;        /* V */
+  double* y = o + V;            /* V */
+  double* gt = y + V;           /* V */
+  double* nw = gt + V;          /* V */
+  double* x = nw + V;           /* W */
+  double* wt = x + W;           /* W */
+  double* S = wt + W;           /* K*V */
+  uint16_t* win = (uint16_t*)(S + (size_t)K * V); /* (2K+V) channels x (W-1) taps, oldest first */
+
+  /* the head's channels of the three blocks, in q | k | v order */
+  const int dims[3] = {K, K, V};
+  const int64_t offs[3] = {0, Dq, 2 * Dq};
+  const int64_t Ds[3] = {Dq, Dq, Dv};
+  const float* wbase[3] = {p->conv_weight, p->conv_weight + (int64_t)W * Dq, p->conv_weight + 2 * (int64_t)W * Dq};
+  uint16_t* cs0 = p->conv_state + (int64_t)s * C * (W - 1);
+
+  /* window <- the slot's conv state */
+  for (int c = 0, m = 0; c < 3; ++c)
+    for (int j = 0; j < dims[c]; ++j, ++m) {
+      const int64_t ch = offs[c] + (int64_t)h * dims[c] + j;
+      for (int t = 0; t < W - 1; ++t) win[(size_t)m * (W - 1) + t] = cs0[ch * (W - 1) + t];
+    }
+
+  float* Sg = p->state + (((int64_t)s * H + h) * K) * V;
+  for (int64_t e = 0; e < (int64_t)K * V; ++e) S[e] = (double)Sg[e];
+  const double scale = (p->q_scale != 0.0) ? p->q_scale : pow((double)K, -0.5);
+
+  for (int32_t r = r0; r < r1; ++r) {
+    /* 1. conv + SiLU with the window, then slide the window */
+    for (int c = 0, m = 0; c < 3; ++c) {
+      double* dst = (c == 0) ? qt : (c == 1) ? kt : vt;
+      for (int j = 0; j < dims[c]; ++j, ++m) {
+        const int64_t ch = offs[c] + (int64_t)h * dims[c] + j;
+        uint16_t* wm = win + (size_t)m * (W - 1);
+        const uint16_t xin = p->qkv[(int64_t)r * p->qkv_row_stride + ch];
+        for (int t = 0; t < W - 1; ++t) x[t] = kda_oracle_bf16_to_f64(wm[t]);
+        x[W - 1] = kda_oracle_bf16_to_f64(xin);
+        for (int t = 0; t < W; ++t) wt[t] = (double)wbase[c][(int64_t)t * Ds[c] + (int64_t)h * dims[c] + j];
+        const double bias = p->conv_bias ? (double)p->conv_bias[ch] : 0.0;
+        dst[j] = kda_oracle_silu(kda_oracle_causal_conv(x, wt, W, bias));
+        if (W > 1) {
+          for (int t = 0; t < W - 2; ++t) wm[t] = wm[t + 1];
+          wm[W - 2] = xin;
+        }
+      }
+    }
+    /* 2. L2 norms */
+    kda_oracle_l2norm(qt, K, p->l2_eps, scale, qh);
+    kda_oracle_l2norm(kt, K, p->l2_eps, 1.0, kh);
+    /* 3. gated delta rule, state kept in fp64 */
+    for (int i = 0; i < K; ++i) alpha[i] = exp((double)p->g[((int64_t)r * H + h) * K + i]);
+    const double beta = kda_oracle_bf16_to_f64(p->beta[(int64_t)r * H + h]);
+    kda_oracle_gated_delta_update(K, V, S, alpha, beta, kh, vt);
+    /* 4. readout, 5. gated RMSNorm or raw */
+    kda_oracle_readout(K, V, S, qh, o);
+    if (p->out_norm) {
+      for (int j = 0; j < V; ++j) {
+        gt[j] = kda_oracle_bf16_to_f64(p->gate[(int64_t)r * Dv + (int64_t)h * V + j]);
+        nw[j] = (double)p->norm_weight[j];
+      }
+      kda_oracle_gated_rmsnorm(V, o, nw, gt, p->eps, y);
+    } else {
+      for (int j = 0; j < V; ++j) y[j] = o[j];
+    }
+    for (int j = 0; j < V; ++j) {
+      p->out[(int64_t)r * Dv + (int64_t)h * V + j] = kda_oracle_round_bf16(y[j]);
+      if (p->out_f64) p->out_f64[(int64_t)r * Dv + (int64_t)h * V + j] = y[j];
+    }
+  }
+
+  /* store the final state and window */
+  for (int64_t e = 0; e < (int64_t)K * V; ++e) Sg[e] = (float)S[e];
+  for (int c = 0, m = 0; c < 3; ++c)
+    for (int j = 0; j < dims[c]; ++j, ++m) {
+      const int64_t ch = offs[c] + (int64_t)h * dims[c] + j;
+      for (int t = 0; t < W - 1; ++t) cs0[ch * (W - 1) + t] = win[(size_t)m * (W - 1) + t];
+    }
+  return 0;
+}
+
+int kda_oracle_prefill(const kda_oracle_prefill_problem* p, int num_threads) {
+  if (!p || p->B < 0 || p->H < 1 || p->K < 1 || p->V < 1 || p->W < 2 || p->num_slots < 1) return -1;
+  if (p->B == 0) return 0;
+  if (!p->cu_seqlens || !p->conv_weight || !p->conv_state || !p->state || !p->slot_idx) return -1;
+  if (p->cu_seqlens[0] != 0) return -1;
+  for (int b = 0; b < p->B; ++b)
+    if (p->cu_seqlens[b + 1] < p->cu_seqlens[b]) return -1;
+  if (p->cu_seqlens[p->B] > 0 && (!p->qkv || !p->g || !p->beta || !p->out)) return -1;
+  if (p->out_norm && p->cu_seqlens[p->B] > 0 && (!p->gate || !p->norm_weight)) return -1;
+  const int64_t C = 2 * (int64_t)p->H * p->K + (int64_t)p->H * p->V;
+  if (p->qkv_row_stride < C) return -1;
+
+  const int64_t units = (int64_t)p->B * p->H;
+  const size_t work_len = (size_t)(5 * p->K + 5 * p->V + 2 * p->W) + (size_t)p->K * p->V +
+                          ((size_t)(2 * p->K + p->V) * (p->W - 1) * sizeof(uint16_t) + sizeof(double) - 1) / sizeof(double);
+  int oob = 0;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+  (void)num_threads;
+#endif
+#pragma omp parallel reduction(+ : oob)
+  {
+    double* work = (double*)malloc(work_len * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t u = 0; u < units; ++u) {
+      const int b = (int)(u / p->H), h = (int)(u % p->H);
+      const int r = prefill_unit(p, b, h, work);
+      if (h == 0) oob += r;
+    }
+    free(work);
+  }
+  return oob;
+}

@@ -81,6 +81,33 @@
  * Parity unpinned by the pages: the q scale (1/sqrt(K)) and the L2-norm
  * epsilon's placement have no passage behind them; both sides follow the
  * formulation written here.
+ *
+ * ---------------------------------------------------------------------------
+ * PREFILL (multi-token sequences)
+ *
+ * Source cited as "P2": the web page "[ROCm][Perf] Kimi-K3 Remove prefill
+ * pipeline stall in chunk KDA" (vLLM PR #51862 report).  P2 feeds a varlen
+ * batch of sequences (cu_seqlens) to the chunked KDA prefill kernel together
+ * with the (sequence, chunk) metadata (实现拆解 #2, #3); it names the
+ * kernel's arguments but prints none of its arithmetic.  The chunked form is
+ * a way of evaluating the same recurrence, so the oracle is the recurrence
+ * itself, token by token:
+ *
+ * For each sequence b in [0,B) with tokens r = cu_seqlens[b] .. cu_seqlens[b+1]-1
+ * (in order) and s = slot_idx[b], and each head h:
+ *   - s <= 0: padding sequence, out rows of all its tokens are zero, nothing
+ *     else is read or written; s >= num_slots: the same, counted out of range.
+ *   - otherwise steps 1-5 above run for every token r in order, with:
+ *       * the conv window sliding over the sequence: for its first token the
+ *         W-1 older taps come from conv_state[s] (DS layout), after that from
+ *         the sequence's own preceding tokens;
+ *       * the state carried from token to token in fp64, never rounded in
+ *         between (no intermediate state is ever stored);
+ *       * at the end, S (rounded to fp32) is stored to slot s and
+ *         conv_state[s] holds the last W-1 inputs of the window (the bit
+ *         patterns of the newest W-1 taps, which reach back into the old
+ *         conv state when the sequence is shorter than W-1).
+ *   - an empty sequence (no tokens) leaves everything unchanged.
  * ---------------------------------------------------------------------------
  */
 #ifndef KDA_ORACLE_H
@@ -129,6 +156,32 @@ int kda_oracle_decode(const kda_oracle_problem* p, int num_threads);
 /* Size of kda_oracle_problem, so a foreign-function caller can check that its
  * mirror of the struct matches. */
 int kda_oracle_problem_size(void);
+
+/* Varlen prefill problem (see PREFILL above).  Host memory, caller-owned. */
+typedef struct {
+  int32_t B, H, K, V, W, num_slots;
+  const int32_t* cu_seqlens;  /* [B+1], non-decreasing, cu_seqlens[0] = 0 */
+  const uint16_t* qkv;        /* [T][qkv_row_stride] */
+  int64_t qkv_row_stride;
+  const float* conv_weight;   /* as kda_oracle_problem */
+  const float* conv_bias;     /* [C] or NULL */
+  uint16_t* conv_state;       /* [num_slots][C][W-1] (DS) */
+  float* state;               /* [num_slots][H][K][V] */
+  const float* g;             /* [T][H][K] */
+  const uint16_t* beta;       /* [T][H] */
+  const uint16_t* gate;       /* [T][H*V]; ignored when out_norm == 0 */
+  const float* norm_weight;   /* [V]; ignored when out_norm == 0 */
+  const int32_t* slot_idx;    /* [B] */
+  uint16_t* out;              /* [T][H*V] */
+  double* out_f64;            /* optional [T][H*V] */
+  double eps, l2_eps, q_scale;
+  int32_t out_norm;
+} kda_oracle_prefill_problem;
+
+/* Runs the prefill of every sequence.  Returns the number of sequences whose
+ * slot was >= num_slots, or -1 on a bad argument. */
+int kda_oracle_prefill(const kda_oracle_prefill_problem* p, int num_threads);
+int kda_oracle_prefill_problem_size(void);
 
 /* ---- the individual steps, fp64, exposed for the fact tests ---- */
 

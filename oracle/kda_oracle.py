@@ -56,6 +56,22 @@ class _Problem(ctypes.Structure):
     ]
 
 
+class _PrefillProblem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("V", ctypes.c_int32), ("W", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p),
+        ("qkv", ctypes.c_void_p), ("qkv_row_stride", ctypes.c_int64),
+        ("conv_weight", ctypes.c_void_p), ("conv_bias", ctypes.c_void_p),
+        ("conv_state", ctypes.c_void_p), ("state", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("gate", ctypes.c_void_p),
+        ("norm_weight", ctypes.c_void_p), ("slot_idx", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("out_f64", ctypes.c_void_p),
+        ("eps", ctypes.c_double), ("l2_eps", ctypes.c_double), ("q_scale", ctypes.c_double),
+        ("out_norm", ctypes.c_int32),
+    ]
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
@@ -87,8 +103,13 @@ def lib() -> ctypes.CDLL:
             L.kda_oracle_round_bf16.restype = ctypes.c_uint16
             L.kda_oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
             L.kda_oracle_bf16_to_f64.restype = ctypes.c_double
+            L.kda_oracle_prefill.argtypes = [ctypes.POINTER(_PrefillProblem), ctypes.c_int]
+            L.kda_oracle_prefill.restype = ctypes.c_int
+            L.kda_oracle_prefill_problem_size.restype = ctypes.c_int
             if L.kda_oracle_problem_size() != ctypes.sizeof(_Problem):
                 raise RuntimeError("oracle struct layout mismatch")
+            if L.kda_oracle_prefill_problem_size() != ctypes.sizeof(_PrefillProblem):
+                raise RuntimeError("oracle prefill struct layout mismatch")
             _lib = L
     return _lib
 
@@ -242,4 +263,57 @@ def decode(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, H: int,
     rc = lib().kda_oracle_decode(ctypes.byref(p), int(threads))
     if rc < 0:
         raise ValueError("kda_oracle_decode rejected its arguments")
+    return OracleResult(out=out, out_f64=out64, conv_state=cs, state=st, n_out_of_range=rc)
+
+
+def prefill(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, cu_seqlens, H: int,
+            K: int = 128, V: int = 128, W: int = 4, gate=None, norm_weight=None,
+            conv_bias=None, eps: float = 1e-6, l2_eps: float = 1e-6, q_scale: float = 0.0,
+            out_norm: bool = True, threads: int = 0, want_f64: bool = True,
+            in_place: bool = False) -> OracleResult:
+    """Prefill of a varlen batch: every sequence's tokens run through the
+    decode steps in order (window and state carried along, state never
+    rounded in between); final state and conv window stored to the
+    sequence's slot.  ``slot_idx`` has one entry per sequence; ``qkv``, ``g``,
+    ``beta``, ``gate`` one row per token.  Pools are copied unless
+    ``in_place``."""
+    qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    B = cu.size - 1
+    T = int(cu[-1]) if B > 0 else 0
+    C = 2 * H * K + H * V
+    conv_weight = np.ascontiguousarray(conv_weight, dtype=np.float32)
+    assert conv_weight.size == W * C
+    if in_place:
+        assert conv_state.dtype == np.uint16 and conv_state.flags.c_contiguous
+        assert state.dtype == np.float32 and state.flags.c_contiguous
+        cs, st = conv_state, state
+    else:
+        cs = np.array(conv_state, dtype=np.uint16, order="C", copy=True)
+        st = np.array(state, dtype=np.float32, order="C", copy=True)
+    num_slots = st.shape[0]
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    beta = np.ascontiguousarray(beta, dtype=np.uint16)
+    slot_idx = np.ascontiguousarray(slot_idx, dtype=np.int32)
+    assert qkv.shape[0] >= T and g.size >= T * H * K and beta.size >= T * H and slot_idx.size == B
+    if out_norm:
+        gate = np.ascontiguousarray(gate, dtype=np.uint16)
+        norm_weight = np.ascontiguousarray(norm_weight, dtype=np.float32)
+        assert gate.size >= T * H * V and norm_weight.size == V
+    else:
+        gate = norm_weight = None
+    if conv_bias is not None:
+        conv_bias = np.ascontiguousarray(conv_bias, dtype=np.float32)
+    out = np.zeros((T, H * V), dtype=np.uint16)
+    out64 = np.zeros((T, H * V), dtype=np.float64) if want_f64 else None
+    p = _PrefillProblem(B=B, H=H, K=K, V=V, W=W, num_slots=num_slots, cu_seqlens=_ptr(cu),
+                        qkv=_ptr(qkv), qkv_row_stride=qkv.shape[1] if qkv.ndim == 2 else C,
+                        conv_weight=_ptr(conv_weight), conv_bias=_ptr(conv_bias),
+                        conv_state=_ptr(cs), state=_ptr(st), g=_ptr(g), beta=_ptr(beta),
+                        gate=_ptr(gate), norm_weight=_ptr(norm_weight), slot_idx=_ptr(slot_idx),
+                        out=_ptr(out), out_f64=_ptr(out64), eps=eps, l2_eps=l2_eps,
+                        q_scale=q_scale, out_norm=int(bool(out_norm)))
+    rc = lib().kda_oracle_prefill(ctypes.byref(p), int(threads))
+    if rc < 0:
+        raise ValueError("kda_oracle_prefill rejected its arguments")
     return OracleResult(out=out, out_f64=out64, conv_state=cs, state=st, n_out_of_range=rc)

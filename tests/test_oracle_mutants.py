@@ -45,7 +45,27 @@ MUTANTS = {
     "readout_skips_last_key": (
         "for (int i = 0; i < K; ++i) acc += S[(size_t)i * V + j] * q[i];",
         "for (int i = 0; i < K - 1; ++i) acc += S[(size_t)i * V + j] * q[i];"),
+    # prefill (token loop of the varlen batch)
+    "prefill_window_not_slid": ("          wm[W - 2] = xin;\n", ""),
+    "prefill_state_reloaded_every_token": (
+        "    /* 1. conv + SiLU with the window, then slide the window */",
+        "    for (int64_t e = 0; e < (int64_t)K * V; ++e) S[e] = (double)Sg[e];"),
+    "prefill_final_window_not_stored": (
+        "      for (int t = 0; t < W - 1; ++t) cs0[ch * (W - 1) + t] = win[(size_t)m * (W - 1) + t];",
+        "      (void)0;"),
+    "prefill_beta_of_first_token": (
+        "kda_oracle_bf16_to_f64(p->beta[(int64_t)r * H + h]);",
+        "kda_oracle_bf16_to_f64(p->beta[(int64_t)r0 * H + h]);"),
+    "prefill_slot_zero_not_padding": (
+        "if (s < 1 || s >= p->num_slots) { /* padding or out of range */",
+        "if (s < 0 || s >= p->num_slots) { /* padding or out of range */"),
+    "prefill_q_scale_from_value_dim": ("pow((double)K, -0.5);", "pow((double)V, -0.5);"),
+    "prefill_decay_of_previous_token": (
+        "alpha[i] = exp((double)p->g[((int64_t)r * H + h) * K + i]);",
+        "alpha[i] = exp((double)p->g[((int64_t)(r > r0 ? r - 1 : r) * H + h) * K + i]);"),
 }
+
+PIN_FILES = ("test_oracle_pins.py", "test_prefill_oracle_pins.py")
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -61,7 +81,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                    check=True)
     env = dict(os.environ, KDA_ORACLE_SO=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        *[os.path.join(ROOT, "tests", f) for f in PIN_FILES]],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     # exit code 1 = some test failed (not a crash, not a collection error)
     assert r.returncode == 1, f"mutant {name} survived or crashed:\n{r.stdout[-2000:]}\n{r.stderr[-2000:]}"
