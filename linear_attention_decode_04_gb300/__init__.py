@@ -1,4 +1,5 @@
-"""GB300-native fused KDA (Kimi Delta Attention) single-token decode step.
+"""GB300-native fused KDA (Kimi Delta Attention) single-token decode step and
+chunked varlen prefill.
 
 The compute lives in one hand-written CUDA library (``csrc/``) behind a C ABI
 (``include/kda_decode.h``); ``kda_decode`` here only marshals torch tensors
@@ -12,9 +13,11 @@ from .binding import (  # noqa: F401
     KDA_OUT_NORM,
     KDA_UPDATE_CONV_STATE,
     KdaDecodeCall,
+    KdaPrefillCall,
     KdaError,
     kda_chunk_metadata,
     kda_decode,
+    kda_prefill,
     kda_status_string,
     library_path,
     load_library,

@@ -56,6 +56,26 @@ class KdaDecodeArgs(ctypes.Structure):
     ]
 
 
+class KdaPrefillArgs(ctypes.Structure):
+    """Mirror of ``KdaPrefillArgs`` in ``include/kda_prefill.h`` (field order matters)."""
+    _fields_ = [
+        ("struct_size", ctypes.c_size_t),
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("conv_width", ctypes.c_int32),
+        ("T", ctypes.c_int64),
+        ("cu_seqlens", ctypes.c_void_p),
+        ("qkv", ctypes.c_void_p), ("qkv_row_stride", ctypes.c_int64),
+        ("conv_weight", ctypes.c_void_p), ("conv_bias", ctypes.c_void_p),
+        ("conv_state", ctypes.c_void_p), ("state", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("gate", ctypes.c_void_p), ("gate_row_stride", ctypes.c_int64),
+        ("norm_weight", ctypes.c_void_p), ("slot_idx", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("out_row_stride", ctypes.c_int64),
+        ("eps", ctypes.c_float), ("q_scale", ctypes.c_float),
+        ("flags", ctypes.c_uint32), ("err_flag", ctypes.c_void_p),
+    ]
+
+
 def library_path() -> str:
     return _LIB_PATH
 
@@ -83,6 +103,8 @@ def load_library() -> ctypes.CDLL:
                                              ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                              ctypes.c_void_p, ctypes.c_void_p]
             L.kda_chunk_metadata.restype = ctypes.c_int
+            L.kda_prefill.argtypes = [ctypes.POINTER(KdaPrefillArgs), ctypes.c_void_p]
+            L.kda_prefill.restype = ctypes.c_int
             L.kda_abi_version.argtypes = []
             L.kda_abi_version.restype = ctypes.c_int
             if L.kda_abi_version() != ABI_VERSION:
@@ -310,3 +332,98 @@ def kda_chunk_metadata(cu_seqlens: torch.Tensor, cu_seqlens_cpu: torch.Tensor, c
     if rc != 0:
         raise KdaError(rc, kda_status_string(rc))
     return idx[:total], off
+
+
+class KdaPrefillCall:
+    """A prepared ``kda_prefill`` call (``include/kda_prefill.h``): validates
+    and packs the arguments once; each ``__call__`` is one C call.  Keeps
+    references to the tensors it points at.
+
+    Shapes: T token rows, B sequences, H heads, D = H * 128.
+      qkv [T, >=3D] bf16, conv_weight [3, 4, D] f32, conv_state [slots, 3D, 3]
+      bf16, state [slots, H, 128, 128] f32, g [T, H, 128] f32, beta [T, H]
+      bf16, cu_seqlens [B + 1] int32 (device), slot_idx [B] int32, out
+      [T, >=D] bf16, gate [T, >=D] bf16 and norm_weight [128] f32 with
+      out_norm."""
+
+    def __init__(self, qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
+                 gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
+                 q_scale: float = 0.0, out_norm: bool = True, err_flag=None):
+        self._lib = load_library()
+        dev = state.device
+        _check(state, "state", torch.float32, None)
+        _dense(state, "state")
+        if state.dim() != 4 or state.shape[2:] != (128, 128):
+            raise ValueError(f"state must be [slots, H, 128, 128] (got {tuple(state.shape)})")
+        num_slots, H = state.shape[0], state.shape[1]
+        D = H * 128
+        T = qkv.shape[0]
+        _check(qkv, "qkv", torch.bfloat16, dev)
+        qkv_stride = _rows(qkv, "qkv", T, 3 * D)
+        for name, t, dt in (("conv_weight", conv_weight, torch.float32),
+                            ("conv_state", conv_state, torch.bfloat16), ("g", g, torch.float32),
+                            ("beta", beta, torch.bfloat16), ("cu_seqlens", cu_seqlens, torch.int32),
+                            ("slot_idx", slot_idx, torch.int32)):
+            _check(t, name, dt, dev)
+            _dense(t, name)
+        if conv_weight.numel() != 3 * 4 * D:
+            raise ValueError("conv_weight must be [3, 4, H*128]")
+        if conv_state.numel() != num_slots * 3 * D * 3:
+            raise ValueError("conv_state must be [slots, 3*H*128, 3]")
+        if g.numel() != T * D or beta.numel() != T * H:
+            raise ValueError("g must be [T, H, 128] and beta [T, H]")
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be [B + 1]")
+        B = cu_seqlens.numel() - 1
+        if slot_idx.numel() != B:
+            raise ValueError(f"slot_idx must have one entry per sequence ({B})")
+        _check(out, "out", torch.bfloat16, dev)
+        out_stride = _rows(out, "out", T, D)
+        gate_stride = 0
+        if out_norm:
+            if gate is None or norm_weight is None:
+                raise ValueError("out_norm needs gate and norm_weight")
+            _check(gate, "gate", torch.bfloat16, dev)
+            gate_stride = _rows(gate, "gate", T, D)
+            _check(norm_weight, "norm_weight", torch.float32, dev)
+            _dense(norm_weight, "norm_weight")
+            if norm_weight.numel() != 128:
+                raise ValueError("norm_weight must be [128]")
+        if conv_bias is not None:
+            _check(conv_bias, "conv_bias", torch.float32, dev)
+            _dense(conv_bias, "conv_bias")
+            if conv_bias.numel() != 3 * D:
+                raise ValueError("conv_bias must be [3*H*128]")
+        if err_flag is not None:
+            _check(err_flag, "err_flag", torch.int32, dev)
+        self.device = dev
+        self._keep = (qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, gate,
+                      norm_weight, conv_bias, err_flag)
+        ptr = (lambda t: None if t is None else t.data_ptr())
+        self.args = KdaPrefillArgs(
+            struct_size=ctypes.sizeof(KdaPrefillArgs), B=B, H=H, num_slots=num_slots,
+            head_dim=128, conv_width=4, T=T, cu_seqlens=ptr(cu_seqlens), qkv=ptr(qkv),
+            qkv_row_stride=qkv_stride, conv_weight=ptr(conv_weight), conv_bias=ptr(conv_bias),
+            conv_state=ptr(conv_state), state=ptr(state), g=ptr(g), beta=ptr(beta),
+            gate=ptr(gate) if out_norm else None, gate_row_stride=gate_stride,
+            norm_weight=ptr(norm_weight) if out_norm else None, slot_idx=ptr(slot_idx), out=ptr(out),
+            out_row_stride=out_stride, eps=eps, q_scale=q_scale,
+            flags=KDA_OUT_NORM if out_norm else 0, err_flag=ptr(err_flag))
+
+    def __call__(self, stream: torch.cuda.Stream | None = None) -> None:
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        rc = self._lib.kda_prefill(ctypes.byref(self.args), ctypes.c_void_p(stream.cuda_stream))
+        if rc != 0:
+            raise KdaError(rc, f"{kda_status_string(rc)}: {self._lib.kda_last_error().decode()}")
+
+
+def kda_prefill(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
+                gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
+                q_scale: float = 0.0, out_norm: bool = True, err_flag=None,
+                stream: torch.cuda.Stream | None = None) -> None:
+    """Chunked prefill of a varlen batch (see ``include/kda_prefill.h``):
+    ``out``, ``state`` and ``conv_state`` are written in place."""
+    KdaPrefillCall(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out,
+                   gate=gate, norm_weight=norm_weight, conv_bias=conv_bias, eps=eps,
+                   q_scale=q_scale, out_norm=out_norm, err_flag=err_flag)(stream)

@@ -23,6 +23,7 @@
 
 #include "kda_decode.h"
 #include "kda_decode_kernel.cuh"
+#include "kda_internal.h"
 
 namespace {
 
@@ -94,6 +95,16 @@ cudaError_t launch(const Params& p, int sms, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int kda_internal_fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+void kda_internal_clear_error() { g_last_error[0] = '\0'; }
 
 extern "C" int kda_abi_version(void) { return KDA_DECODE_ABI_VERSION; }
 

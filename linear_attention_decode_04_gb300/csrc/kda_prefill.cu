@@ -1,0 +1,610 @@
+// kda_prefill.cu -- chunked KDA prefill over a varlen batch for GB300
+// (sm_103a): device code and C ABI.
+//
+// "P2" is the page "[ROCm][Perf] Kimi-K3 Remove prefill pipeline stall in
+// chunk KDA" (vLLM PR #51862 report): prefill runs the KDA layer over whole
+// sequences of a varlen batch with a chunked kernel (实现拆解 items 2-3).  P2
+// prints none of that kernel's arithmetic; what it computes is the decode
+// recurrence of include/kda_decode.h applied token by token, and the chunked
+// evaluation below is exact up to rounding (derivation in the comments).
+//
+// Chunk form.  Within a chunk of L tokens t = 0..L-1 of one (sequence, head),
+// with S0 the state before the chunk, G_t = g_0 + ... + g_t (per key channel,
+// cumulative log decay), k^, q^ the normalised keys and queries, v~ the
+// values and beta_t the write strengths, the recurrence
+//     S_t = Diag(exp g_t) S_{t-1} + k^_t delta_t^T,
+//     delta_t = beta_t (v~_t - (Diag(exp g_t) S_{t-1})^T k^_t),   o_t = S_t^T q^_t
+// unrolls to S_t = Diag(exp G_t) S0 + sum_{s<=t} Diag(exp(G_t - G_s)) k^_s delta_s^T, so
+//     (I + Diag(beta) P) Delta = Diag(beta) (V~ - K_G S0),   P_ts = sum_i k^_ti k^_si exp(G_ti - G_si)  (s < t)
+//     O = Q_G S0 + R Delta,                                 R_ts = sum_i q^_ti k^_si exp(G_ti - G_si)  (s <= t)
+//     S_L = Diag(exp G_{L-1}) S0 + K_E^T Delta
+// with K_G = exp(G) . K^, Q_G = exp(G) . Q^ and K_E = exp(G_{L-1} - G) . K^
+// (row-wise).  The triangular system is solved once for both right-hand
+// sides, X = [U | W] with (I + Diag(beta) P) X = Diag(beta) [V~ | K_G], so
+// Delta = U - W S0.  P and R are contractions over the key channels once the
+// decay factor is split around a reference token m of the chunk:
+// exp(G_t - G_s) = exp(G_t - G_m) exp(G_m - G_s); when a factor could leave
+// the fp32 range the chunk takes them element by element instead.
+//
+// Tensor cores: every contraction with the state (W S0, Q_G S0, K_E^T Delta)
+// and between tokens (P, R, R Delta) is a warp-level m16n8k8 tf32 MMA, each
+// operand split into a tf32 high part and a tf32 remainder and three
+// products accumulated in fp32, which keeps fp32-level accuracy.  The state
+// is held in registers for the whole sequence, transposed (value rows x key
+// columns) in the accumulator layout, which doubles as the A operand of the
+// next chunk's products (the k index of an m16n8k8 operand may be permuted as
+// long as both operands use the same permutation).
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kda_chunk_metadata.h"
+#include "kda_internal.h"
+#include "kda_prefill.h"
+
+namespace {
+
+constexpr int kD = 128;           // head dim (key = value)
+constexpr int kWidth = 4;         // conv taps
+constexpr int kHist = kWidth - 1; // older taps carried between chunks
+constexpr int kL = KDA_PREFILL_CHUNK;  // 32 tokens per chunk
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kCh = 3 * kD;       // q | k | v channels of one head
+constexpr int kSA = 136;          // row stride (floats) of [token][128] operands
+constexpr int kST = 40;           // row stride (floats) of [128][token] and [token][token] operands
+constexpr int kSP = 36;           // row stride (floats) of P (rows read as float4)
+constexpr int kRef = 15;          // reference token of the split decay factors
+constexpr float kMaxExponent = 80.0f;  // |G_t - G_m| above this: element-wise path
+
+struct PrefillParams {
+  const int32_t* cu;
+  const uint16_t* qkv;
+  int64_t qkv_stride;
+  const float* conv_w;
+  const float* conv_b;
+  uint16_t* conv_state;
+  float* state;
+  const float* g;
+  const uint16_t* beta;
+  const uint16_t* gate;
+  int64_t gate_stride;
+  const float* norm_w;
+  const int32_t* slot_idx;
+  uint16_t* out;
+  int64_t out_stride;
+  int64_t T;
+  int B, H, num_slots;
+  float eps, q_scale;
+  int32_t* err;
+};
+
+// Shared memory of one CTA (about 170 KB).  Buffers whose lifetimes do not
+// overlap within a chunk share storage.
+struct __align__(16) PSmem {
+  uint16_t raw[kHist + kL][kCh];  // conv window: 3 older rows, then the chunk's inputs
+  uint16_t gate[kL][kD];
+  float beta[kL];
+  float q[kL][kSA];               // q^, then Q_G
+  float k[kL][kSA];               // k^
+  float v[kL][kSA];               // v~, then the chunk's output O (staging)
+  float G[kL][kD];                // cumulative log decay
+  union { float ek[kL][kSA]; float w[kL][kSA]; };        // exp(G - G_m) k^, then W
+  union { float fk[kL][kSA]; float ket[kD][kST]; };      // exp(G_m - G) k^, then K_E^T
+  union { float eq[kL][kSA]; float ut[kD][kST]; };       // exp(G - G_m) q^, then U^T
+  float P[kL][kSP];               // P (strictly lower)
+  float r[kL][kST];               // R (lower, diagonal included)
+  float gC[kD];                   // exp(G_{L-1}): decay of the whole chunk
+  float nrm[kWarps][kL];          // per-warp partial sums of o^2
+  int slow;                       // this chunk takes the element-wise P / R path
+};
+
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// An A operand (16 x 8 tile) in registers, split into tf32 high and low parts.
+struct FragA {
+  uint32_t hi[4], lo[4];
+};
+
+__device__ __forceinline__ FragA make_a(float a0, float a1, float a2, float a3) {
+  FragA f;
+  const float a[4] = {a0, a1, a2, a3};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f.hi[e] = to_tf32(a[e]);
+    f.lo[e] = to_tf32(a[e] - __uint_as_float(f.hi[e]));
+  }
+  return f;
+}
+
+// c += A * B with B's two elements split as well: lo*hi + hi*lo + hi*hi.
+__device__ __forceinline__ void mma3(float (&c)[4], const FragA& a, float b0, float b1) {
+  const uint32_t h0 = to_tf32(b0), h1 = to_tf32(b1);
+  const uint32_t l0 = to_tf32(b0 - __uint_as_float(h0)), l1 = to_tf32(b1 - __uint_as_float(h1));
+  mma_tf32(c, a.lo, h0, h1);
+  mma_tf32(c, a.hi, l0, l1);
+  mma_tf32(c, a.hi, h0, h1);
+}
+
+// One CTA per (sequence, head); blockIdx.x = b * H + h.
+template <bool kOutNorm>
+__global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  PSmem& S = *reinterpret_cast<PSmem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, tq = lane & 3;
+  const int b = blockIdx.x / p.H, h = blockIdx.x - b * p.H;
+  const int64_t D = static_cast<int64_t>(p.H) * kD;
+
+  const int64_t r0 = p.cu[b], r1 = p.cu[b + 1];
+  if (r0 < 0 || r1 < r0 || r1 > p.T) {
+    if (tid == 0 && h == 0 && p.err) atomicOr(p.err, KDA_DEVERR_SEQLENS);
+    return;
+  }
+  if (r1 == r0) return;  // empty sequence
+  const int slot = p.slot_idx[b];
+  if (slot <= 0 || slot >= p.num_slots) {
+    // padding sequence: zero output rows of this head, touch nothing else
+    for (int64_t e = tid; e < (r1 - r0) * (kD / 4); e += kThreads) {
+      const int64_t row = r0 + e / (kD / 4);
+      reinterpret_cast<uint2*>(p.out + row * p.out_stride + static_cast<int64_t>(h) * kD)[e % (kD / 4)] =
+          make_uint2(0, 0);
+    }
+    if (slot >= p.num_slots && tid == 0 && h == 0 && p.err) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
+    return;
+  }
+
+  // ---- sequence start: state into registers, conv window, conv weights
+  // st[kk][*] holds S^T rows (value) jr, jr + 8 and columns (key)
+  // 8kk + 2tq, 8kk + 2tq + 1, in the m16n8 accumulator layout.
+  float* Sg = p.state + (static_cast<int64_t>(slot) * p.H + h) * (kD * kD);
+  const int jr = warp * 16 + g8;
+  float st[16][4];
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) {
+    const int i0 = 8 * kk + 2 * tq;
+    st[kk][0] = Sg[i0 * kD + jr];
+    st[kk][1] = Sg[(i0 + 1) * kD + jr];
+    st[kk][2] = Sg[i0 * kD + jr + 8];
+    st[kk][3] = Sg[(i0 + 1) * kD + jr + 8];
+  }
+  auto ch_global = [&](int c) { return static_cast<int64_t>(c >> 7) * D + static_cast<int64_t>(h) * kD + (c & 127); };
+  uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
+  for (int c = tid; c < kCh; c += kThreads)
+#pragma unroll
+    for (int r = 0; r < kHist; ++r) S.raw[r][c] = cs[ch_global(c) * kHist + r];
+  const float qs = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
+
+  for (int64_t t0 = r0; t0 < r1; t0 += kL) {
+    const int L = static_cast<int>(r1 - t0 < kL ? r1 - t0 : kL);
+
+    // ---- 1. the chunk's inputs (rows past L are zero)
+    for (int e = tid; e < kL * 48; e += kThreads) {
+      const int t = e / 48, q = e - t * 48, seg = q >> 4, u = q & 15;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (t < L)
+        val = __ldg(reinterpret_cast<const uint4*>(p.qkv + (t0 + t) * p.qkv_stride + seg * D +
+                                                   static_cast<int64_t>(h) * kD) + u);
+      reinterpret_cast<uint4*>(&S.raw[kHist + t][seg * kD])[u] = val;
+    }
+    if (kOutNorm)
+      for (int e = tid; e < kL * 16; e += kThreads) {
+        const int t = e >> 4, u = e & 15;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (t < L)
+          val = __ldg(reinterpret_cast<const uint4*>(p.gate + (t0 + t) * p.gate_stride + static_cast<int64_t>(h) * kD) + u);
+        reinterpret_cast<uint4*>(S.gate[t])[u] = val;
+      }
+    for (int e = tid; e < kL * 32; e += kThreads) {
+      const int t = e >> 5, u = e & 31;
+      float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < L) val = __ldg(reinterpret_cast<const float4*>(p.g + ((t0 + t) * p.H + h) * kD) + u);
+      reinterpret_cast<float4*>(S.G[t])[u] = val;
+    }
+    if (tid < kL) S.beta[tid] = tid < L ? bf16f(p.beta[(t0 + tid) * p.H + h]) : 0.0f;
+    if (tid == 0) S.slow = 0;
+    __syncthreads();
+
+    // ---- 2. conv + SiLU over the window (outputs past L are zero); thread
+    // tid convolves channel tid (q or k block) and, below 128, v channel tid
+    {
+      float wa[kWidth], wv[kWidth], ba = 0.0f, bv = 0.0f;
+#pragma unroll
+      for (int t = 0; t < kWidth; ++t) {
+        wa[t] = __ldg(p.conv_w + ((tid >> 7) * kWidth + t) * D + static_cast<int64_t>(h) * kD + (tid & 127));
+        wv[t] = tid < kD ? __ldg(p.conv_w + (2 * kWidth + t) * D + static_cast<int64_t>(h) * kD + tid) : 0.0f;
+      }
+      if (p.conv_b) {
+        ba = __ldg(p.conv_b + ch_global(tid));
+        if (tid < kD) bv = __ldg(p.conv_b + ch_global(2 * kD + tid));
+      }
+      float x0 = bf16f(S.raw[0][tid]), x1 = bf16f(S.raw[1][tid]), x2 = bf16f(S.raw[2][tid]);
+      float* dst = tid < kD ? &S.q[0][tid] : &S.k[0][tid - kD];
+#pragma unroll 4
+      for (int t = 0; t < kL; ++t) {
+        const float x3 = bf16f(S.raw[kHist + t][tid]);
+        float y = ba;
+        y = fmaf(wa[0], x0, y);
+        y = fmaf(wa[1], x1, y);
+        y = fmaf(wa[2], x2, y);
+        y = fmaf(wa[3], x3, y);
+        dst[t * kSA] = t < L ? y / (1.0f + expf(-y)) : 0.0f;
+        x0 = x1; x1 = x2; x2 = x3;
+      }
+      if (tid < kD) {
+        const int c = 2 * kD + tid;
+        float z0 = bf16f(S.raw[0][c]), z1 = bf16f(S.raw[1][c]), z2 = bf16f(S.raw[2][c]);
+#pragma unroll 4
+        for (int t = 0; t < kL; ++t) {
+          const float z3 = bf16f(S.raw[kHist + t][c]);
+          float y = bv;
+          y = fmaf(wv[0], z0, y);
+          y = fmaf(wv[1], z1, y);
+          y = fmaf(wv[2], z2, y);
+          y = fmaf(wv[3], z3, y);
+          S.v[t][tid] = t < L ? y / (1.0f + expf(-y)) : 0.0f;
+          z0 = z1; z1 = z2; z2 = z3;
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- 3. L2 norms (warp w: tokens 4w..4w+3); cumulative decay; window slide
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt) {
+      const int t = warp * 4 + tt;
+      float4 qv = reinterpret_cast<float4*>(S.q[t])[lane];
+      float4 kv = reinterpret_cast<float4*>(S.k[t])[lane];
+      const float sq = warp_sum((qv.x * qv.x + qv.y * qv.y) + (qv.z * qv.z + qv.w * qv.w));
+      const float sk = warp_sum((kv.x * kv.x + kv.y * kv.y) + (kv.z * kv.z + kv.w * kv.w));
+      const float rq = qs / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
+      qv.x *= rq; qv.y *= rq; qv.z *= rq; qv.w *= rq;
+      kv.x *= rk; kv.y *= rk; kv.z *= rk; kv.w *= rk;
+      reinterpret_cast<float4*>(S.q[t])[lane] = qv;
+      reinterpret_cast<float4*>(S.k[t])[lane] = kv;
+    }
+    if (tid < kD) {
+      float acc = 0.0f;
+#pragma unroll 8
+      for (int t = 0; t < kL; ++t) {
+        acc += S.G[t][tid];
+        S.G[t][tid] = acc;
+      }
+    } else {
+      // the window's last three rows become the next chunk's older taps
+      for (int c = tid - kD; c < kCh; c += kThreads - kD) {
+        const uint16_t a0 = S.raw[L][c], a1 = S.raw[L + 1][c], a2 = S.raw[L + 2][c];
+        S.raw[0][c] = a0;
+        S.raw[1][c] = a1;
+        S.raw[2][c] = a2;
+      }
+    }
+    __syncthreads();
+
+    // ---- 4. split decay factors around the reference token; clear P and R
+    for (int e = tid; e < kL * kD; e += kThreads) {
+      const int t = e >> 7, i = e & (kD - 1);
+      const float d = S.G[t][i] - S.G[kRef][i];
+      if (fabsf(d) > kMaxExponent) S.slow = 1;
+      const float E = expf(d), F = expf(-d);
+      const float kv = S.k[t][i];
+      S.ek[t][i] = E * kv;
+      S.eq[t][i] = E * S.q[t][i];
+      S.fk[t][i] = F * kv;
+    }
+    for (int e = tid; e < kL * kSP; e += kThreads) (&S.P[0][0])[e] = 0.0f;
+    for (int e = tid; e < kL * kST; e += kThreads) (&S.r[0][0])[e] = 0.0f;
+    __syncthreads();
+
+    // ---- 5. P (strictly lower) and R (lower) over the key channels
+    if (!S.slow) {
+      // 6 tiles of 16 x 8 per matrix on or below the diagonal: (mm, nn)
+      for (int x = warp; x < 12; x += kWarps) {
+        const int mat = x / 6, y = x - mat * 6;
+        const int mm = y < 2 ? 0 : 1, nn = y < 2 ? y : y - 2;
+        const float(*A)[kSA] = mat ? S.eq : S.ek;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int kk = 0; kk < kD / 8; ++kk) {
+          const float2 a02 = *reinterpret_cast<const float2*>(&A[16 * mm + g8][8 * kk + 2 * tq]);
+          const float2 a13 = *reinterpret_cast<const float2*>(&A[16 * mm + g8 + 8][8 * kk + 2 * tq]);
+          const float2 bb = *reinterpret_cast<const float2*>(&S.fk[8 * nn + g8][8 * kk + 2 * tq]);
+          mma3(acc, make_a(a02.x, a13.x, a02.y, a13.y), bb.x, bb.y);
+        }
+        const int t = 16 * mm + g8, s = 8 * nn + 2 * tq;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int te = t + (e >> 1) * 8, se = s + (e & 1);
+          if (mat == 0) {
+            if (te > se) S.P[te][se] = acc[e];
+          } else {
+            if (te >= se) S.r[te][se] = acc[e];
+          }
+        }
+      }
+    } else {
+      // element-wise: pairs (t, s), s <= t
+      for (int e = tid; e < kL * (kL + 1) / 2; e += kThreads) {
+        int t = static_cast<int>((sqrtf(8.0f * e + 1.0f) - 1.0f) * 0.5f);
+        while ((t + 1) * (t + 2) / 2 <= e) ++t;
+        while (t * (t + 1) / 2 > e) --t;
+        const int s = e - t * (t + 1) / 2;
+        float pk = 0.0f, pq = 0.0f;
+        for (int i = 0; i < kD; ++i) {
+          const float f = expf(S.G[t][i] - S.G[s][i]) * S.k[s][i];
+          pk = fmaf(S.k[t][i], f, pk);
+          pq = fmaf(S.q[t][i], f, pq);
+        }
+        if (t > s) S.P[t][s] = pk;
+        S.r[t][s] = pq;
+      }
+    }
+    __syncthreads();
+
+    // ---- 6. triangular solve (thread = one column of [U | W]), left-looking:
+    // x_t = beta_t (y_t - sum_{s<t} P_ts x_s); Q_G, K_E and gamma alongside
+    {
+      const bool vcol = tid < kD;
+      const int i = tid - kD;
+      float x[kL];
+      if (!vcol) {
+        const float GL = S.G[kL - 1][i];
+#pragma unroll 1
+        for (int t = 0; t < kL; ++t) S.ket[i][t] = expf(GL - S.G[t][i]) * S.k[t][i];
+        S.gC[i] = expf(GL);
+      }
+#pragma unroll
+      for (int t = 0; t < kL; ++t) {
+        float a0 = vcol ? S.v[t][tid] : expf(S.G[t][i]) * S.k[t][i];
+        float a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+        for (int s4 = 0; s4 < t / 4 + 1; ++s4) {
+          if (4 * s4 >= t) break;
+          const float4 pr = reinterpret_cast<const float4*>(S.P[t])[s4];
+          if (4 * s4 + 0 < t) a0 = fmaf(-pr.x, x[4 * s4 + 0], a0);
+          if (4 * s4 + 1 < t) a1 = fmaf(-pr.y, x[4 * s4 + 1], a1);
+          if (4 * s4 + 2 < t) a2 = fmaf(-pr.z, x[4 * s4 + 2], a2);
+          if (4 * s4 + 3 < t) a3 = fmaf(-pr.w, x[4 * s4 + 3], a3);
+        }
+        x[t] = S.beta[t] * ((a0 + a1) + (a2 + a3));
+        if (vcol) S.ut[tid][t] = x[t];
+        else S.w[t][i] = x[t];
+      }
+      if (vcol) {
+#pragma unroll 8
+        for (int t = 0; t < kL; ++t) S.q[t][tid] *= expf(S.G[t][tid]);  // Q_G
+      }
+    }
+    __syncthreads();
+
+    // ---- 7. per warp (value rows jr, jr + 8): Delta^T = U^T - S^T W^T,
+    // O^T = S^T Q_G^T + Delta^T R^T, S^T <- S^T Diag(gamma) + Delta^T K_E
+    {
+      float d[4][4], o[4][4];
+#pragma unroll
+      for (int nn = 0; nn < 4; ++nn) {
+        const float2 u0 = *reinterpret_cast<const float2*>(&S.ut[jr][8 * nn + 2 * tq]);
+        const float2 u1 = *reinterpret_cast<const float2*>(&S.ut[jr + 8][8 * nn + 2 * tq]);
+        d[nn][0] = u0.x; d[nn][1] = u0.y; d[nn][2] = u1.x; d[nn][3] = u1.y;
+        o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.0f;
+      }
+#pragma unroll
+      for (int kk = 0; kk < kD / 8; ++kk) {
+        const FragA a = make_a(st[kk][0], st[kk][2], st[kk][1], st[kk][3]);
+#pragma unroll
+        for (int nn = 0; nn < 4; ++nn) {
+          const float2 wv2 = *reinterpret_cast<const float2*>(&S.w[8 * nn + g8][8 * kk + 2 * tq]);
+          mma3(d[nn], a, -wv2.x, -wv2.y);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < kD / 8; ++kk) {
+        const FragA a = make_a(st[kk][0], st[kk][2], st[kk][1], st[kk][3]);
+#pragma unroll
+        for (int nn = 0; nn < 4; ++nn) {
+          const float2 qv2 = *reinterpret_cast<const float2*>(&S.q[8 * nn + g8][8 * kk + 2 * tq]);
+          mma3(o[nn], a, qv2.x, qv2.y);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < kL / 8; ++kk) {
+        const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
+#pragma unroll
+        for (int nn = 0; nn < 4; ++nn) {
+          const float2 rv = *reinterpret_cast<const float2*>(&S.r[8 * nn + g8][8 * kk + 2 * tq]);
+          mma3(o[nn], a, rv.x, rv.y);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < kD / 8; ++kk) {
+        const float2 gc = *reinterpret_cast<const float2*>(&S.gC[8 * kk + 2 * tq]);
+        st[kk][0] *= gc.x; st[kk][1] *= gc.y; st[kk][2] *= gc.x; st[kk][3] *= gc.y;
+      }
+#pragma unroll
+      for (int kk = 0; kk < kL / 8; ++kk) {
+        const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
+#pragma unroll
+        for (int nn = 0; nn < kD / 8; ++nn) {
+          const float2 kv2 = *reinterpret_cast<const float2*>(&S.ket[8 * nn + g8][8 * kk + 2 * tq]);
+          mma3(st[nn], a, kv2.x, kv2.y);
+        }
+      }
+      // stage O (rows = tokens) and the per-warp partial sums of o^2
+#pragma unroll
+      for (int nn = 0; nn < 4; ++nn) {
+        const int t = 8 * nn + 2 * tq;
+        S.v[t][jr] = o[nn][0];
+        S.v[t + 1][jr] = o[nn][1];
+        S.v[t][jr + 8] = o[nn][2];
+        S.v[t + 1][jr + 8] = o[nn][3];
+        float p0 = o[nn][0] * o[nn][0] + o[nn][2] * o[nn][2];
+        float p1 = o[nn][1] * o[nn][1] + o[nn][3] * o[nn][3];
+#pragma unroll
+        for (int m = 4; m < 32; m <<= 1) {
+          p0 += __shfl_xor_sync(0xffffffffu, p0, m);
+          p1 += __shfl_xor_sync(0xffffffffu, p1, m);
+        }
+        if (g8 == 0) {
+          S.nrm[warp][t] = p0;
+          S.nrm[warp][t + 1] = p1;
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- 8. gated RMSNorm (or raw o) to bf16; warp w writes tokens 4w..4w+3
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt) {
+      const int t = warp * 4 + tt;
+      if (t >= L) break;
+      float4 y = reinterpret_cast<const float4*>(S.v[t])[lane];
+      if (kOutNorm) {
+        const float4 nw4 = __ldg(reinterpret_cast<const float4*>(p.norm_w) + lane);
+        float ss = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) ss += S.nrm[w][t];
+        const float rr = 1.0f / sqrtf(ss * (1.0f / kD) + p.eps);
+        const uint2 gb = reinterpret_cast<const uint2*>(S.gate[t])[lane];
+        y.x = y.x * rr * nw4.x / (1.0f + expf(-__uint_as_float(gb.x << 16)));
+        y.y = y.y * rr * nw4.y / (1.0f + expf(-__uint_as_float(gb.x & 0xFFFF0000u)));
+        y.z = y.z * rr * nw4.z / (1.0f + expf(-__uint_as_float(gb.y << 16)));
+        y.w = y.w * rr * nw4.w / (1.0f + expf(-__uint_as_float(gb.y & 0xFFFF0000u)));
+      }
+      reinterpret_cast<uint2*>(p.out + (t0 + t) * p.out_stride + static_cast<int64_t>(h) * kD)[lane] =
+          make_uint2(pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+    }
+    __syncthreads();
+  }
+
+  // ---- sequence end: state and conv window back to the slot
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) {
+    const int i0 = 8 * kk + 2 * tq;
+    Sg[i0 * kD + jr] = st[kk][0];
+    Sg[(i0 + 1) * kD + jr] = st[kk][1];
+    Sg[i0 * kD + jr + 8] = st[kk][2];
+    Sg[(i0 + 1) * kD + jr + 8] = st[kk][3];
+  }
+  for (int c = tid; c < kCh; c += kThreads)
+#pragma unroll
+    for (int r = 0; r < kHist; ++r) cs[ch_global(c) * kHist + r] = S.raw[r][c];
+}
+
+std::mutex g_mutex;
+bool g_attrs_set[64];
+
+cudaError_t setup() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_attrs_set[dev]) {
+    const int bytes = static_cast<int>(sizeof(PSmem));
+    if ((e = cudaFuncSetAttribute(kda_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(kda_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
+        cudaSuccess)
+      return e;
+    g_attrs_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
+  kda_internal_clear_error();
+  if (!a) return kda_internal_fail(KDA_ERR_NULLPTR, "args is NULL");
+  if (a->struct_size != sizeof(KdaPrefillArgs))
+    return kda_internal_fail(KDA_ERR_ABI, "struct_size %zu, library expects %zu", a->struct_size,
+                             sizeof(KdaPrefillArgs));
+  if (a->head_dim != KDA_HEAD_DIM || a->conv_width != KDA_CONV_WIDTH)
+    return kda_internal_fail(KDA_ERR_SHAPE, "head_dim %d / conv_width %d (need 128 / 4)", a->head_dim,
+                             a->conv_width);
+  if (a->B < 0 || a->H < 1 || a->num_slots < 1 || a->T < 0)
+    return kda_internal_fail(KDA_ERR_SHAPE, "B=%d H=%d num_slots=%d T=%lld", a->B, a->H, a->num_slots,
+                             static_cast<long long>(a->T));
+  if (a->flags & ~KDA_OUT_NORM) return kda_internal_fail(KDA_ERR_FLAGS, "flags 0x%x (only KDA_OUT_NORM)", a->flags);
+  if (static_cast<int64_t>(a->B) * a->H > 0x7fffffffLL) return kda_internal_fail(KDA_ERR_SHAPE, "B*H too large");
+  if (a->B == 0 || a->T == 0) return KDA_OK;
+  const bool norm = (a->flags & KDA_OUT_NORM) != 0;
+  const int64_t D = static_cast<int64_t>(a->H) * KDA_HEAD_DIM;
+  if (!a->cu_seqlens || !a->qkv || !a->conv_weight || !a->conv_state || !a->state || !a->g || !a->beta ||
+      !a->slot_idx || !a->out)
+    return kda_internal_fail(KDA_ERR_NULLPTR, "a required pointer is NULL");
+  if (norm && (!a->gate || !a->norm_weight))
+    return kda_internal_fail(KDA_ERR_NULLPTR, "KDA_OUT_NORM needs gate and norm_weight");
+  if (a->qkv_row_stride < 3 * D || a->out_row_stride < D || (norm && a->gate_row_stride < D))
+    return kda_internal_fail(KDA_ERR_SHAPE, "a row stride is smaller than the row");
+  if (!aligned(a->qkv, 16) || (a->qkv_row_stride & 7) || !aligned(a->state, 16) || !aligned(a->g, 16) ||
+      !aligned(a->out, 8) || (a->out_row_stride & 3) || !aligned(a->cu_seqlens, 4) || !aligned(a->slot_idx, 4) ||
+      !aligned(a->conv_weight, 4) || !aligned(a->conv_state, 2) || !aligned(a->beta, 2) ||
+      !aligned(a->err_flag, 4) || (a->conv_bias && !aligned(a->conv_bias, 4)) ||
+      (norm && (!aligned(a->gate, 16) || (a->gate_row_stride & 7) || !aligned(a->norm_weight, 16))))
+    return kda_internal_fail(KDA_ERR_ALIGN, "a pointer or row stride is not aligned as required");
+  cudaError_t e = setup();
+  if (e != cudaSuccess) return kda_internal_fail(KDA_ERR_LAUNCH, "setup: %s", cudaGetErrorString(e));
+
+  PrefillParams p;
+  p.cu = a->cu_seqlens;
+  p.qkv = a->qkv;
+  p.qkv_stride = a->qkv_row_stride;
+  p.conv_w = a->conv_weight;
+  p.conv_b = a->conv_bias;
+  p.conv_state = a->conv_state;
+  p.state = a->state;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.gate = a->gate;
+  p.gate_stride = a->gate_row_stride;
+  p.norm_w = a->norm_weight;
+  p.slot_idx = a->slot_idx;
+  p.out = a->out;
+  p.out_stride = a->out_row_stride;
+  p.T = a->T;
+  p.B = a->B;
+  p.H = a->H;
+  p.num_slots = a->num_slots;
+  p.eps = a->eps;
+  p.q_scale = a->q_scale;
+  p.err = a->err_flag;
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(a->B) * a->H));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (norm)
+    kda_prefill_kernel<true><<<grid, kThreads, sizeof(PSmem), s>>>(p);
+  else
+    kda_prefill_kernel<false><<<grid, kThreads, sizeof(PSmem), s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return kda_internal_fail(KDA_ERR_LAUNCH, "launch: %s", cudaGetErrorString(e));
+  return KDA_OK;
+}

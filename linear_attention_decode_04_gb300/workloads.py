@@ -1,7 +1,9 @@
-"""Seeded synthetic inputs for the fused KDA decode step.
+"""Seeded synthetic inputs for the fused KDA decode step and the varlen prefill.
 
 This module only draws random numbers and lays them out in the storage
-dtypes and shapes of the decode step; it holds none of the step's arithmetic.
+dtypes and shapes of the decode step (one row per sequence) and of the
+prefill (one row per token, sequences given by their lengths); it holds none
+of the method's arithmetic.
 Both the CUDA path (through the tests and the benchmark) and the fp64 oracle
 consume the same arrays it returns.
 
@@ -191,6 +193,132 @@ def make_inputs(spec: Spec, threads: int | None = None) -> Inputs:
     return Inputs(spec=spec, qkv=step["qkv"], conv_weight=cw, conv_bias=bias, conv_state=cs,
                   state=st, g=step["g"], beta=step["beta"], gate=step["gate"],
                   norm_weight=nw, slot_idx=draw_slots(spec))
+
+
+# ----------------------------------------------------------------- prefill
+
+_T_PREFILL = 100  # seed-stream tags of the prefill inputs start here
+
+
+@dataclass(frozen=True)
+class PrefillSpec:
+    """One synthetic varlen prefill batch: ``lens`` tokens per sequence (0 =
+    empty sequence); sequences listed in ``pad_seqs`` get slot 0 (padding).
+    Same value distributions as the decode step, one row per token; ``g_mode``
+    "uniform20" draws g = -20 (1 - U) (decays down to e^-20 per token)."""
+    name: str
+    lens: tuple
+    H: int
+    num_slots: int
+    seed: int
+    out_norm: bool = True
+    pad_seqs: tuple = ()
+    g_mode: str = "softplus"          # "softplus" | "uniform5" | "uniform20"
+    eps: float = 1e-6
+    with_bias: bool = False
+
+    @property
+    def B(self) -> int: return len(self.lens)
+
+    @property
+    def T(self) -> int: return int(sum(self.lens))
+
+
+# Ragged lengths: partial chunks, exact multiples of the 32-token chunk, a
+# one-token and an empty sequence, a padding sequence.
+PREFILL_SMALL = PrefillSpec("prefill_b6_h3_pool12", lens=(37, 1, 0, 64, 5, 96), H=3, num_slots=12,
+                            seed=50, pad_seqs=(4,), with_bias=True)
+PREFILL_NORM_OFF = PrefillSpec("prefill_b2_h2_pool6_normoff", lens=(70, 33), H=2, num_slots=6, seed=51,
+                               out_norm=False, g_mode="uniform5")
+PREFILL_STRONG_DECAY = PrefillSpec("prefill_b2_h2_pool5_decay20", lens=(45, 96), H=2, num_slots=5,
+                                   seed=52, g_mode="uniform20")
+# The measured prefill batch: 16 sequences, 16,384 tokens, H = 48.
+PREFILL_BENCH = PrefillSpec("prefill_b16_t16384_h48_pool64",
+                            lens=(2900, 1, 1800, 417, 64, 2048, 999, 17, 1500, 700, 2345, 100, 33,
+                                  1210, 230, 2020),
+                            H=48, num_slots=64, seed=53)
+
+
+@dataclass
+class PrefillInputs:
+    spec: PrefillSpec
+    qkv: np.ndarray          # uint16 [T, 3D]
+    conv_weight: np.ndarray  # f32 [3, 4, D]
+    conv_bias: np.ndarray | None
+    conv_state: np.ndarray   # uint16 [slots, 3D, 3]
+    state: np.ndarray        # f32 [slots, H, 128, 128]
+    g: np.ndarray            # f32 [T, H, 128]
+    beta: np.ndarray         # uint16 [T, H]
+    gate: np.ndarray         # uint16 [T, D]
+    norm_weight: np.ndarray  # f32 [128]
+    slot_idx: np.ndarray     # int32 [B]
+    cu_seqlens: np.ndarray   # int32 [B + 1]
+
+
+def make_prefill_inputs(spec: PrefillSpec, threads: int | None = None) -> PrefillInputs:
+    if threads is None:
+        threads = min(16, os.cpu_count() or 1)
+    H, D, T, B = spec.H, spec.H * HEAD_DIM, spec.T, spec.B
+    C = 3 * D
+    base = _T_PREFILL
+    qkv = f32_to_bf16_bits(_rng(spec.seed, base + _T_QKV).standard_normal((T, C), dtype=np.float32))
+    if spec.g_mode == "softplus":
+        g = (-np.logaddexp(0.0, _rng(spec.seed, base + _T_G).standard_normal((T, H, HEAD_DIM)))).astype(np.float32)
+    elif spec.g_mode in ("uniform5", "uniform20"):
+        a = 5.0 if spec.g_mode == "uniform5" else 20.0
+        g = (-a * (1.0 - _rng(spec.seed, base + _T_G).random((T, H, HEAD_DIM)))).astype(np.float32)
+    else:
+        raise ValueError(spec.g_mode)
+    zb = _rng(spec.seed, base + _T_BETA).standard_normal((T, H))
+    beta = f32_to_bf16_bits((1.0 / (1.0 + np.exp(-zb))).astype(np.float32))
+    gate = f32_to_bf16_bits(_rng(spec.seed, base + _T_GATE).standard_normal((T, D), dtype=np.float32))
+    cw = _rng(spec.seed, base + _T_CW).standard_normal((3, CONV_WIDTH, D), dtype=np.float32) * np.float32(0.5)
+    bias = None
+    if spec.with_bias:
+        bias = _rng(spec.seed, base + _T_BIAS).standard_normal(C, dtype=np.float32) * np.float32(0.1)
+    cs = _fill_pool((C, CONV_WIDTH - 1), spec.num_slots, spec.seed, base + _T_CS, 1.0, "bf16", threads)
+    st = _fill_pool((H, HEAD_DIM, HEAD_DIM), spec.num_slots, spec.seed, base + _T_STATE, 0.02, "f32", threads)
+    nw = (1.0 + 0.1 * _rng(spec.seed, base + _T_NW).standard_normal(HEAD_DIM)).astype(np.float32)
+    assert B <= spec.num_slots - 1, "not enough distinct slots"
+    perm = _rng(spec.seed, base + _T_SLOT).permutation(np.arange(1, spec.num_slots, dtype=np.int32))
+    slots = perm[:B].copy()
+    for b in spec.pad_seqs:
+        slots[b] = 0
+    cu = np.concatenate([[0], np.cumsum(spec.lens)]).astype(np.int32)
+    return PrefillInputs(spec=spec, qkv=qkv, conv_weight=cw, conv_bias=bias, conv_state=cs, state=st,
+                         g=g, beta=beta, gate=gate, norm_weight=nw, slot_idx=slots, cu_seqlens=cu)
+
+
+def prefill_algorithmic_bytes(spec: PrefillSpec) -> int:
+    """Bytes a prefill launch must move at minimum: per token of an active
+    sequence and head its q/k/v inputs, g, beta, gate (norm on) and output;
+    per token of a padding sequence its zeroed output; per active (sequence,
+    head) the state read and write and the conv state read and write; the
+    conv weights, norm weight, slots and sequence starts once."""
+    K = V = HEAD_DIM
+    H = spec.H
+    per_tok = 3 * K * 2 + K * 4 + 2 + V * 2 + (V * 2 if spec.out_norm else 0)
+    per_seq_head = 2 * K * V * 4 + 2 * 3 * K * 3 * 2
+    act = [n for b, n in enumerate(spec.lens) if b not in spec.pad_seqs and n > 0]
+    pad_tokens = sum(n for b, n in enumerate(spec.lens) if b in spec.pad_seqs)
+    fixed = 3 * CONV_WIDTH * H * K * 4 + (V * 4 if spec.out_norm else 0) + 4 * spec.B + 4 * (spec.B + 1)
+    return H * (sum(act) * per_tok + len(act) * per_seq_head + pad_tokens * V * 2) + fixed
+
+
+def prefill_algorithmic_flops(spec: PrefillSpec, chunk: int = 32) -> int:
+    """Dense-contraction FLOPs of the chunked form per active (sequence, head),
+    counted once (2 per multiply-add): for each chunk of c tokens
+    W S0 and Q_G S0 (c x 128 x 128 each), K_E^T Delta (128 x c x 128),
+    R Delta (c x c x 128), P and R (c x c x 128 each)."""
+    K = HEAD_DIM
+    total = 0
+    for b, n in enumerate(spec.lens):
+        if b in spec.pad_seqs or n == 0:
+            continue
+        for t0 in range(0, n, chunk):
+            c = min(chunk, n - t0)
+            total += 2 * (3 * c * K * K + 3 * c * c * K)
+    return spec.H * total
 
 
 def algorithmic_bytes(N: int, H: int, n_active_rows: int, out_norm: bool = True) -> int:

@@ -47,6 +47,52 @@ def test_struct_layout_matches_header(lib):
     assert fields == [f for f, _ in binding.KdaDecodeArgs._fields_]
 
 
+def test_prefill_struct_layout_matches_header(lib):
+    text = open(os.path.join(ROOT, "include", "kda_prefill.h")).read()
+    body = text[text.index("typedef struct KdaPrefillArgs {"):text.index("} KdaPrefillArgs;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in re.findall(r"([^;{]+);", body):   # "int32_t B, H, num_slots" declares three
+        first, *rest = decl.split(",")
+        fields += [first.split()[-1].lstrip("*")] + [r.strip().lstrip("*") for r in rest]
+    assert fields == [f for f, _ in binding.KdaPrefillArgs._fields_]
+
+
+def _pargs(**kw):
+    a = binding.KdaPrefillArgs(struct_size=ctypes.sizeof(binding.KdaPrefillArgs), B=3, H=4,
+                               num_slots=8, head_dim=128, conv_width=4, T=40, eps=1e-6, flags=1)
+    fake = 0x10000
+    for f in ("cu_seqlens", "qkv", "conv_weight", "conv_state", "state", "g", "beta", "gate",
+              "norm_weight", "slot_idx", "out"):
+        setattr(a, f, fake)
+        fake += 0x100000
+    a.qkv_row_stride = 3 * 4 * 128
+    a.gate_row_stride = a.out_row_stride = 4 * 128
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_prefill_host_validation_codes(lib):
+    L = binding.load_library()
+    call = lambda a: L.kda_prefill(ctypes.byref(a), None)  # noqa: E731
+    assert L.kda_prefill(None, None) == -1
+    assert call(_pargs(struct_size=8)) == -6
+    assert call(_pargs(head_dim=64)) == -2
+    assert call(_pargs(B=-1)) == -2
+    assert call(_pargs(T=-1)) == -2
+    assert call(_pargs(flags=2)) == -4                  # conv-state flag is not a prefill option
+    assert call(_pargs(B=0)) == 0                       # no-op, no launch
+    assert call(_pargs(T=0)) == 0
+    assert call(_pargs(cu_seqlens=None)) == -1
+    assert call(_pargs(gate=None)) == -1                # norm on needs the gate
+    assert call(_pargs(qkv_row_stride=100)) == -2
+    assert call(_pargs(qkv_row_stride=3 * 4 * 128 + 4)) == -3
+    assert call(_pargs(state=0x10004)) == -3
+    assert call(_pargs(out=0x10004)) == -3
+    assert b"aligned" in L.kda_last_error()
+
+
 def _args(**kw):
     a = binding.KdaDecodeArgs(struct_size=ctypes.sizeof(binding.KdaDecodeArgs), N=4, H=12,
                               num_slots=8, head_dim=128, conv_width=4, eps=1e-6, flags=3)

@@ -1,0 +1,193 @@
+"""GPU parity of the chunked prefill (``kda_prefill``) against the fp64
+prefill oracle (the decode recurrence run token by token).
+
+Tolerances are the decode step's: bf16 output within 3e-2 and within one
+bf16 ulp (+1e-5) of the exact value; recurrent state within 1e-4 + 1e-4|ref|
+(fp32 arithmetic; the tensor-core products use split tf32 operands, whose
+three partial products keep about 21 significant bits per operand); conv
+state bit-exact; every slot no sequence uses bit-identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_testlib as T
+import oracle
+from linear_attention_decode_04_gb300 import KdaPrefillCall, kda_decode, kda_prefill
+from linear_attention_decode_04_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def to_device(x: W.PrefillInputs, dev, out_row_pad: int = 0):
+    D = x.spec.H * W.HEAD_DIM
+    d = dict(
+        qkv=T.bf16_tensor(x.qkv, dev), conv_weight=torch.from_numpy(x.conv_weight).to(dev),
+        conv_bias=None if x.conv_bias is None else torch.from_numpy(x.conv_bias).to(dev),
+        conv_state=T.bf16_tensor(x.conv_state, dev), state=torch.from_numpy(x.state).to(dev),
+        g=torch.from_numpy(x.g).to(dev), beta=T.bf16_tensor(x.beta, dev),
+        gate=T.bf16_tensor(x.gate, dev), norm_weight=torch.from_numpy(x.norm_weight).to(dev),
+        cu_seqlens=torch.from_numpy(x.cu_seqlens).to(dev), slot_idx=torch.from_numpy(x.slot_idx).to(dev),
+        err_flag=torch.zeros(1, dtype=torch.int32, device=dev))
+    # NaN-filled: any row the kernel should write and does not is caught
+    d["out_full"] = torch.full((x.spec.T, D + out_row_pad), float("nan"), dtype=torch.bfloat16, device=dev)
+    d["out"] = d["out_full"][:, :D]
+    return d
+
+
+def run_gpu(x: W.PrefillInputs, d: dict):
+    kda_prefill(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
+                d["cu_seqlens"], d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"],
+                conv_bias=d["conv_bias"], eps=x.spec.eps, out_norm=x.spec.out_norm, err_flag=d["err_flag"])
+
+
+def run_oracle(x: W.PrefillInputs, seqs=None):
+    """Oracle over all sequences, or over a subset (sequences are independent:
+    the subset is re-batched with its own cu_seqlens)."""
+    if seqs is None:
+        return oracle.prefill(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state,
+                              g=x.g, beta=x.beta, gate=x.gate, norm_weight=x.norm_weight,
+                              conv_bias=x.conv_bias, slot_idx=x.slot_idx, cu_seqlens=x.cu_seqlens,
+                              H=x.spec.H, eps=x.spec.eps, out_norm=x.spec.out_norm), None
+    rows = np.concatenate([np.arange(x.cu_seqlens[b], x.cu_seqlens[b + 1]) for b in seqs]).astype(np.int64)
+    lens = [int(x.cu_seqlens[b + 1] - x.cu_seqlens[b]) for b in seqs]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    r = oracle.prefill(qkv=x.qkv[rows], conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state,
+                       g=x.g[rows], beta=x.beta[rows], gate=x.gate[rows], norm_weight=x.norm_weight,
+                       conv_bias=x.conv_bias, slot_idx=x.slot_idx[list(seqs)], cu_seqlens=cu,
+                       H=x.spec.H, eps=x.spec.eps, out_norm=x.spec.out_norm)
+    return r, rows
+
+
+def compare(x: W.PrefillInputs, d: dict, ref, rows=None, seqs=None):
+    out = T.bf16_bits(d["out"])
+    if rows is None:
+        covered = np.zeros(x.spec.T, bool)
+        for b in range(x.spec.B):
+            covered[x.cu_seqlens[b]:x.cu_seqlens[b + 1]] = True
+        assert covered.all()
+        T.check_out(out, ref)
+    else:
+        T.check_out(out[rows], ref)
+    followed = range(x.spec.B) if seqs is None else seqs
+    written = {int(x.slot_idx[b]) for b in followed
+               if 0 < x.slot_idx[b] < x.spec.num_slots and x.cu_seqlens[b + 1] > x.cu_seqlens[b]}
+    used = {int(v) for v in x.slot_idx}
+    st = d["state"].cpu().numpy()
+    cs = T.bf16_bits(d["conv_state"])
+    worst = 0.0
+    for s in range(x.spec.num_slots):
+        if s in written:
+            worst = max(worst, T.check_state_slot(st[s], ref.state[s], f"slot {s}"))
+            assert np.array_equal(cs[s], ref.conv_state[s]), f"conv state of slot {s}"
+        elif seqs is None or s not in used:
+            # no sequence writes it (or the oracle followed every sequence)
+            assert np.array_equal(st[s], x.state[s]), f"untouched slot {s} changed"
+            assert np.array_equal(cs[s], x.conv_state[s]), f"untouched conv slot {s} changed"
+    return worst
+
+
+@pytest.mark.parametrize("spec", [W.PREFILL_SMALL, W.PREFILL_NORM_OFF, W.PREFILL_STRONG_DECAY],
+                         ids=lambda s: s.name)
+def test_prefill_matches_oracle(cuda_device, spec):
+    x = W.make_prefill_inputs(spec)
+    d = to_device(x, cuda_device)
+    run_gpu(x, d)
+    torch.cuda.synchronize(cuda_device)
+    assert int(d["err_flag"].item()) == 0
+    ref, _ = run_oracle(x)
+    compare(x, d, ref)
+
+
+def test_prefill_padding_rows_zero_and_row_stride(cuda_device):
+    # a padding sequence writes zeros; rows are strided (out row padding untouched)
+    x = W.make_prefill_inputs(W.PREFILL_SMALL)
+    d = to_device(x, cuda_device, out_row_pad=8)
+    run_gpu(x, d)
+    torch.cuda.synchronize(cuda_device)
+    pad = 4
+    rows = slice(int(x.cu_seqlens[pad]), int(x.cu_seqlens[pad + 1]))
+    assert np.all(T.bf16_bits(d["out"])[rows] == 0)
+    assert torch.isnan(d["out_full"][:, -8:].float()).all()
+
+
+def test_prefill_full_batch_sampled(cuda_device):
+    # the measured batch (16 sequences, 16,384 tokens, H = 48); the oracle
+    # follows six sequences: one token, a partial chunk, exact chunks, long
+    x = W.make_prefill_inputs(W.PREFILL_BENCH)
+    d = to_device(x, cuda_device)
+    run_gpu(x, d)
+    torch.cuda.synchronize(cuda_device)
+    assert int(d["err_flag"].item()) == 0
+    seqs = (1, 4, 7, 11, 12, 3)
+    ref, rows = run_oracle(x, seqs)
+    compare(x, d, ref, rows=rows, seqs=seqs)
+
+
+def test_prefill_then_decode_continues_the_state(cuda_device):
+    # prefill a batch, then one decode step on the same pools: both against
+    # the oracle chained the same way
+    x = W.make_prefill_inputs(W.PREFILL_SMALL)
+    d = to_device(x, cuda_device)
+    run_gpu(x, d)
+    ref, _ = run_oracle(x)
+    # one decode token per sequence, same slots
+    B, H = x.spec.B, x.spec.H
+    step = W.draw_step_inputs(W.Spec("prefill_next_token", N=B, H=H, num_slots=x.spec.num_slots, seed=77))
+    out = torch.full((B, H * 128), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+    kda_decode(T.bf16_tensor(step["qkv"], cuda_device), d["conv_weight"], d["conv_state"], d["state"],
+               torch.from_numpy(step["g"]).to(cuda_device), T.bf16_tensor(step["beta"], cuda_device),
+               d["slot_idx"], out, gate=T.bf16_tensor(step["gate"], cuda_device),
+               norm_weight=d["norm_weight"], conv_bias=d["conv_bias"], eps=x.spec.eps)
+    torch.cuda.synchronize(cuda_device)
+    dec = oracle.decode(qkv=step["qkv"], conv_weight=x.conv_weight, conv_state=ref.conv_state,
+                        state=ref.state, g=step["g"], beta=step["beta"], slot_idx=x.slot_idx, H=H,
+                        gate=step["gate"], norm_weight=x.norm_weight, conv_bias=x.conv_bias, eps=x.spec.eps)
+    T.check_out(T.bf16_bits(out), dec)
+    st = d["state"].cpu().numpy()
+    for s in {int(v) for v in x.slot_idx if v > 0}:
+        T.check_state_slot(st[s], dec.state[s], f"slot {s} after prefill + decode")
+
+
+def test_prefill_device_errors_flagged(cuda_device):
+    # a slot past the pool and a decreasing cu_seqlens entry: flagged, the
+    # other sequences still correct, nothing written for the bad ones
+    x = W.make_prefill_inputs(W.PREFILL_SMALL)
+    x.slot_idx[0] = x.spec.num_slots + 3
+    d = to_device(x, cuda_device)
+    run_gpu(x, d)
+    torch.cuda.synchronize(cuda_device)
+    assert int(d["err_flag"].item()) & 1
+    ref, _ = run_oracle(x)
+    compare(x, d, ref)
+
+    y = W.make_prefill_inputs(W.PREFILL_SMALL)
+    d2 = to_device(y, cuda_device)
+    bad = d2["cu_seqlens"].clone()
+    bad[2] = bad[1] - 1   # sequence 1 ends before it starts; sequence 2 starts past its end
+    d2["cu_seqlens"] = bad
+    run_gpu(y, d2)
+    torch.cuda.synchronize(cuda_device)
+    assert int(d2["err_flag"].item()) & 4
+
+
+def test_prefill_graph_capture_and_prepared_call(cuda_device):
+    x = W.make_prefill_inputs(W.PREFILL_NORM_OFF)
+    d = to_device(x, cuda_device)
+    call = KdaPrefillCall(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
+                          d["cu_seqlens"], d["slot_idx"], d["out"], gate=d["gate"],
+                          norm_weight=d["norm_weight"], conv_bias=d["conv_bias"], eps=x.spec.eps,
+                          out_norm=x.spec.out_norm, err_flag=d["err_flag"])
+    state0, cs0 = d["state"].clone(), d["conv_state"].clone()
+    s = torch.cuda.Stream(cuda_device)
+    call(s)          # eager once (device set-up), then restore the pools and capture
+    torch.cuda.synchronize(cuda_device)
+    d["state"].copy_(state0)
+    d["conv_state"].copy_(cs0)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call(s)
+    graph.replay()
+    torch.cuda.synchronize(cuda_device)
+    ref, _ = run_oracle(x)
+    compare(x, d, ref)
