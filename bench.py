@@ -381,6 +381,91 @@ def run_case(args) -> dict | None:
             "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup}
 
 
+def measured_tf32_peak() -> tuple[float, str]:
+    """Dense tf32 tensor peak: the measured bf16 burst figure scaled by the
+    nominal tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        return bf16 * 1.1 / 2.25, "measured bf16_tflops x 1.1/2.25"
+    except Exception:
+        return 1900.0 * 1.1 / 2.25, "fallback 1.9 PFLOP/s bf16 x 1.1/2.25"
+
+
+def run_prefill(args) -> dict:
+    """Chunked prefill of one varlen batch (16 sequences, 16,384 tokens,
+    H = 48): each step is one kda_prefill launch over the whole batch, inputs
+    resident in HBM (1.5 GB, larger than L2).  The state pools carry over from
+    step to step.  ``value`` = (token, head) updates per second."""
+    import torch
+
+    from linear_attention_decode_04_gb300 import KdaPrefillCall
+    from linear_attention_decode_04_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    spec = W.PREFILL_BENCH
+    x = W.make_prefill_inputs(spec)
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    t = dict(qkv=bf(x.qkv), conv_weight=torch.from_numpy(x.conv_weight).to(dev), conv_state=bf(x.conv_state),
+             state=torch.from_numpy(x.state).to(dev), g=torch.from_numpy(x.g).to(dev), beta=bf(x.beta),
+             cu_seqlens=torch.from_numpy(x.cu_seqlens).to(dev), slot_idx=torch.from_numpy(x.slot_idx).to(dev),
+             out=torch.empty(spec.T, spec.H * 128, dtype=torch.bfloat16, device=dev), gate=bf(x.gate),
+             norm_weight=torch.from_numpy(x.norm_weight).to(dev),
+             err_flag=torch.zeros(1, dtype=torch.int32, device=dev))
+    call = KdaPrefillCall(t["qkv"], t["conv_weight"], t["conv_state"], t["state"], t["g"], t["beta"],
+                          t["cu_seqlens"], t["slot_idx"], t["out"], gate=t["gate"],
+                          norm_weight=t["norm_weight"], eps=spec.eps, out_norm=spec.out_norm,
+                          err_flag=t["err_flag"])
+    stream = torch.cuda.Stream(dev)
+    for _ in range(args.warmup):
+        call(stream)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            call(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if int(t["err_flag"].item()):
+        raise SystemExit("device error flag raised")
+    ms = ev0.elapsed_time(ev1) / args.steps
+    act_tokens = sum(n for b, n in enumerate(spec.lens) if b not in spec.pad_seqs)
+    nbytes = W.prefill_algorithmic_bytes(spec)
+    flops = W.prefill_algorithmic_flops(spec)
+    peak, kind = measured_peak()
+    tpeak, tkind = measured_tf32_peak()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    tflops = flops / (ms / 1e3) / 1e12
+    res = {"mode": "prefill", "metric": "chunked KDA prefill: (token, head) updates/s",
+           "value": act_tokens * spec.H / (ms / 1e3), "unit": "updates/s", "ms_per_launch": ms,
+           "workload": spec.name, "tokens": spec.T, "sequences": spec.B, "H": spec.H,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                        "peak_source": f"{kind} hbm_gbs", "algorithmic_bytes_per_launch": nbytes},
+           "tensor": {"achieved_tflops": tflops, "peak_tflops": tpeak, "frac": tflops / tpeak,
+                      "peak_source": tkind, "algorithmic_flops_per_launch": flops,
+                      "note": "chunk-form contractions counted once; the kernel issues three tf32 "
+                              "products per contraction (split operands)"},
+           "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup, "gpu_launches": args.steps}
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = os.cpu_count() or 1
+        sample = (1, 4, 7, 11, 12, 3, 9)      # 2,231 tokens of 7 sequences
+        rows = np.concatenate([np.arange(x.cu_seqlens[b], x.cu_seqlens[b + 1]) for b in sample])
+        cu = np.concatenate([[0], np.cumsum([spec.lens[b] for b in sample])]).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.prefill(qkv=x.qkv[rows], conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state,
+                       g=x.g[rows], beta=x.beta[rows], gate=x.gate[rows], norm_weight=x.norm_weight,
+                       slot_idx=x.slot_idx[list(sample)], cu_seqlens=cu, H=spec.H, eps=spec.eps,
+                       threads=threads, want_f64=False)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": len(rows) * spec.H / dt, "unit": "updates/s", "cores": threads,
+                               "kind": "oracle",
+                               "sample": f"fp64 C prefill oracle, {len(sample)} of {spec.B} sequences "
+                                         f"({len(rows)} tokens x {spec.H} heads, {dt:.1f} s)"}
+    return res
+
+
 def run_chunk_metadata(args) -> dict:
     """Timing of the device-side chunk metadata build for a prefill batch
     (256 sequences, lengths 1..8192 tokens, chunk size 64): 20 builds
@@ -468,9 +553,11 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--ref-layers", type=int, default=2, help="layers per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata"), default="stack69",
+    ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill"),
+                    default="stack69",
                     help="stack69: the headline 69-layer graph step; layer / roofline: one "
-                         "launch configuration timed on its own (profiling aid)")
+                         "launch configuration timed on its own (profiling aid); prefill: the "
+                         "chunked varlen prefill")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -478,6 +565,8 @@ def main(argv=None):
         res = run_reference(args)
     elif args.case == "chunk_metadata":
         res = run_chunk_metadata(args)
+    elif args.case == "prefill":
+        res = run_prefill(args)
     elif args.case != "stack69":
         res = run_case(args)
     else:

@@ -54,7 +54,8 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kCh = 3 * kD;       // q | k | v channels of one head
 constexpr int kSA = 136;          // row stride (floats) of [token][128] operands
-constexpr int kST = 40;           // row stride (floats) of [128][token] and [token][token] operands
+constexpr int kST = 40;           // row stride (floats) of R [token][token] (float2 reads)
+constexpr int kSK = 132;          // row stride (floats) of K_E and U, read as scalars
 constexpr int kSP = 36;           // row stride (floats) of P (rows read as float4)
 constexpr int kRef = 15;          // reference token of the split decay factors
 constexpr float kMaxExponent = 80.0f;  // |G_t - G_m| above this: element-wise path
@@ -92,8 +93,8 @@ struct __align__(16) PSmem {
   float v[kL][kSA];               // v~, then the chunk's output O (staging)
   float G[kL][kD];                // cumulative log decay
   union { float ek[kL][kSA]; float w[kL][kSA]; };        // exp(G - G_m) k^, then W
-  union { float fk[kL][kSA]; float ket[kD][kST]; };      // exp(G_m - G) k^, then K_E^T
-  union { float eq[kL][kSA]; float ut[kD][kST]; };       // exp(G - G_m) q^, then U^T
+  union { float fk[kL][kSA]; float ke[kL][kSK]; };       // exp(G_m - G) k^, then K_E
+  union { float eq[kL][kSA]; float u[kL][kSK]; };        // exp(G - G_m) q^, then U
   float P[kL][kSP];               // P (strictly lower)
   float r[kL][kST];               // R (lower, diagonal included)
   float gC[kD];                   // exp(G_{L-1}): decay of the whole chunk
@@ -151,6 +152,15 @@ __device__ __forceinline__ void mma3(float (&c)[4], const FragA& a, float b0, fl
   mma_tf32(c, a.lo, h0, h1);
   mma_tf32(c, a.hi, l0, l1);
   mma_tf32(c, a.hi, h0, h1);
+}
+
+// The same with the small terms in a separate accumulator: c += hi*hi, cl += lo*hi + hi*lo.
+__device__ __forceinline__ void mma3s(float (&c)[4], float (&cl)[4], const FragA& a, float b0, float b1) {
+  const uint32_t h0 = to_tf32(b0), h1 = to_tf32(b1);
+  const uint32_t l0 = to_tf32(b0 - __uint_as_float(h0)), l1 = to_tf32(b1 - __uint_as_float(h1));
+  mma_tf32(cl, a.lo, h0, h1);
+  mma_tf32(c, a.hi, h0, h1);
+  mma_tf32(cl, a.hi, l0, l1);
 }
 
 // One CTA per (sequence, head); blockIdx.x = b * H + h.
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
         y = fmaf(wa[1], x1, y);
         y = fmaf(wa[2], x2, y);
         y = fmaf(wa[3], x3, y);
-        dst[t * kSA] = t < L ? y / (1.0f + expf(-y)) : 0.0f;
+        dst[t * kSA] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
         x0 = x1; x1 = x2; x2 = x3;
       }
       if (tid < kD) {
@@ -268,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
           y = fmaf(wv[1], z1, y);
           y = fmaf(wv[2], z2, y);
           y = fmaf(wv[3], z3, y);
-          S.v[t][tid] = t < L ? y / (1.0f + expf(-y)) : 0.0f;
+          S.v[t][tid] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
           z0 = z1; z1 = z2; z2 = z3;
         }
       }
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
       const int t = e >> 7, i = e & (kD - 1);
       const float d = S.G[t][i] - S.G[kRef][i];
       if (fabsf(d) > kMaxExponent) S.slow = 1;
-      const float E = expf(d), F = expf(-d);
+      const float E = __expf(d), F = __expf(-d);
       const float kv = S.k[t][i];
       S.ek[t][i] = E * kv;
       S.eq[t][i] = E * S.q[t][i];
@@ -376,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
       if (!vcol) {
         const float GL = S.G[kL - 1][i];
 #pragma unroll 1
-        for (int t = 0; t < kL; ++t) S.ket[i][t] = expf(GL - S.G[t][i]) * S.k[t][i];
+        for (int t = 0; t < kL; ++t) S.ke[t][i] = expf(GL - S.G[t][i]) * S.k[t][i];
         S.gC[i] = expf(GL);
       }
 #pragma unroll
@@ -393,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
           if (4 * s4 + 3 < t) a3 = fmaf(-pr.w, x[4 * s4 + 3], a3);
         }
         x[t] = S.beta[t] * ((a0 + a1) + (a2 + a3));
-        if (vcol) S.ut[tid][t] = x[t];
+        if (vcol) S.u[t][tid] = x[t];
         else S.w[t][i] = x[t];
       }
       if (vcol) {
@@ -404,15 +414,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
     __syncthreads();
 
     // ---- 7. per warp (value rows jr, jr + 8): Delta^T = U^T - S^T W^T,
-    // O^T = S^T Q_G^T + Delta^T R^T, S^T <- S^T Diag(gamma) + Delta^T K_E
+    // O^T = S^T Q_G^T + Delta^T R^T, S^T <- S^T Diag(gamma) + Delta^T K_E.
+    // The two products with S^T share its split fragments; the small
+    // (high x low) terms go to their own accumulators so that the chains of
+    // dependent MMAs stay short.
     {
-      float d[4][4], o[4][4];
+      float d[4][4], o[4][4], dl[4][4], ol[4][4];
 #pragma unroll
       for (int nn = 0; nn < 4; ++nn) {
-        const float2 u0 = *reinterpret_cast<const float2*>(&S.ut[jr][8 * nn + 2 * tq]);
-        const float2 u1 = *reinterpret_cast<const float2*>(&S.ut[jr + 8][8 * nn + 2 * tq]);
-        d[nn][0] = u0.x; d[nn][1] = u0.y; d[nn][2] = u1.x; d[nn][3] = u1.y;
-        o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.0f;
+        d[nn][0] = S.u[8 * nn + 2 * tq][jr];
+        d[nn][1] = S.u[8 * nn + 2 * tq + 1][jr];
+        d[nn][2] = S.u[8 * nn + 2 * tq][jr + 8];
+        d[nn][3] = S.u[8 * nn + 2 * tq + 1][jr + 8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nn][e] = dl[nn][e] = ol[nn][e] = 0.0f;
       }
 #pragma unroll
       for (int kk = 0; kk < kD / 8; ++kk) {
@@ -420,18 +435,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
 #pragma unroll
         for (int nn = 0; nn < 4; ++nn) {
           const float2 wv2 = *reinterpret_cast<const float2*>(&S.w[8 * nn + g8][8 * kk + 2 * tq]);
-          mma3(d[nn], a, -wv2.x, -wv2.y);
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < kD / 8; ++kk) {
-        const FragA a = make_a(st[kk][0], st[kk][2], st[kk][1], st[kk][3]);
-#pragma unroll
-        for (int nn = 0; nn < 4; ++nn) {
+          mma3s(d[nn], dl[nn], a, -wv2.x, -wv2.y);
           const float2 qv2 = *reinterpret_cast<const float2*>(&S.q[8 * nn + g8][8 * kk + 2 * tq]);
-          mma3(o[nn], a, qv2.x, qv2.y);
+          mma3s(o[nn], ol[nn], a, qv2.x, qv2.y);
         }
       }
+#pragma unroll
+      for (int nn = 0; nn < 4; ++nn)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          d[nn][e] += dl[nn][e];
+          o[nn][e] += ol[nn][e];
+        }
 #pragma unroll
       for (int kk = 0; kk < kL / 8; ++kk) {
         const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
@@ -451,8 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
         const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
 #pragma unroll
         for (int nn = 0; nn < kD / 8; ++nn) {
-          const float2 kv2 = *reinterpret_cast<const float2*>(&S.ket[8 * nn + g8][8 * kk + 2 * tq]);
-          mma3(st[nn], a, kv2.x, kv2.y);
+          mma3(st[nn], a, S.ke[8 * kk + 2 * tq][8 * nn + g8], S.ke[8 * kk + 2 * tq + 1][8 * nn + g8]);
         }
       }
       // stage O (rows = tokens) and the per-warp partial sums of o^2
@@ -491,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
         for (int w = 0; w < kWarps; ++w) ss += S.nrm[w][t];
         const float rr = 1.0f / sqrtf(ss * (1.0f / kD) + p.eps);
         const uint2 gb = reinterpret_cast<const uint2*>(S.gate[t])[lane];
-        y.x = y.x * rr * nw4.x / (1.0f + expf(-__uint_as_float(gb.x << 16)));
-        y.y = y.y * rr * nw4.y / (1.0f + expf(-__uint_as_float(gb.x & 0xFFFF0000u)));
-        y.z = y.z * rr * nw4.z / (1.0f + expf(-__uint_as_float(gb.y << 16)));
-        y.w = y.w * rr * nw4.w / (1.0f + expf(-__uint_as_float(gb.y & 0xFFFF0000u)));
+        y.x = __fdividef(y.x * rr * nw4.x, 1.0f + __expf(-__uint_as_float(gb.x << 16)));
+        y.y = __fdividef(y.y * rr * nw4.y, 1.0f + __expf(-__uint_as_float(gb.x & 0xFFFF0000u)));
+        y.z = __fdividef(y.z * rr * nw4.z, 1.0f + __expf(-__uint_as_float(gb.y << 16)));
+        y.w = __fdividef(y.w * rr * nw4.w, 1.0f + __expf(-__uint_as_float(gb.y & 0xFFFF0000u)));
       }
       reinterpret_cast<uint2*>(p.out + (t0 + t) * p.out_stride + static_cast<int64_t>(h) * kD)[lane] =
           make_uint2(pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
