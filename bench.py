@@ -413,7 +413,8 @@ def run_prefill(args) -> dict:
              norm_weight=torch.from_numpy(x.norm_weight).to(dev),
              err_flag=torch.zeros(1, dtype=torch.int32, device=dev))
     call = KdaPrefillCall(t["qkv"], t["conv_weight"], t["conv_state"], t["state"], t["g"], t["beta"],
-                          t["cu_seqlens"], t["slot_idx"], t["out"], gate=t["gate"],
+                          t["cu_seqlens"], t["slot_idx"], t["out"],
+                          cu_seqlens_cpu=torch.from_numpy(x.cu_seqlens), gate=t["gate"],
                           norm_weight=t["norm_weight"], eps=spec.eps, out_norm=spec.out_norm,
                           err_flag=t["err_flag"])
     stream = torch.cuda.Stream(dev)
@@ -446,7 +447,9 @@ def run_prefill(args) -> dict:
                       "peak_source": tkind, "algorithmic_flops_per_launch": flops,
                       "note": "chunk-form contractions counted once; the kernel issues three tf32 "
                               "products per contraction (split operands)"},
-           "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup, "gpu_launches": args.steps}
+           "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup,
+           "gpu_launches": 3 * args.steps,
+           "kernels": "per step: chunk metadata, chunk-parallel kernel, scan kernel"}
     if not args.no_cpu_baseline:
         import oracle
         threads = os.cpu_count() or 1

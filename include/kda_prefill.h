@@ -28,13 +28,20 @@
  * This is the definition in the decode header (kda_decode.h) applied to a
  * sequence; the state between tokens is never stored, so it is not rounded.
  *
- * Method (device side): one CTA per (sequence, head) walks the sequence in
- * chunks of 32 tokens.  Within a chunk the recurrence is solved in closed
- * form (cumulative decays, a lower-triangular solve for the chunk's deltas);
- * the contractions with the state and between tokens run on the tensor cores
+ * Method (device side), two kernels per call:
+ *   1. chunk-parallel: one CTA per (chunk, head), the chunks taken from the
+ *      (sequence, chunk) metadata of kda_chunk_metadata.h (P2 实现拆解 item
+ *      2) built with chunk size KDA_PREFILL_CHUNK.  Each CTA does the work of
+ *      its chunk that does not depend on the state entering it (conv, norms,
+ *      cumulative decays, the chunk's lower-triangular solve) and writes it
+ *      to the workspace;
+ *   2. scan: one CTA per (sequence, head) walks that sequence's chunks in
+ *      order (its rows in the workspace start at chunk_offsets[b]) with the
+ *      state held in registers, and applies each chunk to the state and the
+ *      outputs.
+ * The contractions with the state and between tokens run on the tensor cores
  * (tf32 operands split into high and low parts, three products per
- * contraction, fp32 accumulation), the state stays in registers for the whole
- * sequence.
+ * contraction, fp32 accumulation).
  *
  * Memory: all pointers are caller-owned device memory; the library allocates,
  * frees and synchronises nothing and reads no device memory from the host, so
@@ -69,7 +76,7 @@ extern "C" {
  *   g            fp32 [T][H][128] log-decay, already activated (alpha = exp(g))
  *   beta         bf16 [T][H], already activated
  *   gate         bf16 [T][gate_row_stride] (KDA_OUT_NORM only; stride >= D,
- *                a multiple of 8)
+ *                a multiple of 4)
  *   norm_weight  fp32 [128] (KDA_OUT_NORM only)
  *   cu_seqlens   int32 [B+1] on the device: cu_seqlens[0] = 0, non-decreasing,
  *                cu_seqlens[B] <= T.  A sequence whose bounds break this is
@@ -78,10 +85,20 @@ extern "C" {
  *                sequences of a call)
  *   out          bf16 [T][out_row_stride] (stride >= D, a multiple of 4);
  *                rows outside every sequence are not written
+ *   chunk_indices int32 [num_chunks][2] and chunk_offsets int64 [B+1]: the
+ *                output of kda_chunk_metadata(cu_seqlens, B, KDA_PREFILL_CHUNK,
+ *                ...) for this batch (enqueued before this call on the same
+ *                stream); num_chunks is their row count, known on the host
+ *                from the sequence lengths.  If chunk_offsets does not match
+ *                cu_seqlens, the sequence is skipped and KDA_DEVERR_SEQLENS set.
+ *   workspace    device scratch of workspace_bytes >=
+ *                kda_prefill_workspace_bytes(num_chunks, H) bytes
  *   err_flag     int32 or NULL: device-side error bits (KDA_DEVERR_*)
  *
- * Alignment: state, g and norm_weight 16 bytes; qkv, gate, out 16 / 16 / 8
- * bytes with row strides as stated; cu_seqlens, slot_idx, err_flag 4 bytes.
+ * Alignment: state, g, norm_weight and workspace 16 bytes; qkv 16 bytes with
+ * a row stride that is a multiple of 8 elements; gate and out 8 bytes with row
+ * strides that are multiples of 4; chunk_indices and chunk_offsets 8 bytes;
+ * cu_seqlens, slot_idx, err_flag 4 bytes.
  */
 typedef struct KdaPrefillArgs {
   size_t struct_size; /* sizeof(KdaPrefillArgs) */
@@ -106,13 +123,23 @@ typedef struct KdaPrefillArgs {
   float q_scale; /* 0 => 1/sqrt(128) */
   uint32_t flags; /* KDA_OUT_NORM or 0; other bits are rejected */
   int32_t* err_flag;
+  const int32_t* chunk_indices;
+  const int64_t* chunk_offsets;
+  int64_t num_chunks;
+  void* workspace;
+  int64_t workspace_bytes;
 } KdaPrefillArgs;
+
+/* Workspace bytes a call with `num_chunks` chunks and H heads needs (about
+ * 72.5 KiB per (chunk, head)); -1 for a negative count or H < 1. */
+int64_t kda_prefill_workspace_bytes(int64_t num_chunks, int32_t H);
 
 /*
  * Enqueue the prefill on `stream` (a cudaStream_t; NULL = legacy default).
  * Returns KDA_OK or a negative KDA_ERR_* code of kda_decode.h; on an error
  * nothing is launched and kda_last_error() describes it.  B == 0 or T == 0
- * is a no-op.
+ * is a no-op.  The chunk kernel reads the slots' old conv state; the scan
+ * kernel, which runs after it, writes the new one.
  */
 int kda_prefill(const KdaPrefillArgs* args, void* stream);
 

@@ -73,7 +73,13 @@ class KdaPrefillArgs(ctypes.Structure):
         ("out", ctypes.c_void_p), ("out_row_stride", ctypes.c_int64),
         ("eps", ctypes.c_float), ("q_scale", ctypes.c_float),
         ("flags", ctypes.c_uint32), ("err_flag", ctypes.c_void_p),
+        ("chunk_indices", ctypes.c_void_p), ("chunk_offsets", ctypes.c_void_p),
+        ("num_chunks", ctypes.c_int64), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_int64),
     ]
+
+
+PREFILL_CHUNK = 32  # KDA_PREFILL_CHUNK
 
 
 def library_path() -> str:
@@ -105,6 +111,8 @@ def load_library() -> ctypes.CDLL:
             L.kda_chunk_metadata.restype = ctypes.c_int
             L.kda_prefill.argtypes = [ctypes.POINTER(KdaPrefillArgs), ctypes.c_void_p]
             L.kda_prefill.restype = ctypes.c_int
+            L.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
+            L.kda_prefill_workspace_bytes.restype = ctypes.c_int64
             L.kda_abi_version.argtypes = []
             L.kda_abi_version.restype = ctypes.c_int
             if L.kda_abi_version() != ABI_VERSION:
@@ -336,8 +344,11 @@ def kda_chunk_metadata(cu_seqlens: torch.Tensor, cu_seqlens_cpu: torch.Tensor, c
 
 class KdaPrefillCall:
     """A prepared ``kda_prefill`` call (``include/kda_prefill.h``): validates
-    and packs the arguments once; each ``__call__`` is one C call.  Keeps
-    references to the tensors it points at.
+    and packs the arguments once, allocates the chunk metadata and the
+    workspace (sized from ``cu_seqlens_cpu``, the host copy of the sequence
+    starts, so nothing waits for the device); each ``__call__`` enqueues the
+    device-side metadata build and the prefill.  Keeps references to the
+    tensors it points at.
 
     Shapes: T token rows, B sequences, H heads, D = H * 128.
       qkv [T, >=3D] bf16, conv_weight [3, 4, D] f32, conv_state [slots, 3D, 3]
@@ -347,7 +358,7 @@ class KdaPrefillCall:
       out_norm."""
 
     def __init__(self, qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
-                 gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
+                 cu_seqlens_cpu=None, gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, err_flag=None):
         self._lib = load_library()
         dev = state.device
@@ -377,6 +388,13 @@ class KdaPrefillCall:
         B = cu_seqlens.numel() - 1
         if slot_idx.numel() != B:
             raise ValueError(f"slot_idx must have one entry per sequence ({B})")
+        if cu_seqlens_cpu is None:
+            cu_seqlens_cpu = cu_seqlens.cpu()  # a device read; pass the host copy to avoid it
+        cu_cpu = torch.as_tensor(cu_seqlens_cpu).to(torch.int64).reshape(-1)
+        if cu_cpu.numel() != B + 1:
+            raise ValueError("cu_seqlens_cpu must match cu_seqlens")
+        lens = (cu_cpu[1:] - cu_cpu[:-1]).clamp(min=0)
+        num_chunks = int(((lens + PREFILL_CHUNK - 1) // PREFILL_CHUNK).sum()) if B > 0 else 0
         _check(out, "out", torch.bfloat16, dev)
         out_stride = _rows(out, "out", T, D)
         gate_stride = 0
@@ -396,9 +414,15 @@ class KdaPrefillCall:
                 raise ValueError("conv_bias must be [3*H*128]")
         if err_flag is not None:
             _check(err_flag, "err_flag", torch.int32, dev)
+        ws_bytes = int(self._lib.kda_prefill_workspace_bytes(num_chunks, H))
+        self.num_chunks, self.B = num_chunks, B
+        self.chunk_indices = torch.empty(max(num_chunks, 1), 2, dtype=torch.int32, device=dev)
+        self.chunk_offsets = torch.empty(B + 1, dtype=torch.int64, device=dev)
+        self.workspace = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
         self.device = dev
         self._keep = (qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, gate,
                       norm_weight, conv_bias, err_flag)
+        self._cu, self._err = cu_seqlens, err_flag
         ptr = (lambda t: None if t is None else t.data_ptr())
         self.args = KdaPrefillArgs(
             struct_size=ctypes.sizeof(KdaPrefillArgs), B=B, H=H, num_slots=num_slots,
@@ -408,22 +432,36 @@ class KdaPrefillCall:
             gate=ptr(gate) if out_norm else None, gate_row_stride=gate_stride,
             norm_weight=ptr(norm_weight) if out_norm else None, slot_idx=ptr(slot_idx), out=ptr(out),
             out_row_stride=out_stride, eps=eps, q_scale=q_scale,
-            flags=KDA_OUT_NORM if out_norm else 0, err_flag=ptr(err_flag))
+            flags=KDA_OUT_NORM if out_norm else 0, err_flag=ptr(err_flag),
+            chunk_indices=ptr(self.chunk_indices), chunk_offsets=ptr(self.chunk_offsets),
+            num_chunks=num_chunks, workspace=ptr(self.workspace), workspace_bytes=ws_bytes)
 
     def __call__(self, stream: torch.cuda.Stream | None = None) -> None:
         if stream is None:
             stream = torch.cuda.current_stream(self.device)
-        rc = self._lib.kda_prefill(ctypes.byref(self.args), ctypes.c_void_p(stream.cuda_stream))
+        if self.B == 0:
+            return
+        sp = ctypes.c_void_p(stream.cuda_stream)
+        rc = self._lib.kda_chunk_metadata(self._cu.data_ptr(), self.B, PREFILL_CHUNK,
+                                          self.chunk_indices.data_ptr(), self.num_chunks,
+                                          self.chunk_offsets.data_ptr(),
+                                          None if self._err is None else self._err.data_ptr(), sp)
+        if rc != 0:
+            raise KdaError(rc, kda_status_string(rc))
+        rc = self._lib.kda_prefill(ctypes.byref(self.args), sp)
         if rc != 0:
             raise KdaError(rc, f"{kda_status_string(rc)}: {self._lib.kda_last_error().decode()}")
 
 
 def kda_prefill(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
-                gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
+                cu_seqlens_cpu=None, gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                 q_scale: float = 0.0, out_norm: bool = True, err_flag=None,
                 stream: torch.cuda.Stream | None = None) -> None:
     """Chunked prefill of a varlen batch (see ``include/kda_prefill.h``):
-    ``out``, ``state`` and ``conv_state`` are written in place."""
+    ``out``, ``state`` and ``conv_state`` are written in place.  Pass
+    ``cu_seqlens_cpu`` (the host copy of ``cu_seqlens``) to keep the call free
+    of device reads."""
     KdaPrefillCall(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out,
-                   gate=gate, norm_weight=norm_weight, conv_bias=conv_bias, eps=eps,
-                   q_scale=q_scale, out_norm=out_norm, err_flag=err_flag)(stream)
+                   cu_seqlens_cpu=cu_seqlens_cpu, gate=gate, norm_weight=norm_weight,
+                   conv_bias=conv_bias, eps=eps, q_scale=q_scale, out_norm=out_norm,
+                   err_flag=err_flag)(stream)

@@ -62,6 +62,10 @@ constexpr float kMaxExponent = 80.0f;  // |G_t - G_m| above this: element-wise p
 
 struct PrefillParams {
   const int32_t* cu;
+  const int32_t* chunk_idx;   // [num_chunks][2] (sequence, chunk)
+  const int64_t* chunk_off;   // [B + 1]
+  int64_t num_chunks;
+  float* ws;                  // per (chunk row, head) one image of kImg floats
   const uint16_t* qkv;
   int64_t qkv_stride;
   const float* conv_w;
@@ -82,26 +86,43 @@ struct PrefillParams {
   int32_t* err;
 };
 
-// Shared memory of one CTA (about 170 KB).  Buffers whose lifetimes do not
-// overlap within a chunk share storage.
-struct __align__(16) PSmem {
-  uint16_t raw[kHist + kL][kCh];  // conv window: 3 older rows, then the chunk's inputs
-  uint16_t gate[kL][kD];
+// Workspace image of one (chunk, head), written by the chunk kernel and
+// copied verbatim into the scan kernel's shared memory; the row strides are
+// the ones its tensor-core fragment reads want.
+constexpr int kOffW = 0;                      // W   [kL][kSA]
+constexpr int kOffQ = kOffW + kL * kSA;       // Q_G [kL][kSA]
+constexpr int kOffU = kOffQ + kL * kSA;       // U   [kL][kSK]
+constexpr int kOffK = kOffU + kL * kSK;       // K_E [kL][kSK]
+constexpr int kOffR = kOffK + kL * kSK;       // R   [kL][kST] (lower, zeros above)
+constexpr int kOffC = kOffR + kL * kST;       // gamma = exp(G_{L-1}) [kD]
+constexpr int kImg = kOffC + kD;              // 18,560 floats = 74,240 bytes
+static_assert((kImg * 4) % 16 == 0, "image must be a whole number of 16-byte pieces");
+
+// Chunk kernel shared memory (about 106 KB: two CTAs per SM).
+struct __align__(16) ChunkSmem {
+  union {
+    uint16_t raw[kHist + kL][kCh];  // conv window: 3 older rows, then the chunk's inputs
+    struct {
+      float ek[kL][kSA];            // exp(G - G_m) k^
+      float fk[kL][kSA];            // exp(G_m - G) k^
+    } f;
+  };
+  float q[kL][kSA];                 // q^
+  float k[kL][kSA];                 // k^
+  float v[kL][kSA];                 // v~
+  float G[kL][kD];                  // cumulative log decay
+  float P[kL][kSP];                 // P (strictly lower)
   float beta[kL];
-  float q[kL][kSA];               // q^, then Q_G
-  float k[kL][kSA];               // k^
-  float v[kL][kSA];               // v~, then the chunk's output O (staging)
-  float G[kL][kD];                // cumulative log decay
-  union { float ek[kL][kSA]; float w[kL][kSA]; };        // exp(G - G_m) k^, then W
-  union { float fk[kL][kSA]; float ke[kL][kSK]; };       // exp(G_m - G) k^, then K_E
-  union { float eq[kL][kSA]; float u[kL][kSK]; };        // exp(G - G_m) q^, then U
-  float P[kL][kSP];               // P (strictly lower)
-  float r[kL][kST];               // R (lower, diagonal included)
-  float gC[kD];                   // exp(G_{L-1}): decay of the whole chunk
-  float nrm[kWarps][kL];          // per-warp partial sums of o^2
-  int slow;                       // this chunk takes the element-wise P / R path
+  int slow;                         // this chunk takes the element-wise P / R path
 };
 
+// Scan kernel shared memory (about 163 KB): two images (double buffer), the
+// chunk's output and the per-warp partial sums of o^2.
+struct __align__(16) ScanSmem {
+  float img[2][kImg];
+  float o[kL][kSA];
+  float nrm[kWarps][kL];
+};
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -163,18 +184,269 @@ __device__ __forceinline__ void mma3s(float (&c)[4], float (&cl)[4], const FragA
   mma_tf32(cl, a.hi, l0, l1);
 }
 
-// One CTA per (sequence, head); blockIdx.x = b * H + h.
-template <bool kOutNorm>
-__global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillParams p) {
+
+__device__ __forceinline__ void flag(const PrefillParams& p, int bits) {
+  if (p.err) atomicOr(p.err, bits);
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// ===================================================================== chunk
+// One CTA per (chunk row c, head h), chunk row = (sequence b, chunk j) from
+// the chunk metadata.  Everything that does not depend on the state entering
+// the chunk: conv, norms, cumulative decays, P and R, the triangular solve
+// for U and W, and the decayed Q_G and K_E.  Results go to the workspace
+// image of (c, h).
+__global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const PrefillParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  PSmem& S = *reinterpret_cast<PSmem*>(smem_raw);
+  ChunkSmem& S = *reinterpret_cast<ChunkSmem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, tq = lane & 3;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y;
+  const int64_t D = static_cast<int64_t>(p.H) * kD;
+
+  const int b = p.chunk_idx[2 * c], j = p.chunk_idx[2 * c + 1];
+  if (b < 0 || b >= p.B || j < 0) {
+    if (tid == 0 && h == 0) flag(p, KDA_DEVERR_SEQLENS);
+    return;
+  }
+  const int64_t r0 = p.cu[b], r1 = p.cu[b + 1];
+  const int64_t t0 = r0 + static_cast<int64_t>(kL) * j;
+  if (r0 < 0 || r1 < r0 || r1 > p.T || t0 >= r1) {
+    if (tid == 0 && h == 0) flag(p, KDA_DEVERR_SEQLENS);
+    return;
+  }
+  const int slot = p.slot_idx[b];
+  if (slot <= 0 || slot >= p.num_slots) return;  // the scan kernel zeroes and flags
+  const int L = static_cast<int>(r1 - t0 < kL ? r1 - t0 : kL);
+  float* ws = p.ws + (c * p.H + h) * static_cast<int64_t>(kImg);
+  auto ch_global = [&](int ch) { return static_cast<int64_t>(ch >> 7) * D + static_cast<int64_t>(h) * kD + (ch & 127); };
+
+  // ---- 1. inputs: the three older taps (conv state for the first chunk,
+  // else the sequence's preceding tokens), the chunk's rows (zero past L),
+  // g, beta
+  if (j == 0) {
+    const uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
+    for (int ch = tid; ch < kCh; ch += kThreads)
+#pragma unroll
+      for (int r = 0; r < kHist; ++r) S.raw[r][ch] = cs[ch_global(ch) * kHist + r];
+  } else {
+    for (int e = tid; e < kHist * 48; e += kThreads) {
+      const int r = e / 48, q = e - r * 48, seg = q >> 4, u = q & 15;
+      reinterpret_cast<uint4*>(&S.raw[r][seg * kD])[u] = __ldg(reinterpret_cast<const uint4*>(
+          p.qkv + (t0 - kHist + r) * p.qkv_stride + seg * D + static_cast<int64_t>(h) * kD) + u);
+    }
+  }
+  for (int e = tid; e < kL * 48; e += kThreads) {
+    const int t = e / 48, q = e - t * 48, seg = q >> 4, u = q & 15;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (t < L)
+      val = __ldg(reinterpret_cast<const uint4*>(p.qkv + (t0 + t) * p.qkv_stride + seg * D +
+                                                 static_cast<int64_t>(h) * kD) + u);
+    reinterpret_cast<uint4*>(&S.raw[kHist + t][seg * kD])[u] = val;
+  }
+  for (int e = tid; e < kL * 32; e += kThreads) {
+    const int t = e >> 5, u = e & 31;
+    float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < L) val = __ldg(reinterpret_cast<const float4*>(p.g + ((t0 + t) * p.H + h) * kD) + u);
+    reinterpret_cast<float4*>(S.G[t])[u] = val;
+  }
+  if (tid < kL) S.beta[tid] = tid < L ? bf16f(p.beta[(t0 + tid) * p.H + h]) : 0.0f;
+  if (tid == 0) S.slow = 0;
+  __syncthreads();
+
+  // ---- 2. conv + SiLU over the window (outputs past L are zero); thread
+  // tid convolves channel tid (q or k block) and, below 128, v channel tid
+  {
+    float wa[kWidth], wv[kWidth], ba = 0.0f, bv = 0.0f;
+#pragma unroll
+    for (int t = 0; t < kWidth; ++t) {
+      wa[t] = __ldg(p.conv_w + ((tid >> 7) * kWidth + t) * D + static_cast<int64_t>(h) * kD + (tid & 127));
+      wv[t] = tid < kD ? __ldg(p.conv_w + (2 * kWidth + t) * D + static_cast<int64_t>(h) * kD + tid) : 0.0f;
+    }
+    if (p.conv_b) {
+      ba = __ldg(p.conv_b + ch_global(tid));
+      if (tid < kD) bv = __ldg(p.conv_b + ch_global(2 * kD + tid));
+    }
+    float x0 = bf16f(S.raw[0][tid]), x1 = bf16f(S.raw[1][tid]), x2 = bf16f(S.raw[2][tid]);
+    float* dst = tid < kD ? &S.q[0][tid] : &S.k[0][tid - kD];
+#pragma unroll 4
+    for (int t = 0; t < kL; ++t) {
+      const float x3 = bf16f(S.raw[kHist + t][tid]);
+      float y = ba;
+      y = fmaf(wa[0], x0, y);
+      y = fmaf(wa[1], x1, y);
+      y = fmaf(wa[2], x2, y);
+      y = fmaf(wa[3], x3, y);
+      dst[t * kSA] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
+      x0 = x1; x1 = x2; x2 = x3;
+    }
+    if (tid < kD) {
+      const int cv = 2 * kD + tid;
+      float z0 = bf16f(S.raw[0][cv]), z1 = bf16f(S.raw[1][cv]), z2 = bf16f(S.raw[2][cv]);
+#pragma unroll 4
+      for (int t = 0; t < kL; ++t) {
+        const float z3 = bf16f(S.raw[kHist + t][cv]);
+        float y = bv;
+        y = fmaf(wv[0], z0, y);
+        y = fmaf(wv[1], z1, y);
+        y = fmaf(wv[2], z2, y);
+        y = fmaf(wv[3], z3, y);
+        S.v[t][tid] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
+        z0 = z1; z1 = z2; z2 = z3;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. L2 norms (warp w: tokens 4w..4w+3); cumulative decay
+  const float qs = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
+#pragma unroll
+  for (int tt = 0; tt < 4; ++tt) {
+    const int t = warp * 4 + tt;
+    float4 qv = reinterpret_cast<float4*>(S.q[t])[lane];
+    float4 kv = reinterpret_cast<float4*>(S.k[t])[lane];
+    const float sq = warp_sum((qv.x * qv.x + qv.y * qv.y) + (qv.z * qv.z + qv.w * qv.w));
+    const float sk = warp_sum((kv.x * kv.x + kv.y * kv.y) + (kv.z * kv.z + kv.w * kv.w));
+    const float rq = qs / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
+    qv.x *= rq; qv.y *= rq; qv.z *= rq; qv.w *= rq;
+    kv.x *= rk; kv.y *= rk; kv.z *= rk; kv.w *= rk;
+    reinterpret_cast<float4*>(S.q[t])[lane] = qv;
+    reinterpret_cast<float4*>(S.k[t])[lane] = kv;
+  }
+  if (tid < kD) {
+    float acc = 0.0f;
+#pragma unroll 8
+    for (int t = 0; t < kL; ++t) {
+      acc += S.G[t][tid];
+      S.G[t][tid] = acc;
+    }
+  }
+  __syncthreads();
+
+  // ---- 4. split decay factors around the reference token (shared memory);
+  // Q_G = exp(G) q^, K_E = exp(G_{L-1} - G) k^ and gamma to the image; R's
+  // image cleared (its lower triangle is written next); P cleared
+  for (int e = tid; e < kL * kD; e += kThreads) {
+    const int t = e >> 7, i = e & (kD - 1);
+    const float Gt = S.G[t][i];
+    const float d = Gt - S.G[kRef][i];
+    if (fabsf(d) > kMaxExponent) S.slow = 1;
+    const float kv = S.k[t][i];
+    S.f.ek[t][i] = __expf(d) * kv;
+    S.f.fk[t][i] = __expf(-d) * kv;
+    ws[kOffQ + t * kSA + i] = expf(Gt) * S.q[t][i];
+    ws[kOffK + t * kSK + i] = expf(S.G[kL - 1][i] - Gt) * kv;
+  }
+  if (tid < kD) ws[kOffC + tid] = expf(S.G[kL - 1][tid]);
+  for (int e = tid; e < kL * kST; e += kThreads) ws[kOffR + e] = 0.0f;
+  for (int e = tid; e < kL * kSP; e += kThreads) (&S.P[0][0])[e] = 0.0f;
+  __syncthreads();
+
+  // ---- 5. P (strictly lower, shared memory) and R (lower, image) over the
+  // key channels; R's A operand exp(G - G_m) q^ is formed while loading
+  if (!S.slow) {
+    for (int x = warp; x < 12; x += kWarps) {
+      const int mat = x / 6, y = x - mat * 6;
+      const int mm = y < 2 ? 0 : 1, nn = y < 2 ? y : y - 2;
+      const int ta = 16 * mm + g8;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int kk = 0; kk < kD / 8; ++kk) {
+        const int i0 = 8 * kk + 2 * tq;
+        float2 a02, a13;
+        if (mat == 0) {
+          a02 = *reinterpret_cast<const float2*>(&S.f.ek[ta][i0]);
+          a13 = *reinterpret_cast<const float2*>(&S.f.ek[ta + 8][i0]);
+        } else {
+          const float2 q0 = *reinterpret_cast<const float2*>(&S.q[ta][i0]);
+          const float2 q1 = *reinterpret_cast<const float2*>(&S.q[ta + 8][i0]);
+          const float2 g0 = *reinterpret_cast<const float2*>(&S.G[ta][i0]);
+          const float2 g1 = *reinterpret_cast<const float2*>(&S.G[ta + 8][i0]);
+          const float2 gm = *reinterpret_cast<const float2*>(&S.G[kRef][i0]);
+          a02 = make_float2(__expf(g0.x - gm.x) * q0.x, __expf(g0.y - gm.y) * q0.y);
+          a13 = make_float2(__expf(g1.x - gm.x) * q1.x, __expf(g1.y - gm.y) * q1.y);
+        }
+        const float2 bb = *reinterpret_cast<const float2*>(&S.f.fk[8 * nn + g8][i0]);
+        mma3(acc, make_a(a02.x, a13.x, a02.y, a13.y), bb.x, bb.y);
+      }
+      const int s = 8 * nn + 2 * tq;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int te = ta + (e >> 1) * 8, se = s + (e & 1);
+        if (mat == 0) {
+          if (te > se) S.P[te][se] = acc[e];
+        } else {
+          if (te >= se) ws[kOffR + te * kST + se] = acc[e];
+        }
+      }
+    }
+  } else {
+    // element-wise: pairs (t, s), s <= t
+    for (int e = tid; e < kL * (kL + 1) / 2; e += kThreads) {
+      int t = static_cast<int>((sqrtf(8.0f * e + 1.0f) - 1.0f) * 0.5f);
+      while ((t + 1) * (t + 2) / 2 <= e) ++t;
+      while (t * (t + 1) / 2 > e) --t;
+      const int s = e - t * (t + 1) / 2;
+      float pk = 0.0f, pq = 0.0f;
+      for (int i = 0; i < kD; ++i) {
+        const float fct = expf(S.G[t][i] - S.G[s][i]) * S.k[s][i];
+        pk = fmaf(S.k[t][i], fct, pk);
+        pq = fmaf(S.q[t][i], fct, pq);
+      }
+      if (t > s) S.P[t][s] = pk;
+      ws[kOffR + t * kST + s] = pq;
+    }
+  }
+  __syncthreads();
+
+  // ---- 6. triangular solve (thread = one column of [U | W]), left-looking:
+  // x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or exp(G) k^ (W)
+  {
+    const bool vcol = tid < kD;
+    const int i = tid - kD;
+    float x[kL];
+#pragma unroll
+    for (int t = 0; t < kL; ++t) {
+      float a0 = vcol ? S.v[t][tid] : expf(S.G[t][i]) * S.k[t][i];
+      float a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+      for (int s4 = 0; s4 < t / 4 + 1; ++s4) {
+        if (4 * s4 >= t) break;
+        const float4 pr = reinterpret_cast<const float4*>(S.P[t])[s4];
+        if (4 * s4 + 0 < t) a0 = fmaf(-pr.x, x[4 * s4 + 0], a0);
+        if (4 * s4 + 1 < t) a1 = fmaf(-pr.y, x[4 * s4 + 1], a1);
+        if (4 * s4 + 2 < t) a2 = fmaf(-pr.z, x[4 * s4 + 2], a2);
+        if (4 * s4 + 3 < t) a3 = fmaf(-pr.w, x[4 * s4 + 3], a3);
+      }
+      x[t] = S.beta[t] * ((a0 + a1) + (a2 + a3));
+      if (vcol) ws[kOffU + t * kSK + tid] = x[t];
+      else ws[kOffW + t * kSA + i] = x[t];
+    }
+  }
+}
+
+// ====================================================================== scan
+// One CTA per (sequence, head): walks the sequence's chunks in order with
+// the state in registers; chunk j's image (row chunk_offsets[b] + j of the
+// workspace) is copied into shared memory while chunk j - 1 computes.
+template <bool kOutNorm>
+__global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const PrefillParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  ScanSmem& S = *reinterpret_cast<ScanSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, tq = lane & 3;
   const int b = blockIdx.x / p.H, h = blockIdx.x - b * p.H;
   const int64_t D = static_cast<int64_t>(p.H) * kD;
 
   const int64_t r0 = p.cu[b], r1 = p.cu[b + 1];
   if (r0 < 0 || r1 < r0 || r1 > p.T) {
-    if (tid == 0 && h == 0 && p.err) atomicOr(p.err, KDA_DEVERR_SEQLENS);
+    if (tid == 0 && h == 0) flag(p, KDA_DEVERR_SEQLENS);
     return;
   }
   if (r1 == r0) return;  // empty sequence
@@ -186,13 +458,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
       reinterpret_cast<uint2*>(p.out + row * p.out_stride + static_cast<int64_t>(h) * kD)[e % (kD / 4)] =
           make_uint2(0, 0);
     }
-    if (slot >= p.num_slots && tid == 0 && h == 0 && p.err) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
+    if (slot >= p.num_slots && tid == 0 && h == 0) flag(p, KDA_DEVERR_SLOT_RANGE);
+    return;
+  }
+  const int64_t n_chunks = (r1 - r0 + kL - 1) / kL;
+  const int64_t c0 = p.chunk_off[b];
+  if (c0 < 0 || p.chunk_off[b + 1] - c0 != n_chunks || c0 + n_chunks > p.num_chunks) {
+    if (tid == 0 && h == 0) flag(p, KDA_DEVERR_SEQLENS);  // metadata does not match cu_seqlens
     return;
   }
 
-  // ---- sequence start: state into registers, conv window, conv weights
-  // st[kk][*] holds S^T rows (value) jr, jr + 8 and columns (key)
-  // 8kk + 2tq, 8kk + 2tq + 1, in the m16n8 accumulator layout.
+  // state S^T in registers: st[kk][*] = rows (value) jr, jr + 8, columns
+  // (key) 8kk + 2tq, 8kk + 2tq + 1, in the m16n8 accumulator layout
   float* Sg = p.state + (static_cast<int64_t>(slot) * p.H + h) * (kD * kD);
   const int jr = warp * 16 + g8;
   float st[16][4];
@@ -204,307 +481,120 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
     st[kk][2] = Sg[i0 * kD + jr + 8];
     st[kk][3] = Sg[(i0 + 1) * kD + jr + 8];
   }
-  auto ch_global = [&](int c) { return static_cast<int64_t>(c >> 7) * D + static_cast<int64_t>(h) * kD + (c & 127); };
-  uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
-  for (int c = tid; c < kCh; c += kThreads)
-#pragma unroll
-    for (int r = 0; r < kHist; ++r) S.raw[r][c] = cs[ch_global(c) * kHist + r];
-  const float qs = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
 
-  for (int64_t t0 = r0; t0 < r1; t0 += kL) {
+  auto fetch = [&](int64_t jj, int buf) {
+    const float4* src = reinterpret_cast<const float4*>(p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kImg));
+    float4* dst = reinterpret_cast<float4*>(S.img[buf]);
+    for (int e = tid; e < kImg / 4; e += kThreads) cp_async16(dst + e, src + e);
+    cp_async_commit();
+  };
+  fetch(0, 0);
+
+  for (int64_t jj = 0; jj < n_chunks; ++jj) {
+    const int64_t t0 = r0 + kL * jj;
     const int L = static_cast<int>(r1 - t0 < kL ? r1 - t0 : kL);
+    const int buf = static_cast<int>(jj & 1);
+    cp_async_wait_all();
+    __syncthreads();                       // image jj landed; the other buffer is free
+    if (jj + 1 < n_chunks) fetch(jj + 1, buf ^ 1);
+    const float* img = S.img[buf];
+    const float(*W)[kSA] = reinterpret_cast<const float(*)[kSA]>(img + kOffW);
+    const float(*QG)[kSA] = reinterpret_cast<const float(*)[kSA]>(img + kOffQ);
+    const float(*U)[kSK] = reinterpret_cast<const float(*)[kSK]>(img + kOffU);
+    const float(*KE)[kSK] = reinterpret_cast<const float(*)[kSK]>(img + kOffK);
+    const float(*R)[kST] = reinterpret_cast<const float(*)[kST]>(img + kOffR);
+    const float* gC = img + kOffC;
 
-    // ---- 1. the chunk's inputs (rows past L are zero)
-    for (int e = tid; e < kL * 48; e += kThreads) {
-      const int t = e / 48, q = e - t * 48, seg = q >> 4, u = q & 15;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (t < L)
-        val = __ldg(reinterpret_cast<const uint4*>(p.qkv + (t0 + t) * p.qkv_stride + seg * D +
-                                                   static_cast<int64_t>(h) * kD) + u);
-      reinterpret_cast<uint4*>(&S.raw[kHist + t][seg * kD])[u] = val;
-    }
-    if (kOutNorm)
-      for (int e = tid; e < kL * 16; e += kThreads) {
-        const int t = e >> 4, u = e & 15;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (t < L)
-          val = __ldg(reinterpret_cast<const uint4*>(p.gate + (t0 + t) * p.gate_stride + static_cast<int64_t>(h) * kD) + u);
-        reinterpret_cast<uint4*>(S.gate[t])[u] = val;
-      }
-    for (int e = tid; e < kL * 32; e += kThreads) {
-      const int t = e >> 5, u = e & 31;
-      float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < L) val = __ldg(reinterpret_cast<const float4*>(p.g + ((t0 + t) * p.H + h) * kD) + u);
-      reinterpret_cast<float4*>(S.G[t])[u] = val;
-    }
-    if (tid < kL) S.beta[tid] = tid < L ? bf16f(p.beta[(t0 + tid) * p.H + h]) : 0.0f;
-    if (tid == 0) S.slow = 0;
-    __syncthreads();
-
-    // ---- 2. conv + SiLU over the window (outputs past L are zero); thread
-    // tid convolves channel tid (q or k block) and, below 128, v channel tid
-    {
-      float wa[kWidth], wv[kWidth], ba = 0.0f, bv = 0.0f;
-#pragma unroll
-      for (int t = 0; t < kWidth; ++t) {
-        wa[t] = __ldg(p.conv_w + ((tid >> 7) * kWidth + t) * D + static_cast<int64_t>(h) * kD + (tid & 127));
-        wv[t] = tid < kD ? __ldg(p.conv_w + (2 * kWidth + t) * D + static_cast<int64_t>(h) * kD + tid) : 0.0f;
-      }
-      if (p.conv_b) {
-        ba = __ldg(p.conv_b + ch_global(tid));
-        if (tid < kD) bv = __ldg(p.conv_b + ch_global(2 * kD + tid));
-      }
-      float x0 = bf16f(S.raw[0][tid]), x1 = bf16f(S.raw[1][tid]), x2 = bf16f(S.raw[2][tid]);
-      float* dst = tid < kD ? &S.q[0][tid] : &S.k[0][tid - kD];
-#pragma unroll 4
-      for (int t = 0; t < kL; ++t) {
-        const float x3 = bf16f(S.raw[kHist + t][tid]);
-        float y = ba;
-        y = fmaf(wa[0], x0, y);
-        y = fmaf(wa[1], x1, y);
-        y = fmaf(wa[2], x2, y);
-        y = fmaf(wa[3], x3, y);
-        dst[t * kSA] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
-        x0 = x1; x1 = x2; x2 = x3;
-      }
-      if (tid < kD) {
-        const int c = 2 * kD + tid;
-        float z0 = bf16f(S.raw[0][c]), z1 = bf16f(S.raw[1][c]), z2 = bf16f(S.raw[2][c]);
-#pragma unroll 4
-        for (int t = 0; t < kL; ++t) {
-          const float z3 = bf16f(S.raw[kHist + t][c]);
-          float y = bv;
-          y = fmaf(wv[0], z0, y);
-          y = fmaf(wv[1], z1, y);
-          y = fmaf(wv[2], z2, y);
-          y = fmaf(wv[3], z3, y);
-          S.v[t][tid] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
-          z0 = z1; z1 = z2; z2 = z3;
-        }
-      }
-    }
-    __syncthreads();
-
-    // ---- 3. L2 norms (warp w: tokens 4w..4w+3); cumulative decay; window slide
-#pragma unroll
-    for (int tt = 0; tt < 4; ++tt) {
-      const int t = warp * 4 + tt;
-      float4 qv = reinterpret_cast<float4*>(S.q[t])[lane];
-      float4 kv = reinterpret_cast<float4*>(S.k[t])[lane];
-      const float sq = warp_sum((qv.x * qv.x + qv.y * qv.y) + (qv.z * qv.z + qv.w * qv.w));
-      const float sk = warp_sum((kv.x * kv.x + kv.y * kv.y) + (kv.z * kv.z + kv.w * kv.w));
-      const float rq = qs / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
-      qv.x *= rq; qv.y *= rq; qv.z *= rq; qv.w *= rq;
-      kv.x *= rk; kv.y *= rk; kv.z *= rk; kv.w *= rk;
-      reinterpret_cast<float4*>(S.q[t])[lane] = qv;
-      reinterpret_cast<float4*>(S.k[t])[lane] = kv;
-    }
-    if (tid < kD) {
-      float acc = 0.0f;
-#pragma unroll 8
-      for (int t = 0; t < kL; ++t) {
-        acc += S.G[t][tid];
-        S.G[t][tid] = acc;
-      }
-    } else {
-      // the window's last three rows become the next chunk's older taps
-      for (int c = tid - kD; c < kCh; c += kThreads - kD) {
-        const uint16_t a0 = S.raw[L][c], a1 = S.raw[L + 1][c], a2 = S.raw[L + 2][c];
-        S.raw[0][c] = a0;
-        S.raw[1][c] = a1;
-        S.raw[2][c] = a2;
-      }
-    }
-    __syncthreads();
-
-    // ---- 4. split decay factors around the reference token; clear P and R
-    for (int e = tid; e < kL * kD; e += kThreads) {
-      const int t = e >> 7, i = e & (kD - 1);
-      const float d = S.G[t][i] - S.G[kRef][i];
-      if (fabsf(d) > kMaxExponent) S.slow = 1;
-      const float E = __expf(d), F = __expf(-d);
-      const float kv = S.k[t][i];
-      S.ek[t][i] = E * kv;
-      S.eq[t][i] = E * S.q[t][i];
-      S.fk[t][i] = F * kv;
-    }
-    for (int e = tid; e < kL * kSP; e += kThreads) (&S.P[0][0])[e] = 0.0f;
-    for (int e = tid; e < kL * kST; e += kThreads) (&S.r[0][0])[e] = 0.0f;
-    __syncthreads();
-
-    // ---- 5. P (strictly lower) and R (lower) over the key channels
-    if (!S.slow) {
-      // 6 tiles of 16 x 8 per matrix on or below the diagonal: (mm, nn)
-      for (int x = warp; x < 12; x += kWarps) {
-        const int mat = x / 6, y = x - mat * 6;
-        const int mm = y < 2 ? 0 : 1, nn = y < 2 ? y : y - 2;
-        const float(*A)[kSA] = mat ? S.eq : S.ek;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int kk = 0; kk < kD / 8; ++kk) {
-          const float2 a02 = *reinterpret_cast<const float2*>(&A[16 * mm + g8][8 * kk + 2 * tq]);
-          const float2 a13 = *reinterpret_cast<const float2*>(&A[16 * mm + g8 + 8][8 * kk + 2 * tq]);
-          const float2 bb = *reinterpret_cast<const float2*>(&S.fk[8 * nn + g8][8 * kk + 2 * tq]);
-          mma3(acc, make_a(a02.x, a13.x, a02.y, a13.y), bb.x, bb.y);
-        }
-        const int t = 16 * mm + g8, s = 8 * nn + 2 * tq;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int te = t + (e >> 1) * 8, se = s + (e & 1);
-          if (mat == 0) {
-            if (te > se) S.P[te][se] = acc[e];
-          } else {
-            if (te >= se) S.r[te][se] = acc[e];
-          }
-        }
-      }
-    } else {
-      // element-wise: pairs (t, s), s <= t
-      for (int e = tid; e < kL * (kL + 1) / 2; e += kThreads) {
-        int t = static_cast<int>((sqrtf(8.0f * e + 1.0f) - 1.0f) * 0.5f);
-        while ((t + 1) * (t + 2) / 2 <= e) ++t;
-        while (t * (t + 1) / 2 > e) --t;
-        const int s = e - t * (t + 1) / 2;
-        float pk = 0.0f, pq = 0.0f;
-        for (int i = 0; i < kD; ++i) {
-          const float f = expf(S.G[t][i] - S.G[s][i]) * S.k[s][i];
-          pk = fmaf(S.k[t][i], f, pk);
-          pq = fmaf(S.q[t][i], f, pq);
-        }
-        if (t > s) S.P[t][s] = pk;
-        S.r[t][s] = pq;
-      }
-    }
-    __syncthreads();
-
-    // ---- 6. triangular solve (thread = one column of [U | W]), left-looking:
-    // x_t = beta_t (y_t - sum_{s<t} P_ts x_s); Q_G, K_E and gamma alongside
-    {
-      const bool vcol = tid < kD;
-      const int i = tid - kD;
-      float x[kL];
-      if (!vcol) {
-        const float GL = S.G[kL - 1][i];
-#pragma unroll 1
-        for (int t = 0; t < kL; ++t) S.ke[t][i] = expf(GL - S.G[t][i]) * S.k[t][i];
-        S.gC[i] = expf(GL);
-      }
-#pragma unroll
-      for (int t = 0; t < kL; ++t) {
-        float a0 = vcol ? S.v[t][tid] : expf(S.G[t][i]) * S.k[t][i];
-        float a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll
-        for (int s4 = 0; s4 < t / 4 + 1; ++s4) {
-          if (4 * s4 >= t) break;
-          const float4 pr = reinterpret_cast<const float4*>(S.P[t])[s4];
-          if (4 * s4 + 0 < t) a0 = fmaf(-pr.x, x[4 * s4 + 0], a0);
-          if (4 * s4 + 1 < t) a1 = fmaf(-pr.y, x[4 * s4 + 1], a1);
-          if (4 * s4 + 2 < t) a2 = fmaf(-pr.z, x[4 * s4 + 2], a2);
-          if (4 * s4 + 3 < t) a3 = fmaf(-pr.w, x[4 * s4 + 3], a3);
-        }
-        x[t] = S.beta[t] * ((a0 + a1) + (a2 + a3));
-        if (vcol) S.u[t][tid] = x[t];
-        else S.w[t][i] = x[t];
-      }
-      if (vcol) {
-#pragma unroll 8
-        for (int t = 0; t < kL; ++t) S.q[t][tid] *= expf(S.G[t][tid]);  // Q_G
-      }
-    }
-    __syncthreads();
-
-    // ---- 7. per warp (value rows jr, jr + 8): Delta^T = U^T - S^T W^T,
+    // ---- per warp (value rows jr, jr + 8): Delta^T = U^T - S^T W^T,
     // O^T = S^T Q_G^T + Delta^T R^T, S^T <- S^T Diag(gamma) + Delta^T K_E.
     // The two products with S^T share its split fragments; the small
     // (high x low) terms go to their own accumulators so that the chains of
     // dependent MMAs stay short.
-    {
-      float d[4][4], o[4][4], dl[4][4], ol[4][4];
+    float d[4][4], o[4][4], dl[4][4], ol[4][4];
+#pragma unroll
+    for (int nn = 0; nn < 4; ++nn) {
+      d[nn][0] = U[8 * nn + 2 * tq][jr];
+      d[nn][1] = U[8 * nn + 2 * tq + 1][jr];
+      d[nn][2] = U[8 * nn + 2 * tq][jr + 8];
+      d[nn][3] = U[8 * nn + 2 * tq + 1][jr + 8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nn][e] = dl[nn][e] = ol[nn][e] = 0.0f;
+    }
+#pragma unroll
+    for (int kk = 0; kk < kD / 8; ++kk) {
+      const FragA a = make_a(st[kk][0], st[kk][2], st[kk][1], st[kk][3]);
 #pragma unroll
       for (int nn = 0; nn < 4; ++nn) {
-        d[nn][0] = S.u[8 * nn + 2 * tq][jr];
-        d[nn][1] = S.u[8 * nn + 2 * tq + 1][jr];
-        d[nn][2] = S.u[8 * nn + 2 * tq][jr + 8];
-        d[nn][3] = S.u[8 * nn + 2 * tq + 1][jr + 8];
+        const float2 wv2 = *reinterpret_cast<const float2*>(&W[8 * nn + g8][8 * kk + 2 * tq]);
+        mma3s(d[nn], dl[nn], a, -wv2.x, -wv2.y);
+        const float2 qv2 = *reinterpret_cast<const float2*>(&QG[8 * nn + g8][8 * kk + 2 * tq]);
+        mma3s(o[nn], ol[nn], a, qv2.x, qv2.y);
+      }
+    }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[nn][e] = dl[nn][e] = ol[nn][e] = 0.0f;
+    for (int nn = 0; nn < 4; ++nn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        d[nn][e] += dl[nn][e];
+        o[nn][e] += ol[nn][e];
       }
 #pragma unroll
-      for (int kk = 0; kk < kD / 8; ++kk) {
-        const FragA a = make_a(st[kk][0], st[kk][2], st[kk][1], st[kk][3]);
-#pragma unroll
-        for (int nn = 0; nn < 4; ++nn) {
-          const float2 wv2 = *reinterpret_cast<const float2*>(&S.w[8 * nn + g8][8 * kk + 2 * tq]);
-          mma3s(d[nn], dl[nn], a, -wv2.x, -wv2.y);
-          const float2 qv2 = *reinterpret_cast<const float2*>(&S.q[8 * nn + g8][8 * kk + 2 * tq]);
-          mma3s(o[nn], ol[nn], a, qv2.x, qv2.y);
-        }
-      }
-#pragma unroll
-      for (int nn = 0; nn < 4; ++nn)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          d[nn][e] += dl[nn][e];
-          o[nn][e] += ol[nn][e];
-        }
-#pragma unroll
-      for (int kk = 0; kk < kL / 8; ++kk) {
-        const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
-#pragma unroll
-        for (int nn = 0; nn < 4; ++nn) {
-          const float2 rv = *reinterpret_cast<const float2*>(&S.r[8 * nn + g8][8 * kk + 2 * tq]);
-          mma3(o[nn], a, rv.x, rv.y);
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < kD / 8; ++kk) {
-        const float2 gc = *reinterpret_cast<const float2*>(&S.gC[8 * kk + 2 * tq]);
-        st[kk][0] *= gc.x; st[kk][1] *= gc.y; st[kk][2] *= gc.x; st[kk][3] *= gc.y;
-      }
-#pragma unroll
-      for (int kk = 0; kk < kL / 8; ++kk) {
-        const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
-#pragma unroll
-        for (int nn = 0; nn < kD / 8; ++nn) {
-          mma3(st[nn], a, S.ke[8 * kk + 2 * tq][8 * nn + g8], S.ke[8 * kk + 2 * tq + 1][8 * nn + g8]);
-        }
-      }
-      // stage O (rows = tokens) and the per-warp partial sums of o^2
+    for (int kk = 0; kk < kL / 8; ++kk) {
+      const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
 #pragma unroll
       for (int nn = 0; nn < 4; ++nn) {
-        const int t = 8 * nn + 2 * tq;
-        S.v[t][jr] = o[nn][0];
-        S.v[t + 1][jr] = o[nn][1];
-        S.v[t][jr + 8] = o[nn][2];
-        S.v[t + 1][jr + 8] = o[nn][3];
-        float p0 = o[nn][0] * o[nn][0] + o[nn][2] * o[nn][2];
-        float p1 = o[nn][1] * o[nn][1] + o[nn][3] * o[nn][3];
+        const float2 rv = *reinterpret_cast<const float2*>(&R[8 * nn + g8][8 * kk + 2 * tq]);
+        mma3(o[nn], a, rv.x, rv.y);
+      }
+    }
 #pragma unroll
-        for (int m = 4; m < 32; m <<= 1) {
-          p0 += __shfl_xor_sync(0xffffffffu, p0, m);
-          p1 += __shfl_xor_sync(0xffffffffu, p1, m);
-        }
-        if (g8 == 0) {
-          S.nrm[warp][t] = p0;
-          S.nrm[warp][t + 1] = p1;
-        }
+    for (int kk = 0; kk < kD / 8; ++kk) {
+      const float2 gc = *reinterpret_cast<const float2*>(&gC[8 * kk + 2 * tq]);
+      st[kk][0] *= gc.x; st[kk][1] *= gc.y; st[kk][2] *= gc.x; st[kk][3] *= gc.y;
+    }
+#pragma unroll
+    for (int kk = 0; kk < kL / 8; ++kk) {
+      const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
+#pragma unroll
+      for (int nn = 0; nn < kD / 8; ++nn)
+        mma3(st[nn], a, KE[8 * kk + 2 * tq][8 * nn + g8], KE[8 * kk + 2 * tq + 1][8 * nn + g8]);
+    }
+    // stage O (rows = tokens) and the per-warp partial sums of o^2
+#pragma unroll
+    for (int nn = 0; nn < 4; ++nn) {
+      const int t = 8 * nn + 2 * tq;
+      S.o[t][jr] = o[nn][0];
+      S.o[t + 1][jr] = o[nn][1];
+      S.o[t][jr + 8] = o[nn][2];
+      S.o[t + 1][jr + 8] = o[nn][3];
+      float p0 = o[nn][0] * o[nn][0] + o[nn][2] * o[nn][2];
+      float p1 = o[nn][1] * o[nn][1] + o[nn][3] * o[nn][3];
+#pragma unroll
+      for (int m = 4; m < 32; m <<= 1) {
+        p0 += __shfl_xor_sync(0xffffffffu, p0, m);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, m);
+      }
+      if (g8 == 0) {
+        S.nrm[warp][t] = p0;
+        S.nrm[warp][t + 1] = p1;
       }
     }
     __syncthreads();
 
-    // ---- 8. gated RMSNorm (or raw o) to bf16; warp w writes tokens 4w..4w+3
+    // ---- gated RMSNorm (or raw o) to bf16; warp w writes tokens 4w..4w+3
 #pragma unroll
     for (int tt = 0; tt < 4; ++tt) {
       const int t = warp * 4 + tt;
       if (t >= L) break;
-      float4 y = reinterpret_cast<const float4*>(S.v[t])[lane];
+      float4 y = reinterpret_cast<const float4*>(S.o[t])[lane];
       if (kOutNorm) {
         const float4 nw4 = __ldg(reinterpret_cast<const float4*>(p.norm_w) + lane);
         float ss = 0.0f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) ss += S.nrm[w][t];
         const float rr = 1.0f / sqrtf(ss * (1.0f / kD) + p.eps);
-        const uint2 gb = reinterpret_cast<const uint2*>(S.gate[t])[lane];
+        const uint2 gb = __ldg(reinterpret_cast<const uint2*>(p.gate + (t0 + t) * p.gate_stride +
+                                                               static_cast<int64_t>(h) * kD) + lane);
         y.x = __fdividef(y.x * rr * nw4.x, 1.0f + __expf(-__uint_as_float(gb.x << 16)));
         y.y = __fdividef(y.y * rr * nw4.y, 1.0f + __expf(-__uint_as_float(gb.x & 0xFFFF0000u)));
         y.z = __fdividef(y.z * rr * nw4.z, 1.0f + __expf(-__uint_as_float(gb.y << 16)));
@@ -513,10 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
       reinterpret_cast<uint2*>(p.out + (t0 + t) * p.out_stride + static_cast<int64_t>(h) * kD)[lane] =
           make_uint2(pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
     }
-    __syncthreads();
   }
 
-  // ---- sequence end: state and conv window back to the slot
+  // ---- sequence end: state and conv window back to the slot.  The window
+  // [old taps | tokens] ends with its last three inputs; for sequences of
+  // fewer than three tokens some of them are old taps.
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk) {
     const int i0 = 8 * kk + 2 * tq;
@@ -525,9 +616,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const PrefillP
     Sg[i0 * kD + jr + 8] = st[kk][2];
     Sg[(i0 + 1) * kD + jr + 8] = st[kk][3];
   }
-  for (int c = tid; c < kCh; c += kThreads)
+  uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
+  const int64_t len = r1 - r0;
+  for (int ch = tid; ch < kCh; ch += kThreads) {
+    const int64_t cg = static_cast<int64_t>(ch >> 7) * D + static_cast<int64_t>(h) * kD + (ch & 127);
+    uint16_t w3[kHist];
 #pragma unroll
-    for (int r = 0; r < kHist; ++r) cs[ch_global(c) * kHist + r] = S.raw[r][c];
+    for (int r = 0; r < kHist; ++r) {
+      const int64_t pos = len + r;  // position in the window [old taps (3) | tokens (len)]
+      w3[r] = pos < kHist ? cs[cg * kHist + pos] : p.qkv[(r0 + pos - kHist) * p.qkv_stride + cg];
+    }
+#pragma unroll
+    for (int r = 0; r < kHist; ++r) cs[cg * kHist + r] = w3[r];
+  }
 }
 
 std::mutex g_mutex;
@@ -540,12 +641,15 @@ cudaError_t setup() {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mutex);
   if (!g_attrs_set[dev]) {
-    const int bytes = static_cast<int>(sizeof(PSmem));
-    if ((e = cudaFuncSetAttribute(kda_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
-        cudaSuccess)
+    if ((e = cudaFuncSetAttribute(kda_prefill_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sizeof(ChunkSmem)))) != cudaSuccess)
       return e;
-    if ((e = cudaFuncSetAttribute(kda_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
-        cudaSuccess)
+    const int scan = static_cast<int>(sizeof(ScanSmem));
+    if ((e = cudaFuncSetAttribute(kda_prefill_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  scan)) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(kda_prefill_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  scan)) != cudaSuccess)
       return e;
     g_attrs_set[dev] = true;
   }
@@ -556,6 +660,11 @@ bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 
 }  // namespace
 
+extern "C" int64_t kda_prefill_workspace_bytes(int64_t num_chunks, int32_t H) {
+  if (num_chunks < 0 || H < 1) return -1;
+  return num_chunks * H * static_cast<int64_t>(kImg) * 4;
+}
+
 extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   kda_internal_clear_error();
   if (!a) return kda_internal_fail(KDA_ERR_NULLPTR, "args is NULL");
@@ -565,32 +674,42 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   if (a->head_dim != KDA_HEAD_DIM || a->conv_width != KDA_CONV_WIDTH)
     return kda_internal_fail(KDA_ERR_SHAPE, "head_dim %d / conv_width %d (need 128 / 4)", a->head_dim,
                              a->conv_width);
-  if (a->B < 0 || a->H < 1 || a->num_slots < 1 || a->T < 0)
-    return kda_internal_fail(KDA_ERR_SHAPE, "B=%d H=%d num_slots=%d T=%lld", a->B, a->H, a->num_slots,
-                             static_cast<long long>(a->T));
+  if (a->B < 0 || a->H < 1 || a->H > 65535 || a->num_slots < 1 || a->T < 0 || a->num_chunks < 0)
+    return kda_internal_fail(KDA_ERR_SHAPE, "B=%d H=%d num_slots=%d T=%lld num_chunks=%lld", a->B, a->H,
+                             a->num_slots, static_cast<long long>(a->T), static_cast<long long>(a->num_chunks));
   if (a->flags & ~KDA_OUT_NORM) return kda_internal_fail(KDA_ERR_FLAGS, "flags 0x%x (only KDA_OUT_NORM)", a->flags);
-  if (static_cast<int64_t>(a->B) * a->H > 0x7fffffffLL) return kda_internal_fail(KDA_ERR_SHAPE, "B*H too large");
+  if (static_cast<int64_t>(a->B) * a->H > 0x7fffffffLL || a->num_chunks > 0x7fffffffLL)
+    return kda_internal_fail(KDA_ERR_SHAPE, "B*H or num_chunks too large");
   if (a->B == 0 || a->T == 0) return KDA_OK;
   const bool norm = (a->flags & KDA_OUT_NORM) != 0;
   const int64_t D = static_cast<int64_t>(a->H) * KDA_HEAD_DIM;
-  if (!a->cu_seqlens || !a->qkv || !a->conv_weight || !a->conv_state || !a->state || !a->g || !a->beta ||
-      !a->slot_idx || !a->out)
+  if (!a->cu_seqlens || !a->chunk_offsets || !a->qkv || !a->conv_weight || !a->conv_state || !a->state || !a->g ||
+      !a->beta || !a->slot_idx || !a->out || (a->num_chunks > 0 && (!a->chunk_indices || !a->workspace)))
     return kda_internal_fail(KDA_ERR_NULLPTR, "a required pointer is NULL");
   if (norm && (!a->gate || !a->norm_weight))
     return kda_internal_fail(KDA_ERR_NULLPTR, "KDA_OUT_NORM needs gate and norm_weight");
   if (a->qkv_row_stride < 3 * D || a->out_row_stride < D || (norm && a->gate_row_stride < D))
     return kda_internal_fail(KDA_ERR_SHAPE, "a row stride is smaller than the row");
+  if (a->workspace_bytes < kda_prefill_workspace_bytes(a->num_chunks, a->H))
+    return kda_internal_fail(KDA_ERR_SHAPE, "workspace of %lld bytes, %lld needed",
+                             static_cast<long long>(a->workspace_bytes),
+                             static_cast<long long>(kda_prefill_workspace_bytes(a->num_chunks, a->H)));
   if (!aligned(a->qkv, 16) || (a->qkv_row_stride & 7) || !aligned(a->state, 16) || !aligned(a->g, 16) ||
       !aligned(a->out, 8) || (a->out_row_stride & 3) || !aligned(a->cu_seqlens, 4) || !aligned(a->slot_idx, 4) ||
+      !aligned(a->chunk_indices, 8) || !aligned(a->chunk_offsets, 8) || !aligned(a->workspace, 16) ||
       !aligned(a->conv_weight, 4) || !aligned(a->conv_state, 2) || !aligned(a->beta, 2) ||
       !aligned(a->err_flag, 4) || (a->conv_bias && !aligned(a->conv_bias, 4)) ||
-      (norm && (!aligned(a->gate, 16) || (a->gate_row_stride & 7) || !aligned(a->norm_weight, 16))))
+      (norm && (!aligned(a->gate, 8) || (a->gate_row_stride & 3) || !aligned(a->norm_weight, 16))))
     return kda_internal_fail(KDA_ERR_ALIGN, "a pointer or row stride is not aligned as required");
   cudaError_t e = setup();
   if (e != cudaSuccess) return kda_internal_fail(KDA_ERR_LAUNCH, "setup: %s", cudaGetErrorString(e));
 
   PrefillParams p;
   p.cu = a->cu_seqlens;
+  p.chunk_idx = a->chunk_indices;
+  p.chunk_off = a->chunk_offsets;
+  p.num_chunks = a->num_chunks;
+  p.ws = static_cast<float*>(a->workspace);
   p.qkv = a->qkv;
   p.qkv_stride = a->qkv_row_stride;
   p.conv_w = a->conv_weight;
@@ -612,12 +731,15 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   p.eps = a->eps;
   p.q_scale = a->q_scale;
   p.err = a->err_flag;
-  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(a->B) * a->H));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->num_chunks > 0)
+    kda_prefill_chunk_kernel<<<dim3(static_cast<unsigned>(a->num_chunks), static_cast<unsigned>(a->H)), kThreads,
+                               sizeof(ChunkSmem), s>>>(p);
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(a->B) * a->H));
   if (norm)
-    kda_prefill_kernel<true><<<grid, kThreads, sizeof(PSmem), s>>>(p);
+    kda_prefill_scan_kernel<true><<<grid, kThreads, sizeof(ScanSmem), s>>>(p);
   else
-    kda_prefill_kernel<false><<<grid, kThreads, sizeof(PSmem), s>>>(p);
+    kda_prefill_scan_kernel<false><<<grid, kThreads, sizeof(ScanSmem), s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return kda_internal_fail(KDA_ERR_LAUNCH, "launch: %s", cudaGetErrorString(e));
   return KDA_OK;

@@ -63,9 +63,11 @@ def _pargs(**kw):
                                num_slots=8, head_dim=128, conv_width=4, T=40, eps=1e-6, flags=1)
     fake = 0x10000
     for f in ("cu_seqlens", "qkv", "conv_weight", "conv_state", "state", "g", "beta", "gate",
-              "norm_weight", "slot_idx", "out"):
+              "norm_weight", "slot_idx", "out", "chunk_indices", "chunk_offsets", "workspace"):
         setattr(a, f, fake)
         fake += 0x100000
+    a.num_chunks = 3
+    a.workspace_bytes = 1 << 30
     a.qkv_row_stride = 3 * 4 * 128
     a.gate_row_stride = a.out_row_stride = 4 * 128
     for k, v in kw.items():
@@ -91,6 +93,15 @@ def test_prefill_host_validation_codes(lib):
     assert call(_pargs(state=0x10004)) == -3
     assert call(_pargs(out=0x10004)) == -3
     assert b"aligned" in L.kda_last_error()
+    assert call(_pargs(workspace=0x10008)) == -3        # workspace needs 16-byte alignment
+    assert call(_pargs(chunk_offsets=None)) == -1
+    assert call(_pargs(workspace_bytes=1000)) == -2     # smaller than the chunks need
+    assert b"workspace" in L.kda_last_error()
+    assert call(_pargs(num_chunks=-1)) == -2
+    L.kda_prefill_workspace_bytes.restype = ctypes.c_int64
+    L.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
+    assert L.kda_prefill_workspace_bytes(10, 4) == 10 * 4 * 74240
+    assert L.kda_prefill_workspace_bytes(-1, 4) == -1
 
 
 def _args(**kw):

@@ -27,7 +27,8 @@ def to_device(x: W.PrefillInputs, dev, out_row_pad: int = 0):
         conv_state=T.bf16_tensor(x.conv_state, dev), state=torch.from_numpy(x.state).to(dev),
         g=torch.from_numpy(x.g).to(dev), beta=T.bf16_tensor(x.beta, dev),
         gate=T.bf16_tensor(x.gate, dev), norm_weight=torch.from_numpy(x.norm_weight).to(dev),
-        cu_seqlens=torch.from_numpy(x.cu_seqlens).to(dev), slot_idx=torch.from_numpy(x.slot_idx).to(dev),
+        cu_seqlens=torch.from_numpy(x.cu_seqlens).to(dev), cu_seqlens_cpu=torch.from_numpy(x.cu_seqlens),
+        slot_idx=torch.from_numpy(x.slot_idx).to(dev),
         err_flag=torch.zeros(1, dtype=torch.int32, device=dev))
     # NaN-filled: any row the kernel should write and does not is caught
     d["out_full"] = torch.full((x.spec.T, D + out_row_pad), float("nan"), dtype=torch.bfloat16, device=dev)
@@ -37,8 +38,9 @@ def to_device(x: W.PrefillInputs, dev, out_row_pad: int = 0):
 
 def run_gpu(x: W.PrefillInputs, d: dict):
     kda_prefill(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
-                d["cu_seqlens"], d["slot_idx"], d["out"], gate=d["gate"], norm_weight=d["norm_weight"],
-                conv_bias=d["conv_bias"], eps=x.spec.eps, out_norm=x.spec.out_norm, err_flag=d["err_flag"])
+                d["cu_seqlens"], d["slot_idx"], d["out"], cu_seqlens_cpu=d["cu_seqlens_cpu"], gate=d["gate"],
+                norm_weight=d["norm_weight"], conv_bias=d["conv_bias"], eps=x.spec.eps,
+                out_norm=x.spec.out_norm, err_flag=d["err_flag"])
 
 
 def run_oracle(x: W.PrefillInputs, seqs=None):
@@ -175,9 +177,9 @@ def test_prefill_graph_capture_and_prepared_call(cuda_device):
     x = W.make_prefill_inputs(W.PREFILL_NORM_OFF)
     d = to_device(x, cuda_device)
     call = KdaPrefillCall(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
-                          d["cu_seqlens"], d["slot_idx"], d["out"], gate=d["gate"],
-                          norm_weight=d["norm_weight"], conv_bias=d["conv_bias"], eps=x.spec.eps,
-                          out_norm=x.spec.out_norm, err_flag=d["err_flag"])
+                          d["cu_seqlens"], d["slot_idx"], d["out"], cu_seqlens_cpu=d["cu_seqlens_cpu"],
+                          gate=d["gate"], norm_weight=d["norm_weight"], conv_bias=d["conv_bias"],
+                          eps=x.spec.eps, out_norm=x.spec.out_norm, err_flag=d["err_flag"])
     state0, cs0 = d["state"].clone(), d["conv_state"].clone()
     s = torch.cuda.Stream(cuda_device)
     call(s)          # eager once (device set-up), then restore the pools and capture
