@@ -29,7 +29,7 @@
 // Tensor cores: every contraction with the state (W S0, Q_G S0, K_E^T Delta)
 // and between tokens (P, R, R Delta) is a warp-level m16n8k8 tf32 MMA, each
 // operand split into a tf32 high part and a tf32 remainder and three
-// products accumulated in fp32, which keeps fp32-level accuracy.  The state
+// products accumulated in fp32, which keeps close to fp32 accuracy.  The state
 // is held in registers for the whole sequence, transposed (value rows x key
 // columns) in the accumulator layout, which doubles as the A operand of the
 // next chunk's products (the k index of an m16n8k8 operand may be permuted as
@@ -110,7 +110,7 @@ struct __align__(16) ChunkSmem {
   float q[kL][kSA];                 // q^
   float k[kL][kSA];                 // k^
   float v[kL][kSA];                 // v~
-  float G[kL][kD];                  // cumulative log decay
+  float G[kL][kSA];                 // cumulative log decay
   float P[kL][kSP];                 // P (strictly lower)
   float beta[kL];
   int slow;                         // this chunk takes the element-wise P / R path
@@ -136,10 +136,13 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
+// tf32 keeps the top 19 bits of an fp32 word (sign, exponent, 10 mantissa
+// bits).  An fp32 value x is split as hi = x with its low 13 bits cleared and
+// lo = x - hi (exact in fp32), lo again cut to 19 bits: hi + lo carries 21
+// significant bits, and the split costs integer and add instructions only.
+__device__ __forceinline__ uint32_t tf32_hi(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
+__device__ __forceinline__ uint32_t tf32_lo(float x, uint32_t hi) {
+  return __float_as_uint(x - __uint_as_float(hi)) & 0xFFFFE000u;
 }
 
 __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -160,16 +163,16 @@ __device__ __forceinline__ FragA make_a(float a0, float a1, float a2, float a3) 
   const float a[4] = {a0, a1, a2, a3};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    f.hi[e] = to_tf32(a[e]);
-    f.lo[e] = to_tf32(a[e] - __uint_as_float(f.hi[e]));
+    f.hi[e] = tf32_hi(a[e]);
+    f.lo[e] = tf32_lo(a[e], f.hi[e]);
   }
   return f;
 }
 
 // c += A * B with B's two elements split as well: lo*hi + hi*lo + hi*hi.
 __device__ __forceinline__ void mma3(float (&c)[4], const FragA& a, float b0, float b1) {
-  const uint32_t h0 = to_tf32(b0), h1 = to_tf32(b1);
-  const uint32_t l0 = to_tf32(b0 - __uint_as_float(h0)), l1 = to_tf32(b1 - __uint_as_float(h1));
+  const uint32_t h0 = tf32_hi(b0), h1 = tf32_hi(b1);
+  const uint32_t l0 = tf32_lo(b0, h0), l1 = tf32_lo(b1, h1);
   mma_tf32(c, a.lo, h0, h1);
   mma_tf32(c, a.hi, l0, l1);
   mma_tf32(c, a.hi, h0, h1);
@@ -177,8 +180,8 @@ __device__ __forceinline__ void mma3(float (&c)[4], const FragA& a, float b0, fl
 
 // The same with the small terms in a separate accumulator: c += hi*hi, cl += lo*hi + hi*lo.
 __device__ __forceinline__ void mma3s(float (&c)[4], float (&cl)[4], const FragA& a, float b0, float b1) {
-  const uint32_t h0 = to_tf32(b0), h1 = to_tf32(b1);
-  const uint32_t l0 = to_tf32(b0 - __uint_as_float(h0)), l1 = to_tf32(b1 - __uint_as_float(h1));
+  const uint32_t h0 = tf32_hi(b0), h1 = tf32_hi(b1);
+  const uint32_t l0 = tf32_lo(b0, h0), l1 = tf32_lo(b1, h1);
   mma_tf32(cl, a.lo, h0, h1);
   mma_tf32(c, a.hi, h0, h1);
   mma_tf32(cl, a.hi, l0, l1);
@@ -341,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
     const float kv = S.k[t][i];
     S.f.ek[t][i] = __expf(d) * kv;
     S.f.fk[t][i] = __expf(-d) * kv;
-    ws[kOffQ + t * kSA + i] = expf(Gt) * S.q[t][i];
+    ws[kOffQ + t * kSA + i] = __expf(Gt) * S.q[t][i];
     ws[kOffK + t * kSK + i] = expf(S.G[kL - 1][i] - Gt) * kv;
   }
   if (tid < kD) ws[kOffC + tid] = expf(S.G[kL - 1][tid]);
@@ -507,9 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
 
     // ---- per warp (value rows jr, jr + 8): Delta^T = U^T - S^T W^T,
     // O^T = S^T Q_G^T + Delta^T R^T, S^T <- S^T Diag(gamma) + Delta^T K_E.
-    // The two products with S^T share its split fragments; the small
-    // (high x low) terms go to their own accumulators so that the chains of
-    // dependent MMAs stay short.
+    // Every product uses split operands and three tf32 products (one tf32
+    // product alone leaves outputs more than a bf16 ulp off); in the loop
+    // over the state's key tiles the small (high x low) terms go to their own
+    // accumulators so that chains of dependent MMAs stay short.
     float d[4][4], o[4][4], dl[4][4], ol[4][4];
 #pragma unroll
     for (int nn = 0; nn < 4; ++nn) {
