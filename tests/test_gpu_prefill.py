@@ -193,3 +193,75 @@ def test_prefill_graph_capture_and_prepared_call(cuda_device):
     torch.cuda.synchronize(cuda_device)
     ref, _ = run_oracle(x)
     compare(x, d, ref)
+
+
+def test_prefill_long_single_sequence(cuda_device):
+    # one sequence of 4,133 tokens (130 chunks, a ragged last one): the state
+    # runs through 129 chunk updates before the last outputs
+    spec = W.PrefillSpec("prefill_b1_t4133_h4", lens=(4133,), H=4, num_slots=3, seed=61)
+    x = W.make_prefill_inputs(spec)
+    d = to_device(x, cuda_device)
+    run_gpu(x, d)
+    torch.cuda.synchronize(cuda_device)
+    assert int(d["err_flag"].item()) == 0
+    ref, _ = run_oracle(x)
+    compare(x, d, ref)
+
+
+def test_prefill_many_short_sequences_and_wide_heads(cuda_device):
+    rng = np.random.default_rng(5)
+    lens = tuple(int(v) for v in rng.integers(0, 41, 48))  # 0..40 tokens, empty ones included
+    for spec in (W.PrefillSpec("prefill_b48_short_h2", lens=lens, H=2, num_slots=64, seed=62,
+                               pad_seqs=(3, 17)),
+                 W.PrefillSpec("prefill_b3_h96", lens=(33, 64, 7), H=96, num_slots=4, seed=63)):
+        x = W.make_prefill_inputs(spec)
+        d = to_device(x, cuda_device)
+        run_gpu(x, d)
+        torch.cuda.synchronize(cuda_device)
+        assert int(d["err_flag"].item()) == 0
+        ref, _ = run_oracle(x)
+        compare(x, d, ref)
+
+
+def test_prefill_continues_across_calls_strided_qkv_q_scale(cuda_device):
+    # a batch prefilled in two calls (first 45 tokens, then the rest of each
+    # sequence) equals one call over the whole sequences; qkv rows strided;
+    # q_scale given
+    spec = W.PrefillSpec("prefill_b2_h2_split", lens=(100, 77), H=2, num_slots=4, seed=64)
+    x = W.make_prefill_inputs(spec)
+    q_scale = 0.25
+    ref = oracle.prefill(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state,
+                         g=x.g, beta=x.beta, gate=x.gate, norm_weight=x.norm_weight, slot_idx=x.slot_idx,
+                         cu_seqlens=x.cu_seqlens, H=spec.H, eps=spec.eps, q_scale=q_scale)
+    dev = cuda_device
+    D = spec.H * 128
+    qkv_pad = np.zeros((spec.T, 3 * D + 16), np.uint16)
+    qkv_pad[:, :3 * D] = x.qkv
+    qkv_t = T.bf16_tensor(qkv_pad, dev)
+    cs, st = T.bf16_tensor(x.conv_state, dev), torch.from_numpy(x.state).to(dev)
+    out = torch.full((spec.T, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    cw, nw = torch.from_numpy(x.conv_weight).to(dev), torch.from_numpy(x.norm_weight).to(dev)
+    g_t, beta_t, gate_t = torch.from_numpy(x.g).to(dev), T.bf16_tensor(x.beta, dev), T.bf16_tensor(x.gate, dev)
+    slots = torch.from_numpy(x.slot_idx).to(dev)
+    first, second = [], []
+    for b in range(spec.B):
+        r0, r1 = int(x.cu_seqlens[b]), int(x.cu_seqlens[b + 1])
+        first.append(np.arange(r0, r0 + 45))
+        second.append(np.arange(r0 + 45, r1))
+    for part in (first, second):
+        rows = torch.from_numpy(np.concatenate(part)).to(dev)
+        cu = np.concatenate([[0], np.cumsum([len(r) for r in part])]).astype(np.int32)
+        o_part = torch.empty(len(rows), D, dtype=torch.bfloat16, device=dev)
+        kda_prefill(qkv_t[rows][:, :3 * D + 16][:, :], cw, cs, st, g_t[rows].contiguous(),
+                    beta_t[rows].contiguous(), torch.from_numpy(cu).to(dev), slots, o_part[:, :],
+                    cu_seqlens_cpu=torch.from_numpy(cu), gate=gate_t[rows], norm_weight=nw, eps=spec.eps,
+                    q_scale=q_scale, err_flag=err)
+        out[rows] = o_part
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0
+    T.check_out(T.bf16_bits(out), ref)
+    assert np.array_equal(T.bf16_bits(cs), ref.conv_state)
+    s_got = st.cpu().numpy()
+    for s in {int(v) for v in x.slot_idx}:
+        T.check_state_slot(s_got[s], ref.state[s], f"slot {s}")
