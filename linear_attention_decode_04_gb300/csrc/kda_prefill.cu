@@ -54,8 +54,6 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kCh = 3 * kD;       // q | k | v channels of one head
 constexpr int kSA = 136;          // row stride (floats) of [token][128] operands
-constexpr int kST = 40;           // row stride (floats) of R [token][token] (float2 reads)
-constexpr int kSK = 132;          // row stride (floats) of K_E and U, read as scalars
 constexpr int kSP = 36;           // row stride (floats) of P (rows read as float4)
 constexpr int kRef = 15;          // reference token of the split decay factors
 constexpr float kMaxExponent = 80.0f;  // |G_t - G_m| above this: element-wise path
@@ -86,17 +84,37 @@ struct PrefillParams {
   int32_t* err;
 };
 
-// Workspace image of one (chunk, head), written by the chunk kernel and
-// copied verbatim into the scan kernel's shared memory; the row strides are
-// the ones its tensor-core fragment reads want.
-constexpr int kOffW = 0;                      // W   [kL][kSA]
-constexpr int kOffQ = kOffW + kL * kSA;       // Q_G [kL][kSA]
-constexpr int kOffU = kOffQ + kL * kSA;       // U   [kL][kSK]
-constexpr int kOffK = kOffU + kL * kSK;       // K_E [kL][kSK]
-constexpr int kOffR = kOffK + kL * kSK;       // R   [kL][kST] (lower, zeros above)
-constexpr int kOffC = kOffR + kL * kST;       // gamma = exp(G_{L-1}) [kD]
-constexpr int kImg = kOffC + kD;              // 18,560 floats = 74,240 bytes
+// Workspace image of one (chunk, head), written by the chunk kernel with
+// plain row-major rows (coalesced stores) and copied by the scan kernel into
+// shared memory, where the operands its tensor-core products read (W, Q_G,
+// K_E^T, R) take the canonical K-major layout without swizzle: an N x K fp32
+// matrix is tiled into core matrices of 8 rows x 16 bytes (4 values), element
+// (n, k) at (n / 8) * SBO + (k / 4) * LBO + (n % 8) * 4 + k % 4 floats, with
+// the core matrices adjacent in K 128 bytes apart (LBO = 32 floats) and the
+// 8-row groups K / 4 core matrices apart (SBO = K * 8 floats).  A 16-byte
+// piece of a row (4 consecutive k) is one core-matrix row, so the copy
+// places each piece on its own.
+__host__ __device__ constexpr int kmajor(int n, int k, int K) {
+  return (n >> 3) * (K * 8) + (k >> 2) * 32 + (n & 7) * 4 + (k & 3);
+}
+constexpr int kOffW = 0;                      // W     [32 tokens][128 keys]
+constexpr int kOffQ = kOffW + kL * kD;        // Q_G   [32 tokens][128 keys]
+constexpr int kOffK = kOffQ + kL * kD;        // K_E^T [128 keys][32 tokens]
+constexpr int kOffR = kOffK + kD * kL;        // R     [32 tokens t][32 tokens s] (zeros above)
+constexpr int kOffU = kOffR + kL * kL;        // U     [32 tokens][128 values] (row-major in both)
+constexpr int kOffC = kOffU + kL * kD;        // gamma = exp(G_{L-1}) [128]
+constexpr int kImg = kOffC + kD;              // 17,536 floats = 70,144 bytes
+constexpr int kSplit = kOffU;                 // the operands the scan splits (W, Q_G, K_E^T, R)
 static_assert((kImg * 4) % 16 == 0, "image must be a whole number of 16-byte pieces");
+
+// Shared-memory position (floats) of the 16-byte piece e of an image.
+__device__ __forceinline__ int image_piece_dst(int e) {
+  if (e < kOffQ / 4) return kOffW + kmajor(e >> 5, 4 * (e & 31), kD);
+  if (e < kOffK / 4) { e -= kOffQ / 4; return kOffQ + kmajor(e >> 5, 4 * (e & 31), kD); }
+  if (e < kOffR / 4) { e -= kOffK / 4; return kOffK + kmajor(e >> 3, 4 * (e & 7), kL); }
+  if (e < kOffU / 4) { e -= kOffR / 4; return kOffR + kmajor(e >> 3, 4 * (e & 7), kL); }
+  return 4 * e;  // U and gamma: as stored
+}
 
 // Chunk kernel shared memory (about 106 KB: two CTAs per SM).
 struct __align__(16) ChunkSmem {
@@ -116,13 +134,22 @@ struct __align__(16) ChunkSmem {
   int slow;                         // this chunk takes the element-wise P / R path
 };
 
-// Scan kernel shared memory (about 163 KB): two images (double buffer), the
-// chunk's output and the per-warp partial sums of o^2.
+// Scan kernel shared memory (about 210 KB): two images (double buffer), the
+// tf32 remainders of the image's tensor-core operands, the chunk's output,
+// the two MMA-completion barriers and the tensor-memory base address.
 struct __align__(16) ScanSmem {
   float img[2][kImg];
+  float lo[kSplit];
   float o[kL][kSA];
-  float nrm[kWarps][kL];
+  unsigned long long bar[2];
+  uint32_t tmem;
 };
+
+// Tensor-memory columns of the scan kernel (512 allocated; lane = value row):
+// the fp32 state S^T, its tf32 high and low words (the A operand of the
+// products with the state), the chunk's S^T W^T and output accumulators, and
+// Delta^T's high and low words (the A operand of the products with Delta).
+constexpr uint32_t kTS = 0, kTSH = 128, kTSL = 256, kTD = 384, kTO = 416, kTDH = 448, kTDL = 480;
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -178,14 +205,6 @@ __device__ __forceinline__ void mma3(float (&c)[4], const FragA& a, float b0, fl
   mma_tf32(c, a.hi, h0, h1);
 }
 
-// The same with the small terms in a separate accumulator: c += hi*hi, cl += lo*hi + hi*lo.
-__device__ __forceinline__ void mma3s(float (&c)[4], float (&cl)[4], const FragA& a, float b0, float b1) {
-  const uint32_t h0 = tf32_hi(b0), h1 = tf32_hi(b1);
-  const uint32_t l0 = tf32_lo(b0, h0), l1 = tf32_lo(b1, h1);
-  mma_tf32(cl, a.lo, h0, h1);
-  mma_tf32(c, a.hi, h0, h1);
-  mma_tf32(cl, a.hi, l0, l1);
-}
 
 
 __device__ __forceinline__ void flag(const PrefillParams& p, int bits) {
@@ -334,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   __syncthreads();
 
   // ---- 4. split decay factors around the reference token (shared memory);
-  // Q_G = exp(G) q^, K_E = exp(G_{L-1} - G) k^ and gamma to the image; R's
-  // image cleared (its lower triangle is written next); P cleared
+  // Q_G = exp(G) q^ and gamma to the image; R's image cleared (its lower
+  // triangle is written next); P cleared
   for (int e = tid; e < kL * kD; e += kThreads) {
     const int t = e >> 7, i = e & (kD - 1);
     const float Gt = S.G[t][i];
@@ -344,11 +363,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
     const float kv = S.k[t][i];
     S.f.ek[t][i] = __expf(d) * kv;
     S.f.fk[t][i] = __expf(-d) * kv;
-    ws[kOffQ + t * kSA + i] = __expf(Gt) * S.q[t][i];
-    ws[kOffK + t * kSK + i] = expf(S.G[kL - 1][i] - Gt) * kv;
+    ws[kOffQ + t * kD + i] = __expf(Gt) * S.q[t][i];
   }
   if (tid < kD) ws[kOffC + tid] = expf(S.G[kL - 1][tid]);
-  for (int e = tid; e < kL * kST; e += kThreads) ws[kOffR + e] = 0.0f;
+  for (int e = tid; e < kL * kL; e += kThreads) ws[kOffR + e] = 0.0f;
   for (int e = tid; e < kL * kSP; e += kThreads) (&S.P[0][0])[e] = 0.0f;
   __syncthreads();
 
@@ -386,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
         if (mat == 0) {
           if (te > se) S.P[te][se] = acc[e];
         } else {
-          if (te >= se) ws[kOffR + te * kST + se] = acc[e];
+          if (te >= se) ws[kOffR + te * kL + se] = acc[e];
         }
       }
     }
@@ -404,16 +422,29 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
         pq = fmaf(S.q[t][i], fct, pq);
       }
       if (t > s) S.P[t][s] = pk;
-      ws[kOffR + t * kST + s] = pq;
+      ws[kOffR + t * kL + s] = pq;
     }
   }
   __syncthreads();
 
   // ---- 6. triangular solve (thread = one column of [U | W]), left-looking:
-  // x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or exp(G) k^ (W)
+  // x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or exp(G) k^ (W);
+  // the key-column threads also write their row of K_E^T = exp(G_{L-1} - G) k^
   {
     const bool vcol = tid < kD;
     const int i = tid - kD;
+    if (!vcol) {
+      const float GL = S.G[kL - 1][i];
+#pragma unroll 4
+      for (int t = 0; t < kL; t += 4) {
+        float4 ke;
+        ke.x = expf(GL - S.G[t][i]) * S.k[t][i];
+        ke.y = expf(GL - S.G[t + 1][i]) * S.k[t + 1][i];
+        ke.z = expf(GL - S.G[t + 2][i]) * S.k[t + 2][i];
+        ke.w = expf(GL - S.G[t + 3][i]) * S.k[t + 3][i];
+        reinterpret_cast<float4*>(ws + kOffK + i * kL)[t >> 2] = ke;
+      }
+    }
     float x[kL];
 #pragma unroll
     for (int t = 0; t < kL; ++t) {
@@ -429,21 +460,121 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
         if (4 * s4 + 3 < t) a3 = fmaf(-pr.w, x[4 * s4 + 3], a3);
       }
       x[t] = S.beta[t] * ((a0 + a1) + (a2 + a3));
-      if (vcol) ws[kOffU + t * kSK + tid] = x[t];
-      else ws[kOffW + t * kSA + i] = x[t];
+      if (vcol) ws[kOffU + t * kD + tid] = x[t];
+      else ws[kOffW + t * kD + i] = x[t];
     }
   }
 }
 
 // ====================================================================== scan
-// One CTA per (sequence, head): walks the sequence's chunks in order with
-// the state in registers; chunk j's image (row chunk_offsets[b] + j of the
+// tcgen05 helpers.  Shared-memory matrix descriptor of a canonical K-major
+// operand without swizzle: start address, LBO = 128 bytes (core matrices
+// adjacent in K), SBO (8-row groups), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t sbo_bytes) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFF) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+// Instruction descriptor, kind::tf32: f32 accumulator, tf32 A and B, both
+// K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t n) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+// D (tensor memory) (+)= A (tensor memory) x B (shared memory descriptor)
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+// three tf32 products of split operands: D += Alo*Bhi + Ahi*Blo + Ahi*Bhi
+__device__ __forceinline__ void mma_ts3(uint32_t d, uint32_t ahi, uint32_t alo, uint64_t bhi, uint64_t blo,
+                                        uint32_t idesc, uint32_t accumulate) {
+  mma_ts(d, alo, bhi, idesc, accumulate);
+  mma_ts(d, ahi, blo, idesc, 1);
+  mma_ts(d, ahi, bhi, idesc, 1);
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// 16 consecutive columns of this warp's 32 lanes
+__device__ __forceinline__ void tm_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tm_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+__device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tm_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 consecutive columns of this warp's 32 lanes; no wait (tm_wait_ld before use)
+__device__ __forceinline__ void tm_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+
+// Bounded wait on an mbarrier phase (2 s); false if it gave up.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    uint64_t now;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+    if (it == 0) t0 = now;
+    else if (now - t0 > 2000000000ull) return false;
+  }
+}
+
+// One CTA per (sequence, head): walks the sequence's chunks in order.  The
+// state lives in tensor memory for the whole sequence (lane = value row,
+// column = key) and every product with it runs on the 5th-generation tensor
+// cores (tcgen05.mma, kind::tf32, issued by one thread, accumulators in
+// tensor memory); chunk j's image (row chunk_offsets[b] + j of the
 // workspace) is copied into shared memory while chunk j - 1 computes.
+// Per chunk:  Delta^T = U^T - S^T W^T  and  O^T = S^T Q_G^T   (M = 128, N = 32, K = 128)
+//             O^T += Delta^T R^T                               (K = 32)
+//             S^T <- S^T Diag(gamma) + Delta^T K_E            (M = 128, N = 128, K = 32)
+// Every operand is split into a tf32 high word and a tf32 remainder and three
+// products are accumulated (lo*hi + hi*lo + hi*hi) in fp32.
 template <bool kOutNorm>
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const PrefillParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ScanSmem& S = *reinterpret_cast<ScanSmem*>(smem_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, tq = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / p.H, h = blockIdx.x - b * p.H;
   const int64_t D = static_cast<int64_t>(p.H) * kD;
 
@@ -471,119 +602,188 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     return;
   }
 
-  // state S^T in registers: st[kk][*] = rows (value) jr, jr + 8, columns
-  // (key) 8kk + 2tq, 8kk + 2tq + 1, in the m16n8 accumulator layout
-  float* Sg = p.state + (static_cast<int64_t>(slot) * p.H + h) * (kD * kD);
-  const int jr = warp * 16 + g8;
-  float st[16][4];
-#pragma unroll
-  for (int kk = 0; kk < 16; ++kk) {
-    const int i0 = 8 * kk + 2 * tq;
-    st[kk][0] = Sg[i0 * kD + jr];
-    st[kk][1] = Sg[(i0 + 1) * kD + jr];
-    st[kk][2] = Sg[i0 * kD + jr + 8];
-    st[kk][3] = Sg[(i0 + 1) * kD + jr + 8];
+  // warps w and w + 4 share tensor-memory lanes 32 (w % 4) .. + 31 and split
+  // the columns: value row j = this thread's lane
+  const int quad = warp & 3, half = warp >> 2;
+  const int j = 32 * quad + lane;
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.bar[0])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.bar[1])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&S.tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = S.tmem;
+  const uint32_t tm = tbase + (static_cast<uint32_t>(32 * quad) << 16);  // this warp's lanes
+
+  // state S^T row j, keys [64 half, 64 half + 64): fp32, high and low words
+  float* Sg = p.state + (static_cast<int64_t>(slot) * p.H + h) * (kD * kD);
+#pragma unroll
+  for (int cc = 0; cc < 64; cc += 16) {
+    uint32_t v[16], hi[16], lo[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float x = Sg[static_cast<int64_t>(64 * half + cc + e) * kD + j];
+      v[e] = __float_as_uint(x);
+      hi[e] = tf32_hi(x);
+      lo[e] = tf32_lo(x, hi[e]);
+    }
+    tm_st16(tm + kTS + 64 * half + cc, v);
+    tm_st16(tm + kTSH + 64 * half + cc, hi);
+    tm_st16(tm + kTSL + 64 * half + cc, lo);
+  }
+  tm_wait_st();
 
   auto fetch = [&](int64_t jj, int buf) {
     const float4* src = reinterpret_cast<const float4*>(p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kImg));
-    float4* dst = reinterpret_cast<float4*>(S.img[buf]);
-    for (int e = tid; e < kImg / 4; e += kThreads) cp_async16(dst + e, src + e);
+    float* dst = S.img[buf];
+    for (int e = tid; e < kImg / 4; e += kThreads) cp_async16(dst + image_piece_dst(e), src + e);
     cp_async_commit();
   };
   fetch(0, 0);
+  constexpr uint32_t kId32 = idesc_tf32(32), kId128 = idesc_tf32(128);
+  const uint32_t lo_addr = smem_u32(S.lo);
+  bool ok = true;
 
   for (int64_t jj = 0; jj < n_chunks; ++jj) {
     const int64_t t0 = r0 + kL * jj;
     const int L = static_cast<int>(r1 - t0 < kL ? r1 - t0 : kL);
     const int buf = static_cast<int>(jj & 1);
+    const uint32_t par = static_cast<uint32_t>(jj & 1);
     cp_async_wait_all();
-    __syncthreads();                       // image jj landed; the other buffer is free
+    __syncthreads();                       // image jj landed; the other buffer and lo are free
     if (jj + 1 < n_chunks) fetch(jj + 1, buf ^ 1);
-    const float* img = S.img[buf];
-    const float(*W)[kSA] = reinterpret_cast<const float(*)[kSA]>(img + kOffW);
-    const float(*QG)[kSA] = reinterpret_cast<const float(*)[kSA]>(img + kOffQ);
-    const float(*U)[kSK] = reinterpret_cast<const float(*)[kSK]>(img + kOffU);
-    const float(*KE)[kSK] = reinterpret_cast<const float(*)[kSK]>(img + kOffK);
-    const float(*R)[kST] = reinterpret_cast<const float(*)[kST]>(img + kOffR);
-    const float* gC = img + kOffC;
+    float* img = S.img[buf];
+    const uint32_t img_addr = smem_u32(img);
 
-    // ---- per warp (value rows jr, jr + 8): Delta^T = U^T - S^T W^T,
-    // O^T = S^T Q_G^T + Delta^T R^T, S^T <- S^T Diag(gamma) + Delta^T K_E.
-    // Every product uses split operands and three tf32 products (one tf32
-    // product alone leaves outputs more than a bf16 ulp off); in the loop
-    // over the state's key tiles the small (high x low) terms go to their own
-    // accumulators so that chains of dependent MMAs stay short.
-    float d[4][4], o[4][4], dl[4][4], ol[4][4];
-#pragma unroll
-    for (int nn = 0; nn < 4; ++nn) {
-      d[nn][0] = U[8 * nn + 2 * tq][jr];
-      d[nn][1] = U[8 * nn + 2 * tq + 1][jr];
-      d[nn][2] = U[8 * nn + 2 * tq][jr + 8];
-      d[nn][3] = U[8 * nn + 2 * tq + 1][jr + 8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[nn][e] = dl[nn][e] = ol[nn][e] = 0.0f;
-    }
-#pragma unroll
-    for (int kk = 0; kk < kD / 8; ++kk) {
-      const FragA a = make_a(st[kk][0], st[kk][2], st[kk][1], st[kk][3]);
-#pragma unroll
-      for (int nn = 0; nn < 4; ++nn) {
-        const float2 wv2 = *reinterpret_cast<const float2*>(&W[8 * nn + g8][8 * kk + 2 * tq]);
-        mma3s(d[nn], dl[nn], a, -wv2.x, -wv2.y);
-        const float2 qv2 = *reinterpret_cast<const float2*>(&QG[8 * nn + g8][8 * kk + 2 * tq]);
-        mma3s(o[nn], ol[nn], a, qv2.x, qv2.y);
+    // split the image's tensor-core operands: high words in place, remainders aside
+    {
+      float4* im = reinterpret_cast<float4*>(img);
+      float4* lo4 = reinterpret_cast<float4*>(S.lo);
+      for (int e = tid; e < kSplit / 4; e += kThreads) {
+        float4 x = im[e], l;
+        uint32_t hb;
+        hb = tf32_hi(x.x); l.x = __uint_as_float(tf32_lo(x.x, hb)); x.x = __uint_as_float(hb);
+        hb = tf32_hi(x.y); l.y = __uint_as_float(tf32_lo(x.y, hb)); x.y = __uint_as_float(hb);
+        hb = tf32_hi(x.z); l.z = __uint_as_float(tf32_lo(x.z, hb)); x.z = __uint_as_float(hb);
+        hb = tf32_hi(x.w); l.w = __uint_as_float(tf32_lo(x.w, hb)); x.w = __uint_as_float(hb);
+        im[e] = x;
+        lo4[e] = l;
       }
     }
-#pragma unroll
-    for (int nn = 0; nn < 4; ++nn)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        d[nn][e] += dl[nn][e];
-        o[nn][e] += ol[nn][e];
-      }
-#pragma unroll
-    for (int kk = 0; kk < kL / 8; ++kk) {
-      const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
-#pragma unroll
-      for (int nn = 0; nn < 4; ++nn) {
-        const float2 rv = *reinterpret_cast<const float2*>(&R[8 * nn + g8][8 * kk + 2 * tq]);
-        mma3(o[nn], a, rv.x, rv.y);
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < kD / 8; ++kk) {
-      const float2 gc = *reinterpret_cast<const float2*>(&gC[8 * kk + 2 * tq]);
-      st[kk][0] *= gc.x; st[kk][1] *= gc.y; st[kk][2] *= gc.x; st[kk][3] *= gc.y;
-    }
-#pragma unroll
-    for (int kk = 0; kk < kL / 8; ++kk) {
-      const FragA a = make_a(d[kk][0], d[kk][2], d[kk][1], d[kk][3]);
-#pragma unroll
-      for (int nn = 0; nn < kD / 8; ++nn)
-        mma3(st[nn], a, KE[8 * kk + 2 * tq][8 * nn + g8], KE[8 * kk + 2 * tq + 1][8 * nn + g8]);
-    }
-    // stage O (rows = tokens) and the per-warp partial sums of o^2
-#pragma unroll
-    for (int nn = 0; nn < 4; ++nn) {
-      const int t = 8 * nn + 2 * tq;
-      S.o[t][jr] = o[nn][0];
-      S.o[t + 1][jr] = o[nn][1];
-      S.o[t][jr + 8] = o[nn][2];
-      S.o[t + 1][jr + 8] = o[nn][3];
-      float p0 = o[nn][0] * o[nn][0] + o[nn][2] * o[nn][2];
-      float p1 = o[nn][1] * o[nn][1] + o[nn][3] * o[nn][3];
-#pragma unroll
-      for (int m = 4; m < 32; m <<= 1) {
-        p0 += __shfl_xor_sync(0xffffffffu, p0, m);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, m);
-      }
-      if (g8 == 0) {
-        S.nrm[warp][t] = p0;
-        S.nrm[warp][t + 1] = p1;
-      }
-    }
+    fence_proxy_async();                   // generic writes -> the tensor cores' view
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+
+    // ---- D_Delta = S^T W^T, D_O = S^T Q_G^T  (K = 128 keys, 16 steps of 8)
+    if (tid == 0) {
+#pragma unroll 1
+      for (int ks = 0; ks < kD / 8; ++ks) {
+        const uint32_t acc = ks > 0;
+        const uint32_t ahi = tbase + kTSH + 8 * ks, alo = tbase + kTSL + 8 * ks;
+        mma_ts3(tbase + kTD, ahi, alo, sdesc(img_addr + 4 * kOffW + 256 * ks, 4096),
+                sdesc(lo_addr + 4 * kOffW + 256 * ks, 4096), kId32, acc);
+        mma_ts3(tbase + kTO, ahi, alo, sdesc(img_addr + 4 * kOffQ + 256 * ks, 4096),
+                sdesc(lo_addr + 4 * kOffQ + 256 * ks, 4096), kId32, acc);
+      }
+      mma_commit(smem_u32(&S.bar[0]));
+    }
+    // While those run (they read the split words, not the fp32 state):
+    // S^T <- S^T Diag(gamma) over this thread's 64 keys, and the gate rows of
+    // the tokens this warp writes out
+    {
+      const float* gC = img + kOffC + 64 * half;
+      uint32_t r0[32], r1[32];
+      tm_ld32_nowait(tm + kTS + 64 * half, r0);
+      tm_ld32_nowait(tm + kTS + 64 * half + 32, r1);
+      tm_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        r0[e] = __float_as_uint(__uint_as_float(r0[e]) * gC[e]);
+        r1[e] = __float_as_uint(__uint_as_float(r1[e]) * gC[32 + e]);
+      }
+      tm_st32(tm + kTS + 64 * half, r0);
+      tm_st32(tm + kTS + 64 * half + 32, r1);
+    }
+    uint2 gate_pf[4];
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt) {
+      const int t = warp * 4 + tt;
+      gate_pf[tt] = make_uint2(0, 0);
+      if (kOutNorm && t < L)
+        gate_pf[tt] = __ldg(reinterpret_cast<const uint2*>(p.gate + (t0 + t) * p.gate_stride +
+                                                           static_cast<int64_t>(h) * kD) + lane);
+    }
+    ok = bar_wait(smem_u32(&S.bar[0]), par);
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+
+    // Delta^T = U^T - D_Delta for row j, tokens [16 half, 16 half + 16): split
+    {
+      uint32_t r[16], dh[16], dl[16];
+      tm_ld16(tm + kTD + 16 * half, r);
+      const float* ucol = img + kOffU + (16 * half) * kD + j;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float dv = ucol[e * kD] - __uint_as_float(r[e]);
+        dh[e] = tf32_hi(dv);
+        dl[e] = tf32_lo(dv, dh[e]);
+      }
+      tm_st16(tm + kTDH + 16 * half, dh);
+      tm_st16(tm + kTDL + 16 * half, dl);
+    }
+    tm_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- D_O += Delta^T R^T;  S^T += Delta^T K_E   (K = 32 tokens, 4 steps of 8)
+    if (tid == 0) {
+#pragma unroll 1
+      for (int ks = 0; ks < kL / 8; ++ks) {
+        const uint32_t ahi = tbase + kTDH + 8 * ks, alo = tbase + kTDL + 8 * ks;
+        mma_ts3(tbase + kTO, ahi, alo, sdesc(img_addr + 4 * kOffR + 256 * ks, 1024),
+                sdesc(lo_addr + 4 * kOffR + 256 * ks, 1024), kId32, 1);
+        mma_ts3(tbase + kTS, ahi, alo, sdesc(img_addr + 4 * kOffK + 256 * ks, 1024),
+                sdesc(lo_addr + 4 * kOffK + 256 * ks, 1024), kId128, 1);
+      }
+      mma_commit(smem_u32(&S.bar[1]));
+    }
+    ok = bar_wait(smem_u32(&S.bar[1]), par);
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+
+    // the chunk's output rows to shared memory; the new state's split words
+    {
+      uint32_t r[16];
+      tm_ld16(tm + kTO + 16 * half, r);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) S.o[16 * half + e][j] = __uint_as_float(r[e]);
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t v[32], hi[32];
+        tm_ld32_nowait(tm + kTS + 64 * half + cc, v);
+        tm_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float x = __uint_as_float(v[e]);
+          hi[e] = tf32_hi(x);
+          v[e] = tf32_lo(x, hi[e]);
+        }
+        tm_st32(tm + kTSH + 64 * half + cc, hi);
+        tm_st32(tm + kTSL + 64 * half + cc, v);
+      }
+    }
+    tm_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     // ---- gated RMSNorm (or raw o) to bf16; warp w writes tokens 4w..4w+3
 #pragma unroll
@@ -593,12 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
       float4 y = reinterpret_cast<const float4*>(S.o[t])[lane];
       if (kOutNorm) {
         const float4 nw4 = __ldg(reinterpret_cast<const float4*>(p.norm_w) + lane);
-        float ss = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) ss += S.nrm[w][t];
+        const float ss = warp_sum((y.x * y.x + y.y * y.y) + (y.z * y.z + y.w * y.w));
         const float rr = 1.0f / sqrtf(ss * (1.0f / kD) + p.eps);
-        const uint2 gb = __ldg(reinterpret_cast<const uint2*>(p.gate + (t0 + t) * p.gate_stride +
-                                                               static_cast<int64_t>(h) * kD) + lane);
+        const uint2 gb = gate_pf[tt];
         y.x = __fdividef(y.x * rr * nw4.x, 1.0f + __expf(-__uint_as_float(gb.x << 16)));
         y.y = __fdividef(y.y * rr * nw4.y, 1.0f + __expf(-__uint_as_float(gb.x & 0xFFFF0000u)));
         y.z = __fdividef(y.z * rr * nw4.z, 1.0f + __expf(-__uint_as_float(gb.y << 16)));
@@ -608,31 +805,38 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
           make_uint2(pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
     }
   }
+  cp_async_wait_all();
 
-  // ---- sequence end: state and conv window back to the slot.  The window
-  // [old taps | tokens] ends with its last three inputs; for sequences of
-  // fewer than three tokens some of them are old taps.
+  if (ok) {
+    // ---- sequence end: state and conv window back to the slot.  The window
+    // [old taps | tokens] ends with its last three inputs; for sequences of
+    // fewer than three tokens some of them are old taps.
 #pragma unroll
-  for (int kk = 0; kk < 16; ++kk) {
-    const int i0 = 8 * kk + 2 * tq;
-    Sg[i0 * kD + jr] = st[kk][0];
-    Sg[(i0 + 1) * kD + jr] = st[kk][1];
-    Sg[i0 * kD + jr + 8] = st[kk][2];
-    Sg[(i0 + 1) * kD + jr + 8] = st[kk][3];
-  }
-  uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
-  const int64_t len = r1 - r0;
-  for (int ch = tid; ch < kCh; ch += kThreads) {
-    const int64_t cg = static_cast<int64_t>(ch >> 7) * D + static_cast<int64_t>(h) * kD + (ch & 127);
-    uint16_t w3[kHist];
+    for (int cc = 0; cc < 64; cc += 16) {
+      uint32_t r[16];
+      tm_ld16(tm + kTS + 64 * half + cc, r);
 #pragma unroll
-    for (int r = 0; r < kHist; ++r) {
-      const int64_t pos = len + r;  // position in the window [old taps (3) | tokens (len)]
-      w3[r] = pos < kHist ? cs[cg * kHist + pos] : p.qkv[(r0 + pos - kHist) * p.qkv_stride + cg];
+      for (int e = 0; e < 16; ++e) Sg[static_cast<int64_t>(64 * half + cc + e) * kD + j] = __uint_as_float(r[e]);
     }
+    uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
+    const int64_t len = r1 - r0;
+    for (int ch = tid; ch < kCh; ch += kThreads) {
+      const int64_t cg = static_cast<int64_t>(ch >> 7) * D + static_cast<int64_t>(h) * kD + (ch & 127);
+      uint16_t w3[kHist];
 #pragma unroll
-    for (int r = 0; r < kHist; ++r) cs[cg * kHist + r] = w3[r];
+      for (int r = 0; r < kHist; ++r) {
+        const int64_t pos = len + r;  // position in the window [old taps (3) | tokens (len)]
+        w3[r] = pos < kHist ? cs[cg * kHist + pos] : p.qkv[(r0 + pos - kHist) * p.qkv_stride + cg];
+      }
+#pragma unroll
+      for (int r = 0; r < kHist; ++r) cs[cg * kHist + r] = w3[r];
+    }
+  } else if (tid == 0) {
+    flag(p, KDA_DEVERR_TIMEOUT);  // a tensor-core step never completed; the slot is left as it was
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tbase));
 }
 
 std::mutex g_mutex;

@@ -100,7 +100,7 @@ def test_prefill_host_validation_codes(lib):
     assert call(_pargs(num_chunks=-1)) == -2
     L.kda_prefill_workspace_bytes.restype = ctypes.c_int64
     L.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
-    assert L.kda_prefill_workspace_bytes(10, 4) == 10 * 4 * 74240
+    assert L.kda_prefill_workspace_bytes(10, 4) == 10 * 4 * 70144
     assert L.kda_prefill_workspace_bytes(-1, 4) == -1
 
 
