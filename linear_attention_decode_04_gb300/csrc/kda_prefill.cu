@@ -26,14 +26,13 @@
 // exp(G_t - G_s) = exp(G_t - G_m) exp(G_m - G_s); when a factor could leave
 // the fp32 range the chunk takes them element by element instead.
 //
-// Tensor cores: every contraction with the state (W S0, Q_G S0, K_E^T Delta)
-// and between tokens (P, R, R Delta) is a warp-level m16n8k8 tf32 MMA, each
-// operand split into a tf32 high part and a tf32 remainder and three
-// products accumulated in fp32, which keeps close to fp32 accuracy.  The state
-// is held in registers for the whole sequence, transposed (value rows x key
-// columns) in the accumulator layout, which doubles as the A operand of the
-// next chunk's products (the k index of an m16n8k8 operand may be permuted as
-// long as both operands use the same permutation).
+// Tensor cores.  The contractions with the state (W S0, Q_G S0, K_E^T Delta)
+// and R Delta run in the scan kernel as tcgen05.mma (kind::tf32, M = 128),
+// with the state held in tensor memory for the whole sequence; P and R
+// (between the tokens of a chunk) run in the chunk kernel as warp-level
+// m16n8k8 tf32 MMAs.  Every operand is split into a tf32 high part and a
+// tf32 remainder and three products are accumulated in fp32, which keeps
+// close to fp32 accuracy.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
