@@ -641,11 +641,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
   auto fetch = [&](int64_t jj, int buf) {
     const float4* src = reinterpret_cast<const float4*>(p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kImg));
     float* dst = S.img[buf];
-    for (int e = tid; e < kImg / 4; e += kThreads) cp_async16(dst + image_piece_dst(e), src + e);
+    // piece e = tid + 256 k: k selects the region (W 0-3, Q_G 4-7, K_E^T 8-11, R 12, U and gamma after)
+#pragma unroll
+    for (int k = 0; k < (kImg / 4 + kThreads - 1) / kThreads; ++k) {
+      const int e = tid + kThreads * k;
+      if (k < kOffU / 4 / kThreads) {
+        cp_async16(dst + image_piece_dst(e), src + e);
+      } else if (e < kImg / 4) {
+        cp_async16(dst + 4 * e, src + e);
+      }
+    }
     cp_async_commit();
   };
   fetch(0, 0);
-  constexpr uint32_t kId32 = idesc_tf32(32), kId128 = idesc_tf32(128);
+  constexpr uint32_t kId32 = idesc_tf32(32), kId64 = idesc_tf32(64), kId128 = idesc_tf32(128);
+  static_assert(kOffQ == kOffW + kL * kD && kTO == kTD + kL, "W / Q_G and their accumulators must be adjacent");
   const uint32_t lo_addr = smem_u32(S.lo);
   bool ok = true;
 
@@ -680,17 +690,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     __syncthreads();
     tc_fence_after();
 
-    // ---- D_Delta = S^T W^T, D_O = S^T Q_G^T  (K = 128 keys, 16 steps of 8)
+    // ---- [D_Delta | D_O] = S^T [W; Q_G]^T  (N = 64: W's and Q_G's row groups are
+    // adjacent in shared memory, and so are the two accumulators; K = 128
+    // keys, 16 steps of 8 = 256 bytes, i.e. 16 in the descriptor's address field)
     if (tid == 0) {
+      const uint64_t bh = sdesc(img_addr + 4 * kOffW, 4096), bl = sdesc(lo_addr + 4 * kOffW, 4096);
 #pragma unroll 1
-      for (int ks = 0; ks < kD / 8; ++ks) {
-        const uint32_t acc = ks > 0;
-        const uint32_t ahi = tbase + kTSH + 8 * ks, alo = tbase + kTSL + 8 * ks;
-        mma_ts3(tbase + kTD, ahi, alo, sdesc(img_addr + 4 * kOffW + 256 * ks, 4096),
-                sdesc(lo_addr + 4 * kOffW + 256 * ks, 4096), kId32, acc);
-        mma_ts3(tbase + kTO, ahi, alo, sdesc(img_addr + 4 * kOffQ + 256 * ks, 4096),
-                sdesc(lo_addr + 4 * kOffQ + 256 * ks, 4096), kId32, acc);
-      }
+      for (int ks = 0; ks < kD / 8; ++ks)
+        mma_ts3(tbase + kTD, tbase + kTSH + 8 * ks, tbase + kTSL + 8 * ks, bh + 16 * ks, bl + 16 * ks, kId64,
+                ks > 0);
       mma_commit(smem_u32(&S.bar[0]));
     }
     // While those run (they read the split words, not the fp32 state):
@@ -744,13 +752,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
 
     // ---- D_O += Delta^T R^T;  S^T += Delta^T K_E   (K = 32 tokens, 4 steps of 8)
     if (tid == 0) {
+      const uint64_t rh = sdesc(img_addr + 4 * kOffR, 1024), rl = sdesc(lo_addr + 4 * kOffR, 1024);
+      const uint64_t kh = sdesc(img_addr + 4 * kOffK, 1024), kl = sdesc(lo_addr + 4 * kOffK, 1024);
 #pragma unroll 1
       for (int ks = 0; ks < kL / 8; ++ks) {
         const uint32_t ahi = tbase + kTDH + 8 * ks, alo = tbase + kTDL + 8 * ks;
-        mma_ts3(tbase + kTO, ahi, alo, sdesc(img_addr + 4 * kOffR + 256 * ks, 1024),
-                sdesc(lo_addr + 4 * kOffR + 256 * ks, 1024), kId32, 1);
-        mma_ts3(tbase + kTS, ahi, alo, sdesc(img_addr + 4 * kOffK + 256 * ks, 1024),
-                sdesc(lo_addr + 4 * kOffK + 256 * ks, 1024), kId128, 1);
+        mma_ts3(tbase + kTO, ahi, alo, rh + 16 * ks, rl + 16 * ks, kId32, 1);
+        mma_ts3(tbase + kTS, ahi, alo, kh + 16 * ks, kl + 16 * ks, kId128, 1);
       }
       mma_commit(smem_u32(&S.bar[1]));
     }
@@ -784,24 +792,39 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     __syncthreads();
     tc_fence_after();
 
-    // ---- gated RMSNorm (or raw o) to bf16; warp w writes tokens 4w..4w+3
+    // ---- gated RMSNorm (or raw o) to bf16; warp w writes tokens 4w..4w+3,
+    // the four reductions interleaved
+    {
+      float4 y[4];
+      float ss[4];
 #pragma unroll
-    for (int tt = 0; tt < 4; ++tt) {
-      const int t = warp * 4 + tt;
-      if (t >= L) break;
-      float4 y = reinterpret_cast<const float4*>(S.o[t])[lane];
-      if (kOutNorm) {
-        const float4 nw4 = __ldg(reinterpret_cast<const float4*>(p.norm_w) + lane);
-        const float ss = warp_sum((y.x * y.x + y.y * y.y) + (y.z * y.z + y.w * y.w));
-        const float rr = 1.0f / sqrtf(ss * (1.0f / kD) + p.eps);
-        const uint2 gb = gate_pf[tt];
-        y.x = __fdividef(y.x * rr * nw4.x, 1.0f + __expf(-__uint_as_float(gb.x << 16)));
-        y.y = __fdividef(y.y * rr * nw4.y, 1.0f + __expf(-__uint_as_float(gb.x & 0xFFFF0000u)));
-        y.z = __fdividef(y.z * rr * nw4.z, 1.0f + __expf(-__uint_as_float(gb.y << 16)));
-        y.w = __fdividef(y.w * rr * nw4.w, 1.0f + __expf(-__uint_as_float(gb.y & 0xFFFF0000u)));
+      for (int tt = 0; tt < 4; ++tt) {
+        y[tt] = reinterpret_cast<const float4*>(S.o[warp * 4 + tt])[lane];
+        ss[tt] = (y[tt].x * y[tt].x + y[tt].y * y[tt].y) + (y[tt].z * y[tt].z + y[tt].w * y[tt].w);
       }
-      reinterpret_cast<uint2*>(p.out + (t0 + t) * p.out_stride + static_cast<int64_t>(h) * kD)[lane] =
-          make_uint2(pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+      if (kOutNorm) {
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+          for (int tt = 0; tt < 4; ++tt) ss[tt] += __shfl_xor_sync(0xffffffffu, ss[tt], m);
+        const float4 nw4 = __ldg(reinterpret_cast<const float4*>(p.norm_w) + lane);
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          const float rr = 1.0f / sqrtf(ss[tt] * (1.0f / kD) + p.eps);
+          const uint2 gb = gate_pf[tt];
+          y[tt].x = __fdividef(y[tt].x * rr * nw4.x, 1.0f + __expf(-__uint_as_float(gb.x << 16)));
+          y[tt].y = __fdividef(y[tt].y * rr * nw4.y, 1.0f + __expf(-__uint_as_float(gb.x & 0xFFFF0000u)));
+          y[tt].z = __fdividef(y[tt].z * rr * nw4.z, 1.0f + __expf(-__uint_as_float(gb.y << 16)));
+          y[tt].w = __fdividef(y[tt].w * rr * nw4.w, 1.0f + __expf(-__uint_as_float(gb.y & 0xFFFF0000u)));
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) {
+        const int t = warp * 4 + tt;
+        if (t < L)
+          reinterpret_cast<uint2*>(p.out + (t0 + t) * p.out_stride + static_cast<int64_t>(h) * kD)[lane] =
+              make_uint2(pack_bf16x2(y[tt].x, y[tt].y), pack_bf16x2(y[tt].z, y[tt].w));
+      }
     }
   }
   cp_async_wait_all();
