@@ -96,9 +96,9 @@ struct PrefillParams {
 __host__ __device__ constexpr int kmajor(int n, int k, int K) {
   return (n >> 3) * (K * 8) + (k >> 2) * 32 + (n & 7) * 4 + (k & 3);
 }
-constexpr int kOffW = 0;                      // W     [32 tokens][128 keys]
-constexpr int kOffQ = kOffW + kL * kD;        // Q_G   [32 tokens][128 keys]
-constexpr int kOffK = kOffQ + kL * kD;        // K_E^T [128 keys][32 tokens]
+constexpr int kOffQ = 0;                      // Q_G   [32 tokens][128 keys]
+constexpr int kOffW = kOffQ + kL * kD;        // W     [32 tokens][128 keys]
+constexpr int kOffK = kOffW + kL * kD;        // K_E^T [128 keys][32 tokens]
 constexpr int kOffR = kOffK + kD * kL;        // R     [32 tokens t][32 tokens s] (zeros above)
 constexpr int kOffU = kOffR + kL * kL;        // U     [32 tokens][128 values] (row-major in both)
 constexpr int kOffC = kOffU + kL * kD;        // gamma = exp(G_{L-1}) [128]
@@ -108,8 +108,8 @@ static_assert((kImg * 4) % 16 == 0, "image must be a whole number of 16-byte pie
 
 // Shared-memory position (floats) of the 16-byte piece e of an image.
 __device__ __forceinline__ int image_piece_dst(int e) {
-  if (e < kOffQ / 4) return kOffW + kmajor(e >> 5, 4 * (e & 31), kD);
-  if (e < kOffK / 4) { e -= kOffQ / 4; return kOffQ + kmajor(e >> 5, 4 * (e & 31), kD); }
+  if (e < kOffW / 4) return kOffQ + kmajor(e >> 5, 4 * (e & 31), kD);
+  if (e < kOffK / 4) { e -= kOffW / 4; return kOffW + kmajor(e >> 5, 4 * (e & 31), kD); }
   if (e < kOffR / 4) { e -= kOffK / 4; return kOffK + kmajor(e >> 3, 4 * (e & 7), kL); }
   if (e < kOffU / 4) { e -= kOffR / 4; return kOffR + kmajor(e >> 3, 4 * (e & 7), kL); }
   return 4 * e;  // U and gamma: as stored
@@ -145,10 +145,12 @@ struct __align__(16) ScanSmem {
 };
 
 // Tensor-memory columns of the scan kernel (512 allocated; lane = value row):
-// the fp32 state S^T, its tf32 high and low words (the A operand of the
-// products with the state), the chunk's S^T W^T and output accumulators, and
-// Delta^T's high and low words (the A operand of the products with Delta).
-constexpr uint32_t kTS = 0, kTSH = 128, kTSL = 256, kTD = 384, kTO = 416, kTDH = 448, kTDL = 480;
+// the fp32 state S^T, the chunk's output and S^T W^T accumulators, the
+// state's tf32 high and low words (the A operand of the products with the
+// state) and Delta^T's high and low words (the A operand of the products
+// with Delta).  [S^T | O] and [O | S^T W^T] are each contiguous, so each of
+// the two product batches is one MMA per step.
+constexpr uint32_t kTS = 0, kTO = 128, kTD = 160, kTSH = 192, kTSL = 320, kTDH = 448, kTDL = 480;
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -641,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
   auto fetch = [&](int64_t jj, int buf) {
     const float4* src = reinterpret_cast<const float4*>(p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kImg));
     float* dst = S.img[buf];
-    // piece e = tid + 256 k: k selects the region (W 0-3, Q_G 4-7, K_E^T 8-11, R 12, U and gamma after)
+    // piece e = tid + 256 k: k selects the region (Q_G 0-3, W 4-7, K_E^T 8-11, R 12, U and gamma after)
 #pragma unroll
     for (int k = 0; k < (kImg / 4 + kThreads - 1) / kThreads; ++k) {
       const int e = tid + kThreads * k;
@@ -654,8 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     cp_async_commit();
   };
   fetch(0, 0);
-  constexpr uint32_t kId32 = idesc_tf32(32), kId64 = idesc_tf32(64), kId128 = idesc_tf32(128);
-  static_assert(kOffQ == kOffW + kL * kD && kTO == kTD + kL, "W / Q_G and their accumulators must be adjacent");
+  constexpr uint32_t kId64 = idesc_tf32(64), kId160 = idesc_tf32(kD + kL);
+  static_assert(kOffW == kOffQ + kL * kD && kTD == kTO + kL, "Q_G / W and their accumulators must be adjacent");
+  static_assert(kOffR == kOffK + kD * kL && kTO == kTS + kD, "K_E^T / R and their accumulators must be adjacent");
   const uint32_t lo_addr = smem_u32(S.lo);
   bool ok = true;
 
@@ -690,14 +693,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     __syncthreads();
     tc_fence_after();
 
-    // ---- [D_Delta | D_O] = S^T [W; Q_G]^T  (N = 64: W's and Q_G's row groups are
-    // adjacent in shared memory, and so are the two accumulators; K = 128
+    // ---- [D_O | D_Delta] = S^T [Q_G; W]^T  (N = 64: Q_G's and W's row groups
+    // are adjacent in shared memory, and so are the two accumulators; K = 128
     // keys, 16 steps of 8 = 256 bytes, i.e. 16 in the descriptor's address field)
     if (tid == 0) {
-      const uint64_t bh = sdesc(img_addr + 4 * kOffW, 4096), bl = sdesc(lo_addr + 4 * kOffW, 4096);
+      const uint64_t bh = sdesc(img_addr + 4 * kOffQ, 4096), bl = sdesc(lo_addr + 4 * kOffQ, 4096);
 #pragma unroll 1
       for (int ks = 0; ks < kD / 8; ++ks)
-        mma_ts3(tbase + kTD, tbase + kTSH + 8 * ks, tbase + kTSL + 8 * ks, bh + 16 * ks, bl + 16 * ks, kId64,
+        mma_ts3(tbase + kTO, tbase + kTSH + 8 * ks, tbase + kTSL + 8 * ks, bh + 16 * ks, bl + 16 * ks, kId64,
                 ks > 0);
       mma_commit(smem_u32(&S.bar[0]));
     }
@@ -750,16 +753,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     __syncthreads();
     tc_fence_after();
 
-    // ---- D_O += Delta^T R^T;  S^T += Delta^T K_E   (K = 32 tokens, 4 steps of 8)
+    // ---- [S^T | D_O] += Delta^T [K_E^T; R]^T  (N = 160: K_E^T's and R's row
+    // groups are adjacent in shared memory, and so are S^T and the output
+    // accumulator; K = 32 tokens, 4 steps of 8)
     if (tid == 0) {
-      const uint64_t rh = sdesc(img_addr + 4 * kOffR, 1024), rl = sdesc(lo_addr + 4 * kOffR, 1024);
-      const uint64_t kh = sdesc(img_addr + 4 * kOffK, 1024), kl = sdesc(lo_addr + 4 * kOffK, 1024);
+      const uint64_t bh = sdesc(img_addr + 4 * kOffK, 1024), bl = sdesc(lo_addr + 4 * kOffK, 1024);
 #pragma unroll 1
-      for (int ks = 0; ks < kL / 8; ++ks) {
-        const uint32_t ahi = tbase + kTDH + 8 * ks, alo = tbase + kTDL + 8 * ks;
-        mma_ts3(tbase + kTO, ahi, alo, rh + 16 * ks, rl + 16 * ks, kId32, 1);
-        mma_ts3(tbase + kTS, ahi, alo, kh + 16 * ks, kl + 16 * ks, kId128, 1);
-      }
+      for (int ks = 0; ks < kL / 8; ++ks)
+        mma_ts3(tbase + kTS, tbase + kTDH + 8 * ks, tbase + kTDL + 8 * ks, bh + 16 * ks, bl + 16 * ks, kId160, 1);
       mma_commit(smem_u32(&S.bar[1]));
     }
     ok = bar_wait(smem_u32(&S.bar[1]), par);
