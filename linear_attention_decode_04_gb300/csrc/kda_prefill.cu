@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
     }
     float x0 = bf16f(S.raw[0][tid]), x1 = bf16f(S.raw[1][tid]), x2 = bf16f(S.raw[2][tid]);
     float* dst = tid < kD ? &S.q[0][tid] : &S.k[0][tid - kD];
-#pragma unroll 4
+#pragma unroll
     for (int t = 0; t < kL; ++t) {
       const float x3 = bf16f(S.raw[kHist + t][tid]);
       float y = ba;
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
     if (tid < kD) {
       const int cv = 2 * kD + tid;
       float z0 = bf16f(S.raw[0][cv]), z1 = bf16f(S.raw[1][cv]), z2 = bf16f(S.raw[2][cv]);
-#pragma unroll 4
+#pragma unroll
       for (int t = 0; t < kL; ++t) {
         const float z3 = bf16f(S.raw[kHist + t][cv]);
         float y = bv;
@@ -430,20 +430,21 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
 
   // ---- 6. triangular solve (thread = one column of [U | W]), left-looking:
   // x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or exp(G) k^ (W);
-  // the key-column threads also write their row of K_E^T = exp(G_{L-1} - G) k^
+  // the value-column threads also write row `tid` of K_E^T = exp(G_{L-1} - G) k^
+  // (the key-column threads spend as many exponentials on exp(G) k^)
   {
     const bool vcol = tid < kD;
     const int i = tid - kD;
-    if (!vcol) {
-      const float GL = S.G[kL - 1][i];
+    if (vcol) {
+      const float GL = S.G[kL - 1][tid];
 #pragma unroll 4
       for (int t = 0; t < kL; t += 4) {
         float4 ke;
-        ke.x = expf(GL - S.G[t][i]) * S.k[t][i];
-        ke.y = expf(GL - S.G[t + 1][i]) * S.k[t + 1][i];
-        ke.z = expf(GL - S.G[t + 2][i]) * S.k[t + 2][i];
-        ke.w = expf(GL - S.G[t + 3][i]) * S.k[t + 3][i];
-        reinterpret_cast<float4*>(ws + kOffK + i * kL)[t >> 2] = ke;
+        ke.x = expf(GL - S.G[t][tid]) * S.k[t][tid];
+        ke.y = expf(GL - S.G[t + 1][tid]) * S.k[t + 1][tid];
+        ke.z = expf(GL - S.G[t + 2][tid]) * S.k[t + 2][tid];
+        ke.w = expf(GL - S.G[t + 3][tid]) * S.k[t + 3][tid];
+        reinterpret_cast<float4*>(ws + kOffK + tid * kL)[t >> 2] = ke;
       }
     }
     float x[kL];
