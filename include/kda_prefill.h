@@ -73,8 +73,9 @@ extern "C" {
  *   conv_bias    fp32 [C] or NULL
  *   conv_state   bf16 [num_slots][C][3], oldest tap first (dim-first)
  *   state        fp32 [num_slots][H][128][128], S[key][value], value contiguous
- *   g            fp32 [T][H][128] log-decay, already activated (alpha = exp(g))
- *   beta         bf16 [T][H], already activated
+ *   g            fp32 [T][H][128] log-decay, already activated (alpha = exp(g)),
+ *                or raw logits with KDA_FUSED_GATE
+ *   beta         bf16 [T][H], already activated, or raw with KDA_FUSED_GATE
  *   gate         bf16 [T][gate_row_stride] (KDA_OUT_NORM only; stride >= D,
  *                a multiple of 4)
  *   norm_weight  fp32 [128] (KDA_OUT_NORM only)
@@ -121,13 +122,20 @@ typedef struct KdaPrefillArgs {
   int64_t out_row_stride;
   float eps;     /* RMSNorm epsilon */
   float q_scale; /* 0 => 1/sqrt(128) */
-  uint32_t flags; /* KDA_OUT_NORM or 0; other bits are rejected */
+  uint32_t flags; /* KDA_OUT_NORM and / or KDA_FUSED_GATE; other bits are rejected */
   int32_t* err_flag;
   const int32_t* chunk_indices;
   const int64_t* chunk_offsets;
   int64_t num_chunks;
   void* workspace;
   int64_t workspace_bytes;
+  /* KDA_FUSED_GATE only (as in KdaDecodeArgs): g and beta hold raw logits;
+   * A_log fp32 [H], dt_bias fp32 [H*128] or NULL, lower_bound < 0 selects the
+   * bounded gate.  P2's prefill kernel is this variant
+   * (chunk_kda_with_fused_gate, 实现拆解 item 3). */
+  const float* A_log;
+  const float* dt_bias;
+  float lower_bound;
 } KdaPrefillArgs;
 
 /* Workspace bytes a call with `num_chunks` chunks and H heads needs (about

@@ -76,6 +76,7 @@ class KdaPrefillArgs(ctypes.Structure):
         ("chunk_indices", ctypes.c_void_p), ("chunk_offsets", ctypes.c_void_p),
         ("num_chunks", ctypes.c_int64), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_int64),
+        ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("lower_bound", ctypes.c_float),
     ]
 
 
@@ -359,7 +360,8 @@ class KdaPrefillCall:
 
     def __init__(self, qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
                  cu_seqlens_cpu=None, gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
-                 q_scale: float = 0.0, out_norm: bool = True, err_flag=None):
+                 q_scale: float = 0.0, out_norm: bool = True, err_flag=None, A_log=None, dt_bias=None,
+                 lower_bound: float = 0.0):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -414,6 +416,20 @@ class KdaPrefillCall:
                 raise ValueError("conv_bias must be [3*H*128]")
         if err_flag is not None:
             _check(err_flag, "err_flag", torch.int32, dev)
+        flags = KDA_OUT_NORM if out_norm else 0
+        if A_log is not None:  # g and beta are raw logits
+            _check(A_log, "A_log", torch.float32, dev)
+            _dense(A_log, "A_log")
+            if A_log.numel() != H:
+                raise ValueError("A_log must be [H]")
+            if dt_bias is not None:
+                _check(dt_bias, "dt_bias", torch.float32, dev)
+                _dense(dt_bias, "dt_bias")
+                if dt_bias.numel() != D:
+                    raise ValueError("dt_bias must be [H*128]")
+            flags |= KDA_FUSED_GATE
+        elif dt_bias is not None:
+            raise ValueError("dt_bias needs A_log (the fused gate)")
         ws_bytes = int(self._lib.kda_prefill_workspace_bytes(num_chunks, H))
         self.num_chunks, self.B = num_chunks, B
         self.chunk_indices = torch.empty(max(num_chunks, 1), 2, dtype=torch.int32, device=dev)
@@ -421,7 +437,7 @@ class KdaPrefillCall:
         self.workspace = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
         self.device = dev
         self._keep = (qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, gate,
-                      norm_weight, conv_bias, err_flag)
+                      norm_weight, conv_bias, err_flag, A_log, dt_bias)
         self._cu, self._err = cu_seqlens, err_flag
         ptr = (lambda t: None if t is None else t.data_ptr())
         self.args = KdaPrefillArgs(
@@ -432,9 +448,10 @@ class KdaPrefillCall:
             gate=ptr(gate) if out_norm else None, gate_row_stride=gate_stride,
             norm_weight=ptr(norm_weight) if out_norm else None, slot_idx=ptr(slot_idx), out=ptr(out),
             out_row_stride=out_stride, eps=eps, q_scale=q_scale,
-            flags=KDA_OUT_NORM if out_norm else 0, err_flag=ptr(err_flag),
+            flags=flags, err_flag=ptr(err_flag),
             chunk_indices=ptr(self.chunk_indices), chunk_offsets=ptr(self.chunk_offsets),
-            num_chunks=num_chunks, workspace=ptr(self.workspace), workspace_bytes=ws_bytes)
+            num_chunks=num_chunks, workspace=ptr(self.workspace), workspace_bytes=ws_bytes,
+            A_log=ptr(A_log), dt_bias=ptr(dt_bias), lower_bound=lower_bound)
 
     def __call__(self, stream: torch.cuda.Stream | None = None) -> None:
         if stream is None:
@@ -455,13 +472,14 @@ class KdaPrefillCall:
 
 def kda_prefill(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
                 cu_seqlens_cpu=None, gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
-                q_scale: float = 0.0, out_norm: bool = True, err_flag=None,
-                stream: torch.cuda.Stream | None = None) -> None:
+                q_scale: float = 0.0, out_norm: bool = True, err_flag=None, A_log=None, dt_bias=None,
+                lower_bound: float = 0.0, stream: torch.cuda.Stream | None = None) -> None:
     """Chunked prefill of a varlen batch (see ``include/kda_prefill.h``):
     ``out``, ``state`` and ``conv_state`` are written in place.  Pass
     ``cu_seqlens_cpu`` (the host copy of ``cu_seqlens``) to keep the call free
-    of device reads."""
+    of device reads.  Passing ``A_log`` sets KDA_FUSED_GATE: ``g`` and
+    ``beta`` are then raw logits."""
     KdaPrefillCall(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out,
                    cu_seqlens_cpu=cu_seqlens_cpu, gate=gate, norm_weight=norm_weight,
                    conv_bias=conv_bias, eps=eps, q_scale=q_scale, out_norm=out_norm,
-                   err_flag=err_flag)(stream)
+                   err_flag=err_flag, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound)(stream)

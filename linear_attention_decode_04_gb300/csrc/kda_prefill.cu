@@ -81,6 +81,10 @@ struct PrefillParams {
   int B, H, num_slots;
   float eps, q_scale;
   int32_t* err;
+  int fused_gate;             // g and beta hold raw logits (activated on load)
+  const float* A_log;
+  const float* dt_bias;
+  float lower_bound;
 };
 
 // Workspace image of one (chunk, head), written by the chunk kernel with
@@ -277,10 +281,36 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   for (int e = tid; e < kL * 32; e += kThreads) {
     const int t = e >> 5, u = e & 31;
     float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < L) val = __ldg(reinterpret_cast<const float4*>(p.g + ((t0 + t) * p.H + h) * kD) + u);
+    if (t < L) {
+      val = __ldg(reinterpret_cast<const float4*>(p.g + ((t0 + t) * p.H + h) * kD) + u);
+      if (p.fused_gate) {
+        // the gate activation on the raw logits (the page's safe-gate variant;
+        // standard KDA form): z = raw + dt_bias, g = lb * sigmoid(e^A_log z)
+        // for a lower bound lb < 0, else g = -e^A_log softplus(z)
+        const float a = expf(__ldg(p.A_log + h));
+        float* vv = &val.x;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float z = vv[c] + (p.dt_bias ? __ldg(p.dt_bias + static_cast<int64_t>(h) * kD + 4 * u + c) : 0.0f);
+          if (p.lower_bound < 0.0f) {
+            vv[c] = p.lower_bound / (1.0f + expf(-a * z));
+          } else {
+            const float sp = (z > 0.0f) ? z + log1pf(expf(-z)) : log1pf(expf(z));
+            vv[c] = -a * sp;
+          }
+        }
+      }
+    }
     reinterpret_cast<float4*>(S.G[t])[u] = val;
   }
-  if (tid < kL) S.beta[tid] = tid < L ? bf16f(p.beta[(t0 + tid) * p.H + h]) : 0.0f;
+  if (tid < kL) {
+    float bt = 0.0f;
+    if (tid < L) {
+      bt = bf16f(p.beta[(t0 + tid) * p.H + h]);
+      if (p.fused_gate) bt = 1.0f / (1.0f + expf(-bt));
+    }
+    S.beta[tid] = bt;
+  }
   if (tid == 0) S.slow = 0;
   __syncthreads();
 
@@ -909,7 +939,8 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   if (a->B < 0 || a->H < 1 || a->H > 65535 || a->num_slots < 1 || a->T < 0 || a->num_chunks < 0)
     return kda_internal_fail(KDA_ERR_SHAPE, "B=%d H=%d num_slots=%d T=%lld num_chunks=%lld", a->B, a->H,
                              a->num_slots, static_cast<long long>(a->T), static_cast<long long>(a->num_chunks));
-  if (a->flags & ~KDA_OUT_NORM) return kda_internal_fail(KDA_ERR_FLAGS, "flags 0x%x (only KDA_OUT_NORM)", a->flags);
+  if (a->flags & ~(KDA_OUT_NORM | KDA_FUSED_GATE))
+    return kda_internal_fail(KDA_ERR_FLAGS, "flags 0x%x (KDA_OUT_NORM and KDA_FUSED_GATE only)", a->flags);
   if (static_cast<int64_t>(a->B) * a->H > 0x7fffffffLL || a->num_chunks > 0x7fffffffLL)
     return kda_internal_fail(KDA_ERR_SHAPE, "B*H or num_chunks too large");
   if (a->B == 0 || a->T == 0) return KDA_OK;
@@ -920,6 +951,10 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
     return kda_internal_fail(KDA_ERR_NULLPTR, "a required pointer is NULL");
   if (norm && (!a->gate || !a->norm_weight))
     return kda_internal_fail(KDA_ERR_NULLPTR, "KDA_OUT_NORM needs gate and norm_weight");
+  const bool fused = (a->flags & KDA_FUSED_GATE) != 0;
+  if (fused && !a->A_log) return kda_internal_fail(KDA_ERR_NULLPTR, "KDA_FUSED_GATE needs A_log");
+  if (fused && (!aligned(a->A_log, 4) || (a->dt_bias && !aligned(a->dt_bias, 4))))
+    return kda_internal_fail(KDA_ERR_ALIGN, "A_log / dt_bias must be 4-byte aligned");
   if (a->qkv_row_stride < 3 * D || a->out_row_stride < D || (norm && a->gate_row_stride < D))
     return kda_internal_fail(KDA_ERR_SHAPE, "a row stride is smaller than the row");
   if (a->workspace_bytes < kda_prefill_workspace_bytes(a->num_chunks, a->H))
@@ -963,6 +998,10 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   p.eps = a->eps;
   p.q_scale = a->q_scale;
   p.err = a->err_flag;
+  p.fused_gate = fused ? 1 : 0;
+  p.A_log = fused ? a->A_log : nullptr;
+  p.dt_bias = fused ? a->dt_bias : nullptr;
+  p.lower_bound = a->lower_bound;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a->num_chunks > 0)
     kda_prefill_chunk_kernel<<<dim3(static_cast<unsigned>(a->num_chunks), static_cast<unsigned>(a->H)), kThreads,

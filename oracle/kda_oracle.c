@@ -355,8 +355,18 @@ static int prefill_unit(const kda_oracle_prefill_problem* p, int b, int h, doubl
     kda_oracle_l2norm(qt, K, p->l2_eps, scale, qh);
     kda_oracle_l2norm(kt, K, p->l2_eps, 1.0, kh);
     /* 3. gated delta rule, state kept in fp64 */
-    for (int i = 0; i < K; ++i) alpha[i] = exp((double)p->g[((int64_t)r * H + h) * K + i]);
-    const double beta = kda_oracle_bf16_to_f64(p->beta[(int64_t)r * H + h]);
+    double beta = kda_oracle_bf16_to_f64(p->beta[(int64_t)r * H + h]);
+    if (p->fused_gate) {
+      const double a_log = (double)p->A_log[h];
+      for (int i = 0; i < K; ++i) {
+        double zz = (double)p->g[((int64_t)r * H + h) * K + i];
+        if (p->dt_bias) zz += (double)p->dt_bias[(int64_t)h * K + i];
+        alpha[i] = exp(kda_oracle_kda_gate(zz, a_log, p->lower_bound));
+      }
+      beta = kda_oracle_sigmoid(beta);
+    } else {
+      for (int i = 0; i < K; ++i) alpha[i] = exp((double)p->g[((int64_t)r * H + h) * K + i]);
+    }
     kda_oracle_gated_delta_update(K, V, S, alpha, beta, kh, vt);
     /* 4. readout, 5. gated RMSNorm or raw */
     kda_oracle_readout(K, V, S, qh, o);
@@ -394,6 +404,7 @@ int kda_oracle_prefill(const kda_oracle_prefill_problem* p, int num_threads) {
     if (p->cu_seqlens[b + 1] < p->cu_seqlens[b]) return -1;
   if (p->cu_seqlens[p->B] > 0 && (!p->qkv || !p->g || !p->beta || !p->out)) return -1;
   if (p->out_norm && p->cu_seqlens[p->B] > 0 && (!p->gate || !p->norm_weight)) return -1;
+  if (p->fused_gate && !p->A_log) return -1;
   const int64_t C = 2 * (int64_t)p->H * p->K + (int64_t)p->H * p->V;
   if (p->qkv_row_stride < C) return -1;
 

@@ -176,6 +176,10 @@ typedef struct {
   double* out_f64;            /* optional [T][H*V] */
   double eps, l2_eps, q_scale;
   int32_t out_norm;
+  int32_t fused_gate;         /* 1: g and beta hold raw logits (see "Fused gate") */
+  const float* A_log;         /* [H]; fused_gate only */
+  const float* dt_bias;       /* [H*K] or NULL; fused_gate only */
+  double lower_bound;         /* < 0: bounded gate; fused_gate only */
 } kda_oracle_prefill_problem;
 
 /* Runs the prefill of every sequence.  Returns the number of sequences whose

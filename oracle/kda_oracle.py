@@ -68,7 +68,8 @@ class _PrefillProblem(ctypes.Structure):
         ("norm_weight", ctypes.c_void_p), ("slot_idx", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("out_f64", ctypes.c_void_p),
         ("eps", ctypes.c_double), ("l2_eps", ctypes.c_double), ("q_scale", ctypes.c_double),
-        ("out_norm", ctypes.c_int32),
+        ("out_norm", ctypes.c_int32), ("fused_gate", ctypes.c_int32), ("A_log", ctypes.c_void_p),
+        ("dt_bias", ctypes.c_void_p), ("lower_bound", ctypes.c_double),
     ]
 
 
@@ -270,11 +271,13 @@ def prefill(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, cu_seqlen
             K: int = 128, V: int = 128, W: int = 4, gate=None, norm_weight=None,
             conv_bias=None, eps: float = 1e-6, l2_eps: float = 1e-6, q_scale: float = 0.0,
             out_norm: bool = True, threads: int = 0, want_f64: bool = True,
-            in_place: bool = False) -> OracleResult:
+            in_place: bool = False, fused_gate: bool = False, A_log=None, dt_bias=None,
+            lower_bound: float = 0.0) -> OracleResult:
     """Prefill of a varlen batch: every sequence's tokens run through the
     decode steps in order (window and state carried along, state never
     rounded in between); final state and conv window stored to the
-    sequence's slot.  ``slot_idx`` has one entry per sequence; ``qkv``, ``g``,
+    sequence's slot.  With ``fused_gate``, ``g`` and ``beta`` hold raw
+    logits activated with ``A_log``, ``dt_bias`` and ``lower_bound``.  ``slot_idx`` has one entry per sequence; ``qkv``, ``g``,
     ``beta``, ``gate`` one row per token.  Pools are copied unless
     ``in_place``."""
     qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
@@ -304,6 +307,14 @@ def prefill(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, cu_seqlen
         gate = norm_weight = None
     if conv_bias is not None:
         conv_bias = np.ascontiguousarray(conv_bias, dtype=np.float32)
+    if fused_gate:
+        A_log = np.ascontiguousarray(A_log, dtype=np.float32)
+        assert A_log.size == H
+        if dt_bias is not None:
+            dt_bias = np.ascontiguousarray(dt_bias, dtype=np.float32)
+            assert dt_bias.size == H * K
+    else:
+        A_log = dt_bias = None
     out = np.zeros((T, H * V), dtype=np.uint16)
     out64 = np.zeros((T, H * V), dtype=np.float64) if want_f64 else None
     p = _PrefillProblem(B=B, H=H, K=K, V=V, W=W, num_slots=num_slots, cu_seqlens=_ptr(cu),
@@ -312,7 +323,8 @@ def prefill(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, cu_seqlen
                         conv_state=_ptr(cs), state=_ptr(st), g=_ptr(g), beta=_ptr(beta),
                         gate=_ptr(gate), norm_weight=_ptr(norm_weight), slot_idx=_ptr(slot_idx),
                         out=_ptr(out), out_f64=_ptr(out64), eps=eps, l2_eps=l2_eps,
-                        q_scale=q_scale, out_norm=int(bool(out_norm)))
+                        q_scale=q_scale, out_norm=int(bool(out_norm)), fused_gate=int(bool(fused_gate)),
+                        A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), lower_bound=float(lower_bound))
     rc = lib().kda_oracle_prefill(ctypes.byref(p), int(threads))
     if rc < 0:
         raise ValueError("kda_oracle_prefill rejected its arguments")

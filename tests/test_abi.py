@@ -98,6 +98,8 @@ def test_prefill_host_validation_codes(lib):
     assert call(_pargs(workspace_bytes=1000)) == -2     # smaller than the chunks need
     assert b"workspace" in L.kda_last_error()
     assert call(_pargs(num_chunks=-1)) == -2
+    assert call(_pargs(flags=1 | 8)) == -1              # fused gate needs A_log
+    assert call(_pargs(flags=1 | 8, A_log=0x20002)) == -3
     L.kda_prefill_workspace_bytes.restype = ctypes.c_int64
     L.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
     assert L.kda_prefill_workspace_bytes(10, 4) == 10 * 4 * 70144

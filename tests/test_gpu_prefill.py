@@ -265,3 +265,30 @@ def test_prefill_continues_across_calls_strided_qkv_q_scale(cuda_device):
     s_got = st.cpu().numpy()
     for s in {int(v) for v in x.slot_idx}:
         T.check_state_slot(s_got[s], ref.state[s], f"slot {s}")
+
+
+@pytest.mark.parametrize("lower_bound,with_dt", [(-5.0, True), (0.0, True), (0.0, False)])
+def test_prefill_fused_gate(cuda_device, lower_bound, with_dt):
+    # KDA_FUSED_GATE: g and beta arrive as raw logits and the chunk kernel
+    # activates them (the page's prefill kernel is the fused-gate variant)
+    spec = W.PrefillSpec("prefill_gate_b3_h4", lens=(40, 1, 97), H=4, num_slots=6, seed=71, pad_seqs=())
+    x = W.make_prefill_inputs(spec)
+    rng = np.random.default_rng(72)
+    x.g = rng.standard_normal(x.g.shape).astype(np.float32)
+    x.beta = W.f32_to_bf16_bits(rng.standard_normal(x.beta.shape).astype(np.float32))
+    A_log = (0.5 * rng.standard_normal(spec.H)).astype(np.float32)
+    dt_bias = (0.5 * rng.standard_normal(spec.H * 128)).astype(np.float32) if with_dt else None
+    d = to_device(x, cuda_device)
+    kda_prefill(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"], d["cu_seqlens"],
+                d["slot_idx"], d["out"], cu_seqlens_cpu=d["cu_seqlens_cpu"], gate=d["gate"],
+                norm_weight=d["norm_weight"], conv_bias=d["conv_bias"], eps=spec.eps, err_flag=d["err_flag"],
+                A_log=torch.from_numpy(A_log).to(cuda_device),
+                dt_bias=None if dt_bias is None else torch.from_numpy(dt_bias).to(cuda_device),
+                lower_bound=lower_bound)
+    torch.cuda.synchronize(cuda_device)
+    assert int(d["err_flag"].item()) == 0
+    ref = oracle.prefill(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state, g=x.g,
+                         beta=x.beta, gate=x.gate, norm_weight=x.norm_weight, conv_bias=x.conv_bias,
+                         slot_idx=x.slot_idx, cu_seqlens=x.cu_seqlens, H=spec.H, eps=spec.eps, fused_gate=True,
+                         A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound)
+    compare(x, d, ref)

@@ -60,6 +60,9 @@ MUTANTS = {
         "if (s < 1 || s >= p->num_slots) { /* padding or out of range */",
         "if (s < 0 || s >= p->num_slots) { /* padding or out of range */"),
     "prefill_q_scale_from_value_dim": ("pow((double)K, -0.5);", "pow((double)V, -0.5);"),
+    "prefill_gate_drops_dt_bias": (
+        "        if (p->dt_bias) zz += (double)p->dt_bias[(int64_t)h * K + i];", "        (void)zz;"),
+    "prefill_gate_beta_not_activated": ("      beta = kda_oracle_sigmoid(beta);\n    } else {", "    } else {"),
     "prefill_decay_of_previous_token": (
         "alpha[i] = exp((double)p->g[((int64_t)r * H + h) * K + i]);",
         "alpha[i] = exp((double)p->g[((int64_t)(r > r0 ? r - 1 : r) * H + h) * K + i]);"),

@@ -52,9 +52,11 @@ def run(p, **kw):
     return oracle.prefill(**a)
 
 
-def brute_force(p, q_scale=None, l2_eps=1e-6, eps=1e-6):
+def brute_force(p, q_scale=None, l2_eps=1e-6, eps=1e-6, gate=None):
     """Dense-matrix evaluation: conv by torch conv1d over [conv state | tokens]
-    per channel, S <- (I - b k k^T) Diag(a) S + b k v^T as explicit matrices."""
+    per channel, S <- (I - b k k^T) Diag(a) S + b k v^T as explicit matrices.
+    ``gate`` = (A_log, dt_bias or None, lower_bound): g and beta are raw
+    logits, activated here with numpy (log1p / exp)."""
     H, K, V, W = p["H"], p["K"], p["V"], p["W"]
     Dq, Dv = H * K, H * V
     C = 2 * Dq + Dv
@@ -88,6 +90,18 @@ def brute_force(p, q_scale=None, l2_eps=1e-6, eps=1e-6):
                 kh = k / np.sqrt(k @ k + l2_eps)
                 al = np.exp(p["g"][r, h].astype(np.float64))
                 be = widen(p["beta"][r, h])
+                if gate is not None:
+                    A_log, dt_bias, lb = gate
+                    z = p["g"][r, h].astype(np.float64)
+                    if dt_bias is not None:
+                        z = z + dt_bias[h * K:(h + 1) * K].astype(np.float64)
+                    ea = np.exp(np.float64(A_log[h]))
+                    if lb < 0:
+                        gg = lb / (1.0 + np.exp(-ea * z))
+                    else:
+                        gg = -ea * (np.maximum(z, 0) + np.log1p(np.exp(-np.abs(z))))
+                    al = np.exp(gg)
+                    be = 1.0 / (1.0 + np.exp(-be))
                 S = (np.eye(K) - be * np.outer(kh, kh)) @ np.diag(al) @ S + be * np.outer(kh, v)
                 o = S.T @ qh
                 if p["out_norm"]:
@@ -210,3 +224,20 @@ def test_prefill_length_one_is_decode():
     assert np.array_equal(r.out, d.out)
     assert np.array_equal(r.state, d.state)
     assert np.array_equal(r.conv_state, d.conv_state)
+
+
+def test_prefill_fused_gate_matches_brute_force():
+    # raw g / beta logits activated inside the prefill (both gate forms, with
+    # and without dt_bias) against the brute force's own numpy activation
+    for seed, lb, with_dt in ((21, -5.0, True), (22, 0.0, True), (23, 0.0, False)):
+        p = tiny_prefill(seed=seed, lens=(6, 3))
+        rng = np.random.default_rng(seed + 100)
+        p["g"] = rng.standard_normal(p["g"].shape).astype(np.float32)
+        p["beta"] = bf16_bits(rng.standard_normal(p["beta"].shape))
+        A_log = (0.5 * rng.standard_normal(p["H"])).astype(np.float32)
+        dt_bias = (0.5 * rng.standard_normal(p["H"] * p["K"])).astype(np.float32) if with_dt else None
+        r = run(p, fused_gate=True, A_log=A_log, dt_bias=dt_bias, lower_bound=lb)
+        want_out, want_state, want_cs = brute_force(p, gate=(A_log, dt_bias, lb))
+        np.testing.assert_allclose(r.out_f64, want_out, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(r.state, want_state, rtol=1e-6, atol=1e-7)
+        assert np.array_equal(r.conv_state, want_cs)
