@@ -71,7 +71,8 @@ extern "C" {
  *                head-major); row stride >= C, a multiple of 8 elements
  *   conv_weight  fp32 [3][4][D] (block, tap oldest..current, channel)
  *   conv_bias    fp32 [C] or NULL
- *   conv_state   bf16 [num_slots][C][3], oldest tap first (dim-first)
+ *   conv_state   bf16 [num_slots][C][3], oldest tap first (dim-first), or
+ *                [num_slots][3][C] with KDA_CONV_STATE_SD (tap-first)
  *   state        fp32 [num_slots][H][128][128], S[key][value], value contiguous
  *   g            fp32 [T][H][128] log-decay, already activated (alpha = exp(g)),
  *                or raw logits with KDA_FUSED_GATE
@@ -122,7 +123,7 @@ typedef struct KdaPrefillArgs {
   int64_t out_row_stride;
   float eps;     /* RMSNorm epsilon */
   float q_scale; /* 0 => 1/sqrt(128) */
-  uint32_t flags; /* KDA_OUT_NORM and / or KDA_FUSED_GATE; other bits are rejected */
+  uint32_t flags; /* KDA_OUT_NORM, KDA_FUSED_GATE, KDA_CONV_STATE_SD; other bits are rejected */
   int32_t* err_flag;
   const int32_t* chunk_indices;
   const int64_t* chunk_offsets;

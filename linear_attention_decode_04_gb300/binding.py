@@ -361,7 +361,7 @@ class KdaPrefillCall:
     def __init__(self, qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
                  cu_seqlens_cpu=None, gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, err_flag=None, A_log=None, dt_bias=None,
-                 lower_bound: float = 0.0):
+                 lower_bound: float = 0.0, conv_state_layout: str = "DS"):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -417,6 +417,10 @@ class KdaPrefillCall:
         if err_flag is not None:
             _check(err_flag, "err_flag", torch.int32, dev)
         flags = KDA_OUT_NORM if out_norm else 0
+        if conv_state_layout not in ("DS", "SD"):
+            raise ValueError('conv_state_layout must be "DS" or "SD"')
+        if conv_state_layout == "SD":
+            flags |= KDA_CONV_STATE_SD
         if A_log is not None:  # g and beta are raw logits
             _check(A_log, "A_log", torch.float32, dev)
             _dense(A_log, "A_log")
@@ -473,7 +477,8 @@ class KdaPrefillCall:
 def kda_prefill(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
                 cu_seqlens_cpu=None, gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                 q_scale: float = 0.0, out_norm: bool = True, err_flag=None, A_log=None, dt_bias=None,
-                lower_bound: float = 0.0, stream: torch.cuda.Stream | None = None) -> None:
+                lower_bound: float = 0.0, conv_state_layout: str = "DS",
+                stream: torch.cuda.Stream | None = None) -> None:
     """Chunked prefill of a varlen batch (see ``include/kda_prefill.h``):
     ``out``, ``state`` and ``conv_state`` are written in place.  Pass
     ``cu_seqlens_cpu`` (the host copy of ``cu_seqlens``) to keep the call free
@@ -482,4 +487,5 @@ def kda_prefill(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_i
     KdaPrefillCall(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out,
                    cu_seqlens_cpu=cu_seqlens_cpu, gate=gate, norm_weight=norm_weight,
                    conv_bias=conv_bias, eps=eps, q_scale=q_scale, out_norm=out_norm,
-                   err_flag=err_flag, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound)(stream)
+                   err_flag=err_flag, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound,
+                   conv_state_layout=conv_state_layout)(stream)

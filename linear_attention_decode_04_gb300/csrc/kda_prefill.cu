@@ -81,6 +81,7 @@ struct PrefillParams {
   int B, H, num_slots;
   float eps, q_scale;
   int32_t* err;
+  int conv_sd;                // conv state stored tap-first [slots][3][C]
   int fused_gate;             // g and beta hold raw logits (activated on load)
   const float* A_log;
   const float* dt_bias;
@@ -119,7 +120,7 @@ __device__ __forceinline__ int image_piece_dst(int e) {
   return 4 * e;  // U and gamma: as stored
 }
 
-// Chunk kernel shared memory (about 106 KB: two CTAs per SM).
+// Chunk kernel shared memory (about 107 KB: two CTAs per SM).
 struct __align__(16) ChunkSmem {
   union {
     uint16_t raw[kHist + kL][kCh];  // conv window: 3 older rows, then the chunk's inputs
@@ -259,10 +260,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   // else the sequence's preceding tokens), the chunk's rows (zero past L),
   // g, beta
   if (j == 0) {
+    // tap r of channel c at c * 3 + r (dim-first) or r * C + c (tap-first)
     const uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
+    const int64_t sc = p.conv_sd ? 1 : kHist, sr = p.conv_sd ? 3 * D : 1;
     for (int ch = tid; ch < kCh; ch += kThreads)
 #pragma unroll
-      for (int r = 0; r < kHist; ++r) S.raw[r][ch] = cs[ch_global(ch) * kHist + r];
+      for (int r = 0; r < kHist; ++r) S.raw[r][ch] = cs[ch_global(ch) * sc + r * sr];
   } else {
     for (int e = tid; e < kHist * 48; e += kThreads) {
       const int r = e / 48, q = e - r * 48, seg = q >> 4, u = q & 15;
@@ -873,6 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
       for (int e = 0; e < 16; ++e) Sg[static_cast<int64_t>(64 * half + cc + e) * kD + j] = __uint_as_float(r[e]);
     }
     uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
+    const int64_t sc = p.conv_sd ? 1 : kHist, sr = p.conv_sd ? 3 * D : 1;  // dim-first or tap-first
     const int64_t len = r1 - r0;
     for (int ch = tid; ch < kCh; ch += kThreads) {
       const int64_t cg = static_cast<int64_t>(ch >> 7) * D + static_cast<int64_t>(h) * kD + (ch & 127);
@@ -880,10 +884,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
 #pragma unroll
       for (int r = 0; r < kHist; ++r) {
         const int64_t pos = len + r;  // position in the window [old taps (3) | tokens (len)]
-        w3[r] = pos < kHist ? cs[cg * kHist + pos] : p.qkv[(r0 + pos - kHist) * p.qkv_stride + cg];
+        w3[r] = pos < kHist ? cs[cg * sc + pos * sr] : p.qkv[(r0 + pos - kHist) * p.qkv_stride + cg];
       }
 #pragma unroll
-      for (int r = 0; r < kHist; ++r) cs[cg * kHist + r] = w3[r];
+      for (int r = 0; r < kHist; ++r) cs[cg * sc + r * sr] = w3[r];
     }
   } else if (tid == 0) {
     flag(p, KDA_DEVERR_TIMEOUT);  // a tensor-core step never completed; the slot is left as it was
@@ -939,8 +943,9 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   if (a->B < 0 || a->H < 1 || a->H > 65535 || a->num_slots < 1 || a->T < 0 || a->num_chunks < 0)
     return kda_internal_fail(KDA_ERR_SHAPE, "B=%d H=%d num_slots=%d T=%lld num_chunks=%lld", a->B, a->H,
                              a->num_slots, static_cast<long long>(a->T), static_cast<long long>(a->num_chunks));
-  if (a->flags & ~(KDA_OUT_NORM | KDA_FUSED_GATE))
-    return kda_internal_fail(KDA_ERR_FLAGS, "flags 0x%x (KDA_OUT_NORM and KDA_FUSED_GATE only)", a->flags);
+  if (a->flags & ~(KDA_OUT_NORM | KDA_FUSED_GATE | KDA_CONV_STATE_SD))
+    return kda_internal_fail(KDA_ERR_FLAGS, "flags 0x%x (KDA_OUT_NORM, KDA_FUSED_GATE, KDA_CONV_STATE_SD only)",
+                             a->flags);
   if (static_cast<int64_t>(a->B) * a->H > 0x7fffffffLL || a->num_chunks > 0x7fffffffLL)
     return kda_internal_fail(KDA_ERR_SHAPE, "B*H or num_chunks too large");
   if (a->B == 0 || a->T == 0) return KDA_OK;
@@ -998,6 +1003,7 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   p.eps = a->eps;
   p.q_scale = a->q_scale;
   p.err = a->err_flag;
+  p.conv_sd = (a->flags & KDA_CONV_STATE_SD) ? 1 : 0;
   p.fused_gate = fused ? 1 : 0;
   p.A_log = fused ? a->A_log : nullptr;
   p.dt_bias = fused ? a->dt_bias : nullptr;

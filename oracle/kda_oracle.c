@@ -321,11 +321,14 @@ static int prefill_unit(const kda_oracle_prefill_problem* p, int b, int h, doubl
   const float* wbase[3] = {p->conv_weight, p->conv_weight + (int64_t)W * Dq, p->conv_weight + 2 * (int64_t)W * Dq};
   uint16_t* cs0 = p->conv_state + (int64_t)s * C * (W - 1);
 
+  /* element (ch, t) of the slot's conv state in either layout */
+  const int64_t cs_ch = p->conv_state_sd ? 1 : (W - 1);
+  const int64_t cs_t = p->conv_state_sd ? C : 1;
   /* window <- the slot's conv state */
   for (int c = 0, m = 0; c < 3; ++c)
     for (int j = 0; j < dims[c]; ++j, ++m) {
       const int64_t ch = offs[c] + (int64_t)h * dims[c] + j;
-      for (int t = 0; t < W - 1; ++t) win[(size_t)m * (W - 1) + t] = cs0[ch * (W - 1) + t];
+      for (int t = 0; t < W - 1; ++t) win[(size_t)m * (W - 1) + t] = cs0[ch * cs_ch + t * cs_t];
     }
 
   float* Sg = p->state + (((int64_t)s * H + h) * K) * V;
@@ -390,7 +393,7 @@ static int prefill_unit(const kda_oracle_prefill_problem* p, int b, int h, doubl
   for (int c = 0, m = 0; c < 3; ++c)
     for (int j = 0; j < dims[c]; ++j, ++m) {
       const int64_t ch = offs[c] + (int64_t)h * dims[c] + j;
-      for (int t = 0; t < W - 1; ++t) cs0[ch * (W - 1) + t] = win[(size_t)m * (W - 1) + t];
+      for (int t = 0; t < W - 1; ++t) cs0[ch * cs_ch + t * cs_t] = win[(size_t)m * (W - 1) + t];
     }
   return 0;
 }

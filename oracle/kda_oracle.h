@@ -165,7 +165,7 @@ typedef struct {
   int64_t qkv_row_stride;
   const float* conv_weight;   /* as kda_oracle_problem */
   const float* conv_bias;     /* [C] or NULL */
-  uint16_t* conv_state;       /* [num_slots][C][W-1] (DS) */
+  uint16_t* conv_state;       /* [num_slots][C][W-1] (DS), or [num_slots][W-1][C] if conv_state_sd */
   float* state;               /* [num_slots][H][K][V] */
   const float* g;             /* [T][H][K] */
   const uint16_t* beta;       /* [T][H] */
@@ -180,6 +180,7 @@ typedef struct {
   const float* A_log;         /* [H]; fused_gate only */
   const float* dt_bias;       /* [H*K] or NULL; fused_gate only */
   double lower_bound;         /* < 0: bounded gate; fused_gate only */
+  int32_t conv_state_sd;      /* 1: conv_state is [num_slots][W-1][C] (tap-first) */
 } kda_oracle_prefill_problem;
 
 /* Runs the prefill of every sequence.  Returns the number of sequences whose

@@ -70,6 +70,7 @@ class _PrefillProblem(ctypes.Structure):
         ("eps", ctypes.c_double), ("l2_eps", ctypes.c_double), ("q_scale", ctypes.c_double),
         ("out_norm", ctypes.c_int32), ("fused_gate", ctypes.c_int32), ("A_log", ctypes.c_void_p),
         ("dt_bias", ctypes.c_void_p), ("lower_bound", ctypes.c_double),
+        ("conv_state_sd", ctypes.c_int32),
     ]
 
 
@@ -272,12 +273,13 @@ def prefill(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, cu_seqlen
             conv_bias=None, eps: float = 1e-6, l2_eps: float = 1e-6, q_scale: float = 0.0,
             out_norm: bool = True, threads: int = 0, want_f64: bool = True,
             in_place: bool = False, fused_gate: bool = False, A_log=None, dt_bias=None,
-            lower_bound: float = 0.0) -> OracleResult:
+            lower_bound: float = 0.0, conv_state_sd: bool = False) -> OracleResult:
     """Prefill of a varlen batch: every sequence's tokens run through the
     decode steps in order (window and state carried along, state never
     rounded in between); final state and conv window stored to the
     sequence's slot.  With ``fused_gate``, ``g`` and ``beta`` hold raw
-    logits activated with ``A_log``, ``dt_bias`` and ``lower_bound``.  ``slot_idx`` has one entry per sequence; ``qkv``, ``g``,
+    logits activated with ``A_log``, ``dt_bias`` and ``lower_bound``;
+    ``conv_state_sd``: the conv state is [slots, W-1, C] (tap-first).  ``slot_idx`` has one entry per sequence; ``qkv``, ``g``,
     ``beta``, ``gate`` one row per token.  Pools are copied unless
     ``in_place``."""
     qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
@@ -324,7 +326,8 @@ def prefill(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, cu_seqlen
                         gate=_ptr(gate), norm_weight=_ptr(norm_weight), slot_idx=_ptr(slot_idx),
                         out=_ptr(out), out_f64=_ptr(out64), eps=eps, l2_eps=l2_eps,
                         q_scale=q_scale, out_norm=int(bool(out_norm)), fused_gate=int(bool(fused_gate)),
-                        A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), lower_bound=float(lower_bound))
+                        A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), lower_bound=float(lower_bound),
+                        conv_state_sd=int(bool(conv_state_sd)))
     rc = lib().kda_oracle_prefill(ctypes.byref(p), int(threads))
     if rc < 0:
         raise ValueError("kda_oracle_prefill rejected its arguments")

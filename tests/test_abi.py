@@ -83,7 +83,8 @@ def test_prefill_host_validation_codes(lib):
     assert call(_pargs(head_dim=64)) == -2
     assert call(_pargs(B=-1)) == -2
     assert call(_pargs(T=-1)) == -2
-    assert call(_pargs(flags=2)) == -4                  # conv-state flag is not a prefill option
+    assert call(_pargs(flags=2)) == -4                  # the conv state is always advanced by prefill
+    assert call(_pargs(flags=32)) == -4
     assert call(_pargs(B=0)) == 0                       # no-op, no launch
     assert call(_pargs(T=0)) == 0
     assert call(_pargs(cu_seqlens=None)) == -1

@@ -292,3 +292,26 @@ def test_prefill_fused_gate(cuda_device, lower_bound, with_dt):
                          slot_idx=x.slot_idx, cu_seqlens=x.cu_seqlens, H=spec.H, eps=spec.eps, fused_gate=True,
                          A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound)
     compare(x, d, ref)
+
+
+def test_prefill_sd_conv_state_layout(cuda_device):
+    # KDA_CONV_STATE_SD: the conv pool stored tap-first [slots, 3, C]; the
+    # whole pool must match the oracle's SD-layout prefill bit for bit
+    x = W.make_prefill_inputs(W.PREFILL_SMALL)
+    x.conv_state = np.ascontiguousarray(x.conv_state.transpose(0, 2, 1))
+    d = to_device(x, cuda_device)
+    kda_prefill(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"], d["cu_seqlens"],
+                d["slot_idx"], d["out"], cu_seqlens_cpu=d["cu_seqlens_cpu"], gate=d["gate"],
+                norm_weight=d["norm_weight"], conv_bias=d["conv_bias"], eps=x.spec.eps, err_flag=d["err_flag"],
+                conv_state_layout="SD")
+    torch.cuda.synchronize(cuda_device)
+    assert int(d["err_flag"].item()) == 0
+    ref = oracle.prefill(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state, g=x.g,
+                         beta=x.beta, gate=x.gate, norm_weight=x.norm_weight, conv_bias=x.conv_bias,
+                         slot_idx=x.slot_idx, cu_seqlens=x.cu_seqlens, H=x.spec.H, eps=x.spec.eps,
+                         conv_state_sd=True)
+    T.check_out(T.bf16_bits(d["out"]), ref)
+    assert np.array_equal(T.bf16_bits(d["conv_state"]), ref.conv_state)
+    st = d["state"].cpu().numpy()
+    for s in range(x.spec.num_slots):
+        T.check_state_slot(st[s], ref.state[s], f"slot {s}")

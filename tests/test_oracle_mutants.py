@@ -63,6 +63,9 @@ MUTANTS = {
     "prefill_gate_drops_dt_bias": (
         "        if (p->dt_bias) zz += (double)p->dt_bias[(int64_t)h * K + i];", "        (void)zz;"),
     "prefill_gate_beta_not_activated": ("      beta = kda_oracle_sigmoid(beta);\n    } else {", "    } else {"),
+    "prefill_sd_taps_newest_first": (
+        "  const int64_t cs_t = p->conv_state_sd ? C : 1;\n  /* window",
+        "  const int64_t cs_t = p->conv_state_sd ? -C : 1;\n  cs0 += p->conv_state_sd ? (W - 2) * C : 0;\n  /* window"),
     "prefill_decay_of_previous_token": (
         "alpha[i] = exp((double)p->g[((int64_t)r * H + h) * K + i]);",
         "alpha[i] = exp((double)p->g[((int64_t)(r > r0 ? r - 1 : r) * H + h) * K + i]);"),

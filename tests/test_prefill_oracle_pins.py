@@ -241,3 +241,15 @@ def test_prefill_fused_gate_matches_brute_force():
         np.testing.assert_allclose(r.out_f64, want_out, rtol=1e-10, atol=1e-12)
         np.testing.assert_allclose(r.state, want_state, rtol=1e-6, atol=1e-7)
         assert np.array_equal(r.conv_state, want_cs)
+
+
+def test_prefill_sd_conv_state_is_the_transposed_ds_result():
+    # the tap-first layout holds the same values: running on the transposed
+    # pool gives the transposed final pool and the same outputs and state
+    p = tiny_prefill(seed=31, lens=(5, 1, 2, 0))
+    ds = run(p)
+    sd_in = np.ascontiguousarray(p["conv_state"].transpose(0, 2, 1))
+    sd = run(p, conv_state=sd_in, conv_state_sd=True)
+    assert np.array_equal(sd.conv_state, ds.conv_state.transpose(0, 2, 1))
+    assert np.array_equal(sd.out, ds.out)
+    assert np.array_equal(sd.state, ds.state)
