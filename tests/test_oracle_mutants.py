@@ -51,7 +51,7 @@ MUTANTS = {
         "    /* 1. conv + SiLU with the window, then slide the window */",
         "    for (int64_t e = 0; e < (int64_t)K * V; ++e) S[e] = (double)Sg[e];"),
     "prefill_final_window_not_stored": (
-        "      for (int t = 0; t < W - 1; ++t) cs0[ch * (W - 1) + t] = win[(size_t)m * (W - 1) + t];",
+        "      for (int t = 0; t < W - 1; ++t) cs0[ch * cs_ch + t * cs_t] = win[(size_t)m * (W - 1) + t];",
         "      (void)0;"),
     "prefill_beta_of_first_token": (
         "kda_oracle_bf16_to_f64(p->beta[(int64_t)r * H + h]);",
