@@ -88,37 +88,26 @@ struct PrefillParams {
   float lower_bound;
 };
 
-// Workspace image of one (chunk, head), written by the chunk kernel with
-// plain row-major rows (coalesced stores) and copied by the scan kernel into
-// shared memory, where the operands its tensor-core products read (W, Q_G,
-// K_E^T, R) take the canonical K-major layout without swizzle: an N x K fp32
-// matrix is tiled into core matrices of 8 rows x 16 bytes (4 values), element
-// (n, k) at (n / 8) * SBO + (k / 4) * LBO + (n % 8) * 4 + k % 4 floats, with
-// the core matrices adjacent in K 128 bytes apart (LBO = 32 floats) and the
-// 8-row groups K / 4 core matrices apart (SBO = K * 8 floats).  A 16-byte
-// piece of a row (4 consecutive k) is one core-matrix row, so the copy
-// places each piece on its own.
-__host__ __device__ constexpr int kmajor(int n, int k, int K) {
-  return (n >> 3) * (K * 8) + (k >> 2) * 32 + (n & 7) * 4 + (k & 3);
-}
-constexpr int kOffQ = 0;                      // Q_G   [32 tokens][128 keys]
-constexpr int kOffW = kOffQ + kL * kD;        // W     [32 tokens][128 keys]
-constexpr int kOffK = kOffW + kL * kD;        // K_E^T [128 keys][32 tokens]
-constexpr int kOffR = kOffK + kD * kL;        // R     [32 tokens t][32 tokens s] (zeros above)
-constexpr int kOffU = kOffR + kL * kL;        // U     [32 tokens][128 values] (row-major in both)
+// Workspace image of one (chunk, head), written by the chunk kernel and
+// copied verbatim (one bulk copy) into the scan kernel's shared memory.  The
+// operands of the scan's tensor-core products are stored in the canonical
+// K-major layout without swizzle, in the variant whose 8-row groups are
+// adjacent: an N x K fp32 operand is tiled into core matrices of 8 rows x 16
+// bytes (4 values of k), element (n, k) at (k / 4) * N * 4 + n * 4 + k % 4
+// floats; the 8-row groups are 128 bytes apart (SBO) and the core matrices
+// adjacent in K are N * 16 bytes apart (LBO).  Each product's B operand is
+// one such block: [Q_G; W] (N = 64, K = 128 keys) and [K_E^T; R]
+// (N = 160, K = 32 tokens).
+__host__ __device__ constexpr int kpos(int n, int k, int N) { return (k >> 2) * (N * 4) + n * 4 + (k & 3); }
+constexpr int kNB1 = 2 * kL;                  // [Q_G; W]: Q_G rows 0..31, W rows 32..63
+constexpr int kNB2 = kD + kL;                 // [K_E^T; R]: K_E^T rows 0..127, R rows 128..159
+constexpr int kOffB1 = 0;                     // [Q_G; W]   64 x 128
+constexpr int kOffB2 = kOffB1 + kNB1 * kD;    // [K_E^T; R] 160 x 32 (R zero above its diagonal)
+constexpr int kOffU = kOffB2 + kNB2 * kL;     // U     [32 tokens][128 values], row-major
 constexpr int kOffC = kOffU + kL * kD;        // gamma = exp(G_{L-1}) [128]
 constexpr int kImg = kOffC + kD;              // 17,536 floats = 70,144 bytes
-constexpr int kSplit = kOffU;                 // the operands the scan splits (W, Q_G, K_E^T, R)
+constexpr int kSplit = kOffU;                 // the operands the scan splits into tf32 words
 static_assert((kImg * 4) % 16 == 0, "image must be a whole number of 16-byte pieces");
-
-// Shared-memory position (floats) of the 16-byte piece e of an image.
-__device__ __forceinline__ int image_piece_dst(int e) {
-  if (e < kOffW / 4) return kOffQ + kmajor(e >> 5, 4 * (e & 31), kD);
-  if (e < kOffK / 4) { e -= kOffW / 4; return kOffW + kmajor(e >> 5, 4 * (e & 31), kD); }
-  if (e < kOffR / 4) { e -= kOffK / 4; return kOffK + kmajor(e >> 3, 4 * (e & 7), kL); }
-  if (e < kOffU / 4) { e -= kOffR / 4; return kOffR + kmajor(e >> 3, 4 * (e & 7), kL); }
-  return 4 * e;  // U and gamma: as stored
-}
 
 // Chunk kernel shared memory (about 107 KB: two CTAs per SM).
 struct __align__(16) ChunkSmem {
@@ -138,14 +127,16 @@ struct __align__(16) ChunkSmem {
   int slow;                         // this chunk takes the element-wise P / R path
 };
 
-// Scan kernel shared memory (about 210 KB): two images (double buffer), the
+// Scan kernel shared memory (about 206 KB): two images (double buffer), the
 // tf32 remainders of the image's tensor-core operands, the chunk's output,
-// the two MMA-completion barriers and the tensor-memory base address.
-struct __align__(16) ScanSmem {
+// the MMA-completion and copy-completion barriers and the tensor-memory base
+// address.
+struct __align__(128) ScanSmem {
   float img[2][kImg];
   float lo[kSplit];
   float o[kL][kSA];
-  unsigned long long bar[2];
+  unsigned long long bar[2];   // the two MMA batches of a chunk
+  unsigned long long full[2];  // image buffer 0 / 1 landed
   uint32_t tmem;
 };
 
@@ -217,13 +208,13 @@ __device__ __forceinline__ void flag(const PrefillParams& p, int bits) {
   if (p.err) atomicOr(p.err, bits);
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
-               "l"(gmem)
+// One bulk copy (TMA engine) global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // ===================================================================== chunk
 // One CTA per (chunk row c, head h), chunk row = (sequence b, chunk j) from
@@ -389,18 +380,30 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   // ---- 4. split decay factors around the reference token (shared memory);
   // Q_G = exp(G) q^ and gamma to the image; R's image cleared (its lower
   // triangle is written next); P cleared
-  for (int e = tid; e < kL * kD; e += kThreads) {
-    const int t = e >> 7, i = e & (kD - 1);
-    const float Gt = S.G[t][i];
-    const float d = Gt - S.G[kRef][i];
-    if (fabsf(d) > kMaxExponent) S.slow = 1;
-    const float kv = S.k[t][i];
-    S.f.ek[t][i] = __expf(d) * kv;
-    S.f.fk[t][i] = __expf(-d) * kv;
-    ws[kOffQ + t * kD + i] = __expf(Gt) * S.q[t][i];
+  // piece (t, keys 4 kg .. 4 kg + 3); consecutive threads take consecutive t,
+  // so the image stores of Q_G are coalesced 16-byte pieces
+  for (int e = tid; e < kL * kD / 4; e += kThreads) {
+    const int t = e & (kL - 1), i0 = 4 * (e >> 5);
+    const float4 G4 = *reinterpret_cast<const float4*>(&S.G[t][i0]);
+    const float4 Gm = *reinterpret_cast<const float4*>(&S.G[kRef][i0]);
+    const float4 k4 = *reinterpret_cast<const float4*>(&S.k[t][i0]);
+    const float4 q4 = *reinterpret_cast<const float4*>(&S.q[t][i0]);
+    const float d[4] = {G4.x - Gm.x, G4.y - Gm.y, G4.z - Gm.z, G4.w - Gm.w};
+    const float gt[4] = {G4.x, G4.y, G4.z, G4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+    float ek[4], fk[4], qg[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (fabsf(d[c]) > kMaxExponent) S.slow = 1;
+      ek[c] = __expf(d[c]) * kv[c];
+      fk[c] = __expf(-d[c]) * kv[c];
+      qg[c] = __expf(gt[c]) * qv[c];
+    }
+    *reinterpret_cast<float4*>(&S.f.ek[t][i0]) = make_float4(ek[0], ek[1], ek[2], ek[3]);
+    *reinterpret_cast<float4*>(&S.f.fk[t][i0]) = make_float4(fk[0], fk[1], fk[2], fk[3]);
+    *reinterpret_cast<float4*>(ws + kOffB1 + kpos(t, i0, kNB1)) = make_float4(qg[0], qg[1], qg[2], qg[3]);
   }
   if (tid < kD) ws[kOffC + tid] = expf(S.G[kL - 1][tid]);
-  for (int e = tid; e < kL * kL; e += kThreads) ws[kOffR + e] = 0.0f;
+  for (int e = tid; e < kL * kL; e += kThreads) ws[kOffB2 + kpos(kD + (e >> 5), e & (kL - 1), kNB2)] = 0.0f;
   for (int e = tid; e < kL * kSP; e += kThreads) (&S.P[0][0])[e] = 0.0f;
   __syncthreads();
 
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
         if (mat == 0) {
           if (te > se) S.P[te][se] = acc[e];
         } else {
-          if (te >= se) ws[kOffR + te * kL + se] = acc[e];
+          if (te >= se) ws[kOffB2 + kpos(kD + te, se, kNB2)] = acc[e];
         }
       }
     }
@@ -456,14 +459,15 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
         pq = fmaf(S.q[t][i], fct, pq);
       }
       if (t > s) S.P[t][s] = pk;
-      ws[kOffR + t * kL + s] = pq;
+      ws[kOffB2 + kpos(kD + t, s, kNB2)] = pq;
     }
   }
   __syncthreads();
 
   // ---- 6. triangular solve (thread = one column of [U | W]), left-looking:
-  // x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or exp(G) k^ (W);
-  // the value-column threads also write row `tid` of K_E^T = exp(G_{L-1} - G) k^
+  // x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or exp(G) k^ (W),
+  // W staged in the (now free) factor buffer; the value-column threads also
+  // write row `tid` of K_E^T = exp(G_{L-1} - G) k^
   // (the key-column threads spend as many exponentials on exp(G) k^)
   {
     const bool vcol = tid < kD;
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
         ke.y = expf(GL - S.G[t + 1][tid]) * S.k[t + 1][tid];
         ke.z = expf(GL - S.G[t + 2][tid]) * S.k[t + 2][tid];
         ke.w = expf(GL - S.G[t + 3][tid]) * S.k[t + 3][tid];
-        reinterpret_cast<float4*>(ws + kOffK + tid * kL)[t >> 2] = ke;
+        *reinterpret_cast<float4*>(ws + kOffB2 + kpos(tid, t, kNB2)) = ke;
       }
     }
     float x[kL];
@@ -496,17 +500,24 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
       }
       x[t] = S.beta[t] * ((a0 + a1) + (a2 + a3));
       if (vcol) ws[kOffU + t * kD + tid] = x[t];
-      else ws[kOffW + t * kD + i] = x[t];
+      else S.f.ek[t][i] = x[t];  // W, staged
     }
+  }
+  __syncthreads();
+  // W to the image as coalesced 16-byte pieces (t, keys 4 kg .. 4 kg + 3)
+  for (int e = tid; e < kL * kD / 4; e += kThreads) {
+    const int t = e & (kL - 1), i0 = 4 * (e >> 5);
+    *reinterpret_cast<float4*>(ws + kOffB1 + kpos(kL + t, i0, kNB1)) =
+        *reinterpret_cast<const float4*>(&S.f.ek[t][i0]);
   }
 }
 
 // ====================================================================== scan
 // tcgen05 helpers.  Shared-memory matrix descriptor of a canonical K-major
-// operand without swizzle: start address, LBO = 128 bytes (core matrices
-// adjacent in K), SBO (8-row groups), descriptor version 1.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t sbo_bytes) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>(128 >> 4) << 16) |
+// operand without swizzle: start address, LBO (core matrices adjacent in K),
+// SBO (8-row groups), descriptor version 1; all in 16-byte units.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFF) << 16) |
          (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFF) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 // Instruction descriptor, kind::tf32: f32 accumulator, tf32 A and B, both
@@ -644,6 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.bar[0])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.bar[1])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.full[0])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.full[1])));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -674,25 +687,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
   }
   tm_wait_st();
 
+  // chunk jj's image: one bulk copy into buffer `buf`, issued by thread 0
   auto fetch = [&](int64_t jj, int buf) {
-    const float4* src = reinterpret_cast<const float4*>(p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kImg));
-    float* dst = S.img[buf];
-    // piece e = tid + 256 k: k selects the region (Q_G 0-3, W 4-7, K_E^T 8-11, R 12, U and gamma after)
-#pragma unroll
-    for (int k = 0; k < (kImg / 4 + kThreads - 1) / kThreads; ++k) {
-      const int e = tid + kThreads * k;
-      if (k < kOffU / 4 / kThreads) {
-        cp_async16(dst + image_piece_dst(e), src + e);
-      } else if (e < kImg / 4) {
-        cp_async16(dst + 4 * e, src + e);
-      }
+    if (tid == 0) {
+      fence_proxy_async();  // earlier generic accesses to the buffer before the async-proxy write
+      bulk_load(smem_u32(S.img[buf]), p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kImg), kImg * 4,
+                smem_u32(&S.full[buf]));
     }
-    cp_async_commit();
   };
   fetch(0, 0);
-  constexpr uint32_t kId64 = idesc_tf32(64), kId160 = idesc_tf32(kD + kL);
-  static_assert(kOffW == kOffQ + kL * kD && kTD == kTO + kL, "Q_G / W and their accumulators must be adjacent");
-  static_assert(kOffR == kOffK + kD * kL && kTO == kTS + kD, "K_E^T / R and their accumulators must be adjacent");
+  int pending = 0;           // buffer whose copy is in flight (-1: none)
+  uint32_t pending_par = 0;  // and the phase its barrier completes
+  constexpr uint32_t kId64 = idesc_tf32(kNB1), kId160 = idesc_tf32(kNB2);
+  static_assert(kTD == kTO + kL, "the accumulators of [Q_G; W] must be adjacent");
+  static_assert(kTO == kTS + kD, "the accumulators of [K_E^T; R] must be adjacent");
   const uint32_t lo_addr = smem_u32(S.lo);
   bool ok = true;
 
@@ -701,9 +709,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     const int L = static_cast<int>(r1 - t0 < kL ? r1 - t0 : kL);
     const int buf = static_cast<int>(jj & 1);
     const uint32_t par = static_cast<uint32_t>(jj & 1);
-    cp_async_wait_all();
-    __syncthreads();                       // image jj landed; the other buffer and lo are free
-    if (jj + 1 < n_chunks) fetch(jj + 1, buf ^ 1);
+    ok = bar_wait(smem_u32(&S.full[buf]), static_cast<uint32_t>((jj >> 1) & 1));
+    if (__syncthreads_or(!ok)) break;      // image jj landed; the other buffer and lo are free
+    pending = -1;
+    if (jj + 1 < n_chunks) {
+      fetch(jj + 1, buf ^ 1);
+      pending = buf ^ 1;
+      pending_par = static_cast<uint32_t>(((jj + 1) >> 1) & 1);
+    }
     float* img = S.img[buf];
     const uint32_t img_addr = smem_u32(img);
 
@@ -727,14 +740,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     __syncthreads();
     tc_fence_after();
 
-    // ---- [D_O | D_Delta] = S^T [Q_G; W]^T  (N = 64: Q_G's and W's row groups
-    // are adjacent in shared memory, and so are the two accumulators; K = 128
-    // keys, 16 steps of 8 = 256 bytes, i.e. 16 in the descriptor's address field)
+    // ---- [D_O | D_Delta] = S^T [Q_G; W]^T  (N = 64, one B block; the two
+    // accumulators are adjacent; K = 128 keys, 16 steps of 8)
     if (tid == 0) {
-      const uint64_t bh = sdesc(img_addr + 4 * kOffQ, 4096), bl = sdesc(lo_addr + 4 * kOffQ, 4096);
+      // LBO = 64 rows x 16 B; one K step of 8 = two core-matrix columns = 2 LBO = 128 address units
+      const uint64_t bh = sdesc(img_addr + 4 * kOffB1, kNB1 * 16, 128), bl = sdesc(lo_addr + 4 * kOffB1, kNB1 * 16, 128);
 #pragma unroll 1
       for (int ks = 0; ks < kD / 8; ++ks)
-        mma_ts3(tbase + kTO, tbase + kTSH + 8 * ks, tbase + kTSL + 8 * ks, bh + 16 * ks, bl + 16 * ks, kId64,
+        mma_ts3(tbase + kTO, tbase + kTSH + 8 * ks, tbase + kTSL + 8 * ks, bh + 128 * ks, bl + 128 * ks, kId64,
                 ks > 0);
       mma_commit(smem_u32(&S.bar[0]));
     }
@@ -787,14 +800,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     __syncthreads();
     tc_fence_after();
 
-    // ---- [S^T | D_O] += Delta^T [K_E^T; R]^T  (N = 160: K_E^T's and R's row
-    // groups are adjacent in shared memory, and so are S^T and the output
-    // accumulator; K = 32 tokens, 4 steps of 8)
+    // ---- [S^T | D_O] += Delta^T [K_E^T; R]^T  (N = 160, one B block; S^T and
+    // the output accumulator are adjacent; K = 32 tokens, 4 steps of 8)
     if (tid == 0) {
-      const uint64_t bh = sdesc(img_addr + 4 * kOffK, 1024), bl = sdesc(lo_addr + 4 * kOffK, 1024);
+      // LBO = 160 rows x 16 B; one K step = 2 LBO = 320 address units
+      const uint64_t bh = sdesc(img_addr + 4 * kOffB2, kNB2 * 16, 128),
+                     bl = sdesc(lo_addr + 4 * kOffB2, kNB2 * 16, 128);
 #pragma unroll 1
       for (int ks = 0; ks < kL / 8; ++ks)
-        mma_ts3(tbase + kTS, tbase + kTDH + 8 * ks, tbase + kTDL + 8 * ks, bh + 16 * ks, bl + 16 * ks, kId160, 1);
+        mma_ts3(tbase + kTS, tbase + kTDH + 8 * ks, tbase + kTDL + 8 * ks, bh + 320 * ks, bl + 320 * ks, kId160, 1);
       mma_commit(smem_u32(&S.bar[1]));
     }
     ok = bar_wait(smem_u32(&S.bar[1]), par);
@@ -862,8 +876,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
       }
     }
   }
-  cp_async_wait_all();
-
+  if (!ok && pending >= 0) {
+    // leaving early: let the copy in flight land before the shared memory goes away
+    bar_wait(smem_u32(&S.full[pending]), pending_par);
+  }
   if (ok) {
     // ---- sequence end: state and conv window back to the slot.  The window
     // [old taps | tokens] ends with its last three inputs; for sequences of
