@@ -202,8 +202,6 @@ __device__ __forceinline__ void mma3(float (&c)[4], const FragA& a, float b0, fl
   mma_tf32(c, a.hi, h0, h1);
 }
 
-
-
 __device__ __forceinline__ void flag(const PrefillParams& p, int bits) {
   if (p.err) atomicOr(p.err, bits);
 }
@@ -610,10 +608,11 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
 // column = key) and every product with it runs on the 5th-generation tensor
 // cores (tcgen05.mma, kind::tf32, issued by one thread, accumulators in
 // tensor memory); chunk j's image (row chunk_offsets[b] + j of the
-// workspace) is copied into shared memory while chunk j - 1 computes.
-// Per chunk:  Delta^T = U^T - S^T W^T  and  O^T = S^T Q_G^T   (M = 128, N = 32, K = 128)
-//             O^T += Delta^T R^T                               (K = 32)
-//             S^T <- S^T Diag(gamma) + Delta^T K_E            (M = 128, N = 128, K = 32)
+// workspace) arrives with one bulk copy while chunk j - 1 computes.
+// Per chunk, two batches of products (M = 128 value rows):
+//   [O^T | S^T W^T] = S^T [Q_G; W]^T              N = 64,  K = 128 keys
+//   Delta^T = U^T - S^T W^T;  S^T <- S^T Diag(gamma)
+//   [S^T | O^T] += Delta^T [K_E^T; R]^T           N = 160, K = 32 tokens
 // Every operand is split into a tf32 high word and a tf32 remainder and three
 // products are accumulated (lo*hi + hi*lo + hi*hi) in fp32.
 template <bool kOutNorm>
