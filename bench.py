@@ -37,6 +37,8 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "kda_decode_stack69_traffic.md")
 KERNEL_SRC = os.path.join(ROOT, "linear_attention_decode_04_gb300", "csrc", "kda_decode_kernel.cuh")
+PREFILL_TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "kda_prefill_traffic.md")
+PREFILL_SRC = os.path.join(ROOT, "linear_attention_decode_04_gb300", "csrc", "kda_prefill.cu")
 
 
 # ----------------------------------------------------------------- host logic
@@ -69,21 +71,23 @@ def measured_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
+def kernel_source_hash(path: str | None = None) -> str:
+    with open(path or KERNEL_SRC, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic() -> float | None:
+def recorded_traffic(note: str | None = None, src: str | None = None) -> float | None:
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    on the current kernel source (else None).  Defaults: the decode note and
+    the decode kernel source."""
+    note, src = note or TRAFFIC_NOTE, src or KERNEL_SRC
     try:
-        text = open(TRAFFIC_NOTE).read()
+        text = open(note).read()
     except OSError:
         return None
     h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not h or not b or h.group(1) != kernel_source_hash():
+    if not h or not b or h.group(1) != kernel_source_hash(src):
         return None
     return float(b.group(1))
 
@@ -442,6 +446,8 @@ def run_prefill(args) -> dict:
            "value": act_tokens * spec.H / (ms / 1e3), "unit": "updates/s", "ms_per_launch": ms,
            "workload": spec.name, "tokens": spec.T, "sequences": spec.B, "H": spec.H,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                        "traffic": recorded_traffic(PREFILL_TRAFFIC_NOTE, PREFILL_SRC),
+                        "traffic_note": "both kernels; includes the workspace written and read back",
                         "peak_source": f"{kind} hbm_gbs", "algorithmic_bytes_per_launch": nbytes},
            "tensor": {"achieved_tflops": tflops, "peak_tflops": tpeak, "frac": tflops / tpeak,
                       "peak_source": tkind, "algorithmic_flops_per_launch": flops,
