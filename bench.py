@@ -455,7 +455,8 @@ def run_prefill(args) -> dict:
                               "products per contraction (split operands)"},
            "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup,
            "gpu_launches": 3 * args.steps,
-           "kernels": "per step: chunk metadata, chunk-parallel kernel, scan kernel"}
+           "kernels": "per step: chunk metadata, chunk-parallel kernel, scan kernel",
+           "scan_order": "longest sequence first" if call.seq_order is not None else "index"}
     if not args.no_cpu_baseline:
         import oracle
         threads = os.cpu_count() or 1

@@ -100,7 +100,7 @@ extern "C" {
  * Alignment: state, g, norm_weight and workspace 16 bytes; qkv 16 bytes with
  * a row stride that is a multiple of 8 elements; gate and out 8 bytes with row
  * strides that are multiples of 4; chunk_indices and chunk_offsets 8 bytes;
- * cu_seqlens, slot_idx, err_flag 4 bytes.
+ * cu_seqlens, slot_idx, seq_order, err_flag 4 bytes.
  */
 typedef struct KdaPrefillArgs {
   size_t struct_size; /* sizeof(KdaPrefillArgs) */
@@ -137,7 +137,27 @@ typedef struct KdaPrefillArgs {
   const float* A_log;
   const float* dt_bias;
   float lower_bound;
+  /* int32 [B] on the device, or NULL for index order: the order in which the
+   * scan kernel's CTAs take the sequences, a permutation of 0 .. B-1.  The
+   * scan runs one CTA per (sequence, head) and a sequence's chunks one after
+   * another, so with ragged lengths the longest sequences should start first
+   * (kda_prefill_longest_first builds that order on the host).  The order
+   * changes no result: every (sequence, head) is computed the same way
+   * wherever it runs.  An entry outside [0, B) sets KDA_DEVERR_ORDER and its
+   * CTAs do nothing; a repeated entry is a caller error (undefined results,
+   * as for repeated slots). */
+  const int32_t* seq_order;
 } KdaPrefillArgs;
+
+/* bit OR-ed into *err_flag (the KDA_DEVERR_* space of kda_decode.h) */
+#define KDA_DEVERR_ORDER 16 /* seq_order held an entry outside [0, B); those CTAs did nothing */
+
+/* Host helper: fill order[0 .. B-1] (host memory) with the sequence indices
+ * sorted by length, longest first, equal lengths in index order, from the
+ * host copy of cu_seqlens [B+1] (a negative length counts as 0).  Returns
+ * KDA_OK, KDA_ERR_NULLPTR (a NULL pointer with B > 0) or KDA_ERR_SHAPE
+ * (B < 0). */
+int kda_prefill_longest_first(const int32_t* cu_seqlens, int32_t B, int32_t* order);
 
 /* Workspace bytes a call with `num_chunks` chunks and H heads needs (about
  * 72.5 KiB per (chunk, head)); -1 for a negative count or H < 1. */

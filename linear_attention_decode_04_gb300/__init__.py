@@ -21,4 +21,5 @@ from .binding import (  # noqa: F401
     kda_status_string,
     library_path,
     load_library,
+    longest_first_order,
 )

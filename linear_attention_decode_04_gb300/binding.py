@@ -77,6 +77,7 @@ class KdaPrefillArgs(ctypes.Structure):
         ("num_chunks", ctypes.c_int64), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_int64),
         ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("lower_bound", ctypes.c_float),
+        ("seq_order", ctypes.c_void_p),
     ]
 
 
@@ -114,6 +115,8 @@ def load_library() -> ctypes.CDLL:
             L.kda_prefill.restype = ctypes.c_int
             L.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
             L.kda_prefill_workspace_bytes.restype = ctypes.c_int64
+            L.kda_prefill_longest_first.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+            L.kda_prefill_longest_first.restype = ctypes.c_int
             L.kda_abi_version.argtypes = []
             L.kda_abi_version.restype = ctypes.c_int
             if L.kda_abi_version() != ABI_VERSION:
@@ -349,7 +352,9 @@ class KdaPrefillCall:
     workspace (sized from ``cu_seqlens_cpu``, the host copy of the sequence
     starts, so nothing waits for the device); each ``__call__`` enqueues the
     device-side metadata build and the prefill.  Keeps references to the
-    tensors it points at.
+    tensors it points at.  With ``longest_first`` (the default) the scan takes
+    the sequences longest first (``seq_order``), which shortens the tail of
+    a batch with ragged lengths and changes no result.
 
     Shapes: T token rows, B sequences, H heads, D = H * 128.
       qkv [T, >=3D] bf16, conv_weight [3, 4, D] f32, conv_state [slots, 3D, 3]
@@ -361,7 +366,7 @@ class KdaPrefillCall:
     def __init__(self, qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,
                  cu_seqlens_cpu=None, gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, err_flag=None, A_log=None, dt_bias=None,
-                 lower_bound: float = 0.0, conv_state_layout: str = "DS"):
+                 lower_bound: float = 0.0, conv_state_layout: str = "DS", longest_first: bool = True):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -440,6 +445,14 @@ class KdaPrefillCall:
         self.chunk_offsets = torch.empty(B + 1, dtype=torch.int64, device=dev)
         self.workspace = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
         self.device = dev
+        # the scan takes the longest sequences first; the order is computed on
+        # the host and uploaded once, and left out where it is the index order
+        # or where the upload would fall inside a stream capture
+        self.seq_order = None
+        if longest_first and B > 1 and not torch.cuda.is_current_stream_capturing():
+            order = longest_first_order(cu_cpu.to(torch.int32))
+            if not torch.equal(order, torch.arange(B, dtype=torch.int32)):
+                self.seq_order = order.to(dev)
         self._keep = (qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, gate,
                       norm_weight, conv_bias, err_flag, A_log, dt_bias)
         self._cu, self._err = cu_seqlens, err_flag
@@ -455,7 +468,7 @@ class KdaPrefillCall:
             flags=flags, err_flag=ptr(err_flag),
             chunk_indices=ptr(self.chunk_indices), chunk_offsets=ptr(self.chunk_offsets),
             num_chunks=num_chunks, workspace=ptr(self.workspace), workspace_bytes=ws_bytes,
-            A_log=ptr(A_log), dt_bias=ptr(dt_bias), lower_bound=lower_bound)
+            A_log=ptr(A_log), dt_bias=ptr(dt_bias), lower_bound=lower_bound, seq_order=ptr(self.seq_order))
 
     def __call__(self, stream: torch.cuda.Stream | None = None) -> None:
         if stream is None:
@@ -472,6 +485,18 @@ class KdaPrefillCall:
         rc = self._lib.kda_prefill(ctypes.byref(self.args), sp)
         if rc != 0:
             raise KdaError(rc, f"{kda_status_string(rc)}: {self._lib.kda_last_error().decode()}")
+
+
+def longest_first_order(cu_seqlens_cpu) -> torch.Tensor:
+    """Sequence indices longest first (equal lengths in index order) from the
+    host copy of ``cu_seqlens``, by ``kda_prefill_longest_first``."""
+    cu = torch.as_tensor(cu_seqlens_cpu, dtype=torch.int32).contiguous().reshape(-1)
+    B = max(cu.numel() - 1, 0)
+    order = torch.empty(B, dtype=torch.int32)
+    rc = load_library().kda_prefill_longest_first(cu.data_ptr(), B, order.data_ptr())
+    if rc != 0:
+        raise KdaError(rc, kda_status_string(rc))
+    return order
 
 
 def kda_prefill(qkv, conv_weight, conv_state, state, g, beta, cu_seqlens, slot_idx, out, *,

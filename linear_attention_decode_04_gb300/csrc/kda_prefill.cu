@@ -37,7 +37,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "kda_chunk_metadata.h"
 #include "kda_internal.h"
@@ -86,6 +88,7 @@ struct PrefillParams {
   const float* A_log;
   const float* dt_bias;
   float lower_bound;
+  const int32_t* seq_order;   // [B] or NULL: the scan's sequence order
 };
 
 // Workspace image of one (chunk, head), written by the chunk kernel and
@@ -620,7 +623,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ScanSmem& S = *reinterpret_cast<ScanSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x / p.H, h = blockIdx.x - b * p.H;
+  const int rank = blockIdx.x / p.H, h = blockIdx.x - rank * p.H;
+  const int b = p.seq_order ? p.seq_order[rank] : rank;
+  if (b < 0 || b >= p.B) {
+    if (tid == 0 && h == 0) flag(p, KDA_DEVERR_ORDER);
+    return;
+  }
   const int64_t D = static_cast<int64_t>(p.H) * kD;
 
   const int64_t r0 = p.cu[b], r1 = p.cu[b + 1];
@@ -946,6 +954,20 @@ extern "C" int64_t kda_prefill_workspace_bytes(int64_t num_chunks, int32_t H) {
   return num_chunks * H * static_cast<int64_t>(kImg) * 4;
 }
 
+extern "C" int kda_prefill_longest_first(const int32_t* cu_seqlens, int32_t B, int32_t* order) {
+  kda_internal_clear_error();
+  if (B < 0) return kda_internal_fail(KDA_ERR_SHAPE, "B=%d", B);
+  if (B > 0 && (!cu_seqlens || !order)) return kda_internal_fail(KDA_ERR_NULLPTR, "cu_seqlens or order is NULL");
+  std::vector<int64_t> len(static_cast<size_t>(B));
+  for (int32_t i = 0; i < B; ++i) {
+    len[i] = static_cast<int64_t>(cu_seqlens[i + 1]) - cu_seqlens[i];
+    if (len[i] < 0) len[i] = 0;
+    order[i] = i;
+  }
+  std::stable_sort(order, order + B, [&](int32_t x, int32_t y) { return len[x] > len[y]; });
+  return KDA_OK;
+}
+
 extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   kda_internal_clear_error();
   if (!a) return kda_internal_fail(KDA_ERR_NULLPTR, "args is NULL");
@@ -985,7 +1007,7 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
       !aligned(a->out, 8) || (a->out_row_stride & 3) || !aligned(a->cu_seqlens, 4) || !aligned(a->slot_idx, 4) ||
       !aligned(a->chunk_indices, 8) || !aligned(a->chunk_offsets, 8) || !aligned(a->workspace, 16) ||
       !aligned(a->conv_weight, 4) || !aligned(a->conv_state, 2) || !aligned(a->beta, 2) ||
-      !aligned(a->err_flag, 4) || (a->conv_bias && !aligned(a->conv_bias, 4)) ||
+      !aligned(a->err_flag, 4) || !aligned(a->seq_order, 4) || (a->conv_bias && !aligned(a->conv_bias, 4)) ||
       (norm && (!aligned(a->gate, 8) || (a->gate_row_stride & 3) || !aligned(a->norm_weight, 16))))
     return kda_internal_fail(KDA_ERR_ALIGN, "a pointer or row stride is not aligned as required");
   cudaError_t e = setup();
@@ -1023,6 +1045,7 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   p.A_log = fused ? a->A_log : nullptr;
   p.dt_bias = fused ? a->dt_bias : nullptr;
   p.lower_bound = a->lower_bound;
+  p.seq_order = a->seq_order;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a->num_chunks > 0)
     kda_prefill_chunk_kernel<<<dim3(static_cast<unsigned>(a->num_chunks), static_cast<unsigned>(a->H)), kThreads,

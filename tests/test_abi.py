@@ -101,6 +101,7 @@ def test_prefill_host_validation_codes(lib):
     assert call(_pargs(num_chunks=-1)) == -2
     assert call(_pargs(flags=1 | 8)) == -1              # fused gate needs A_log
     assert call(_pargs(flags=1 | 8, A_log=0x20002)) == -3
+    assert call(_pargs(seq_order=0x20002)) == -3        # seq_order needs 4-byte alignment
     L.kda_prefill_workspace_bytes.restype = ctypes.c_int64
     L.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
     assert L.kda_prefill_workspace_bytes(10, 4) == 10 * 4 * 70144
@@ -170,3 +171,22 @@ def test_chunk_metadata_validation_codes(lib):
     assert f(0x1000, -1, 64, 0x2000, 8, 0x3000, None, None) == -2   # negative count
     assert f(0x1002, 4, 64, 0x2000, 8, 0x3000, None, None) == -3    # cu_seqlens misaligned
     assert f(0x1000, 4, 64, 0x2004, 8, 0x3000, None, None) == -3    # indices not 8-byte aligned
+
+
+def test_prefill_longest_first_order(lib):
+    # host helper: a stable sort by length, longest first; negative lengths count as 0
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(7)
+    for B in (1, 2, 5, 16, 300):
+        lens = rng.integers(-3, 90, B)
+        lens[rng.integers(0, B, B // 3)] = 40        # ties
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        got = binding.longest_first_order(torch.from_numpy(cu)).tolist()
+        want = sorted(range(B), key=lambda b: -max(int(lens[b]), 0))
+        assert got == want
+    assert binding.longest_first_order(torch.zeros(1, dtype=torch.int32)).numel() == 0
+    L = binding.load_library()
+    assert L.kda_prefill_longest_first(None, 0, None) == 0
+    assert L.kda_prefill_longest_first(None, 3, None) == -1
+    assert L.kda_prefill_longest_first(None, -1, None) == -2

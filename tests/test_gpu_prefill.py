@@ -315,3 +315,63 @@ def test_prefill_sd_conv_state_layout(cuda_device):
     st = d["state"].cpu().numpy()
     for s in range(x.spec.num_slots):
         T.check_state_slot(st[s], ref.state[s], f"slot {s}")
+
+
+def _prepared(x: W.PrefillInputs, d: dict, **kw):
+    return KdaPrefillCall(d["qkv"], d["conv_weight"], d["conv_state"], d["state"], d["g"], d["beta"],
+                          d["cu_seqlens"], d["slot_idx"], d["out"], cu_seqlens_cpu=d["cu_seqlens_cpu"],
+                          gate=d["gate"], norm_weight=d["norm_weight"], conv_bias=d["conv_bias"],
+                          eps=x.spec.eps, out_norm=x.spec.out_norm, err_flag=d["err_flag"], **kw)
+
+
+def _set_order(call, order):
+    call.seq_order = order
+    call.args.seq_order = order.data_ptr()
+
+
+def test_prefill_scan_order_changes_nothing(cuda_device):
+    # the order in which the scan takes the sequences is a scheduling choice:
+    # longest first, index order and reversed give bit-identical results
+    x = W.make_prefill_inputs(W.PREFILL_SMALL)
+    B = x.spec.B
+    got = []
+    for order in ("longest", "index", "reversed"):
+        d = to_device(x, cuda_device)
+        call = _prepared(x, d, longest_first=(order == "longest"))
+        assert (call.seq_order is None) == (order != "longest")
+        if order == "reversed":
+            _set_order(call, torch.arange(B - 1, -1, -1, dtype=torch.int32, device=cuda_device))
+        call()
+        torch.cuda.synchronize(cuda_device)
+        assert int(d["err_flag"].item()) == 0
+        got.append((T.bf16_bits(d["out"]), d["state"].cpu().numpy(), T.bf16_bits(d["conv_state"])))
+        if order == "longest":
+            ref, _ = run_oracle(x)
+            compare(x, d, ref)
+    for other in got[1:]:
+        for a, b in zip(got[0], other):
+            assert np.array_equal(a, b)
+
+
+def test_prefill_scan_order_out_of_range_flagged(cuda_device):
+    # an entry outside [0, B) is flagged; the sequence it displaced is left
+    # untouched (rows unwritten, pools unchanged) and every other one is right
+    x = W.make_prefill_inputs(W.PREFILL_SMALL)
+    B, victim = x.spec.B, 3
+    assert x.cu_seqlens[victim + 1] > x.cu_seqlens[victim] and x.slot_idx[victim] > 0
+    d = to_device(x, cuda_device)
+    call = _prepared(x, d, longest_first=False)
+    order = torch.arange(B, dtype=torch.int32, device=cuda_device)
+    order[victim] = B
+    _set_order(call, order)
+    call()
+    torch.cuda.synchronize(cuda_device)
+    assert int(d["err_flag"].item()) & 16
+    others = [b for b in range(B) if b != victim]
+    ref, rows = run_oracle(x, seqs=others)
+    compare(x, d, ref, rows=rows, seqs=others)
+    r0, r1 = int(x.cu_seqlens[victim]), int(x.cu_seqlens[victim + 1])
+    assert torch.isnan(d["out"][r0:r1].float()).all()
+    s = int(x.slot_idx[victim])
+    assert np.array_equal(d["state"][s].cpu().numpy(), x.state[s])
+    assert np.array_equal(T.bf16_bits(d["conv_state"])[s], x.conv_state[s])
