@@ -217,6 +217,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// One asynchronous 16-byte copy global -> shared (cache-global form); with
+// bytes = 0 nothing is read and the 16 bytes are zero-filled.  Completed by
+// cp.async.wait_all.
+__device__ __forceinline__ void cp16(void* dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+
 // ===================================================================== chunk
 // One CTA per (chunk row c, head h), chunk row = (sequence b, chunk j) from
 // the chunk metadata.  Everything that does not depend on the state entering
@@ -250,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
 
   // ---- 1. inputs: the three older taps (conv state for the first chunk,
   // else the sequence's preceding tokens), the chunk's rows (zero past L),
-  // g, beta
+  // g, beta.  Rows and g arrive by asynchronous 16-byte copies, all of a
+  // thread's copies in flight at once.
   if (j == 0) {
     // tap r of channel c at c * 3 + r (dim-first) or r * C + c (tap-first)
     const uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
@@ -261,28 +272,31 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   } else {
     for (int e = tid; e < kHist * 48; e += kThreads) {
       const int r = e / 48, q = e - r * 48, seg = q >> 4, u = q & 15;
-      reinterpret_cast<uint4*>(&S.raw[r][seg * kD])[u] = __ldg(reinterpret_cast<const uint4*>(
-          p.qkv + (t0 - kHist + r) * p.qkv_stride + seg * D + static_cast<int64_t>(h) * kD) + u);
+      cp16(&S.raw[r][seg * kD + 8 * u],
+           p.qkv + (t0 - kHist + r) * p.qkv_stride + seg * D + static_cast<int64_t>(h) * kD + 8 * u, 16);
     }
   }
   for (int e = tid; e < kL * 48; e += kThreads) {
     const int t = e / 48, q = e - t * 48, seg = q >> 4, u = q & 15;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (t < L)
-      val = __ldg(reinterpret_cast<const uint4*>(p.qkv + (t0 + t) * p.qkv_stride + seg * D +
-                                                 static_cast<int64_t>(h) * kD) + u);
-    reinterpret_cast<uint4*>(&S.raw[kHist + t][seg * kD])[u] = val;
+    const int tr = t < L ? t : L - 1;  // rows past L: zero-filled (the source row is only an address)
+    cp16(&S.raw[kHist + t][seg * kD + 8 * u],
+         p.qkv + (t0 + tr) * p.qkv_stride + seg * D + static_cast<int64_t>(h) * kD + 8 * u, t < L ? 16 : 0);
   }
-  for (int e = tid; e < kL * 32; e += kThreads) {
-    const int t = e >> 5, u = e & 31;
-    float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < L) {
-      val = __ldg(reinterpret_cast<const float4*>(p.g + ((t0 + t) * p.H + h) * kD) + u);
-      if (p.fused_gate) {
-        // the gate activation on the raw logits (the page's safe-gate variant;
-        // standard KDA form): z = raw + dt_bias, g = lb * sigmoid(e^A_log z)
-        // for a lower bound lb < 0, else g = -e^A_log softplus(z)
-        const float a = expf(__ldg(p.A_log + h));
+  if (!p.fused_gate) {
+    for (int e = tid; e < kL * 32; e += kThreads) {
+      const int t = e >> 5, u = e & 31, tr = t < L ? t : L - 1;
+      cp16(&S.G[t][4 * u], p.g + ((t0 + tr) * p.H + h) * kD + 4 * u, t < L ? 16 : 0);
+    }
+  } else {
+    // the gate activation on the raw logits (the page's safe-gate variant;
+    // standard KDA form): z = raw + dt_bias, g = lb * sigmoid(e^A_log z) for
+    // a lower bound lb < 0, else g = -e^A_log softplus(z)
+    const float a = expf(__ldg(p.A_log + h));
+    for (int e = tid; e < kL * 32; e += kThreads) {
+      const int t = e >> 5, u = e & 31;
+      float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < L) {
+        val = __ldg(reinterpret_cast<const float4*>(p.g + ((t0 + t) * p.H + h) * kD) + u);
         float* vv = &val.x;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -295,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
           }
         }
       }
+      reinterpret_cast<float4*>(S.G[t])[u] = val;
     }
-    reinterpret_cast<float4*>(S.G[t])[u] = val;
   }
   if (tid < kL) {
     float bt = 0.0f;
@@ -307,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
     S.beta[tid] = bt;
   }
   if (tid == 0) S.slow = 0;
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 
   // ---- 2. conv + SiLU over the window (outputs past L are zero); thread
