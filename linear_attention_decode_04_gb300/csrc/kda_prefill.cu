@@ -325,17 +325,18 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   __syncthreads();
 
   // ---- 2. conv + SiLU over the window (outputs past L are zero); thread
-  // tid convolves channel tid (q or k block) and, below 128, v channel tid
+  // tid convolves channel tid (q or k block) over all tokens and v channel
+  // tid % 128 over half of them (threads below 128 the first 16 tokens)
   {
     float wa[kWidth], wv[kWidth], ba = 0.0f, bv = 0.0f;
 #pragma unroll
     for (int t = 0; t < kWidth; ++t) {
       wa[t] = __ldg(p.conv_w + ((tid >> 7) * kWidth + t) * D + static_cast<int64_t>(h) * kD + (tid & 127));
-      wv[t] = tid < kD ? __ldg(p.conv_w + (2 * kWidth + t) * D + static_cast<int64_t>(h) * kD + tid) : 0.0f;
+      wv[t] = __ldg(p.conv_w + (2 * kWidth + t) * D + static_cast<int64_t>(h) * kD + (tid & (kD - 1)));
     }
     if (p.conv_b) {
       ba = __ldg(p.conv_b + ch_global(tid));
-      if (tid < kD) bv = __ldg(p.conv_b + ch_global(2 * kD + tid));
+      bv = __ldg(p.conv_b + ch_global(2 * kD + (tid & (kD - 1))));
     }
     float x0 = bf16f(S.raw[0][tid]), x1 = bf16f(S.raw[1][tid]), x2 = bf16f(S.raw[2][tid]);
     float* dst = tid < kD ? &S.q[0][tid] : &S.k[0][tid - kD];
@@ -350,18 +351,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
       dst[t * kSA] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
       x0 = x1; x1 = x2; x2 = x3;
     }
-    if (tid < kD) {
-      const int cv = 2 * kD + tid;
-      float z0 = bf16f(S.raw[0][cv]), z1 = bf16f(S.raw[1][cv]), z2 = bf16f(S.raw[2][cv]);
+    {
+      const int jv = tid & (kD - 1), cv = 2 * kD + jv, th = (tid >> 7) * (kL / 2);
+      float z0 = bf16f(S.raw[th][cv]), z1 = bf16f(S.raw[th + 1][cv]), z2 = bf16f(S.raw[th + 2][cv]);
 #pragma unroll
-      for (int t = 0; t < kL; ++t) {
+      for (int tt = 0; tt < kL / 2; ++tt) {
+        const int t = th + tt;
         const float z3 = bf16f(S.raw[kHist + t][cv]);
         float y = bv;
         y = fmaf(wv[0], z0, y);
         y = fmaf(wv[1], z1, y);
         y = fmaf(wv[2], z2, y);
         y = fmaf(wv[3], z3, y);
-        S.v[t][tid] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
+        S.v[t][jv] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
         z0 = z1; z1 = z2; z2 = z3;
       }
     }
@@ -426,13 +428,18 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   // ---- 5. P (strictly lower, shared memory) and R (lower, image) over the
   // key channels; R's A operand exp(G - G_m) q^ is formed while loading
   if (!S.slow) {
-    for (int x = warp; x < 12; x += kWarps) {
-      const int mat = x / 6, y = x - mat * 6;
+    // one 16 x 8 output tile y of P (mat 0) or R (mat 1); an R tile runs over
+    // all keys, a P tile over the half of them from key block kb and is added
+    // into P (cleared above; the two halves add in either order to the same
+    // value).  R tiles cost more (their A operand takes exponentials), so
+    // warps 0-5 take one R tile and one P half each, warps 6-7 three P halves
+    auto tile = [&](const int mat, const int y, const int kb) {
       const int mm = y < 2 ? 0 : 1, nn = y < 2 ? y : y - 2;
       const int ta = 16 * mm + g8;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int ke = mat == 0 ? kb + kD / 16 : kD / 8;
 #pragma unroll 4
-      for (int kk = 0; kk < kD / 8; ++kk) {
+      for (int kk = kb; kk < ke; ++kk) {
         const int i0 = 8 * kk + 2 * tq;
         float2 a02, a13;
         if (mat == 0) {
@@ -455,11 +462,17 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
       for (int e = 0; e < 4; ++e) {
         const int te = ta + (e >> 1) * 8, se = s + (e & 1);
         if (mat == 0) {
-          if (te > se) S.P[te][se] = acc[e];
+          if (te > se) atomicAdd(&S.P[te][se], acc[e]);
         } else {
           if (te >= se) ws[kOffB2 + kpos(kD + te, se, kNB2)] = acc[e];
         }
       }
+    };
+    if (warp < 6) {
+      tile(1, warp, 0);
+      tile(0, warp >> 1, (warp & 1) * (kD / 16));
+    } else {
+      for (int q = warp; q < 12; q += 2) tile(0, q >> 1, (q & 1) * (kD / 16));
     }
   } else {
     // element-wise: pairs (t, s), s <= t
