@@ -37,15 +37,17 @@
  *      to the workspace;
  *   2. scan: one CTA per (sequence, head) walks that sequence's chunks in
  *      order (its rows in the workspace start at chunk_offsets[b]) with the
- *      state held in registers, and applies each chunk to the state and the
- *      outputs.
+ *      state held in tensor memory, and applies each chunk to the state and
+ *      the outputs.  The CTAs take the sequences in the order seq_order
+ *      gives (longest first balances ragged batches), else in index order.
  * The contractions with the state and between tokens run on the tensor cores
  * (tf32 operands split into high and low parts, three products per
  * contraction, fp32 accumulation).
  *
- * Memory: all pointers are caller-owned device memory; the library allocates,
- * frees and synchronises nothing and reads no device memory from the host, so
- * a call can be captured into a CUDA graph.
+ * Memory: every pointer of KdaPrefillArgs is caller-owned device memory; the
+ * library allocates, frees and synchronises nothing and reads no device
+ * memory from the host, so a kda_prefill call can be captured into a CUDA
+ * graph.  kda_prefill_longest_first works on host memory only.
  */
 #ifndef KDA_PREFILL_H
 #define KDA_PREFILL_H
@@ -160,7 +162,7 @@ typedef struct KdaPrefillArgs {
 int kda_prefill_longest_first(const int32_t* cu_seqlens, int32_t B, int32_t* order);
 
 /* Workspace bytes a call with `num_chunks` chunks and H heads needs (about
- * 72.5 KiB per (chunk, head)); -1 for a negative count or H < 1. */
+ * 68.5 KiB, 70,144 bytes, per (chunk, head)); -1 for a negative count or H < 1. */
 int64_t kda_prefill_workspace_bytes(int64_t num_chunks, int32_t H);
 
 /*
