@@ -68,3 +68,26 @@ def test_traffic_note_requires_matching_source(tmp_path, monkeypatch):
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "1"])
+
+
+def test_reference_arm_line(capsys):
+    # the oracle arm prints one JSON line with the contract's keys (one layer,
+    # one timed step: a few seconds on the host cores)
+    import json
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-layers", "1"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    assert r["impl"] == "reference" and r["metric"] == bench.METRIC and r["unit"] == bench.UNIT
+    assert r["higher_is_better"] is True and r["value"] > 0 and r["steps"] == 1 and r["warmup"] == 3
+    assert r["config"]["workload"] == "stack69_n64_h48_pool96_pad4"
+    assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["value"] == r["value"]
+    assert r["e2e"] == {"value": r["value"], "unit": r["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing(capsys, monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-layers", "1"])
+    assert capsys.readouterr().out.strip() == ""
