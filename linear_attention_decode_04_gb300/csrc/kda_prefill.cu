@@ -39,7 +39,6 @@
 
 #include <algorithm>
 #include <mutex>
-#include <vector>
 
 #include "kda_chunk_metadata.h"
 #include "kda_internal.h"
@@ -986,13 +985,15 @@ extern "C" int kda_prefill_longest_first(const int32_t* cu_seqlens, int32_t B, i
   kda_internal_clear_error();
   if (B < 0) return kda_internal_fail(KDA_ERR_SHAPE, "B=%d", B);
   if (B > 0 && (!cu_seqlens || !order)) return kda_internal_fail(KDA_ERR_NULLPTR, "cu_seqlens or order is NULL");
-  std::vector<int64_t> len(static_cast<size_t>(B));
-  for (int32_t i = 0; i < B; ++i) {
-    len[i] = static_cast<int64_t>(cu_seqlens[i + 1]) - cu_seqlens[i];
-    if (len[i] < 0) len[i] = 0;
-    order[i] = i;
-  }
-  std::stable_sort(order, order + B, [&](int32_t x, int32_t y) { return len[x] > len[y]; });
+  // lengths taken in the comparison, so nothing here allocates; the GNU
+  // std::stable_sort asks for its buffer without throwing and merges in
+  // place when it gets none, so no exception crosses the C boundary
+  const auto len = [cu_seqlens](int32_t i) {
+    const int64_t n = static_cast<int64_t>(cu_seqlens[i + 1]) - cu_seqlens[i];
+    return n < 0 ? int64_t{0} : n;
+  };
+  for (int32_t i = 0; i < B; ++i) order[i] = i;
+  std::stable_sort(order, order + B, [&](int32_t x, int32_t y) { return len(x) > len(y); });
   return KDA_OK;
 }
 
