@@ -190,3 +190,15 @@ def test_prefill_longest_first_order(lib):
     assert L.kda_prefill_longest_first(None, 0, None) == 0
     assert L.kda_prefill_longest_first(None, 3, None) == -1
     assert L.kda_prefill_longest_first(None, -1, None) == -2
+
+
+def test_device_error_bits_are_distinct():
+    # the KDA_DEVERR_* bits of all headers share one err_flag word
+    bits = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        for name, val in re.findall(r"#define\s+(KDA_DEVERR_\w+)\s+(\d+)", open(h).read()):
+            bits[name] = int(val)
+    assert {"KDA_DEVERR_SLOT_RANGE", "KDA_DEVERR_TIMEOUT", "KDA_DEVERR_SEQLENS", "KDA_DEVERR_CAPACITY",
+            "KDA_DEVERR_ORDER"} <= set(bits)
+    vals = list(bits.values())
+    assert all(v > 0 and v & (v - 1) == 0 for v in vals) and len(set(vals)) == len(vals)
