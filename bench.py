@@ -209,6 +209,58 @@ def build_stack_specs(device, specs, keep_host: int = 0):
     return layers, host, x.spec, n_active
 
 
+def replay_stats(step, stream, n: int) -> dict:
+    """Run ``step`` ``n`` times on ``stream`` with a CUDA event before each
+    run and one after the last; per-run device times in ms (median, p10,
+    p90, mean)."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            evs[i].record(stream)
+            step()
+        evs[n].record(stream)
+    torch.cuda.synchronize(stream.device)
+    t = np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(n)])
+    return {"n": n, "median_ms": float(np.median(t)), "p10_ms": float(np.percentile(t, 10)),
+            "p90_ms": float(np.percentile(t, 90)), "mean_ms": float(t.mean())}
+
+
+def single_launch(device, spec, warmup: int, n: int, graph: bool = True) -> dict:
+    """One decode launch of ``spec`` on its own (replayed from a CUDA graph,
+    or launched eagerly), timed per launch over ``n`` runs."""
+    import torch
+
+    from linear_attention_decode_04_gb300 import workloads as W
+    from linear_attention_decode_04_gb300.stack import DecodeStack
+    layers, _, spec, n_active = build_stack_specs(device, [spec])
+    stack = DecodeStack(layers, eps=spec.eps, out_norm=spec.out_norm,
+                        update_conv_state=spec.update_conv_state)
+    stream = torch.cuda.Stream(device)
+    if graph:
+        stack.capture(stream)
+    step = stack.replay if graph else (lambda: stack.run_eager(stream))
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize(device)
+    st = replay_stats(step, stream, n)
+    if int(layers[0]["err_flag"].item()):
+        raise SystemExit("device error flag raised")
+    nbytes = W.algorithmic_bytes(spec.N, spec.H, n_active, spec.out_norm)
+    peak, kind = measured_peak()
+    ms = st["mean_ms"]
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res = {"workload": spec.name, "graph": graph, "ms_per_launch": ms, "stats": st,
+           "updates_per_s": n_active * spec.H / (ms / 1e3), "achieved_gbs": gbs, "peak_gbs": peak,
+           "frac": gbs / peak, "frac_median": nbytes / (st["median_ms"] / 1e3) / 1e9 / peak,
+           "peak_source": f"{kind} hbm_gbs", "algorithmic_bytes_per_launch": nbytes,
+           "work_queue": stack.queue is not None}
+    del stack, layers
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args) -> dict | None:
     import torch
 
@@ -262,6 +314,16 @@ def run_ours(args) -> dict | None:
     ms_step, units_total = aggregate(ms_local, units_step, world, device)
     clocks = clk.summary()
 
+    # ---- spread: per-replay device times over at least 100 graph replays
+    n_stats = max(args.steps, 100)
+    stats = replay_stats(stack.replay, stream, n_stats)
+    # ---- the same step launched eagerly (69 C-ABI calls per step, no graph)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            stack.run_eager(stream)
+    torch.cuda.synchronize(device)
+    eager = replay_stats(lambda: stack.run_eager(stream), stream, max(args.steps, 50))
+
     # ---- end to end: pinned host inputs -> device, graph, output -> host
     # ---- end to end: every layer's per-token inputs and its output live in
     # pinned host memory; the kernels read and write them directly over the
@@ -278,7 +340,7 @@ def run_ours(args) -> dict | None:
     e2e_stack = DecodeStack(host_layers, eps=spec.eps, out_norm=spec.out_norm,
                             update_conv_state=spec.update_conv_state, host_token_io=True)
     e2e_stack.capture(stream)
-    e2e_steps = max(3, args.steps // 4)
+    e2e_steps = max(args.steps, 20)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             e2e_stack.replay()
@@ -297,6 +359,13 @@ def run_ours(args) -> dict | None:
     errs = sum(int(L["err_flag"].item()) for L in layers)
     if errs:
         raise SystemExit(f"device error flag raised ({errs})")
+    del e2e_stack, host_layers
+
+    # ---- the N=256, H=96, 1024-slot step as one launch under graph replay,
+    # the configuration the >= 75% roofline target is judged on
+    cfg3 = None
+    if not args.no_cfg3:
+        cfg3 = single_launch(device, W.ROOFLINE, args.warmup, max(args.steps, 50))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -339,6 +408,15 @@ def run_ours(args) -> dict | None:
         "cpu_baseline": cpu,
         "clocks": clocks,
         "gpu_launches": stack.launches_per_step * args.steps,
+        "stats": dict(stats, what=f"per-replay device time of the 69-layer graph step over "
+                                  f"{stats['n']} replays after the timed region",
+                      updates_per_s_median=units_step / (stats["median_ms"] / 1e3)),
+        "eager": {"ms_per_step": eager["mean_ms"], "median_ms": eager["median_ms"],
+                  "p10_ms": eager["p10_ms"], "p90_ms": eager["p90_ms"], "steps": eager["n"],
+                  "updates_per_s": units_step / (eager["mean_ms"] / 1e3),
+                  "graph_ms_per_step": ms_step,
+                  "how": "the same 69 launches issued one C-ABI call at a time from Python, no graph"},
+        "cfg3": cfg3,
         "impl": "ours",
     }
 
@@ -351,38 +429,13 @@ def run_case(args) -> dict | None:
     import torch
 
     from linear_attention_decode_04_gb300 import workloads as W
-    from linear_attention_decode_04_gb300.stack import DecodeStack
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     spec = W.stack_layer_spec(0) if args.case == "layer" else W.ROOFLINE
-    layers, _, spec, n_active = build_stack_specs(device, [spec])
-    stack = DecodeStack(layers, eps=spec.eps, out_norm=spec.out_norm,
-                        update_conv_state=spec.update_conv_state)
-    stream = torch.cuda.Stream(device)
-    graph = args.case != "layer"
-    if graph:
-        stack.capture(stream)
-    step = stack.replay if graph else (lambda: stack.run_eager(stream))
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    torch.cuda.synchronize(device)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clk:
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(args.steps):
-                step()
-            ev1.record(stream)
-        torch.cuda.synchronize(device)
-    ms = ev0.elapsed_time(ev1) / args.steps
-    nbytes = W.algorithmic_bytes(spec.N, spec.H, n_active, spec.out_norm)
-    peak, kind = measured_peak()
-    gbs = nbytes / (ms / 1e3) / 1e9
-    return {"mode": args.case, "workload": spec.name, "graph": graph, "ms_per_launch": ms,
-            "updates_per_s": n_active * spec.H / (ms / 1e3), "achieved_gbs": gbs, "peak_gbs": peak,
-            "frac": gbs / peak, "peak_source": kind, "algorithmic_bytes_per_launch": nbytes,
-            "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup}
+        res = single_launch(device, spec, args.warmup, args.steps, graph=args.case != "layer")
+    res.update(mode=args.case, clocks=clk.summary(), steps=args.steps, warmup=args.warmup)
+    return res
 
 
 def measured_tf32_peak() -> tuple[float, str]:
@@ -564,6 +617,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--ref-layers", type=int, default=2, help="layers per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cfg3", action="store_true",
+                    help="skip the N=256/H=96 single-launch measurement in the headline line")
     ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill"),
                     default="stack69",
                     help="stack69: the headline 69-layer graph step; layer / roofline: one "

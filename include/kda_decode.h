@@ -166,23 +166,28 @@ int kda_decode_wait_test(const KdaDecodeArgs* args, void* stream, uint64_t wait_
 /*
  * kda_decode_noalloc: the same decode step for callers that cannot allocate
  * device memory (no counterpart on the page; it exists for integration).
- * Code that enqueues work while a CUDA graph is being captured (cudaMalloc
- * synchronises the device and is not a stream operation), plugin interfaces
- * whose enqueue step must not allocate, and serving loops with a memory
- * budget fixed at start-up cannot hand the kernel a work queue of their own.
- * This entry point runs the dynamic schedule with the queue kept in a
- * file-scope device array of 256 bytes inside the library (every GPU that
- * loads the library holds it until the process exits; one call uses 8 bytes,
- * a fixed need whatever N and H, and a larger need would be rejected with
- * KDA_ERR_SHAPE).  args->work_queue is ignored.  The caller still passes all
- * inputs and outputs.  It allocates nothing: it calls no cudaMalloc,
- * cudaFree or allocating library routine.  Each call first clears the queue
- * with an asynchronous memset on `stream`, then launches as kda_decode.
- * Every call shares the one array: calls that overlap on the GPU (other
- * streams, other host threads) race on it and give wrong results; calls
- * ordered on one stream are safe.  The first call on a device looks up the
- * array's device address (and does kda_decode's once-per-device set-up);
- * make that first call before any stream capture on that device.
+ * Plugin interfaces whose enqueue step must not allocate, serving loops with
+ * a device-memory budget fixed at start-up, and callers that reach the
+ * library only through this C ABI and hold no device allocator cannot hand
+ * the kernel a work queue of their own.  This entry point runs the dynamic
+ * schedule with the queue kept in a file-scope device array of 256 bytes
+ * inside the library (every GPU that loads the library holds it until the
+ * process exits).  One call uses 8 bytes of it, a fixed need whatever N and
+ * H, checked against the array's size when the library is compiled.
+ * args->work_queue is ignored.  The caller still passes all inputs and
+ * outputs.  It allocates nothing: it calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * Every argument is checked first, with the codes of kda_decode; on an error
+ * nothing is enqueued.  Then the call clears the queue with an asynchronous
+ * memset on `stream` and launches as kda_decode.  Every call shares the one
+ * array: calls that overlap on the GPU (other streams, other host threads)
+ * race on it and give wrong results; calls ordered on one stream are safe.
+ * The first call on a device looks up the array's device address (and does
+ * kda_decode's once-per-device set-up); make that first call before any
+ * stream capture on that device.  The looked-up address is kept for the life
+ * of the process: the library assumes the device's primary context is never
+ * reset (no cudaDeviceReset) while it is loaded.
  */
 int kda_decode_noalloc(const KdaDecodeArgs* args, void* stream);
 

@@ -124,7 +124,15 @@ extern "C" const char* kda_status_string(int status) {
 }
 
 namespace {
-int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, int32_t withhold_unit);
+int validate(const KdaDecodeArgs* a, uint64_t wait_limit_ns, int32_t withhold_unit, Params* p);
+int launch_validated(const Params& p, uint32_t flags, void* stream);
+
+int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, int32_t withhold_unit) {
+  Params p;
+  const int rc = validate(a, wait_limit_ns, withhold_unit, &p);
+  if (rc != KDA_OK || a->N == 0) return rc;
+  return launch_validated(p, a->flags, stream);
+}
 }  // namespace
 
 extern "C" int kda_decode(const KdaDecodeArgs* a, void* stream) {
@@ -138,9 +146,10 @@ extern "C" int kda_decode_wait_test(const KdaDecodeArgs* a, void* stream, uint64
 }
 
 namespace {
-int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, int32_t withhold_unit) {
+// Checks every argument and fills the kernel's parameter block; touches no
+// CUDA API and no device memory.  N == 0 passes (the caller launches nothing).
+int validate(const KdaDecodeArgs* a, uint64_t wait_limit_ns, int32_t withhold_unit, Params* out) {
   g_last_error[0] = '\0';
-  // Validation touches no CUDA API and no device memory.
   if (!a) return fail(KDA_ERR_NULLPTR, "args is NULL");
   if (a->struct_size != sizeof(KdaDecodeArgs))
     return fail(KDA_ERR_ABI, "struct_size %u, library expects %zu", a->struct_size, sizeof(KdaDecodeArgs));
@@ -177,7 +186,7 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
       (norm && (!aligned16(a->gate) || !aligned16(a->norm_weight))))
     return fail(KDA_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
 
-  Params p;
+  Params& p = *out;
   p.qkv = a->qkv;
   p.qkv_stride = a->qkv_row_stride;
   p.conv_w = a->conv_weight;
@@ -208,12 +217,17 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
   p.queue = a->work_queue;
   p.withhold_unit = withhold_unit;
   p.wait_limit_ns = wait_limit_ns;
+  return KDA_OK;
+}
 
+// Once-per-device set-up, then the launch of a validated parameter block.
+int launch_validated(const Params& p, uint32_t flags, void* stream) {
   int sms = 0;
   cudaError_t es = device_setup(&sms);
   if (es != cudaSuccess) return fail(KDA_ERR_LAUNCH, "device set-up: %s", cudaGetErrorString(es));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool conv = (a->flags & KDA_UPDATE_CONV_STATE) != 0;
+  const bool norm = (flags & KDA_OUT_NORM) != 0;
+  const bool conv = (flags & KDA_UPDATE_CONV_STATE) != 0;
   cudaError_t e = norm ? (conv ? launch<true, true>(p, sms, s) : launch<true, false>(p, sms, s))
                        : (conv ? launch<false, true>(p, sms, s) : launch<false, false>(p, sms, s));
   if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "%s", cudaGetErrorString(e));
@@ -224,34 +238,41 @@ int decode_impl(const KdaDecodeArgs* a, void* stream, uint64_t wait_limit_ns, in
 // ---------------------------------------------------------------------------
 // Allocation-free entry point.
 //
-// Some callers cannot allocate device memory for the work queue: code that
-// enqueues work while a CUDA graph is being captured (cudaMalloc is not a
-// stream operation and synchronises the device), plugin interfaces whose
-// enqueue step must not allocate, and serving loops that fix their memory
-// budget at start-up.  kda_decode_noalloc serves them with the dynamic
-// schedule, keeping the queue in this file-scope device array instead of a
-// caller-provided buffer.  Every GPU that loads the library holds the array
-// until the process exits.
+// Some callers cannot allocate device memory for the work queue: plugin
+// interfaces whose enqueue step must not allocate, serving loops that fix
+// their memory budget at start-up, and callers that reach the library only
+// through this C ABI and hold no device allocator of their own.
+// kda_decode_noalloc serves them with the dynamic schedule, keeping the queue
+// in this file-scope device array instead of a caller-provided buffer.  Every
+// GPU that loads the library holds the array until the process exits.
 namespace {
 constexpr size_t kNoAllocScratchBytes = 256;                    // stated maximum
-constexpr size_t kNoAllocQueueBytes = 2 * sizeof(int32_t);      // what one call uses
+constexpr size_t kNoAllocQueueBytes = 2 * sizeof(int32_t);      // what one call uses, whatever N and H
+static_assert(kNoAllocQueueBytes <= kNoAllocScratchBytes, "the work queue must fit the static scratch array");
 }  // namespace
 
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
 namespace {
-int32_t* g_noalloc_ptr[64];  // device address of g_noalloc_scratch per device (guarded by g_dev_mutex)
+// Device address of g_noalloc_scratch per device ordinal, looked up once with
+// that device current (guarded by g_dev_mutex).  It stays valid as long as
+// the device's primary context lives, which the library assumes for the life
+// of the process.
+int32_t* g_noalloc_ptr[64];
 }  // namespace
 
 extern "C" int kda_decode_noalloc(const KdaDecodeArgs* a, void* stream) {
+  // Every argument is checked before anything is enqueued
+  // (args->work_queue is ignored, so it is cleared in the checked copy).
   g_last_error[0] = '\0';
   if (!a) return fail(KDA_ERR_NULLPTR, "args is NULL");
   if (a->struct_size != sizeof(KdaDecodeArgs))
     return fail(KDA_ERR_ABI, "struct_size %u, library expects %zu", a->struct_size, sizeof(KdaDecodeArgs));
-  if (kNoAllocQueueBytes > kNoAllocScratchBytes)
-    return fail(KDA_ERR_SHAPE, "needs %zu bytes of scratch, the static array holds %zu", kNoAllocQueueBytes,
-                kNoAllocScratchBytes);
-  if (a->N == 0) return decode_impl(a, stream, kWaitLimitNs, -1);
+  KdaDecodeArgs b = *a;
+  b.work_queue = nullptr;
+  Params p;
+  const int rc = validate(&b, kWaitLimitNs, -1, &p);
+  if (rc != KDA_OK || b.N == 0) return rc;
   // Once per device, with that device current: the array's device address
   // (in host code the array's name is only a stand-in, never a pointer the
   // kernel can use).
@@ -273,7 +294,6 @@ extern "C" int kda_decode_noalloc(const KdaDecodeArgs* a, void* stream) {
   // The queue must start at zero; the array keeps whatever the last call left.
   e = cudaMemsetAsync(scratch, 0, kNoAllocQueueBytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "clearing the scratch: %s", cudaGetErrorString(e));
-  KdaDecodeArgs b = *a;
-  b.work_queue = scratch;
-  return decode_impl(&b, stream, kWaitLimitNs, -1);
+  p.queue = scratch;
+  return launch_validated(p, b.flags, stream);
 }

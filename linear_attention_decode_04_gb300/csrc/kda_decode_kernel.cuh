@@ -65,8 +65,8 @@ struct __align__(128) Smem {
   float q[kDim], k[kDim], v[kDim], alpha[kDim];
   float red[2][kConsumerWarps][kDim];
   float delta[kDim];
-  float nsum[kConsumerWarps];     // per-warp |q~|^2 (warps 0-3) and |k~|^2 (warps 4-7)
-  float sum[4][4];                // per-warp q~.k~, |w|^2, w.delta, |delta|^2
+  float4 part[kConsumerWarps];    // per-warp |q~|^2, |k~|^2, q~.k~ over the warp's 16 key rows
+  float osum[4];                  // per-warp sum of o_j^2 (warps 0-3)
   int info[kStages][4];           // slot, n (-1: no more units), h, withheld
   unsigned long long ready[kStages];  // info of the stage is written
   unsigned long long full[kStages];
@@ -548,9 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       y = fmaf(wq[3], bf16_to_f32(S.x[stage][c][j]), y);
       const float act = y / (1.0f + expf(-y));
       (c == 0 ? S.q : S.k)[j] = act;
-      // this warp's share of |q~|^2 (warps 0-3) or |k~|^2 (warps 4-7)
-      const float ss = warp_sum(act * act);
-      if (lane == 0) S.nsum[warp] = ss;
       if (tid < kDim) {
         const uint16_t* csv = S.cs[stage][2] + cs_j * j;
         float yv = bv;
@@ -581,12 +578,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     // key rows with the unnormalised q~, k~ (the L2 norms are applied to the
     // sums afterwards): u~ = A^T k~, w~ = A^T q~, A = Diag(alpha) S kept in
     // registers.
-    const float4* tile4 = reinterpret_cast<const float4*>(S.tile[stage]);
-    float4 a[kRowsPerWarp];
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
-    float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
-    // this warp's 16 rows of alpha, k~, q~ as float4 broadcasts
     float al_r[kRowsPerWarp], kt_r[kRowsPerWarp], qt_r[kRowsPerWarp];
 #pragma unroll
     for (int r4 = 0; r4 < kRowsPerWarp / 4; ++r4) {
@@ -597,6 +588,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       kt_r[4 * r4] = kt4.x; kt_r[4 * r4 + 1] = kt4.y; kt_r[4 * r4 + 2] = kt4.z; kt_r[4 * r4 + 3] = kt4.w;
       qt_r[4 * r4] = qt4.x; qt_r[4 * r4 + 1] = qt4.y; qt_r[4 * r4 + 2] = qt4.z; qt_r[4 * r4 + 3] = qt4.w;
     }
+    const float4* tile4 = reinterpret_cast<const float4*>(S.tile[stage]);
+    float4 a[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
       const float al = al_r[r], kt = kt_r[r], qt = qt_r[r];
@@ -608,37 +604,61 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     }
     reinterpret_cast<float4*>(S.red[0][warp])[lane] = u;
     reinterpret_cast<float4*>(S.red[1][warp])[lane] = w;
+    // The warp's share of |q~|^2, |k~|^2 and q~.k~ over its 16 key rows: lane
+    // l takes row l mod 16, then a 16-lane butterfly.  The three sums run in
+    // the same order, so q~.k~ equals |k~|^2 bit for bit whenever q~ equals k~.
+    {
+      const int i = warp * kRowsPerWarp + (lane & (kRowsPerWarp - 1));
+      const float qi = S.q[i], ki = S.k[i];
+      float pqq = qi * qi, pkk = ki * ki, pqk = qi * ki;
+#pragma unroll
+      for (int off = kRowsPerWarp / 2; off > 0; off >>= 1) {
+        pqq += __shfl_xor_sync(0xffffffffu, pqq, off);
+        pkk += __shfl_xor_sync(0xffffffffu, pkk, off);
+        pqk += __shfl_xor_sync(0xffffffffu, pqk, off);
+      }
+      if (lane == 0) S.part[warp] = make_float4(pqq, pkk, pqk, 0.0f);
+    }
     consumer_sync();
 
-    // L2 norms: q^ = rq q~, k^ = rk k~.  u = rk u~, w = rq w~;
-    // delta_j = beta (v_j - u_j); the readout of the updated state is
-    // o = S'^T q^ = w + (q^ . k^) delta, with no second pass over S'.
-    float rq = 0.0f, rk = 0.0f, wj = 0.0f, dj = 0.0f;
+    // L2 norms: q^ = rq q~, k^ = rk k~, and with u~ = A^T k~, w~ = A^T q~:
+    // delta = beta (v - rk u~).  The readout of the updated state,
+    // o = S'^T q^ = rq w~ + (q^.k^) delta, is evaluated without a second pass
+    // over S' and rearranged so that its one cancellation happens inside a
+    // single fused multiply-add:
+    //   o = rq ((w~ - u~) + m u~) + beta (q^.k^) v,
+    //   m = 1 - beta (q~.k~) rk^2 = (|k~|^2 + 1e-6 - beta q~.k~) rk^2.
+    // When q~ is parallel to k~ and beta = 1, |o| can be far below |w|; the
+    // plain sum w + (q^.k^) delta would then carry an fp32 rounding error of
+    // the size of |w|.
+    float o = 0.0f;
     if (tid < kDim) {
-      const float ssq = (S.nsum[0] + S.nsum[1]) + (S.nsum[2] + S.nsum[3]);
-      const float ssk = (S.nsum[4] + S.nsum[5]) + (S.nsum[6] + S.nsum[7]);
-      rq = scale / sqrtf(ssq + 1e-6f);
-      rk = 1.0f / sqrtf(ssk + 1e-6f);
-      float uj = 0.0f;
+      // the eight warps' partials, summed by an 8-lane butterfly
+      const float4 pr = S.part[lane & (kConsumerWarps - 1)];
+      float ssq = pr.x, ssk = pr.y, sqk = pr.z;
+#pragma unroll
+      for (int off = kConsumerWarps / 2; off > 0; off >>= 1) {
+        ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
+        ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
+        sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
+      }
+      const float rq = scale / sqrtf(ssq + 1e-6f);
+      const float rk = 1.0f / sqrtf(ssk + 1e-6f);
+      float ut = 0.0f, wt = 0.0f;
 #pragma unroll
       for (int r = 0; r < kConsumerWarps; ++r) {
-        uj += S.red[0][r][tid];
-        wj += S.red[1][r][tid];
+        ut += S.red[0][r][tid];
+        wt += S.red[1][r][tid];
       }
-      uj *= rk;
-      wj *= rq;
-      dj = beta * (S.v[tid] - uj);
+      const float vj = S.v[tid];
+      const float dj = beta * (vj - rk * ut);
       S.delta[tid] = rk * dj;  // pass 2 adds k~ (rk delta)^T = k^ delta^T
-      // q~.k~ for (q^ . k^), and the three sums that give sum_j o_j^2
-      const float sqk = warp_sum(S.q[tid] * S.k[tid]);
-      if (lane == 0) S.sum[warp][0] = sqk;
+      const float m = (fmaf(-beta, sqk, ssk) + 1e-6f) * (rk * rk);
+      const float bqk = beta * sqk * rq * rk;  // beta (q^ . k^)
+      o = fmaf(bqk, vj, rq * fmaf(m, ut, wt - ut));
       if (kOutNorm) {
-        const float sww = warp_sum(wj * wj), swd = warp_sum(wj * dj), sdd = warp_sum(dj * dj);
-        if (lane == 0) {
-          S.sum[warp][1] = sww;
-          S.sum[warp][2] = swd;
-          S.sum[warp][3] = sdd;
-        }
+        const float so = warp_sum(o * o);
+        if (lane == 0) S.osum[warp] = so;
       }
     }
     consumer_sync();
@@ -659,18 +679,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&S.done[stage]));
 
-    // Gated RMSNorm epilogue (or the raw readout) to bf16.
+    // Gated RMSNorm epilogue (or the raw readout) to bf16; the sum of o_j^2
+    // is taken from o itself.
     if (tid < kDim) {
-      const float qk = ((S.sum[0][0] + S.sum[1][0]) + (S.sum[2][0] + S.sum[3][0])) * rq * rk;  // q^ . k^
-      const float o = fmaf(qk, dj, wj);
       float y = o;
       if (kOutNorm) {
-        // sum_j o_j^2 = sum w^2 + 2 qk sum w delta + qk^2 sum delta^2
-        const float sww = (S.sum[0][1] + S.sum[1][1]) + (S.sum[2][1] + S.sum[3][1]);
-        const float swd = (S.sum[0][2] + S.sum[1][2]) + (S.sum[2][2] + S.sum[3][2]);
-        const float sdd = (S.sum[0][3] + S.sum[1][3]) + (S.sum[2][3] + S.sum[3][3]);
-        const float ss = fmaf(qk, fmaf(qk, sdd, 2.0f * swd), sww);
-        const float rr = 1.0f / sqrtf(fmaxf(ss, 0.0f) * (1.0f / kDim) + p.eps);
+        const float ss = (S.osum[0] + S.osum[1]) + (S.osum[2] + S.osum[3]);
+        const float rr = 1.0f / sqrtf(ss * (1.0f / kDim) + p.eps);
         y = o * rr * nw * (1.0f / (1.0f + expf(-gate_j)));
       }
       out_row[tid] = f32_to_bf16(y);

@@ -433,3 +433,174 @@ int kda_oracle_prefill(const kda_oracle_prefill_problem* p, int num_threads) {
   }
   return oob;
 }
+
+/* ---------------------------------------------------------------- multi-token decode */
+
+int kda_oracle_multi_problem_size(void) { return (int)sizeof(kda_oracle_multi_problem); }
+
+/* One (sequence n, head h) of the multi-token decode: the decode steps token
+ * by token from the source slot's window and state, each present token's
+ * state and window stored to its own destination slot (formulation in
+ * kda_oracle.h, MULTI-TOKEN DECODE; P1 实现拆解 items 3-4 for the excluded
+ * speculative batches).  Returns the number of out-of-range slots met. */
+static int multi_unit(const kda_oracle_multi_problem* p, int n, int h, double* work) {
+  const int H = p->H, K = p->K, V = p->V, W = p->W, T = p->T;
+  const int64_t Dq = (int64_t)H * K, Dv = (int64_t)H * V, C = 2 * Dq + Dv;
+  const int32_t src = p->src_slot[n];
+
+  if (src <= 0 || src >= p->num_slots) { /* padding or out-of-range sequence */
+    for (int t = 0; t < T; ++t) {
+      const int64_t r = (int64_t)n * T + t;
+      for (int j = 0; j < V; ++j) {
+        p->out[r * Dv + (int64_t)h * V + j] = 0;
+        if (p->out_f64) p->out_f64[r * Dv + (int64_t)h * V + j] = 0.0;
+      }
+    }
+    return src >= p->num_slots;
+  }
+
+  double* qt = work;            /* K */
+  double* kt = qt + K;          /* K */
+  double* vt = kt + K;          /* V */
+  double* qh = vt + V;          /* K */
+  double* kh = qh + K;          /* K */
+  double* alpha = kh + K;       /* K */
+  double* o = alpha + K;        /* V */
+  double* y = o + V;            /* V */
+  double* gt = y + V;           /* V */
+  double* nw = gt + V;          /* V */
+  double* x = nw + V;           /* W */
+  double* wt = x + W;           /* W */
+  double* S = wt + W;           /* K*V */
+  uint16_t* win = (uint16_t*)(S + (size_t)K * V); /* (2K+V) channels x (W-1) taps, oldest first */
+
+  const int dims[3] = {K, K, V};
+  const int64_t offs[3] = {0, Dq, 2 * Dq};
+  const int64_t Ds[3] = {Dq, Dq, Dv};
+  const float* wbase[3] = {p->conv_weight, p->conv_weight + (int64_t)W * Dq, p->conv_weight + 2 * (int64_t)W * Dq};
+  /* element (ch, t) of a slot's conv state in either layout */
+  const int64_t cs_ch = p->conv_state_sd ? 1 : (W - 1);
+  const int64_t cs_t = p->conv_state_sd ? C : 1;
+
+  /* the source: window and state, read in full before anything is stored */
+  const uint16_t* cs_src = p->conv_state + (int64_t)src * C * (W - 1);
+  for (int c = 0, m = 0; c < 3; ++c)
+    for (int j = 0; j < dims[c]; ++j, ++m) {
+      const int64_t ch = offs[c] + (int64_t)h * dims[c] + j;
+      for (int t = 0; t < W - 1; ++t) win[(size_t)m * (W - 1) + t] = cs_src[ch * cs_ch + t * cs_t];
+    }
+  const float* S_src = p->state + (((int64_t)src * H + h) * K) * V;
+  for (int64_t e = 0; e < (int64_t)K * V; ++e) S[e] = (double)S_src[e];
+  const double scale = (p->q_scale != 0.0) ? p->q_scale : 1.0 / sqrt((double)K);
+
+  int oob = 0;
+  for (int t = 0; t < T; ++t) {
+    const int64_t r = (int64_t)n * T + t;
+    const int32_t dst = p->dst_slots[r];
+    uint16_t* out = p->out + r * Dv + (int64_t)h * V;
+    double* out64 = p->out_f64 ? p->out_f64 + r * Dv + (int64_t)h * V : NULL;
+    if (dst <= 0 || dst >= p->num_slots) { /* absent token */
+      for (int j = 0; j < V; ++j) {
+        out[j] = 0;
+        if (out64) out64[j] = 0.0;
+      }
+      oob += dst >= p->num_slots;
+      continue;
+    }
+    /* 1. conv + SiLU with the window, then slide the window */
+    for (int c = 0, m = 0; c < 3; ++c) {
+      double* dstv = (c == 0) ? qt : (c == 1) ? kt : vt;
+      for (int j = 0; j < dims[c]; ++j, ++m) {
+        const int64_t ch = offs[c] + (int64_t)h * dims[c] + j;
+        uint16_t* wm = win + (size_t)m * (W - 1);
+        const uint16_t xin = p->qkv[r * p->qkv_row_stride + ch];
+        for (int k = 0; k < W - 1; ++k) x[k] = kda_oracle_bf16_to_f64(wm[k]);
+        x[W - 1] = kda_oracle_bf16_to_f64(xin);
+        for (int k = 0; k < W; ++k) wt[k] = (double)wbase[c][(int64_t)k * Ds[c] + (int64_t)h * dims[c] + j];
+        const double bias = p->conv_bias ? (double)p->conv_bias[ch] : 0.0;
+        dstv[j] = kda_oracle_silu(kda_oracle_causal_conv(x, wt, W, bias));
+        for (int k = 0; k < W - 2; ++k) wm[k] = wm[k + 1];
+        wm[W - 2] = xin;
+      }
+    }
+    /* 2. L2 norms */
+    kda_oracle_l2norm(qt, K, p->l2_eps, scale, qh);
+    kda_oracle_l2norm(kt, K, p->l2_eps, 1.0, kh);
+    /* 3. gated delta rule on the carried fp64 state */
+    double beta = kda_oracle_bf16_to_f64(p->beta[r * H + h]);
+    if (p->fused_gate) {
+      const double a_log = (double)p->A_log[h];
+      for (int i = 0; i < K; ++i) {
+        double z = (double)p->g[(r * H + h) * K + i];
+        if (p->dt_bias) z += (double)p->dt_bias[(int64_t)h * K + i];
+        alpha[i] = exp(kda_oracle_kda_gate(z, a_log, p->lower_bound));
+      }
+      beta = kda_oracle_sigmoid(beta);
+    } else {
+      for (int i = 0; i < K; ++i) alpha[i] = exp((double)p->g[(r * H + h) * K + i]);
+    }
+    kda_oracle_gated_delta_update(K, V, S, alpha, beta, kh, vt);
+    /* 4. readout, 5. gated RMSNorm or raw */
+    kda_oracle_readout(K, V, S, qh, o);
+    if (p->out_norm) {
+      for (int j = 0; j < V; ++j) {
+        gt[j] = kda_oracle_bf16_to_f64(p->gate[r * Dv + (int64_t)h * V + j]);
+        nw[j] = (double)p->norm_weight[j];
+      }
+      kda_oracle_gated_rmsnorm(V, o, nw, gt, p->eps, y);
+    } else {
+      for (int j = 0; j < V; ++j) y[j] = o[j];
+    }
+    for (int j = 0; j < V; ++j) {
+      out[j] = kda_oracle_round_bf16(y[j]);
+      if (out64) out64[j] = y[j];
+    }
+    /* 6. store the state (rounded) and the window after this token */
+    float* S_dst = p->state + (((int64_t)dst * H + h) * K) * V;
+    for (int64_t e = 0; e < (int64_t)K * V; ++e) S_dst[e] = (float)S[e];
+    if (p->update_conv_state) {
+      uint16_t* cs_dst = p->conv_state + (int64_t)dst * C * (W - 1);
+      for (int c = 0, m = 0; c < 3; ++c)
+        for (int j = 0; j < dims[c]; ++j, ++m) {
+          const int64_t ch = offs[c] + (int64_t)h * dims[c] + j;
+          for (int k = 0; k < W - 1; ++k) cs_dst[ch * cs_ch + k * cs_t] = win[(size_t)m * (W - 1) + k];
+        }
+    }
+  }
+  return oob;
+}
+
+int kda_oracle_decode_multi(const kda_oracle_multi_problem* p, int num_threads) {
+  if (!p || p->N < 0 || p->T < 1 || p->H < 1 || p->K < 1 || p->V < 1 || p->W < 2 || p->num_slots < 1)
+    return -1;
+  if (p->N == 0) return 0;
+  if (!p->src_slot || !p->dst_slots || !p->qkv || !p->conv_weight || !p->conv_state || !p->state || !p->g ||
+      !p->beta || !p->out)
+    return -1;
+  if (p->out_norm && (!p->gate || !p->norm_weight)) return -1;
+  if (p->fused_gate && !p->A_log) return -1;
+  const int64_t C = 2 * (int64_t)p->H * p->K + (int64_t)p->H * p->V;
+  if (p->qkv_row_stride < C) return -1;
+
+  const int64_t units = (int64_t)p->N * p->H;
+  const size_t work_len = (size_t)(5 * p->K + 5 * p->V + 2 * p->W) + (size_t)p->K * p->V +
+                          ((size_t)(2 * p->K + p->V) * (p->W - 1) * sizeof(uint16_t) + sizeof(double) - 1) / sizeof(double);
+  int oob = 0;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+  (void)num_threads;
+#endif
+#pragma omp parallel reduction(+ : oob)
+  {
+    double* work = (double*)malloc(work_len * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t u = 0; u < units; ++u) {
+      const int n = (int)(u / p->H), h = (int)(u % p->H);
+      const int r = multi_unit(p, n, h, work);
+      if (h == 0) oob += r; /* count per sequence, not per (sequence, head) */
+    }
+    free(work);
+  }
+  return oob;
+}

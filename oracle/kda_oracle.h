@@ -109,6 +109,37 @@
  *         conv state when the sequence is shorter than W-1).
  *   - an empty sequence (no tokens) leaves everything unchanged.
  * ---------------------------------------------------------------------------
+ * MULTI-TOKEN DECODE (speculative decoding)
+ *
+ * P1 keeps speculative-decode batches off its fused kernel: the support gate
+ * requires num_spec == 0 (实现拆解 item 3), the model layer takes the fused
+ * path only without a speculative sequence mask and indexes the
+ * non-speculative state indices (实现拆解 item 4; kda.py under 关键源码片段),
+ * and 风险与影响 lists spec decode as not covered.  P1 gives no formulation;
+ * the oracle adopts the plainest one consistent with a per-token state-index
+ * table next to the non-speculative one:
+ *   - sequence n carries T = 1 + num_spec tokens, rows n*T + t (t = 0..T-1,
+ *     in order) of qkv, g, beta, gate and out;
+ *   - src_slot[n] holds the sequence's current recurrent state and conv
+ *     window; dst_slots[n*T + t] receives the state and the window after
+ *     token t;
+ *   - src_slot[n] <= 0: padding sequence, its T output rows are zero and
+ *     nothing else is read or written; src_slot[n] >= num_slots: the same,
+ *     counted out of range;
+ *   - dst_slots[n*T + t] <= 0: token t is absent, its output row is zero and
+ *     it advances neither the window nor the recurrence; >= num_slots: the
+ *     same, counted out of range;
+ *   - every present token runs steps 1-5 in order, the window sliding over
+ *     the sequence's present tokens (its first W-1 taps from conv_state[src])
+ *     and the state carried in fp64 from token to token, never rounded in
+ *     between; after token t, S rounded to fp32 is stored to
+ *     state[dst_slots[n*T + t]] and, with update_conv_state, the window's
+ *     bit patterns to conv_state[dst_slots[n*T + t]];
+ *   - the source is read in full before anything is stored, so a destination
+ *     may be the sequence's own source slot; apart from that, the slots of
+ *     one call are distinct.
+ * With T = 1 and dst_slots = src_slot this is the decode step above.
+ * ---------------------------------------------------------------------------
  */
 #ifndef KDA_ORACLE_H
 #define KDA_ORACLE_H
@@ -187,6 +218,40 @@ typedef struct {
  * slot was >= num_slots, or -1 on a bad argument. */
 int kda_oracle_prefill(const kda_oracle_prefill_problem* p, int num_threads);
 int kda_oracle_prefill_problem_size(void);
+
+/* Multi-token decode problem (see MULTI-TOKEN DECODE above).  Host memory,
+ * caller-owned. */
+typedef struct {
+  int32_t N, T, H, K, V, W, num_slots;
+  const int32_t* src_slot;    /* [N] */
+  const int32_t* dst_slots;   /* [N][T] */
+  const uint16_t* qkv;        /* [N*T][qkv_row_stride] */
+  int64_t qkv_row_stride;
+  const float* conv_weight;   /* as kda_oracle_problem */
+  const float* conv_bias;     /* [C] or NULL */
+  uint16_t* conv_state;       /* [num_slots][C][W-1] (DS), or [num_slots][W-1][C] if conv_state_sd */
+  float* state;               /* [num_slots][H][K][V] */
+  const float* g;             /* [N*T][H][K] */
+  const uint16_t* beta;       /* [N*T][H] */
+  const uint16_t* gate;       /* [N*T][H*V]; ignored when out_norm == 0 */
+  const float* norm_weight;   /* [V]; ignored when out_norm == 0 */
+  uint16_t* out;              /* [N*T][H*V] */
+  double* out_f64;            /* optional [N*T][H*V] */
+  double eps, l2_eps, q_scale;
+  int32_t out_norm;
+  int32_t update_conv_state;
+  int32_t fused_gate;
+  const float* A_log;
+  const float* dt_bias;
+  double lower_bound;
+  int32_t conv_state_sd;
+} kda_oracle_multi_problem;
+
+/* Runs the multi-token decode of every sequence.  Returns the number of
+ * out-of-range slot entries met (a source slot, or a destination slot of a
+ * sequence whose source is in range), or -1 on a bad argument. */
+int kda_oracle_decode_multi(const kda_oracle_multi_problem* p, int num_threads);
+int kda_oracle_multi_problem_size(void);
 
 /* ---- the individual steps, fp64, exposed for the fact tests ---- */
 

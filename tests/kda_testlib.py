@@ -123,3 +123,24 @@ def compare_all(x: W.Inputs, d: dict, ref: oracle.OracleResult, init_state: np.n
             if s not in active:
                 assert np.array_equal(cs[s], init_conv[s])
     return dict(out_max_abs=out_err, state_max_abs=worst)
+
+
+def cancellation_inputs(sigma: float, v_scale: float, seed: int = 5, N: int = 6, H: int = 4,
+                        out_norm: bool = True) -> W.Inputs:
+    """A decode step whose readout is far smaller than the matvec it comes
+    from.  The q and k channels get identical conv weights, taps and inputs
+    (so q~ = k~ exactly), beta = 1, g = 0, the state is scaled to N(0, sigma)
+    and the v conv weights by ``v_scale``.  Then o = S'^T q^ is about
+    v~ / sqrt(128) while w = A^T q^ grows with sigma: |o| << |w|."""
+    spec = W.Spec(f"cancel_s{sigma:g}_v{v_scale:g}", N=N, H=H, num_slots=N + 2, seed=seed,
+                  out_norm=out_norm)
+    x = W.make_inputs(spec)
+    D = H * W.HEAD_DIM
+    x.conv_weight[1] = x.conv_weight[0]
+    x.conv_weight[2] *= np.float32(v_scale)
+    x.qkv[:, D:2 * D] = x.qkv[:, 0:D]
+    x.conv_state[:, D:2 * D, :] = x.conv_state[:, 0:D, :]
+    x.beta[:] = W.f32_to_bf16_bits(np.ones(1, np.float32))[0]
+    x.g[:] = 0.0
+    x.state *= np.float32(sigma / 0.02)
+    return x

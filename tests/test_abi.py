@@ -147,6 +147,25 @@ def test_host_validation_codes(lib):
     assert lib.kda_status_string(-3).decode().startswith("pointer")
 
 
+def test_noalloc_validates_before_enqueueing(lib):
+    """kda_decode_noalloc answers every argument error with the same code as
+    kda_decode before it makes any CUDA call: on this host, with no GPU, a
+    call that got as far as the scratch look-up or its memset would answer
+    KDA_ERR_LAUNCH instead."""
+    fn = lib.kda_decode_noalloc
+    fn.argtypes = [ctypes.POINTER(binding.KdaDecodeArgs), ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    assert fn(None, None) == -1
+    for kw, code in ((dict(struct_size=8), -6), (dict(head_dim=64), -2), (dict(N=-1), -2),
+                     (dict(flags=32), -4), (dict(qkv=None), -1), (dict(state=0x10004), -3),
+                     (dict(qkv_row_stride=100), -2), (dict(N=0), 0)):
+        assert fn(ctypes.byref(_args(**kw)), None) == code, kw
+        assert _call(lib, _args(**kw)) == code, kw
+    # work_queue is ignored by the allocation-free entry (kda_decode checks it)
+    assert _call(lib, _args(work_queue=0x10003)) == -3
+    assert fn(ctypes.byref(_args(work_queue=0x10003)), None) == -5
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "nope.so"))
     monkeypatch.setattr(binding, "_lib", None)
