@@ -1,4 +1,5 @@
-"""fp64 CPU oracle of the fused KDA decode step and of the varlen prefill.
+"""fp64 CPU oracle of the fused KDA decode step, its multi-token (speculative)
+form and the varlen prefill.
 
 TEST INFRASTRUCTURE ONLY: the test-suite, the smoke check and the benchmark's
 CPU-baseline leg load it; the product library never does, and the two share
@@ -8,6 +9,7 @@ from .kda_oracle import (  # noqa: F401
     OracleResult,
     build,
     decode,
+    decode_multi,
     prefill,
     lib,
     round_bf16,

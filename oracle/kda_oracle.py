@@ -74,6 +74,23 @@ class _PrefillProblem(ctypes.Structure):
     ]
 
 
+class _MultiProblem(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("V", ctypes.c_int32), ("W", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+        ("src_slot", ctypes.c_void_p), ("dst_slots", ctypes.c_void_p),
+        ("qkv", ctypes.c_void_p), ("qkv_row_stride", ctypes.c_int64),
+        ("conv_weight", ctypes.c_void_p), ("conv_bias", ctypes.c_void_p),
+        ("conv_state", ctypes.c_void_p), ("state", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("gate", ctypes.c_void_p),
+        ("norm_weight", ctypes.c_void_p), ("out", ctypes.c_void_p), ("out_f64", ctypes.c_void_p),
+        ("eps", ctypes.c_double), ("l2_eps", ctypes.c_double), ("q_scale", ctypes.c_double),
+        ("out_norm", ctypes.c_int32), ("update_conv_state", ctypes.c_int32),
+        ("fused_gate", ctypes.c_int32), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("lower_bound", ctypes.c_double), ("conv_state_sd", ctypes.c_int32),
+    ]
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
@@ -108,6 +125,11 @@ def lib() -> ctypes.CDLL:
             L.kda_oracle_prefill.argtypes = [ctypes.POINTER(_PrefillProblem), ctypes.c_int]
             L.kda_oracle_prefill.restype = ctypes.c_int
             L.kda_oracle_prefill_problem_size.restype = ctypes.c_int
+            L.kda_oracle_decode_multi.argtypes = [ctypes.POINTER(_MultiProblem), ctypes.c_int]
+            L.kda_oracle_decode_multi.restype = ctypes.c_int
+            L.kda_oracle_multi_problem_size.restype = ctypes.c_int
+            if L.kda_oracle_multi_problem_size() != ctypes.sizeof(_MultiProblem):
+                raise RuntimeError("oracle multi-token struct layout mismatch")
             if L.kda_oracle_problem_size() != ctypes.sizeof(_Problem):
                 raise RuntimeError("oracle struct layout mismatch")
             if L.kda_oracle_prefill_problem_size() != ctypes.sizeof(_PrefillProblem):
@@ -331,4 +353,73 @@ def prefill(*, qkv, conv_weight, conv_state, state, g, beta, slot_idx, cu_seqlen
     rc = lib().kda_oracle_prefill(ctypes.byref(p), int(threads))
     if rc < 0:
         raise ValueError("kda_oracle_prefill rejected its arguments")
+    return OracleResult(out=out, out_f64=out64, conv_state=cs, state=st, n_out_of_range=rc)
+
+
+def decode_multi(*, qkv, conv_weight, conv_state, state, g, beta, src_slot, dst_slots, H: int,
+                 K: int = 128, V: int = 128, W: int = 4, gate=None, norm_weight=None,
+                 conv_bias=None, eps: float = 1e-6, l2_eps: float = 1e-6, q_scale: float = 0.0,
+                 out_norm: bool = True, update_conv_state: bool = True, threads: int = 0,
+                 want_f64: bool = True, in_place: bool = False, fused_gate: bool = False,
+                 A_log=None, dt_bias=None, lower_bound: float = 0.0,
+                 conv_state_sd: bool = False) -> OracleResult:
+    """Multi-token (speculative) decode: sequence n starts from the window and
+    state in ``src_slot[n]`` and runs its T tokens (rows n*T + t of ``qkv``,
+    ``g``, ``beta``, ``gate``) in order; the state and window after token t go
+    to ``dst_slots[n, t]`` (an entry <= 0 marks an absent token).  ``dst_slots``
+    is [N, T].  Pools are copied unless ``in_place``."""
+    dst = np.ascontiguousarray(dst_slots, dtype=np.int32)
+    assert dst.ndim == 2
+    N, T = dst.shape
+    src = np.ascontiguousarray(src_slot, dtype=np.int32)
+    assert src.shape == (N,)
+    qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
+    C = 2 * H * K + H * V
+    assert qkv.shape[0] == N * T
+    conv_weight = np.ascontiguousarray(conv_weight, dtype=np.float32)
+    assert conv_weight.size == W * C
+    if in_place:
+        assert conv_state.dtype == np.uint16 and conv_state.flags.c_contiguous
+        assert state.dtype == np.float32 and state.flags.c_contiguous
+        cs, st = conv_state, state
+    else:
+        cs = np.array(conv_state, dtype=np.uint16, order="C", copy=True)
+        st = np.array(state, dtype=np.float32, order="C", copy=True)
+    num_slots = st.shape[0]
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    beta = np.ascontiguousarray(beta, dtype=np.uint16)
+    assert g.size == N * T * H * K and beta.size == N * T * H
+    if out_norm:
+        gate = np.ascontiguousarray(gate, dtype=np.uint16)
+        norm_weight = np.ascontiguousarray(norm_weight, dtype=np.float32)
+        assert gate.size == N * T * H * V and norm_weight.size == V
+    else:
+        gate = norm_weight = None
+    if conv_bias is not None:
+        conv_bias = np.ascontiguousarray(conv_bias, dtype=np.float32)
+        assert conv_bias.size == C
+    if fused_gate:
+        A_log = np.ascontiguousarray(A_log, dtype=np.float32)
+        assert A_log.size == H
+        if dt_bias is not None:
+            dt_bias = np.ascontiguousarray(dt_bias, dtype=np.float32)
+            assert dt_bias.size == H * K
+    else:
+        A_log = dt_bias = None
+    out = np.zeros((N * T, H * V), dtype=np.uint16)
+    out64 = np.zeros((N * T, H * V), dtype=np.float64) if want_f64 else None
+    p = _MultiProblem(N=N, T=T, H=H, K=K, V=V, W=W, num_slots=num_slots, src_slot=_ptr(src),
+                      dst_slots=_ptr(dst), qkv=_ptr(qkv),
+                      qkv_row_stride=qkv.shape[1] if qkv.ndim == 2 else C,
+                      conv_weight=_ptr(conv_weight), conv_bias=_ptr(conv_bias),
+                      conv_state=_ptr(cs), state=_ptr(st), g=_ptr(g), beta=_ptr(beta),
+                      gate=_ptr(gate), norm_weight=_ptr(norm_weight),
+                      out=_ptr(out), out_f64=_ptr(out64), eps=eps, l2_eps=l2_eps,
+                      q_scale=q_scale, out_norm=int(bool(out_norm)),
+                      update_conv_state=int(bool(update_conv_state)), fused_gate=int(bool(fused_gate)),
+                      A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), lower_bound=float(lower_bound),
+                      conv_state_sd=int(bool(conv_state_sd)))
+    rc = lib().kda_oracle_decode_multi(ctypes.byref(p), int(threads))
+    if rc < 0:
+        raise ValueError("kda_oracle_decode_multi rejected its arguments")
     return OracleResult(out=out, out_f64=out64, conv_state=cs, state=st, n_out_of_range=rc)

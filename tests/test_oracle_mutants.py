@@ -69,9 +69,26 @@ MUTANTS = {
     "prefill_decay_of_previous_token": (
         "alpha[i] = exp((double)p->g[((int64_t)r * H + h) * K + i]);",
         "alpha[i] = exp((double)p->g[((int64_t)(r > r0 ? r - 1 : r) * H + h) * K + i]);"),
+    # multi-token (speculative) decode
+    "multi_window_not_slid": ("        for (int k = 0; k < W - 2; ++k) wm[k] = wm[k + 1];\n        wm[W - 2] = xin;\n", ""),
+    "multi_state_reread_every_token": (
+        "    const int32_t dst = p->dst_slots[r];",
+        "    const int32_t dst = p->dst_slots[r];\n    for (int64_t e = 0; e < (int64_t)K * V; ++e) S[e] = (double)S_src[e];"),
+    "multi_window_stored_to_source": (
+        "uint16_t* cs_dst = p->conv_state + (int64_t)dst * C * (W - 1);",
+        "uint16_t* cs_dst = p->conv_state + (int64_t)src * C * (W - 1);"),
+    "multi_slot_zero_not_absent": (
+        "if (dst <= 0 || dst >= p->num_slots) { /* absent token */",
+        "if (dst < 0 || dst >= p->num_slots) { /* absent token */"),
+    "multi_decay_of_first_token": (
+        "alpha[i] = exp((double)p->g[(r * H + h) * K + i]);",
+        "alpha[i] = exp((double)p->g[((int64_t)n * T * H + h) * K + i]);"),
+    "multi_padding_source_processed": (
+        "if (src <= 0 || src >= p->num_slots) { /* padding or out-of-range sequence */",
+        "if (src < 0 || src >= p->num_slots) { /* padding or out-of-range sequence */"),
 }
 
-PIN_FILES = ("test_oracle_pins.py", "test_prefill_oracle_pins.py")
+PIN_FILES = ("test_oracle_pins.py", "test_prefill_oracle_pins.py", "test_multi_oracle_pins.py")
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
