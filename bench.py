@@ -261,6 +261,57 @@ def single_launch(device, spec, warmup: int, n: int, graph: bool = True) -> dict
     return res
 
 
+def spec_launch(device, spec, warmup: int, n: int) -> dict:
+    """One multi-token (speculative) decode launch of ``spec`` (work queue)
+    replayed from a CUDA graph, timed per launch over ``n`` replays."""
+    import torch
+
+    from linear_attention_decode_04_gb300 import KdaDecodeCall
+    from linear_attention_decode_04_gb300 import workloads as W
+    from linear_attention_decode_04_gb300.stack import warm_up
+    x = W.make_multi_inputs(spec)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)  # noqa: E731
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+    t = dict(qkv=bf(x.qkv), conv_weight=f(x.conv_weight), conv_state=bf(x.conv_state), state=f(x.state),
+             g=f(x.g), beta=bf(x.beta), gate=bf(x.gate), norm_weight=f(x.norm_weight), src=f(x.src_slot),
+             dst=f(x.dst_slots), out=torch.empty(x.N * x.T, x.H * 128, dtype=torch.bfloat16, device=device),
+             err=torch.zeros(1, dtype=torch.int32, device=device),
+             queue=torch.zeros(2, dtype=torch.int32, device=device))
+    call = KdaDecodeCall(t["qkv"], t["conv_weight"], t["conv_state"], t["state"], t["g"], t["beta"], t["dst"],
+                         t["out"], gate=t["gate"], norm_weight=t["norm_weight"], eps=spec.eps,
+                         out_norm=spec.out_norm, update_conv_state=spec.update_conv_state, err_flag=t["err"],
+                         work_queue=t["queue"], tokens_per_seq=x.T, src_slot=t["src"])
+    warm_up(device)
+    stream = torch.cuda.Stream(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize(device)
+    st = replay_stats(graph.replay, stream, n)
+    if int(t["err"].item()):
+        raise SystemExit("device error flag raised")
+    valid = lambda sl: 0 < sl < spec.num_slots  # noqa: E731
+    units = sum(1 for nn in range(x.N) if valid(x.src_slot[nn])) * x.H
+    tokens = sum(1 for nn in range(x.N) for tt in range(x.T)
+                 if valid(x.src_slot[nn]) and valid(x.dst_slots[nn, tt])) * x.H
+    nbytes = W.multi_algorithmic_bytes(spec, x.src_slot, x.dst_slots)
+    peak, kind = measured_peak()
+    ms = st["mean_ms"]
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res = {"workload": spec.name, "tokens_per_seq": x.T, "graph": True, "ms_per_launch": ms, "stats": st,
+           "token_updates_per_s": tokens / (ms / 1e3), "sequence_head_units_per_s": units / (ms / 1e3),
+           "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak, "peak_source": f"{kind} hbm_gbs",
+           "algorithmic_bytes_per_launch": nbytes,
+           "bytes_note": "per (sequence, head): 64 KiB state read once + 64 KiB written per present token, "
+                         "plus windows and per-token inputs / outputs"}
+    del call, graph, t
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args) -> dict | None:
     import torch
 
@@ -366,6 +417,9 @@ def run_ours(args) -> dict | None:
     cfg3 = None
     if not args.no_cfg3:
         cfg3 = single_launch(device, W.ROOFLINE, args.warmup, max(args.steps, 50))
+    spec_decode = None
+    if not args.no_cfg3:
+        spec_decode = spec_launch(device, W.MULTI_BENCH, args.warmup, max(args.steps, 50))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -417,6 +471,7 @@ def run_ours(args) -> dict | None:
                   "graph_ms_per_step": ms_step,
                   "how": "the same 69 launches issued one C-ABI call at a time from Python, no graph"},
         "cfg3": cfg3,
+        "spec_decode": spec_decode,
         "impl": "ours",
     }
 
@@ -618,8 +673,8 @@ def main(argv=None):
     ap.add_argument("--ref-layers", type=int, default=2, help="layers per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cfg3", action="store_true",
-                    help="skip the N=256/H=96 single-launch measurement in the headline line")
-    ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill"),
+                    help="skip the N=256/H=96 single-launch and the multi-token measurements in the headline line")
+    ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill", "spec"),
                     default="stack69",
                     help="stack69: the headline 69-layer graph step; layer / roofline: one "
                          "launch configuration timed on its own (profiling aid); prefill: the "
@@ -633,6 +688,14 @@ def main(argv=None):
         res = run_chunk_metadata(args)
     elif args.case == "prefill":
         res = run_prefill(args)
+    elif args.case == "spec":
+        import torch
+
+        from linear_attention_decode_04_gb300 import workloads as W
+        torch.cuda.set_device(0)
+        with ClockSampler(0) as clk:
+            res = spec_launch(torch.device("cuda", 0), W.MULTI_BENCH, args.warmup, args.steps)
+        res.update(mode="spec", clocks=clk.summary(), steps=args.steps, warmup=args.warmup)
     elif args.case != "stack69":
         res = run_case(args)
     else:

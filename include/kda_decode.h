@@ -37,11 +37,13 @@
 extern "C" {
 #endif
 
-#define KDA_DECODE_ABI_VERSION 1
+#define KDA_DECODE_ABI_VERSION 2
 
 /* Fixed problem geometry (P1 实现拆解 item 3: head_dim 128, conv width 4). */
 #define KDA_HEAD_DIM 128
 #define KDA_CONV_WIDTH 4
+/* Largest tokens_per_seq of a multi-token (speculative) call: 1 + num_spec. */
+#define KDA_MAX_TOKENS_PER_SEQ 8
 
 /* flags */
 #define KDA_OUT_NORM          1u /* apply the gated RMSNorm epilogue */
@@ -52,7 +54,7 @@ extern "C" {
  * streaming state and conv state while that kernel is still running; all
  * per-token inputs (qkv, g, beta, gate) are still read only after it has
  * completed.  Without this flag nothing is read before it completes. */
-#define KDA_EARLY_PREFETCH    4u
+#define KDA_EARLY_PREFETCH    4u /* (with src_slot: it too is not written by that kernel) */
 /* g and beta hold raw logits and the kernel activates them (the page's
  * "safe gate" variant; formula below, in KdaDecodeArgs.lower_bound). */
 #define KDA_FUSED_GATE        8u
@@ -65,7 +67,8 @@ extern "C" {
 #define KDA_OK            0
 #define KDA_ERR_NULLPTR  -1 /* a required pointer is NULL */
 #define KDA_ERR_SHAPE    -2 /* head_dim != 128, conv_width != 4, N < 0, H < 1,
-                               num_slots < 1, a stride too small, or N*H too large */
+                               num_slots < 1, a stride too small, N*H too large, or
+                               tokens_per_seq outside 0 .. KDA_MAX_TOKENS_PER_SEQ */
 #define KDA_ERR_ALIGN    -3 /* a pointer or row stride breaks the 16-byte rule */
 #define KDA_ERR_FLAGS    -4 /* unknown flag bits */
 #define KDA_ERR_LAUNCH   -5 /* the CUDA launch failed; see kda_last_error() */
@@ -135,6 +138,34 @@ typedef struct KdaDecodeArgs {
    * example on different streams) need different queues; calls ordered on
    * one stream may share one.  4-byte alignment. */
   int32_t* work_queue;
+
+  /* Multi-token (speculative) decode.  P1 keeps speculative batches off its
+   * fused kernel (实现拆解 items 3-4: the support gate wants num_spec == 0 and
+   * the model layer indexes the non-speculative state indices; 风险与影响:
+   * spec decode not covered) and gives no formulation; this library adopts
+   * the one below.  It is selected by tokens_per_seq >= 2 or by a non-NULL
+   * src_slot.  Then N counts sequences, and sequence n carries
+   * T = max(tokens_per_seq, 1) tokens, rows n*T + t (t = 0 .. T-1, in order)
+   * of qkv, g, beta, gate and out (so those tensors have N*T rows), and
+   * slot_idx is int32 [N][T]:
+   *   - the sequence starts from the recurrent state and conv window of
+   *     src_slot[n] (slot_idx[n*T] when src_slot is NULL);
+   *   - after token t its state and window are stored to slot_idx[n*T + t]
+   *     (the window only with KDA_UPDATE_CONV_STATE); the state is carried
+   *     on chip from token to token;
+   *   - a source slot <= 0 marks a padding sequence: its T output rows are
+   *     zero and nothing else is read or written;
+   *   - a destination slot <= 0 marks an absent token: its output row is
+   *     zero and it advances neither the state nor the window;
+   *   - slots >= num_slots are treated as padding / absent and raise
+   *     KDA_DEVERR_SLOT_RANGE;
+   *   - the source is read in full before anything is stored, so a
+   *     destination may equal its own sequence's source; apart from that all
+   *     slots of a call must be distinct.
+   * With tokens_per_seq <= 1 and src_slot NULL a call is the single-token
+   * step above (one row per sequence, slot_idx both source and destination). */
+  int32_t tokens_per_seq;      /* 0 or 1: single-token step; 2 .. KDA_MAX_TOKENS_PER_SEQ */
+  const int32_t* src_slot;     /* int32 [N] or NULL; 4-byte alignment */
 } KdaDecodeArgs;
 
 /*

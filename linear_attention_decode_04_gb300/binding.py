@@ -22,7 +22,8 @@ KDA_FUSED_GATE = 8
 KDA_CONV_STATE_SD = 16
 KDA_DEVERR_SLOT_RANGE = 1
 KDA_DEVERR_TIMEOUT = 2
-ABI_VERSION = 1
+ABI_VERSION = 2
+MAX_TOKENS_PER_SEQ = 8
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG_DIR, "lib", "libkda_decode.so")
@@ -53,6 +54,7 @@ class KdaDecodeArgs(ctypes.Structure):
         ("flags", ctypes.c_uint32), ("err_flag", ctypes.c_void_p),
         ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("lower_bound", ctypes.c_float),
         ("work_queue", ctypes.c_void_p),
+        ("tokens_per_seq", ctypes.c_int32), ("src_slot", ctypes.c_void_p),
     ]
 
 
@@ -171,14 +173,21 @@ class KdaDecodeCall:
     ``host_token_io=True`` lets the per-token tensors (qkv, g, beta, gate,
     slot_idx, out) be pinned host tensors: the kernel then reads them and
     writes the output straight over the CPU-GPU link, with no copy step.
-    The host must not rewrite them while a launch that uses them may run."""
+    The host must not rewrite them while a launch that uses them may run.
+
+    Multi-token (speculative) decode: with ``tokens_per_seq`` = T >= 2 or a
+    ``src_slot`` tensor (int32 [N]), the per-token tensors hold N*T rows
+    (sequence n's tokens at rows n*T .. n*T + T - 1), ``slot_idx`` is int32
+    [N, T] (the destination of each token's state and conv window; <= 0 =
+    absent token) and each sequence starts from ``src_slot[n]`` (default
+    ``slot_idx[n, 0]``)."""
 
     def __init__(self, qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                  gate=None, norm_weight=None, conv_bias=None, eps: float = 1e-6,
                  q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
                  err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
                  lower_bound: float = 0.0, work_queue=None, conv_state_layout: str = "DS",
-                 host_token_io: bool = False):
+                 host_token_io: bool = False, tokens_per_seq: int = 1, src_slot=None):
         self._lib = load_library()
         dev = state.device
         _check(state, "state", torch.float32, None)
@@ -189,8 +198,15 @@ class KdaDecodeCall:
         D = H * HEAD_DIM
         C = 3 * D
         _check(qkv, "qkv", torch.bfloat16, dev, host_token_io)
-        N = int(qkv.shape[0])
-        qkv_stride = _rows(qkv, "qkv", N, C)
+        T = int(tokens_per_seq)
+        if not 1 <= T <= MAX_TOKENS_PER_SEQ:
+            raise ValueError(f"tokens_per_seq must be 1 .. {MAX_TOKENS_PER_SEQ} (got {T})")
+        multi = T > 1 or src_slot is not None
+        R = int(qkv.shape[0])                # token rows
+        if R % T:
+            raise ValueError(f"qkv has {R} rows, not a multiple of tokens_per_seq={T}")
+        N = R // T                           # sequences (= rows when T = 1)
+        qkv_stride = _rows(qkv, "qkv", R, C)
         _check(conv_weight, "conv_weight", torch.float32, dev)
         if tuple(conv_weight.shape) != (3, CONV_WIDTH, D):
             raise ValueError(f"conv_weight must be [3, 4, {D}] (got {tuple(conv_weight.shape)})")
@@ -203,19 +219,28 @@ class KdaDecodeCall:
             raise ValueError(f"conv_state ({conv_state_layout}) must be {list(want_cs)} (got {tuple(conv_state.shape)})")
         _dense(conv_state, "conv_state")
         _check(g, "g", torch.float32, dev, host_token_io)
-        if tuple(g.shape) != (N, H, HEAD_DIM):
-            raise ValueError(f"g must be [{N}, {H}, 128] (got {tuple(g.shape)})")
+        if tuple(g.shape) != (R, H, HEAD_DIM):
+            raise ValueError(f"g must be [{R}, {H}, 128] (got {tuple(g.shape)})")
         _dense(g, "g")
         _check(beta, "beta", torch.bfloat16, dev, host_token_io)
-        if tuple(beta.shape) != (N, H):
-            raise ValueError(f"beta must be [{N}, {H}] (got {tuple(beta.shape)})")
+        if tuple(beta.shape) != (R, H):
+            raise ValueError(f"beta must be [{R}, {H}] (got {tuple(beta.shape)})")
         _dense(beta, "beta")
         _check(slot_idx, "slot_idx", torch.int32, dev, host_token_io)
-        if tuple(slot_idx.shape) != (N,):
-            raise ValueError(f"slot_idx must be [{N}] (got {tuple(slot_idx.shape)})")
+        if slot_idx.numel() != R or (multi and tuple(slot_idx.shape) not in ((N, T), (R,))) or \
+                (not multi and tuple(slot_idx.shape) != (N,)):
+            want = f"[{N}, {T}]" if multi else f"[{N}]"
+            raise ValueError(f"slot_idx must be {want} (got {tuple(slot_idx.shape)})")
         _dense(slot_idx, "slot_idx")
+        src_ptr = None
+        if src_slot is not None:
+            _check(src_slot, "src_slot", torch.int32, dev, host_token_io)
+            if tuple(src_slot.shape) != (N,):
+                raise ValueError(f"src_slot must be [{N}] (got {tuple(src_slot.shape)})")
+            _dense(src_slot, "src_slot")
+            src_ptr = src_slot.data_ptr()
         _check(out, "out", torch.bfloat16, dev, host_token_io)
-        out_stride = _rows(out, "out", N, D)
+        out_stride = _rows(out, "out", R, D)
         fused_gate = A_log is not None
         flags = ((KDA_OUT_NORM if out_norm else 0) | (KDA_UPDATE_CONV_STATE if update_conv_state else 0)
                  | (KDA_EARLY_PREFETCH if early_prefetch else 0) | (KDA_FUSED_GATE if fused_gate else 0)
@@ -238,7 +263,7 @@ class KdaDecodeCall:
             if gate is None or norm_weight is None:
                 raise ValueError("out_norm needs gate and norm_weight")
             _check(gate, "gate", torch.bfloat16, dev, host_token_io)
-            gate_stride = _rows(gate, "gate", N, D)
+            gate_stride = _rows(gate, "gate", R, D)
             _check(norm_weight, "norm_weight", torch.float32, dev)
             if tuple(norm_weight.shape) != (HEAD_DIM,):
                 raise ValueError("norm_weight must be [128]")
@@ -260,9 +285,9 @@ class KdaDecodeCall:
             _check(err_flag, "err_flag", torch.int32, dev)
             err_ptr = err_flag.data_ptr()
         self.device = dev
-        self.N, self.H, self.num_slots = N, H, num_slots
+        self.N, self.H, self.num_slots, self.T = N, H, num_slots, T
         self._keep = (qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate,
-                      norm_weight, conv_bias, err_flag, A_log, dt_bias, work_queue)
+                      norm_weight, conv_bias, err_flag, A_log, dt_bias, work_queue, src_slot)
         self.args = KdaDecodeArgs(
             struct_size=ctypes.sizeof(KdaDecodeArgs), N=N, H=H, num_slots=num_slots,
             head_dim=HEAD_DIM, conv_width=CONV_WIDTH,
@@ -273,7 +298,8 @@ class KdaDecodeCall:
             norm_weight=nw_ptr, slot_idx=slot_idx.data_ptr(),
             out=out.data_ptr(), out_row_stride=out_stride,
             eps=float(eps), q_scale=float(q_scale), flags=flags, err_flag=err_ptr,
-            A_log=alog_ptr, dt_bias=dtb_ptr, lower_bound=float(lower_bound), work_queue=queue_ptr)
+            A_log=alog_ptr, dt_bias=dtb_ptr, lower_bound=float(lower_bound), work_queue=queue_ptr,
+            tokens_per_seq=T if multi else 0, src_slot=src_ptr)
         self._argp = ctypes.byref(self.args)
 
     def __call__(self, stream: torch.cuda.Stream | None = None) -> None:
@@ -299,6 +325,7 @@ def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
                q_scale: float = 0.0, out_norm: bool = True, update_conv_state: bool = True,
                err_flag=None, early_prefetch: bool = False, A_log=None, dt_bias=None,
                lower_bound: float = 0.0, work_queue=None, conv_state_layout: str = "DS",
+               tokens_per_seq: int = 1, src_slot=None,
                stream: torch.cuda.Stream | None = None) -> None:
     """One fused decode step (see ``include/kda_decode.h``).  ``conv_state``,
     ``state`` and ``out`` are written in place on ``stream`` (default: the
@@ -307,13 +334,16 @@ def kda_decode(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, *,
     stream writes none of slot_idx, state and conv_state.  Passing ``A_log``
     sets KDA_FUSED_GATE: ``g`` and ``beta`` are then raw logits.
     ``work_queue`` (int32[2], zero) enables the dynamic schedule.
-    ``conv_state_layout`` is "DS" ([slots, C, 3]) or "SD" ([slots, 3, C])."""
+    ``conv_state_layout`` is "DS" ([slots, C, 3]) or "SD" ([slots, 3, C]).
+    ``tokens_per_seq`` / ``src_slot`` select the multi-token (speculative)
+    form described on ``KdaDecodeCall``."""
     KdaDecodeCall(qkv, conv_weight, conv_state, state, g, beta, slot_idx, out, gate=gate,
                   norm_weight=norm_weight, conv_bias=conv_bias, eps=eps, q_scale=q_scale,
                   out_norm=out_norm, update_conv_state=update_conv_state,
                   err_flag=err_flag, early_prefetch=early_prefetch, A_log=A_log, dt_bias=dt_bias,
                   lower_bound=lower_bound, work_queue=work_queue,
-                  conv_state_layout=conv_state_layout)(stream)
+                  conv_state_layout=conv_state_layout, tokens_per_seq=tokens_per_seq,
+                  src_slot=src_slot)(stream)
 
 
 def kda_chunk_metadata(cu_seqlens: torch.Tensor, cu_seqlens_cpu: torch.Tensor, chunk_size: int,

@@ -23,6 +23,7 @@
 
 #include "kda_decode.h"
 #include "kda_decode_kernel.cuh"
+#include "kda_decode_multi_kernel.cuh"
 #include "kda_internal.h"
 
 namespace {
@@ -49,8 +50,11 @@ DeviceInfo g_dev[64];
 
 template <bool kOutNorm, bool kUpdateConv>
 cudaError_t set_attrs() {
-  return cudaFuncSetAttribute(kda_decode_persistent_kernel<kOutNorm, kUpdateConv>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(Smem)));
+  cudaError_t e = cudaFuncSetAttribute(kda_decode_persistent_kernel<kOutNorm, kUpdateConv>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(Smem)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kda_decode_multi_kernel<kOutNorm, kUpdateConv>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(MSmem)));
 }
 
 // Once per device: SM count and the large dynamic shared-memory opt-in for
@@ -80,17 +84,19 @@ cudaError_t launch(const Params& p, int sms, cudaStream_t stream) {
   // Every launch is a programmatic dependent launch: the CTAs may become
   // resident while the previous kernel in the stream drains, and wait for
   // it (griddepcontrol.wait) before touching its results.
+  const bool multi = p.T > 1 || p.src_slot != nullptr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.total_units < sms ? p.total_units : sms));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.dynamicSmemBytes = multi ? sizeof(MSmem) : sizeof(Smem);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kda_decode_persistent_kernel<kOutNorm, kUpdateConv>, p);
+  cudaError_t e = multi ? cudaLaunchKernelEx(&cfg, kda_decode_multi_kernel<kOutNorm, kUpdateConv>, p)
+                        : cudaLaunchKernelEx(&cfg, kda_decode_persistent_kernel<kOutNorm, kUpdateConv>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -173,6 +179,12 @@ int validate(const KdaDecodeArgs* a, uint64_t wait_limit_ns, int32_t withhold_un
                      (reinterpret_cast<uintptr_t>(a->dt_bias) & 3u)))
     return fail(KDA_ERR_ALIGN, "A_log and dt_bias must be 4-byte aligned");
   if (reinterpret_cast<uintptr_t>(a->work_queue) & 3u) return fail(KDA_ERR_ALIGN, "work_queue must be 4-byte aligned");
+  if (a->tokens_per_seq < 0 || a->tokens_per_seq > KDA_MAX_TOKENS_PER_SEQ)
+    return fail(KDA_ERR_SHAPE, "tokens_per_seq %d (need 0 .. %d)", a->tokens_per_seq, KDA_MAX_TOKENS_PER_SEQ);
+  if (reinterpret_cast<uintptr_t>(a->src_slot) & 3u) return fail(KDA_ERR_ALIGN, "src_slot must be 4-byte aligned");
+  const int T = a->tokens_per_seq > 1 ? a->tokens_per_seq : 1;
+  if (static_cast<int64_t>(a->N) * T > (1LL << 30))
+    return fail(KDA_ERR_SHAPE, "N*tokens_per_seq = %lld rows is too many", static_cast<long long>(a->N) * T);
   const int64_t D = static_cast<int64_t>(a->H) * KDA_HEAD_DIM;
   if (static_cast<int64_t>(a->N) * a->H > (1LL << 30))
     return fail(KDA_ERR_SHAPE, "N*H = %lld exceeds the grid limit", static_cast<long long>(a->N) * a->H);
@@ -217,6 +229,8 @@ int validate(const KdaDecodeArgs* a, uint64_t wait_limit_ns, int32_t withhold_un
   p.queue = a->work_queue;
   p.withhold_unit = withhold_unit;
   p.wait_limit_ns = wait_limit_ns;
+  p.T = T;
+  p.src_slot = a->src_slot;
   return KDA_OK;
 }
 

@@ -52,6 +52,8 @@ struct Params {
   uint64_t wait_limit_ns;
   float eps, q_scale;
   int32_t* err;
+  int T;                     // tokens per sequence (multi-token kernel; 1 otherwise)
+  const int32_t* src_slot;   // multi-token kernel: source slot per sequence, or null
 };
 
 // Dynamic shared memory of one CTA (about 214 KB): the staged tiles and the

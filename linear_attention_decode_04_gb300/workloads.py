@@ -195,6 +195,114 @@ def make_inputs(spec: Spec, threads: int | None = None) -> Inputs:
                   norm_weight=nw, slot_idx=draw_slots(spec))
 
 
+# ------------------------------------------------- multi-token (speculative)
+
+@dataclass(frozen=True)
+class MultiSpec:
+    """One synthetic multi-token (speculative) decode batch: N sequences of
+    T = 1 + num_spec tokens, with the decode step's value distributions, one
+    row per token.  Slots: N distinct source slots, then N*T distinct
+    destination slots, all drawn from 1..slots-1 without repetition.
+    ``pad_seqs`` get source slot 0; ``absent`` lists (n, t) tokens whose
+    destination is 0; ``alias_last`` stores each sequence's last token back
+    into its own source slot."""
+    name: str
+    N: int
+    T: int
+    H: int
+    num_slots: int
+    seed: int
+    out_norm: bool = True
+    update_conv_state: bool = True
+    pad_seqs: tuple = ()
+    absent: tuple = ()
+    alias_last: bool = False
+    g_mode: str = "softplus"
+    eps: float = 1e-6
+
+    def rows_spec(self) -> Spec:
+        """The per-token draw as a decode Spec with N*T rows."""
+        return Spec(self.name, N=self.N * self.T, H=self.H, num_slots=self.num_slots, seed=self.seed,
+                    out_norm=self.out_norm, update_conv_state=self.update_conv_state,
+                    slots=(0,) * (self.N * self.T), g_mode=self.g_mode, eps=self.eps)
+
+
+@dataclass
+class MultiInputs:
+    spec: MultiSpec
+    qkv: np.ndarray          # uint16 [N*T, 3D]
+    conv_weight: np.ndarray  # f32 [3, 4, D]
+    conv_state: np.ndarray   # uint16 [slots, 3D, 3]
+    state: np.ndarray        # f32 [slots, H, 128, 128]
+    g: np.ndarray            # f32 [N*T, H, 128]
+    beta: np.ndarray         # uint16 [N*T, H]
+    gate: np.ndarray         # uint16 [N*T, D]
+    norm_weight: np.ndarray  # f32 [128]
+    src_slot: np.ndarray     # int32 [N]
+    dst_slots: np.ndarray    # int32 [N, T]
+    conv_bias: np.ndarray | None = None
+
+    @property
+    def N(self) -> int: return self.spec.N
+
+    @property
+    def T(self) -> int: return self.spec.T
+
+    @property
+    def H(self) -> int: return self.spec.H
+
+
+_T_MULTI = 200  # seed-stream tag of the multi-token slot draw
+
+
+def make_multi_inputs(spec: MultiSpec, threads: int | None = None) -> MultiInputs:
+    x = make_inputs(spec.rows_spec(), threads)
+    N, T = spec.N, spec.T
+    need = N + N * T
+    assert need <= spec.num_slots - 1, "not enough distinct slots"
+    perm = _rng(spec.seed, _T_MULTI).permutation(np.arange(1, spec.num_slots, dtype=np.int32))
+    src = perm[:N].copy()
+    dst = perm[N:need].reshape(N, T).copy()
+    if spec.alias_last:
+        dst[:, T - 1] = src
+    for n, t in spec.absent:
+        dst[n, t] = 0
+    for n in spec.pad_seqs:
+        src[n] = 0
+    return MultiInputs(spec=spec, qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state,
+                       state=x.state, g=x.g, beta=x.beta, gate=x.gate, norm_weight=x.norm_weight,
+                       src_slot=src, dst_slots=dst)
+
+
+def multi_algorithmic_bytes(spec: MultiSpec, src_slot: np.ndarray, dst_slots: np.ndarray) -> int:
+    """Bytes one multi-token launch must move at minimum: per active
+    (sequence, head) the source state and window read once, and per present
+    token its state (and, with the flag, window) written, its q/k/v inputs,
+    g, beta, gate and output; per zero output row (padding sequence or
+    absent token) 256 B per head; per launch the conv weight, norm weight and
+    slot indices."""
+    K = V = HEAD_DIM
+    H = spec.H
+    valid = lambda s: 0 < s < spec.num_slots  # noqa: E731
+    per_tok = 3 * K * 2 + K * 4 + 2 + V * 2 + (V * 2 if spec.out_norm else 0) + K * V * 4 \
+        + (3 * K * 3 * 2 if spec.update_conv_state else 0)
+    per_src = K * V * 4 + 3 * K * 3 * 2
+    total = 0
+    for n in range(spec.N):
+        present = [t for t in range(spec.T) if valid(src_slot[n]) and valid(dst_slots[n, t])]
+        if present:
+            total += per_src + len(present) * per_tok
+        total += (spec.T - len(present)) * V * 2
+    fixed = 3 * CONV_WIDTH * H * K * 4 + (V * 4 if spec.out_norm else 0) + 4 * spec.N * (spec.T + 1)
+    return H * total + fixed
+
+
+# The measured multi-token batch: the stack layer's shape with three draft
+# tokens per sequence (T = 4), 60 sequences and 4 padding sequences.
+MULTI_BENCH = MultiSpec("spec_n64_t4_h48_pool336_pad4", N=64, T=4, H=48, num_slots=336, seed=300,
+                        pad_seqs=(60, 61, 62, 63))
+
+
 # ----------------------------------------------------------------- prefill
 
 _T_PREFILL = 100  # seed-stream tags of the prefill inputs start here

@@ -491,7 +491,7 @@ static int multi_unit(const kda_oracle_multi_problem* p, int n, int h, double* w
     }
   const float* S_src = p->state + (((int64_t)src * H + h) * K) * V;
   for (int64_t e = 0; e < (int64_t)K * V; ++e) S[e] = (double)S_src[e];
-  const double scale = (p->q_scale != 0.0) ? p->q_scale : 1.0 / sqrt((double)K);
+  const double scale = (p->q_scale != 0.0) ? p->q_scale : 1.0 / sqrt((double)p->K);
 
   int oob = 0;
   for (int t = 0; t < T; ++t) {
@@ -507,7 +507,7 @@ static int multi_unit(const kda_oracle_multi_problem* p, int n, int h, double* w
       oob += dst >= p->num_slots;
       continue;
     }
-    /* 1. conv + SiLU with the window, then slide the window */
+    /* 1. conv + SiLU over the window and this token's input; the window slides */
     for (int c = 0, m = 0; c < 3; ++c) {
       double* dstv = (c == 0) ? qt : (c == 1) ? kt : vt;
       for (int j = 0; j < dims[c]; ++j, ++m) {
@@ -531,11 +531,11 @@ static int multi_unit(const kda_oracle_multi_problem* p, int n, int h, double* w
     if (p->fused_gate) {
       const double a_log = (double)p->A_log[h];
       for (int i = 0; i < K; ++i) {
-        double z = (double)p->g[(r * H + h) * K + i];
-        if (p->dt_bias) z += (double)p->dt_bias[(int64_t)h * K + i];
-        alpha[i] = exp(kda_oracle_kda_gate(z, a_log, p->lower_bound));
+        double zi = (double)p->g[(r * H + h) * K + i];
+        if (p->dt_bias) zi += (double)p->dt_bias[(int64_t)h * K + i];
+        alpha[i] = exp(kda_oracle_kda_gate(zi, a_log, p->lower_bound));
       }
-      beta = kda_oracle_sigmoid(beta);
+      beta = kda_oracle_sigmoid(beta); /* raw logit */
     } else {
       for (int i = 0; i < K; ++i) alpha[i] = exp((double)p->g[(r * H + h) * K + i]);
     }

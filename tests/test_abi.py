@@ -144,6 +144,11 @@ def test_host_validation_codes(lib):
     assert _call(lib, _args(qkv_row_stride=3 * 12 * 128 + 4)) == -3
     assert _call(lib, _args(state=0x10004)) == -3
     assert b"aligned" in lib.kda_last_error()
+    # multi-token (speculative) form
+    assert _call(lib, _args(tokens_per_seq=9)) == -2
+    assert _call(lib, _args(tokens_per_seq=-1)) == -2
+    assert _call(lib, _args(tokens_per_seq=4, src_slot=0x10002)) == -3
+    assert _call(lib, _args(tokens_per_seq=4, N=0)) == 0
     assert lib.kda_status_string(-3).decode().startswith("pointer")
 
 
