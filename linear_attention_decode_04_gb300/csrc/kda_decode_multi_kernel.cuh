@@ -4,43 +4,40 @@
 // wrappers it uses.
 //
 // A unit is one (sequence n, head h) with T = 1 + num_spec tokens.  Its
-// source state tile (64 KiB) and conv window are streamed in once; the state
-// then stays in the consumers' registers from token to token (after a
-// token's rank-1 update the registers hold exactly the state the next token
-// decays), and after every present token the updated tile is written into
-// the stage and bulk-stored to that token's destination slot, the window
-// likewise.  Per unit: 64 KiB read, 64 KiB written per present token.
+// source state tile (64 KiB) and conv window are streamed in once.  The
+// consumers first do everything that does not depend on the state for all
+// present tokens at once (conv + SiLU, decays, L2 norms, the window after
+// every token, stored straight to that token's slot), then run the
+// recurrence token by token with the state in registers: one pass over the
+// registers applies token m-1's rank-1 update, writes that state into the
+// stage for the bulk store to token m-1's slot, and applies token m's decay
+// and matvecs.  Per unit: 64 KiB read, 64 KiB written per present token.
 #pragma once
 
 #include "kda_decode_kernel.cuh"
 
 namespace {
 
-// Global -> shared bulk copy without a cache hint (data every CTA reuses).
-__device__ __forceinline__ void bulk_load_plain(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
 constexpr int kMaxT = KDA_MAX_TOKENS_PER_SEQ;
 constexpr int kMStages = 2;           // units in flight per CTA (one computing, one loading)
-constexpr int kMInfo = 4 + kMaxT;     // src, n (-1: no more units), h, withheld, dst[kMaxT]
+// per-stage info: src, n (-1: no more units), h, withheld, dst[kMaxT],
+// number of present tokens, present token indices[kMaxT]
+constexpr int kMInfo = 5 + 2 * kMaxT;
+constexpr int kMiDst = 4, kMiNp = 4 + kMaxT, kMiPt = 5 + kMaxT;
 
-// Dynamic shared memory of one CTA (about 188 KB).
+// Dynamic shared memory of one CTA (about 180 KB).
 struct __align__(128) MSmem {
   float tile[kMStages][kDim * kDim];
-  uint16_t cs[kMStages][2][3][kDim * (kWidth - 1)];  // the sliding window (two buffers), in the pool's layout
-  float w[kMStages][3][kWidth][kDim];  // the head's conv taps
-  float b[kMStages][3][kDim];          // and conv bias (zero without one)
+  uint16_t cs[kMStages][3][kDim * (kWidth - 1)];  // the source window, in the pool's layout
   uint16_t x[kMStages][kMaxT][3][kDim];
   float g[kMStages][kMaxT][kDim];
   uint16_t gate[kMStages][kMaxT][kDim];
-  float q[kDim], v[kDim], alpha[kDim];
-  float k[2][kDim];  // by token parity: the rank-1 update of a token reads its k~ while the next token's is written
+  // per present token m of the unit being computed
+  float q[kMaxT][kDim], k[kMaxT][kDim], v[kMaxT][kDim], alpha[kMaxT][kDim];
+  float4 coef[kMaxT];  // rq, rk, m = (|k~|^2 + 1e-6 - beta q~.k~) rk^2, beta (q^.k^)
+  float beta[kMaxT];
   float red[2][kConsumerWarps][kDim];
   float delta[kDim];
-  float4 part[kConsumerWarps];
   float osum[4];
   int info[kMStages][kMInfo];
   unsigned long long ready[kMStages];    // info of the stage is written (producer)
@@ -116,42 +113,33 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
       S.info[st][3] = (u == p.withhold_unit);
       const int32_t* row = p.slot_idx + static_cast<int64_t>(n) * T;
       S.info[st][0] = p.src_slot ? __ldg(p.src_slot + n) : __ldg(row);
-      for (int t = 0; t < T; ++t) S.info[st][4 + t] = __ldg(row + t);
+      int np = 0;
+      for (int t = 0; t < T; ++t) {
+        const int dst = __ldg(row + t);
+        S.info[st][kMiDst + t] = dst;
+        if (valid(dst)) S.info[st][kMiPt + np++] = t;
+      }
+      S.info[st][kMiNp] = np;
     };
-    auto n_present = [&](int st) {
-      int c = 0;
-      for (int t = 0; t < T; ++t) c += valid(S.info[st][4 + t]);
-      return c;
-    };
+    auto n_present = [&](int st) { return S.info[st][kMiNp]; };
     auto active = [&](int st) { return valid(S.info[st][0]) && n_present(st) > 0; };
     const uint32_t tok_bytes = 3 * kXSliceBytes + kDim * 4 + (kOutNorm ? kXSliceBytes : 0);
-    const uint32_t head_bytes = 3 * kWidth * kDim * 4 + (p.conv_b ? 3 * kDim * 4 : 0);
-    auto unit_bytes = [&](int st) {
-      return kTileBytes + 3 * kCsSliceBytes + head_bytes + tok_bytes * n_present(st);
-    };
+    auto unit_bytes = [&](int st) { return kTileBytes + 3 * kCsSliceBytes + tok_bytes * n_present(st); };
     // The source tile and window.
     auto load_src = [&](int st) {
       const int h = S.info[st][2], src = S.info[st][0];
       const uint32_t full = smem_addr(&S.full[st]);
       bulk_load(smem_addr(S.tile[st]), p.state + (static_cast<int64_t>(src) * p.H + h) * (kDim * kDim), kTileBytes,
                 full, policy);
-      // the head's conv taps and bias (L2-resident, shared by all sequences)
-      for (int c = 0; c < 3; ++c) {
-        for (int k = 0; k < kWidth; ++k)
-          bulk_load_plain(smem_addr(S.w[st][c][k]), p.conv_w + (c * kWidth + k) * D + static_cast<int64_t>(h) * kDim,
-                          kDim * 4, full);
-        if (p.conv_b)
-          bulk_load_plain(smem_addr(S.b[st][c]), p.conv_b + c * D + static_cast<int64_t>(h) * kDim, kDim * 4, full);
-      }
       for (int c = 0; c < 3; ++c) {
         if (!p.conv_sd) {
-          bulk_load(smem_addr(S.cs[st][0][c]),
+          bulk_load(smem_addr(S.cs[st][c]),
                     p.conv_state +
                         (static_cast<int64_t>(src) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1),
                     kCsSliceBytes, full, policy);
         } else {
           for (int k = 0; k < kWidth - 1; ++k)
-            bulk_load(smem_addr(S.cs[st][0][c] + k * kDim),
+            bulk_load(smem_addr(S.cs[st][c] + k * kDim),
                       p.conv_state + (static_cast<int64_t>(src) * (kWidth - 1) + k) * 3 * D + c * D +
                           static_cast<int64_t>(h) * kDim,
                       kXSliceBytes, full, policy);
@@ -162,8 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     auto load_tokens = [&](int st) {
       const int n = S.info[st][1], h = S.info[st][2];
       const uint32_t full = smem_addr(&S.full[st]);
-      for (int t = 0; t < T; ++t) {
-        if (!valid(S.info[st][4 + t])) continue;
+      for (int m = 0; m < n_present(st); ++m) {
+        const int t = S.info[st][kMiPt + m];
         const int64_t row = static_cast<int64_t>(n) * T + t;
         for (int c = 0; c < 3; ++c)
           bulk_load(smem_addr(S.x[st][t][c]), p.qkv + row * p.qkv_stride + c * D + static_cast<int64_t>(h) * kDim,
@@ -230,9 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
       if (units[st] < 0) break;  // the end-of-work sentinel (or nothing) is here
       if (active(st) && !S.info[st][3]) {
         const int h = S.info[st][2];
-        for (int t = 0; t < T; ++t) {
-          const int dst = S.info[st][4 + t];
-          if (!valid(dst)) continue;
+        for (int m = 0; m < n_present(st); ++m) {
+          const int dst = S.info[st][kMiDst + S.info[st][kMiPt + m]];
           ok = mbar_wait_bounded(smem_addr(&S.written[st]), wpar[st] & 1u, p.wait_limit_ns);
           if (!ok) break;
           ++wpar[st];
@@ -280,18 +267,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     const bool have_info = mbar_wait_bounded(smem_addr(&S.ready[st]), parity, p.wait_limit_ns);
     int n = -1, h = 0;
     bool ok = have_info;
-    float gate_a = 0.0f, gate_bias = 0.0f;  // fused-gate parameters of key channel tid - 128
     if (have_info) {
       n = S.info[st][1];
       h = S.info[st][2];
-      if (n >= 0) {
-        if (p.fused_gate && tid >= kDim) {
-          gate_a = expf(__ldg(p.A_log + h));
-          if (p.dt_bias) gate_bias = __ldg(p.dt_bias + static_cast<int64_t>(h) * kDim + (tid - kDim));
-        }
-        ok = mbar_wait_bounded(smem_addr(&S.full[st]), parity, p.wait_limit_ns);
-      }
+      if (n >= 0) ok = mbar_wait_bounded(smem_addr(&S.full[st]), parity, p.wait_limit_ns);
     }
+    // Agreement to go on; also the barrier that ends every use of the
+    // previous unit's per-token scratch.
     if (consumer_any(!ok || S.abort)) {
       if (tid == 0) {
         flag_error(p, KDA_DEVERR_TIMEOUT);
@@ -303,81 +285,56 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     const int src = S.info[st][0];
     const bool src_ok = valid(src);
     if (src >= p.num_slots && tid == 0) flag_error(p, KDA_DEVERR_SLOT_RANGE);
-    bool aborted = false;
-    int wb = 0;  // window buffer holding the current window
+    // Padding sequence or absent tokens: zero output rows, no state.
     for (int t = 0; t < T; ++t) {
-      const int dst = S.info[st][4 + t];
-      const int64_t row = static_cast<int64_t>(n) * T + t;
-      uint16_t* out_row = p.out + row * p.out_stride + static_cast<int64_t>(h) * kDim;
-      // Padding sequence or absent token: zero output, no state.
-      if (!src_ok || !valid(dst)) {
-        if (tid < kDim * 2 / 16) reinterpret_cast<uint4*>(out_row)[tid] = make_uint4(0, 0, 0, 0);
-        if (src_ok && dst >= p.num_slots && tid == 0) flag_error(p, KDA_DEVERR_SLOT_RANGE);
-        continue;
-      }
-      const int kb = wb;  // k~ buffer of this token
-      float beta = 0.0f;
-      if (tid < kDim) {
-        const float b = bf16_to_f32(__ldg(p.beta + row * p.H + h));
-        beta = p.fused_gate ? 1.0f / (1.0f + expf(-b)) : b;
-      }
-      // The window after this token (oldest tap dropped, the input appended;
-      // bit patterns) goes into the other window buffer and, with the flag,
-      // to this token's destination slot.
-      if (tid < 3 * kCsU4) {
-        const int c = tid / kCsU4, e = tid - c * kCsU4;
-        const uint16_t* cw = S.cs[st][wb][c];
-        uint4 wnew;
-        if (p.conv_sd) {
-          const int k = e >> 4, q = e & 15;
-          wnew = (k < kWidth - 2) ? reinterpret_cast<const uint4*>(cw + (k + 1) * kDim)[q]
-                                  : reinterpret_cast<const uint4*>(S.x[st][t][c])[q];
-        } else {
-          uint16_t v8[8];
+      const int dst = S.info[st][kMiDst + t];
+      if (src_ok && valid(dst)) continue;
+      uint16_t* out_row = p.out + (static_cast<int64_t>(n) * T + t) * p.out_stride + static_cast<int64_t>(h) * kDim;
+      if (tid < kDim * 2 / 16) reinterpret_cast<uint4*>(out_row)[tid] = make_uint4(0, 0, 0, 0);
+      if (src_ok && dst >= p.num_slots && tid == 0) flag_error(p, KDA_DEVERR_SLOT_RANGE);
+    }
+    const int np = src_ok ? S.info[st][kMiNp] : 0;
+    if (np == 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&S.done[st]));
+      continue;
+    }
+    const int* pt = &S.info[st][kMiPt];  // present token indices
+
+    // ---- state-independent work of every present token.
+    // Tap i of channel j along the sequence: i < 3 the source window, else
+    // the input of present token i - 3.
+    const int cs_j = p.conv_sd ? 1 : kWidth - 1, cs_t = p.conv_sd ? kDim : 1;
+    {
+      const int c = tid >> 7, j = tid & (kDim - 1);
+      const int64_t wbase = static_cast<int64_t>(h) * kDim + j;
+      float wq[kWidth], wv[kWidth];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int pos = e * 8 + i, j = pos / 3, k = pos - 3 * j;
-            v8[i] = (k < kWidth - 2) ? cw[3 * j + k + 1] : S.x[st][t][c][j];
-          }
-          wnew.x = v8[0] | (static_cast<uint32_t>(v8[1]) << 16);
-          wnew.y = v8[2] | (static_cast<uint32_t>(v8[3]) << 16);
-          wnew.z = v8[4] | (static_cast<uint32_t>(v8[5]) << 16);
-          wnew.w = v8[6] | (static_cast<uint32_t>(v8[7]) << 16);
-        }
-        reinterpret_cast<uint4*>(S.cs[st][wb ^ 1][c])[e] = wnew;
-        if (kUpdateConv) {
-          uint4* dstp;
-          if (p.conv_sd) {
-            const int k = e >> 4, q = e & 15;
-            dstp = reinterpret_cast<uint4*>(p.conv_state + (static_cast<int64_t>(dst) * (kWidth - 1) + k) * 3 * D +
-                                            c * D + static_cast<int64_t>(h) * kDim) + q;
-          } else {
-            dstp = reinterpret_cast<uint4*>(
-                       p.conv_state +
-                       (static_cast<int64_t>(dst) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1)) + e;
-          }
-          *dstp = wnew;
-        }
+      for (int k = 0; k < kWidth; ++k) wq[k] = __ldg(p.conv_w + (c * kWidth + k) * D + wbase);
+      const float bq = p.conv_b ? __ldg(p.conv_b + c * D + wbase) : 0.0f;
+      float bv = 0.0f, gate_a = 0.0f, gate_bias = 0.0f;
+      if (tid < kDim) {
+#pragma unroll
+        for (int k = 0; k < kWidth; ++k) wv[k] = __ldg(p.conv_w + (2 * kWidth + k) * D + wbase);
+        if (p.conv_b) bv = __ldg(p.conv_b + 2 * D + wbase);
+      } else if (p.fused_gate) {
+        gate_a = expf(__ldg(p.A_log + h));
+        if (p.dt_bias) gate_bias = __ldg(p.dt_bias + wbase);
       }
-      // Conv (4 taps) + SiLU on the 384 q|k|v channels; decay alpha = exp(g).
-      {
-        const int c = tid >> 7, j = tid & (kDim - 1);
-        const int cs_j = p.conv_sd ? 1 : kWidth - 1, cs_t = p.conv_sd ? kDim : 1;
-        const uint16_t* cs = S.cs[st][wb][c] + cs_j * j;
-        float y = p.conv_b ? S.b[st][c][j] : 0.0f;
-        y = fmaf(S.w[st][c][0][j], bf16_to_f32(cs[0 * cs_t]), y);
-        y = fmaf(S.w[st][c][1][j], bf16_to_f32(cs[1 * cs_t]), y);
-        y = fmaf(S.w[st][c][2][j], bf16_to_f32(cs[2 * cs_t]), y);
-        y = fmaf(S.w[st][c][3][j], bf16_to_f32(S.x[st][t][c][j]), y);
-        (c == 0 ? S.q : S.k[kb])[j] = y / (1.0f + expf(-y));
+      auto tap = [&](int cc, int i) -> float {
+        return bf16_to_f32(i < kWidth - 1 ? S.cs[st][cc][cs_j * j + cs_t * i] : S.x[st][pt[i - (kWidth - 1)]][cc][j]);
+      };
+      for (int m = 0; m < np; ++m) {
+        const int t = pt[m];
+        float y = bq;
+#pragma unroll
+        for (int k = 0; k < kWidth; ++k) y = fmaf(wq[k], tap(c, m + k), y);
+        (c == 0 ? S.q[m] : S.k[m])[j] = y / (1.0f + expf(-y));
         if (tid < kDim) {
-          const uint16_t* csv = S.cs[st][wb][2] + cs_j * j;
-          float yv = p.conv_b ? S.b[st][2][j] : 0.0f;
-          yv = fmaf(S.w[st][2][0][j], bf16_to_f32(csv[0 * cs_t]), yv);
-          yv = fmaf(S.w[st][2][1][j], bf16_to_f32(csv[1 * cs_t]), yv);
-          yv = fmaf(S.w[st][2][2][j], bf16_to_f32(csv[2 * cs_t]), yv);
-          yv = fmaf(S.w[st][2][3][j], bf16_to_f32(S.x[st][t][2][j]), yv);
-          S.v[j] = yv / (1.0f + expf(-yv));
+          float yv = bv;
+#pragma unroll
+          for (int k = 0; k < kWidth; ++k) yv = fmaf(wv[k], tap(2, m + k), yv);
+          S.v[m][j] = yv / (1.0f + expf(-yv));
         } else {
           float g = S.g[st][t][j];
           if (p.fused_gate) {
@@ -389,93 +346,147 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
               g = -gate_a * sp;
             }
           }
-          S.alpha[j] = expf(g);
+          S.alpha[m][j] = expf(g);
         }
       }
-      const float gate_j = (kOutNorm && tid < kDim) ? bf16_to_f32(S.gate[st][t][tid]) : 0.0f;
-      consumer_sync();
-      wb ^= 1;
-
-      // Decay and partial column sums over this warp's 16 key rows of the
-      // stage tile: the source state for the first present token, afterwards
-      // the state the previous token wrote there (each warp reads back only
-      // rows it wrote itself; the store engine only reads them).
-      float4 a[kRowsPerWarp];
-      {
-        const float4* tile4 = reinterpret_cast<const float4*>(S.tile[st]);
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
+      if (tid < np) {  // beta of present token tid
+        const float b = bf16_to_f32(__ldg(p.beta + (static_cast<int64_t>(n) * T + pt[tid]) * p.H + h));
+        S.beta[tid] = p.fused_gate ? 1.0f / (1.0f + expf(-b)) : b;
       }
-      // alpha, k~, q~ of the warp's rows as float4 broadcasts, four rows at a time
+    }
+    // The window after each present token (taps m+1 .. m+3 of the sequence,
+    // bit patterns), stored to that token's slot.
+    if (kUpdateConv && tid < 3 * kCsU4) {
+      const int c = tid / kCsU4, e = tid - c * kCsU4;
+      for (int m = 0; m < np; ++m) {
+        const int dst = S.info[st][kMiDst + pt[m]];
+        uint4 wv4;
+        uint4* dstp;
+        if (p.conv_sd) {  // uint4 e: tap row e / 16, channels 8 (e % 16) .. + 7
+          const int k = e >> 4, q = e & 15, i = m + 1 + k;
+          wv4 = (i < kWidth - 1) ? reinterpret_cast<const uint4*>(S.cs[st][c] + i * kDim)[q]
+                                 : reinterpret_cast<const uint4*>(S.x[st][pt[i - (kWidth - 1)]][c])[q];
+          dstp = reinterpret_cast<uint4*>(p.conv_state + (static_cast<int64_t>(dst) * (kWidth - 1) + k) * 3 * D +
+                                          c * D + static_cast<int64_t>(h) * kDim) + q;
+        } else {  // uint4 e: 8 consecutive (channel, tap) elements
+          uint16_t v8[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const int pos = e * 8 + r, j = pos / 3, i = m + 1 + (pos - 3 * j);
+            v8[r] = (i < kWidth - 1) ? S.cs[st][c][3 * j + i] : S.x[st][pt[i - (kWidth - 1)]][c][j];
+          }
+          wv4.x = v8[0] | (static_cast<uint32_t>(v8[1]) << 16);
+          wv4.y = v8[2] | (static_cast<uint32_t>(v8[3]) << 16);
+          wv4.z = v8[4] | (static_cast<uint32_t>(v8[5]) << 16);
+          wv4.w = v8[6] | (static_cast<uint32_t>(v8[7]) << 16);
+          dstp = reinterpret_cast<uint4*>(
+                     p.conv_state +
+                     (static_cast<int64_t>(dst) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1)) + e;
+        }
+        *dstp = wv4;
+      }
+    }
+    consumer_sync();
+    // Per present token (warp m): |q~|^2, |k~|^2, q~.k~ in one fixed order
+    // (so q~.k~ equals |k~|^2 bit for bit when q~ equals k~), then the
+    // readout coefficients of the decode step's cancellation-safe form.
+    if (warp < np) {
+      const int m = warp;
+      const float4 q4 = reinterpret_cast<const float4*>(S.q[m])[lane];
+      const float4 k4 = reinterpret_cast<const float4*>(S.k[m])[lane];
+      float ssq = fmaf(q4.x, q4.x, fmaf(q4.y, q4.y, fmaf(q4.z, q4.z, q4.w * q4.w)));
+      float ssk = fmaf(k4.x, k4.x, fmaf(k4.y, k4.y, fmaf(k4.z, k4.z, k4.w * k4.w)));
+      float sqk = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, q4.w * k4.w)));
+      ssq = warp_sum(ssq);
+      ssk = warp_sum(ssk);
+      sqk = warp_sum(sqk);
+      if (lane == 0) {
+        const float beta = S.beta[m];
+        const float rq = scale / sqrtf(ssq + 1e-6f);
+        const float rk = 1.0f / sqrtf(ssk + 1e-6f);
+        S.coef[m] = make_float4(rq, rk, (fmaf(-beta, sqk, ssk) + 1e-6f) * (rk * rk), beta * sqk * rq * rk);
+      }
+    }
+    consumer_sync();
+
+    // ---- the recurrence, token by token, state in registers.
+    float4 a[kRowsPerWarp];
+    {
+      const float4* tile4 = reinterpret_cast<const float4*>(S.tile[st]);
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
+    }
+    float4* tile4w = reinterpret_cast<float4*>(S.tile[st]);
+    // Token m-1's rank-1 update S' = A + k^ delta^T, and its state into the
+    // stage for the bulk store to its slot.
+    auto update_and_write = [&](int mp) {
+      const float4 d = reinterpret_cast<const float4*>(S.delta)[lane];
+#pragma unroll
+      for (int r4 = 0; r4 < kRowsPerWarp / 4; ++r4) {
+        const float4 kt4 = reinterpret_cast<const float4*>(S.k[mp] + warp * kRowsPerWarp)[r4];
+        const float kt_4[4] = {kt4.x, kt4.y, kt4.z, kt4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * r4 + i;
+          a[r].x = fmaf(kt_4[i], d.x, a[r].x); a[r].y = fmaf(kt_4[i], d.y, a[r].y);
+          a[r].z = fmaf(kt_4[i], d.z, a[r].z); a[r].w = fmaf(kt_4[i], d.w, a[r].w);
+          tile4w[(warp * kRowsPerWarp + r) * 32 + lane] = a[r];
+        }
+      }
+      fence_proxy_async_smem();  // generic-proxy writes before the async-proxy store
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&S.written[st]));
+      if (st) ++wcnt1; else ++wcnt0;
+    };
+    bool aborted = false;
+    for (int m = 0; m < np; ++m) {
+      if (m > 0) update_and_write(m - 1);
+      // decay and partial column sums of token m over this warp's 16 rows
       float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int r4 = 0; r4 < kRowsPerWarp / 4; ++r4) {
-        const float4 al4 = reinterpret_cast<const float4*>(S.alpha + warp * kRowsPerWarp)[r4];
-        const float4 kt4 = reinterpret_cast<const float4*>(S.k[kb] + warp * kRowsPerWarp)[r4];
-        const float4 qt4 = reinterpret_cast<const float4*>(S.q + warp * kRowsPerWarp)[r4];
+        const float4 al4 = reinterpret_cast<const float4*>(S.alpha[m] + warp * kRowsPerWarp)[r4];
+        const float4 kt4 = reinterpret_cast<const float4*>(S.k[m] + warp * kRowsPerWarp)[r4];
+        const float4 qt4 = reinterpret_cast<const float4*>(S.q[m] + warp * kRowsPerWarp)[r4];
         const float al_4[4] = {al4.x, al4.y, al4.z, al4.w};
         const float kt_4[4] = {kt4.x, kt4.y, kt4.z, kt4.w};
         const float qt_4[4] = {qt4.x, qt4.y, qt4.z, qt4.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 4 * r4 + i;
-          const float al = al_4[i], kt = kt_4[i], qt = qt_4[i];
-          a[r].x *= al; a[r].y *= al; a[r].z *= al; a[r].w *= al;
-          u.x = fmaf(kt, a[r].x, u.x); u.y = fmaf(kt, a[r].y, u.y);
-          u.z = fmaf(kt, a[r].z, u.z); u.w = fmaf(kt, a[r].w, u.w);
-          w.x = fmaf(qt, a[r].x, w.x); w.y = fmaf(qt, a[r].y, w.y);
-          w.z = fmaf(qt, a[r].z, w.z); w.w = fmaf(qt, a[r].w, w.w);
+          a[r].x *= al_4[i]; a[r].y *= al_4[i]; a[r].z *= al_4[i]; a[r].w *= al_4[i];
+          u.x = fmaf(kt_4[i], a[r].x, u.x); u.y = fmaf(kt_4[i], a[r].y, u.y);
+          u.z = fmaf(kt_4[i], a[r].z, u.z); u.w = fmaf(kt_4[i], a[r].w, u.w);
+          w.x = fmaf(qt_4[i], a[r].x, w.x); w.y = fmaf(qt_4[i], a[r].y, w.y);
+          w.z = fmaf(qt_4[i], a[r].z, w.z); w.w = fmaf(qt_4[i], a[r].w, w.w);
         }
       }
       reinterpret_cast<float4*>(S.red[0][warp])[lane] = u;
       reinterpret_cast<float4*>(S.red[1][warp])[lane] = w;
-      {
-        const int i = warp * kRowsPerWarp + (lane & (kRowsPerWarp - 1));
-        const float qi = S.q[i], ki = S.k[kb][i];
-        float pqq = qi * qi, pkk = ki * ki, pqk = qi * ki;
-#pragma unroll
-        for (int off = kRowsPerWarp / 2; off > 0; off >>= 1) {
-          pqq += __shfl_xor_sync(0xffffffffu, pqq, off);
-          pkk += __shfl_xor_sync(0xffffffffu, pkk, off);
-          pqk += __shfl_xor_sync(0xffffffffu, pqk, off);
-        }
-        if (lane == 0) S.part[warp] = make_float4(pqq, pkk, pqk, 0.0f);
-      }
       consumer_sync();
 
-      // delta and the readout, in the decode step's cancellation-safe form.
+      // delta and the readout o = rq ((w~ - u~) + m u~) + beta (q^.k^) v
       float o = 0.0f;
       if (tid < kDim) {
-        const float4 pr = S.part[lane & (kConsumerWarps - 1)];
-        float ssq = pr.x, ssk = pr.y, sqk = pr.z;
-#pragma unroll
-        for (int off = kConsumerWarps / 2; off > 0; off >>= 1) {
-          ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
-          ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
-          sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
-        }
-        const float rq = scale / sqrtf(ssq + 1e-6f);
-        const float rk = 1.0f / sqrtf(ssk + 1e-6f);
+        const float4 cf = S.coef[m];  // rq, rk, m, beta (q^.k^)
         float ut = 0.0f, wt = 0.0f;
 #pragma unroll
         for (int r = 0; r < kConsumerWarps; ++r) {
           ut += S.red[0][r][tid];
           wt += S.red[1][r][tid];
         }
-        const float vj = S.v[tid];
-        const float dj = beta * (vj - rk * ut);
-        S.delta[tid] = rk * dj;
-        const float m = (fmaf(-beta, sqk, ssk) + 1e-6f) * (rk * rk);
-        const float bqk = beta * sqk * rq * rk;
-        o = fmaf(bqk, vj, rq * fmaf(m, ut, wt - ut));
+        const float vj = S.v[m][tid];
+        const float dj = S.beta[m] * (vj - cf.y * ut);
+        S.delta[tid] = cf.y * dj;  // the update adds k~ (rk delta)^T = k^ delta^T
+        o = fmaf(cf.w, vj, cf.x * fmaf(cf.z, ut, wt - ut));
         if (kOutNorm) {
           const float so = warp_sum(o * o);
           if (lane == 0) S.osum[warp] = so;
         }
       }
-      // The stage tile may be rewritten once the store of the tile written
-      // before it has read it out; every consumer agrees before going on
-      // (this vote is also the barrier that publishes delta).
+      // The stage tile is rewritten next (token m's state): the store of the
+      // tile written before has to have read it out.  Every consumer agrees
+      // before going on; this vote is also the barrier that publishes delta.
       const uint32_t wc = st ? wcnt1 : wcnt0;
       bool fok = true;
       if (wc > 0) fok = mbar_wait_bounded(smem_addr(&S.freed[st]), (wc - 1) & 1u, p.wait_limit_ns);
@@ -487,41 +498,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
         aborted = true;
         break;
       }
-
-      // S' = A + k^ delta^T, written into the stage for the bulk store to this
-      // token's slot (and for the next token).
-      const float4 d = reinterpret_cast<const float4*>(S.delta)[lane];
-      float4* tile4w = reinterpret_cast<float4*>(S.tile[st]);
-#pragma unroll
-      for (int r4 = 0; r4 < kRowsPerWarp / 4; ++r4) {
-        const float4 kt4 = reinterpret_cast<const float4*>(S.k[kb] + warp * kRowsPerWarp)[r4];
-        const float kt_4[4] = {kt4.x, kt4.y, kt4.z, kt4.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 4 * r4 + i;
-          const float kt = kt_4[i];
-          a[r].x = fmaf(kt, d.x, a[r].x); a[r].y = fmaf(kt, d.y, a[r].y);
-          a[r].z = fmaf(kt, d.z, a[r].z); a[r].w = fmaf(kt, d.w, a[r].w);
-          tile4w[(warp * kRowsPerWarp + r) * 32 + lane] = a[r];
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&S.written[st]));
-      if (st) ++wcnt1; else ++wcnt0;
-
+      // gated RMSNorm epilogue (or the raw readout) of token m
       if (tid < kDim) {
+        const int t = pt[m];
         float y = o;
         if (kOutNorm) {
           const float ss = (S.osum[0] + S.osum[1]) + (S.osum[2] + S.osum[3]);
           const float rr = 1.0f / sqrtf(ss * (1.0f / kDim) + p.eps);
-          y = o * rr * nw * (1.0f / (1.0f + expf(-gate_j)));
+          y = o * rr * nw * (1.0f / (1.0f + expf(-bf16_to_f32(S.gate[st][t][tid]))));
         }
-        out_row[tid] = f32_to_bf16(y);
+        p.out[(static_cast<int64_t>(n) * T + t) * p.out_stride + static_cast<int64_t>(h) * kDim + tid] = f32_to_bf16(y);
       }
     }
     if (aborted) break;
-    __syncwarp();
+    update_and_write(np - 1);
     if (lane == 0) mbar_arrive(smem_addr(&S.done[st]));
   }
 }
