@@ -48,13 +48,22 @@ struct DeviceInfo {
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[64];
 
+// Dynamic shared memory opt-in limit of one CTA on sm_103a.
+constexpr size_t kMaxDynSmem = 227 * 1024;
+static_assert(sizeof(Smem) <= kMaxDynSmem, "decode kernel shared memory");
+static_assert(sizeof(MSmemT<4>) <= kMaxDynSmem, "multi-token kernel shared memory (4 tokens)");
+static_assert(sizeof(MSmemT<kMaxT>) <= kMaxDynSmem, "multi-token kernel shared memory");
+
 template <bool kOutNorm, bool kUpdateConv>
 cudaError_t set_attrs() {
   cudaError_t e = cudaFuncSetAttribute(kda_decode_persistent_kernel<kOutNorm, kUpdateConv>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(Smem)));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(kda_decode_multi_kernel<kOutNorm, kUpdateConv>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(MSmem)));
+  e = cudaFuncSetAttribute(kda_decode_multi_kernel<kOutNorm, kUpdateConv, 4>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(MSmemT<4>)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kda_decode_multi_kernel<kOutNorm, kUpdateConv, kMaxT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(MSmemT<kMaxT>)));
 }
 
 // Once per device: SM count and the large dynamic shared-memory opt-in for
@@ -88,15 +97,17 @@ cudaError_t launch(const Params& p, int sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.total_units < sms ? p.total_units : sms));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = multi ? sizeof(MSmem) : sizeof(Smem);
+  const bool small_t = p.T <= 4;  // up to 4 tokens: two output buffers per unit
+  cfg.dynamicSmemBytes = !multi ? sizeof(Smem) : small_t ? sizeof(MSmemT<4>) : sizeof(MSmemT<kMaxT>);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = multi ? cudaLaunchKernelEx(&cfg, kda_decode_multi_kernel<kOutNorm, kUpdateConv>, p)
-                        : cudaLaunchKernelEx(&cfg, kda_decode_persistent_kernel<kOutNorm, kUpdateConv>, p);
+  cudaError_t e = !multi   ? cudaLaunchKernelEx(&cfg, kda_decode_persistent_kernel<kOutNorm, kUpdateConv>, p)
+                  : small_t ? cudaLaunchKernelEx(&cfg, kda_decode_multi_kernel<kOutNorm, kUpdateConv, 4>, p)
+                            : cudaLaunchKernelEx(&cfg, kda_decode_multi_kernel<kOutNorm, kUpdateConv, kMaxT>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -25,32 +25,49 @@ constexpr int kMStages = 2;           // units in flight per CTA (one computing,
 constexpr int kMInfo = 5 + 2 * kMaxT;
 constexpr int kMiDst = 4, kMiNp = 4 + kMaxT, kMiPt = 5 + kMaxT;
 
-// Dynamic shared memory of one CTA (about 180 KB).
-struct __align__(128) MSmem {
-  float tile[kMStages][kDim * kDim];
+// Dynamic shared memory of one CTA for up to kTMax tokens per sequence.
+// With kTMax <= 4 a spare tile gives every unit two output buffers: present
+// token m's state goes to the stage tile (m even) or the spare (m odd), so
+// the store of one token's tile runs while the next token's is written
+// (about 225 KB).  With more tokens per sequence only the stage tile is
+// used (about 186 KB).
+template <int kTMax>
+struct __align__(128) MSmemT {
+  static constexpr int kOutBufs = kTMax <= 4 ? 2 : 1;
+  static constexpr int kTiles = kMStages + kOutBufs - 1;  // stage tiles [0, 1], spare [2]
+  float tile[kTiles][kDim * kDim];
   uint16_t cs[kMStages][3][kDim * (kWidth - 1)];  // the source window, in the pool's layout
-  uint16_t x[kMStages][kMaxT][3][kDim];
-  float g[kMStages][kMaxT][kDim];
-  uint16_t gate[kMStages][kMaxT][kDim];
+  uint16_t x[kMStages][kTMax][3][kDim];
+  float g[kMStages][kTMax][kDim];
+  uint16_t gate[kMStages][kTMax][kDim];
   // per present token m of the unit being computed
-  float q[kMaxT][kDim], k[kMaxT][kDim], v[kMaxT][kDim], alpha[kMaxT][kDim];
-  float4 coef[kMaxT];  // rq, rk, m = (|k~|^2 + 1e-6 - beta q~.k~) rk^2, beta (q^.k^)
-  float beta[kMaxT];
+  float q[kTMax][kDim], k[kTMax][kDim], v[kTMax][kDim], alpha[kTMax][kDim];
+  float4 coef[kTMax];  // rq, rk, m = (|k~|^2 + 1e-6 - beta q~.k~) rk^2, beta (q^.k^)
+  float beta[kTMax];
   float red[2][kConsumerWarps][kDim];
   float delta[kDim];
   float osum[4];
   int info[kMStages][kMInfo];
-  unsigned long long ready[kMStages];    // info of the stage is written (producer)
-  unsigned long long full[kMStages];     // the unit's inputs have landed (producer + tx bytes)
-  unsigned long long done[kMStages];     // the consumers are finished with the unit (8 warps)
-  unsigned long long written[kMStages];  // a token's updated tile is in the stage (8 warps)
-  unsigned long long freed[kMStages];    // the store of that tile has read it out (producer)
+  unsigned long long ready[kMStages];   // info of the stage is written (producer)
+  unsigned long long full[kMStages];    // the unit's inputs have landed (producer + tx bytes)
+  unsigned long long done[kMStages];    // the consumers are finished with the unit (8 warps)
+  unsigned long long written[kTiles];   // a token's updated state is in the tile (8 warps)
+  unsigned long long freed[kTiles];     // the store of that tile has read it out (producer)
   volatile int abort;
 };
 
-template <bool kOutNorm, bool kUpdateConv>
+// Wait until at most N of this thread's most recent bulk store groups are
+// still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_pending() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <bool kOutNorm, bool kUpdateConv, int kTMax>
 __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
+  using MSmem = MSmemT<kTMax>;
+  constexpr int kOutBufs = MSmem::kOutBufs, kTiles = MSmem::kTiles;
   MSmem& S = *reinterpret_cast<MSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
@@ -62,8 +79,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
       mbar_init(smem_addr(&S.ready[s]), 1);
       mbar_init(smem_addr(&S.full[s]), 1);
       mbar_init(smem_addr(&S.done[s]), kConsumerWarps);
-      mbar_init(smem_addr(&S.written[s]), kConsumerWarps);
-      mbar_init(smem_addr(&S.freed[s]), 1);
+    }
+    for (int b = 0; b < kTiles; ++b) {
+      mbar_init(smem_addr(&S.written[b]), kConsumerWarps);
+      mbar_init(smem_addr(&S.freed[b]), 1);
     }
     S.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -73,6 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
   griddep_launch_dependents();
 
   auto valid = [&](int slot) { return slot > 0 && slot < p.num_slots; };
+  // output buffer of present token m of a unit in stage st
+  auto out_buf = [&](int st, int m) { return (kOutBufs == 2 && (m & 1)) ? kMStages : st; };
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -211,23 +232,40 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
 
     // Steady state: store each token's tile as the consumers hand it over,
     // then refill the stage with the unit after next.
-    uint32_t wpar[kMStages] = {0u, 0u};
+    uint32_t wpar0 = 0u, wpar1 = 0u, wpar2 = 0u;  // writes seen per output buffer
     bool ok = true;
     for (int it = 0; ok; ++it) {
       const int st = it % kMStages;
       if (units[st] < 0) break;  // the end-of-work sentinel (or nothing) is here
       if (active(st) && !S.info[st][3]) {
         const int h = S.info[st][2];
+        int pending = -1;  // buffer of the issued store not yet known to have read its tile
         for (int m = 0; m < n_present(st); ++m) {
           const int dst = S.info[st][kMiDst + S.info[st][kMiPt + m]];
-          ok = mbar_wait_bounded(smem_addr(&S.written[st]), wpar[st] & 1u, p.wait_limit_ns);
+          const int b = out_buf(st, m);
+          uint32_t& wp = (b == 0) ? wpar0 : (b == 1) ? wpar1 : wpar2;
+          ok = mbar_wait_bounded(smem_addr(&S.written[b]), wp & 1u, p.wait_limit_ns);
           if (!ok) break;
-          ++wpar[st];
-          bulk_store(p.state + (static_cast<int64_t>(dst) * p.H + h) * (kDim * kDim), smem_addr(S.tile[st]),
+          ++wp;
+          bulk_store(p.state + (static_cast<int64_t>(dst) * p.H + h) * (kDim * kDim), smem_addr(S.tile[b]),
                      kTileBytes, policy);
           bulk_commit();
+          // with two output buffers the previous store may finish reading
+          // while this one starts; with one, each must finish first
+          if (kOutBufs == 2) {
+            if (pending >= 0) {
+              bulk_wait_read_pending<1>();
+              mbar_arrive(smem_addr(&S.freed[pending]));
+            }
+            pending = b;
+          } else {
+            bulk_wait_read_all();
+            mbar_arrive(smem_addr(&S.freed[b]));
+          }
+        }
+        if (pending >= 0) {
           bulk_wait_read_all();
-          mbar_arrive(smem_addr(&S.freed[st]));
+          mbar_arrive(smem_addr(&S.freed[pending]));
         }
       }
       if (!ok) break;
@@ -260,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
   griddep_wait();
   const float scale = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
   const float nw = (kOutNorm && tid < kDim) ? __ldg(p.norm_w + tid) : 0.0f;
-  uint32_t wcnt0 = 0u, wcnt1 = 0u;  // updated tiles written into stage 0 / 1 so far
+  uint32_t wcnt0 = 0u, wcnt1 = 0u, wcnt2 = 0u;  // states written into each output buffer so far
   for (int it = 0;; ++it) {
     const int st = it % kMStages;
     const uint32_t parity = (it / kMStages) & 1;
@@ -416,10 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
 #pragma unroll
       for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
     }
-    float4* tile4w = reinterpret_cast<float4*>(S.tile[st]);
-    // Token m-1's rank-1 update S' = A + k^ delta^T, and its state into the
-    // stage for the bulk store to its slot.
+    // Token mp's rank-1 update S' = A + k^ delta^T, and its state into its
+    // output buffer for the bulk store to its slot.
     auto update_and_write = [&](int mp) {
+      const int b = out_buf(st, mp);
+      float4* tile4w = reinterpret_cast<float4*>(S.tile[b]);
       const float4 d = reinterpret_cast<const float4*>(S.delta)[lane];
 #pragma unroll
       for (int r4 = 0; r4 < kRowsPerWarp / 4; ++r4) {
@@ -435,8 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
       }
       fence_proxy_async_smem();  // generic-proxy writes before the async-proxy store
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&S.written[st]));
-      if (st) ++wcnt1; else ++wcnt0;
+      if (lane == 0) mbar_arrive(smem_addr(&S.written[b]));
+      if (b == 0) ++wcnt0; else if (b == 1) ++wcnt1; else ++wcnt2;
     };
     bool aborted = false;
     for (int m = 0; m < np; ++m) {
@@ -484,12 +523,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
           if (lane == 0) S.osum[warp] = so;
         }
       }
-      // The stage tile is rewritten next (token m's state): the store of the
-      // tile written before has to have read it out.  Every consumer agrees
-      // before going on; this vote is also the barrier that publishes delta.
-      const uint32_t wc = st ? wcnt1 : wcnt0;
+      // Token m's state goes into its output buffer next: the store of what
+      // was written there before has to have read it out.  Every consumer
+      // agrees before going on; this vote is also the barrier that publishes
+      // delta.
+      const int bn = out_buf(st, m);
+      const uint32_t wc = (bn == 0) ? wcnt0 : (bn == 1) ? wcnt1 : wcnt2;
       bool fok = true;
-      if (wc > 0) fok = mbar_wait_bounded(smem_addr(&S.freed[st]), (wc - 1) & 1u, p.wait_limit_ns);
+      if (wc > 0) fok = mbar_wait_bounded(smem_addr(&S.freed[bn]), (wc - 1) & 1u, p.wait_limit_ns);
       if (consumer_any(!fok || S.abort)) {
         if (tid == 0) {
           flag_error(p, KDA_DEVERR_TIMEOUT);
