@@ -674,7 +674,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cfg3", action="store_true",
                     help="skip the N=256/H=96 single-launch and the multi-token measurements in the headline line")
-    ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill", "spec"),
+    ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill", "spec",
+                                       "configs"),
                     default="stack69",
                     help="stack69: the headline 69-layer graph step; layer / roofline: one "
                          "launch configuration timed on its own (profiling aid); prefill: the "
@@ -688,6 +689,19 @@ def main(argv=None):
         res = run_chunk_metadata(args)
     elif args.case == "prefill":
         res = run_prefill(args)
+    elif args.case == "configs":
+        import torch
+
+        from linear_attention_decode_04_gb300 import workloads as W
+        torch.cuda.set_device(0)
+        rows = []
+        with ClockSampler(0) as clk:
+            for spec in W.SPECS.values():
+                rows.append(single_launch(torch.device("cuda", 0), spec, args.warmup, max(args.steps, 50)))
+        res = {"mode": "configs", "configs": rows, "clocks": clk.summary(), "steps": args.steps,
+               "warmup": args.warmup,
+               "note": "each decode workload as one launch replayed from a CUDA graph; the state evolves "
+                       "across replays; configurations whose pools fit in L2 read part of them from L2"}
     elif args.case == "spec":
         import torch
 

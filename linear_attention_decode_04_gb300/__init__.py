@@ -3,8 +3,9 @@ chunked varlen prefill.
 
 The compute lives in one hand-written CUDA library (``csrc/``) behind a C ABI
 (``include/kda_decode.h``); ``kda_decode`` here only marshals torch tensors
-into that call.  The library is loaded on first use and a missing or stale
-build raises instead of falling back to anything else.
+into that call.  The library is loaded on first use; a missing library, or
+one built for another ABI version, raises instead of falling back to anything
+else (``build.build()`` recompiles any source newer than its object).
 """
 from .binding import (  # noqa: F401
     KDA_EARLY_PREFETCH,
@@ -13,6 +14,7 @@ from .binding import (  # noqa: F401
     KDA_OUT_NORM,
     KDA_UPDATE_CONV_STATE,
     KdaDecodeCall,
+    MAX_TOKENS_PER_SEQ,
     KdaPrefillCall,
     KdaError,
     kda_chunk_metadata,

@@ -985,15 +985,19 @@ extern "C" int kda_prefill_longest_first(const int32_t* cu_seqlens, int32_t B, i
   kda_internal_clear_error();
   if (B < 0) return kda_internal_fail(KDA_ERR_SHAPE, "B=%d", B);
   if (B > 0 && (!cu_seqlens || !order)) return kda_internal_fail(KDA_ERR_NULLPTR, "cu_seqlens or order is NULL");
-  // lengths taken in the comparison, so nothing here allocates; the GNU
-  // std::stable_sort asks for its buffer without throwing and merges in
-  // place when it gets none, so no exception crosses the C boundary
+  // Lengths are taken in the comparison and the sort is std::sort, which
+  // works in place: nothing here allocates and no exception can cross the C
+  // boundary.  Ties are broken by index, so the order is unique and equals
+  // the stable one (equal lengths in index order).
   const auto len = [cu_seqlens](int32_t i) {
     const int64_t n = static_cast<int64_t>(cu_seqlens[i + 1]) - cu_seqlens[i];
     return n < 0 ? int64_t{0} : n;
   };
   for (int32_t i = 0; i < B; ++i) order[i] = i;
-  std::stable_sort(order, order + B, [&](int32_t x, int32_t y) { return len(x) > len(y); });
+  std::sort(order, order + B, [&](int32_t x, int32_t y) {
+    const int64_t lx = len(x), ly = len(y);
+    return lx > ly || (lx == ly && x < y);
+  });
   return KDA_OK;
 }
 
