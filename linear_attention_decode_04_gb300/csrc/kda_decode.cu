@@ -88,8 +88,21 @@ cudaError_t device_setup(int* sms) {
   return cudaSuccess;
 }
 
+// With a work queue, each CTA takes all but about its last kQueueTailUnits
+// units statically and draws only those last ones from the queue: the
+// static part needs no atomics, and the queue still evens out the CTAs' end
+// times (at least the first ring of every CTA is static).
+constexpr int kQueueTailUnits = 2;
+
 template <bool kOutNorm, bool kUpdateConv>
-cudaError_t launch(const Params& p, int sms, cudaStream_t stream) {
+cudaError_t launch(const Params& p_in, int sms, cudaStream_t stream) {
+  Params p = p_in;
+  {
+    const int G = p.total_units < sms ? p.total_units : sms;
+    const int ring = (p.T > 1 || p.src_slot != nullptr) ? kMStages : kStages;
+    const int per_cta = p.total_units / G - kQueueTailUnits;
+    p.static_units = per_cta > ring ? per_cta : ring;
+  }
   // Every launch is a programmatic dependent launch: the CTAs may become
   // resident while the previous kernel in the stream drains, and wait for
   // it (griddepcontrol.wait) before touching its results.

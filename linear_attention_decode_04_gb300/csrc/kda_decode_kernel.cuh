@@ -48,6 +48,7 @@ struct Params {
   const float* dt_bias;
   float lower_bound;
   int* queue;          // work queue int32[2] (next dynamic unit, finished CTAs) or null
+  int static_units;    // with a queue: units each CTA takes statically before drawing from it
   int withhold_unit;   // wait-path test: this unit's load is never signalled (-1: none)
   uint64_t wait_limit_ns;
   float eps, q_scale;
@@ -234,11 +235,12 @@ __device__ __forceinline__ UnitInputs load_unit_inputs(const Params& p, int n, i
 }
 
 // Persistent kernel, one CTA per SM.  A unit is one (row n, head h) =
-// unit index n*H + h.  Each CTA takes its first kStages units statically
-// (blockIdx.x + k*gridDim.x, so they can be prefetched before the previous
-// kernel finishes); the rest come from the work queue when one is given
-// (an atomic counter: CTAs that run ahead take more units, so every CTA
-// finishes at nearly the same time), else continue the static stride.
+// unit index n*H + h.  Each CTA takes units statically (blockIdx.x +
+// k*gridDim.x; the first ones can be prefetched before the previous kernel
+// finishes).  With a work queue only the first p.static_units are static
+// and the rest come from the queue (an atomic counter: CTAs that run ahead
+// take more units, so every CTA finishes at nearly the same time); without
+// one the static stride covers everything.
 // Warp 8 is the producer: for each unit it publishes (slot, n, h) on the
 // stage's `ready` barrier, streams the 64 KiB state tile and the unit's small
 // inputs into the stage with bulk copies (`full` barrier), and once the
@@ -315,10 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     int k_static = 0;  // static units taken so far
     auto next_unit = [&]() -> int {
       int u;
-      if (k_static < kStages || p.queue == nullptr)
+      if (k_static < p.static_units || p.queue == nullptr)
         u = blockIdx.x + (k_static++) * G;
       else
-        u = kStages * G + atomicAdd(p.queue, 1);
+        u = p.static_units * G + atomicAdd(p.queue, 1);
       return u < p.total_units ? u : -1;
     };
 

@@ -116,10 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     };
     auto next_unit = [&]() -> int {
       int u;
-      if (k_static < kMStages || p.queue == nullptr)
+      if (k_static < p.static_units || p.queue == nullptr)
         u = blockIdx.x + (k_static++) * G;
       else
-        u = kMStages * G + atomicAdd(p.queue, 1);
+        u = p.static_units * G + atomicAdd(p.queue, 1);
       if (u >= p.total_units) {
         finish_queue();
         return -1;

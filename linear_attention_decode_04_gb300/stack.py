@@ -48,7 +48,8 @@ class DecodeStack:
     kernel drains (KDA_EARLY_PREFETCH)."""
 
     def __init__(self, layers: list[dict], eps: float = 1e-6, out_norm: bool = True,
-                 update_conv_state: bool = True, host_token_io: bool = False):
+                 update_conv_state: bool = True, host_token_io: bool = False,
+                 work_queue: bool | None = None):
         self.layers = layers
         ptrs = [L["state"].data_ptr() for L in layers]
         if len(set(ptrs)) != len(ptrs):
@@ -64,7 +65,8 @@ class DecodeStack:
         dev = layers[0]["state"].device
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         units = max(int(L["qkv"].shape[0]) * int(L["state"].shape[1]) for L in layers)
-        self.queue = (torch.zeros(2, dtype=torch.int32, device=dev) if units >= 64 * sms else None)
+        use_queue = (units >= 64 * sms) if work_queue is None else bool(work_queue)
+        self.queue = torch.zeros(2, dtype=torch.int32, device=dev) if use_queue else None
         self.calls = [
             KdaDecodeCall(L["qkv"], L["conv_weight"], L["conv_state"], L["state"], L["g"], L["beta"],
                           L["slot_idx"], L["out"], gate=L.get("gate"),
