@@ -624,6 +624,70 @@ def run_chunk_metadata(args) -> dict:
             "bytes": 257 * 4 + 257 * 8 + total * 8, "steps": args.steps, "warmup": args.warmup}
 
 
+def timeline_summary(rec: np.ndarray, ctas: int) -> dict:
+    """Per-launch figures from the decode kernel's per-CTA records of one
+    step (records sorted by start: each launch's CTAs all start before any
+    CTA of the next launch), medians over the launches after the first; us."""
+    rec = rec[np.argsort(rec[:, 2])].astype(np.float64)
+    per = []
+    for ell in range(len(rec) // ctas):
+        r = rec[ell * ctas:(ell + 1) * ctas]
+        start, first, end, units, comp, wait = (r[:, i] for i in range(2, 8))
+        d = {"duration": end.max() - start.min(), "first_unit_ready_after_cta_start": np.median(first - start),
+             "end_spread": end.max() - end.min(), "tail_after_median_end": end.max() - np.median(end),
+             "consumer_compute_per_unit": comp.sum() / units.sum(),
+             "consumer_wait_per_unit": wait.sum() / units.sum(),
+             "units_per_cta_min": units.min(), "units_per_cta_max": units.max()}
+        if ell > 0:
+            prev_end = rec[(ell - 1) * ctas:ell * ctas, 4].max()
+            d["first_unit_ready_after_previous_launch_end"] = np.median(first) - prev_end
+        per.append(d)
+    out = {}
+    for k in per[-1]:
+        vals = [p[k] for p in per[1:] if k in p]
+        scale = 1.0 if k.startswith("units") else 1e-3
+        out[k] = round(float(np.median(vals)) * scale, 3)
+    out["launches"] = len(per)
+    return out
+
+
+def run_timeline(args) -> dict:
+    """One 69-layer graph step with the timeline build of the library: the
+    per-CTA records summarised per launch, for the dynamic (work queue) and
+    the static schedule.  The recording itself slows the kernel slightly;
+    the step times here are not bench figures."""
+    import torch
+
+    from linear_attention_decode_04_gb300 import binding
+    from linear_attention_decode_04_gb300 import workloads as W
+    from linear_attention_decode_04_gb300.stack import DecodeStack
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    layers, _, spec, _ = build_stack(dev, W.STACK_LAYERS, 0)
+    res = {"mode": "timeline", "workload": W.STACK_LAYER.name, "layers": W.STACK_LAYERS,
+           "note": "timeline build (per-CTA %globaltimer records); us; medians over launches 2..69"}
+    for name, q in (("work_queue", True), ("static", False)):
+        stack = DecodeStack(layers, eps=spec.eps, work_queue=q)
+        stream = torch.cuda.Stream(dev)
+        stack.capture(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                stack.replay()
+        torch.cuda.synchronize(dev)
+        binding.timeline_reset()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            stack.replay()
+        torch.cuda.synchronize(dev)
+        rec = binding.timeline_read()
+        if len(rec) != W.STACK_LAYERS * min(sms, spec.N * spec.H):
+            raise SystemExit(f"timeline: {len(rec)} records")
+        res[name] = timeline_summary(rec, min(sms, spec.N * spec.H))
+        del stack
+    return res
+
+
 def run_reference(args) -> dict | None:
     """The oracle as it stands, timed on the host cores on a bounded sample
     of the same workload (rank 0 only)."""
@@ -675,12 +739,14 @@ def main(argv=None):
     ap.add_argument("--no-cfg3", action="store_true",
                     help="skip the N=256/H=96 single-launch and the multi-token measurements in the headline line")
     ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill", "spec",
-                                       "configs"),
+                                       "configs", "timeline"),
                     default="stack69",
                     help="stack69: the headline 69-layer graph step; layer / roofline: one "
                          "launch configuration timed on its own (profiling aid); prefill: the "
                          "chunked varlen prefill")
     args = ap.parse_args(argv)
+    if args.case == "timeline":  # the library with the per-CTA timeline compiled in
+        os.environ["KDA_DECODE_TIMELINE"] = "1"
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
@@ -689,6 +755,8 @@ def main(argv=None):
         res = run_chunk_metadata(args)
     elif args.case == "prefill":
         res = run_prefill(args)
+    elif args.case == "timeline":
+        res = run_timeline(args)
     elif args.case == "configs":
         import torch
 

@@ -26,7 +26,11 @@ ABI_VERSION = 2
 MAX_TOKENS_PER_SEQ = 8
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_PKG_DIR, "lib", "libkda_decode.so")
+# KDA_DECODE_TIMELINE=1 in the environment (read when the library is first
+# loaded) selects the build with the decode kernel's per-CTA timeline
+# compiled in; results are identical, the kernel also records timestamps.
+_LIB_PATH = os.path.join(_PKG_DIR, "lib", "libkda_decode_timeline.so"
+                         if os.environ.get("KDA_DECODE_TIMELINE") == "1" else "libkda_decode.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -125,6 +129,32 @@ def load_library() -> ctypes.CDLL:
                 raise RuntimeError(f"{_LIB_PATH}: ABI version {L.kda_abi_version()} != {ABI_VERSION}")
             _lib = L
     return _lib
+
+
+def timeline_read(max_records: int = 1 << 16):
+    """Per-CTA records of the decode kernel since the last reset (timeline
+    build only): int64 [n, 8] = block, SM, start ns, first unit ready ns, end
+    ns, units, consumer compute ns, consumer wait ns."""
+    import numpy as np
+    lib = load_library()
+    if not hasattr(lib, "kda_timeline_read"):
+        raise RuntimeError("the loaded library has no timeline (set KDA_DECODE_TIMELINE=1 before loading)")
+    buf = np.zeros((max_records, 8), np.uint64)
+    total = ctypes.c_uint(0)
+    fn = lib.kda_timeline_read
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint)]
+    fn.restype = ctypes.c_int
+    n = fn(buf.ctypes.data, max_records, ctypes.byref(total))
+    if n < 0:
+        raise KdaError(n, lib.kda_last_error().decode())
+    return buf[:n].astype(np.int64)
+
+
+def timeline_reset() -> None:
+    lib = load_library()
+    rc = lib.kda_timeline_reset()
+    if rc != 0:
+        raise KdaError(rc, lib.kda_last_error().decode())
 
 
 def kda_status_string(status: int) -> str:

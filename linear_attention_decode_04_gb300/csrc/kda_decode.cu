@@ -88,11 +88,15 @@ cudaError_t device_setup(int* sms) {
   return cudaSuccess;
 }
 
-// With a work queue, each CTA takes all but about its last kQueueTailUnits
-// units statically and draws only those last ones from the queue: the
-// static part needs no atomics, and the queue still evens out the CTAs' end
-// times (at least the first ring of every CTA is static).
-constexpr int kQueueTailUnits = 2;
+// With a work queue, each CTA first takes a static prefix of its units (no
+// atomics) and then draws from the queue.  The prefix keeps at least
+// kQueueTailMin of a CTA's units dynamic, so the queue can even out the CTAs'
+// end times, and is at most kQueueStaticCap long, so that on long launches
+// (where per-SM bandwidth differences add up) most units stay dynamic.  On
+// short launches (tens of units per CTA) only the last few are dynamic and
+// pay the atomic's latency.  The first ring of every CTA is always static.
+constexpr int kQueueTailMin = 2;
+constexpr int kQueueStaticCap = 16;
 
 template <bool kOutNorm, bool kUpdateConv>
 cudaError_t launch(const Params& p_in, int sms, cudaStream_t stream) {
@@ -100,8 +104,9 @@ cudaError_t launch(const Params& p_in, int sms, cudaStream_t stream) {
   {
     const int G = p.total_units < sms ? p.total_units : sms;
     const int ring = (p.T > 1 || p.src_slot != nullptr) ? kMStages : kStages;
-    const int per_cta = p.total_units / G - kQueueTailUnits;
-    p.static_units = per_cta > ring ? per_cta : ring;
+    int prefix = p.total_units / G - kQueueTailMin;
+    prefix = prefix < kQueueStaticCap ? prefix : kQueueStaticCap;
+    p.static_units = prefix > ring ? prefix : ring;
   }
   // Every launch is a programmatic dependent launch: the CTAs may become
   // resident while the previous kernel in the stream drains, and wait for
@@ -272,6 +277,25 @@ int launch_validated(const Params& p, uint32_t flags, void* stream) {
   return KDA_OK;
 }
 }  // namespace
+
+#ifdef KDA_DECODE_TIMELINE
+// Timeline build only (lib/libkda_decode_timeline.so): read and reset the
+// per-CTA records of the decode kernel.  Not part of the product library.
+extern "C" int kda_timeline_read(unsigned long long* host, int max_records, unsigned int* total) {
+  cudaError_t e = cudaMemcpyFromSymbol(total, g_timeline_n, sizeof(unsigned int));
+  if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "%s", cudaGetErrorString(e));
+  const unsigned int avail = *total < static_cast<unsigned int>(kTimelineMax) ? *total : kTimelineMax;
+  const int n = static_cast<int>(avail) < max_records ? static_cast<int>(avail) : max_records;
+  if (n > 0) e = cudaMemcpyFromSymbol(host, g_timeline, static_cast<size_t>(n) * 8 * sizeof(unsigned long long));
+  return e == cudaSuccess ? n : fail(KDA_ERR_LAUNCH, "%s", cudaGetErrorString(e));
+}
+
+extern "C" int kda_timeline_reset(void) {
+  const unsigned int zero = 0;
+  const cudaError_t e = cudaMemcpyToSymbol(g_timeline_n, &zero, sizeof zero);
+  return e == cudaSuccess ? KDA_OK : fail(KDA_ERR_LAUNCH, "%s", cudaGetErrorString(e));
+}
+#endif
 
 // ---------------------------------------------------------------------------
 // Allocation-free entry point.

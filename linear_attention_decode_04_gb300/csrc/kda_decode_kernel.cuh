@@ -77,6 +77,15 @@ struct __align__(128) Smem {
   volatile int abort;
 };
 
+#ifdef KDA_DECODE_TIMELINE
+// Timeline build only: one record per CTA (block, SM, start, first unit
+// ready, end, units, consumer compute ns, consumer wait ns), appended by
+// consumer thread 0 when the CTA finishes.
+constexpr int kTimelineMax = 1 << 16;
+__device__ unsigned long long g_timeline[kTimelineMax][8];
+__device__ unsigned int g_timeline_n;
+#endif
+
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
@@ -451,7 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
   const float nw = (kOutNorm && tid < kDim) ? __ldg(p.norm_w + tid) : 0.0f;
   UnitInputs cur, nxt;
   bool have_next = false;  // nxt holds the inputs of the coming unit
+#ifdef KDA_DECODE_TIMELINE
+  unsigned long long tl_start = 0, tl_first = 0, tl_wait = 0, tl_comp = 0, tl_units = 0, tl_w0 = 0, tl_r = 0;
+  if (tid == 0) tl_start = global_ns();
+#endif
   for (int it = 0;; ++it) {
+#ifdef KDA_DECODE_TIMELINE
+    if (tid == 0) {
+      tl_w0 = global_ns();
+      if (it > 0) tl_comp += tl_w0 - tl_r;
+    }
+#endif
     const int stage = it % kStages;
     const uint32_t parity = (it / kStages) & 1;
     // Which unit is next, then its staged data.  The per-unit inputs that do
@@ -483,6 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       }
       break;
     }
+#ifdef KDA_DECODE_TIMELINE
+    if (tid == 0) {
+      tl_r = global_ns();
+      tl_wait += tl_r - tl_w0;
+      if (it == 0) tl_first = tl_r;
+      if (n >= 0) ++tl_units;
+    }
+#endif
     if (n < 0) break;  // no more units
     // If the next unit is already published, start loading its inputs now;
     // they arrive while this unit computes.
@@ -695,6 +722,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       out_row[tid] = f32_to_bf16(y);
     }
   }
+#ifdef KDA_DECODE_TIMELINE
+  if (tid == 0) {
+    const unsigned long long te = global_ns();
+    unsigned int smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const unsigned int i = atomicAdd(&g_timeline_n, 1u);
+    if (i < kTimelineMax) {
+      g_timeline[i][0] = blockIdx.x; g_timeline[i][1] = smid; g_timeline[i][2] = tl_start; g_timeline[i][3] = tl_first;
+      g_timeline[i][4] = te; g_timeline[i][5] = tl_units; g_timeline[i][6] = tl_comp; g_timeline[i][7] = tl_wait;
+    }
+  }
+#endif
 }
 
 }  // namespace
