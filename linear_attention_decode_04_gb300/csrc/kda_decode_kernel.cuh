@@ -168,6 +168,13 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
                : "memory");
 }
 
+// L2 prefetch hint of a 16-byte aligned range (a multiple of 16 bytes): it
+// only warms L2, so it may be issued before the data's producer has finished
+// (its writes land in L2 as well and later reads see them).
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -333,10 +340,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       return u < p.total_units ? u : -1;
     };
 
+    // L2 hints for a unit's per-token slices and its head's conv taps.
+    auto warm_l2 = [&](int n, int h) {
+      for (int c = 0; c < 3; ++c) l2_prefetch(p.qkv + n * p.qkv_stride + c * D + static_cast<int64_t>(h) * kDim, kXSliceBytes);
+      l2_prefetch(p.g + (static_cast<int64_t>(n) * p.H + h) * kDim, kDim * 4);
+      if (kOutNorm) l2_prefetch(p.gate + n * p.gate_stride + static_cast<int64_t>(h) * kDim, kXSliceBytes);
+      for (int c = 0; c < 3; ++c)
+        for (int t = 0; t < kWidth; ++t) l2_prefetch(p.conv_w + (c * kWidth + t) * D + static_cast<int64_t>(h) * kDim, kDim * 4);
+    };
     // First ring: static units.  With KDA_EARLY_PREFETCH the first unit's
     // state streams in before the previous kernel in the stream has finished
     // (the caller guarantees that kernel does not write the slot indices,
-    // the state or the conv state); everything per-token waits for it.  The
+    // the state or the conv state), and its per-token slices and conv taps
+    // are pulled into L2; everything per-token is read only after it.  The
     // ring then fills one stage at a time (each stage once the one before
     // it has landed), so that the first tile of every CTA arrives early
     // instead of all CTAs' three tiles arriving together.
@@ -354,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         if (active(slot) && !S.info[it][3]) {
           mbar_arrive_expect_tx(smem_addr(&S.full[it]), in_bytes);
           load_slot_parts(it, h, slot);
+          warm_l2(n, h);
         }
       }
     }

@@ -126,6 +126,8 @@ struct __align__(16) ChunkSmem {
   float G[kL][kSA];                 // cumulative log decay
   float P[kL][kSP];                 // P (strictly lower)
   float beta[kL];
+  float egm[kD];                    // exp(G_m) per key channel (0 when G_m < -kMaxExponent)
+  float cl[kD];                     // exp(G_{L-1} - G_m) per key channel
   int slow;                         // this chunk takes the element-wise P / R path
 };
 
@@ -391,32 +393,57 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
       acc += S.G[t][tid];
       S.G[t][tid] = acc;
     }
+    // Whether the split factors exp(+-(G_t - G_m)) stay in range for this
+    // channel (else the whole chunk takes the element-wise path), and the
+    // per-channel constants that turn them into exp(G_t) and
+    // exp(G_{L-1} - G_t).
+    const float gm = S.G[kRef][tid];
+    float dmax = 0.0f;
+#pragma unroll 8
+    for (int t = 0; t < kL; ++t) dmax = fmaxf(dmax, fabsf(S.G[t][tid] - gm));
+    if (dmax > kMaxExponent) S.slow = 1;
+    S.egm[tid] = gm > -kMaxExponent ? expf(gm) : 0.0f;
+    S.cl[tid] = expf(S.G[kL - 1][tid] - gm);
   }
   __syncthreads();
 
-  // ---- 4. split decay factors around the reference token (shared memory);
-  // Q_G = exp(G) q^ and gamma to the image; R's image cleared (its lower
-  // triangle is written next); P cleared
-  // piece (t, keys 4 kg .. 4 kg + 3); consecutive threads take consecutive t,
-  // so the image stores of Q_G are coalesced 16-byte pieces
+  // ---- 4. split decay factors around the reference token (shared memory):
+  // ek = exp(G - G_m) k^, fk = exp(G_m - G) k^ and, in place of q^, R's A
+  // operand exp(G - G_m) q^; Q_G = exp(G) q^ = exp(G_m) exp(G - G_m) q^ and
+  // gamma to the image; R's image cleared (its lower triangle is written
+  // next); P cleared.  A chunk on the element-wise path keeps q^ and needs
+  // only Q_G here.  Piece (t, keys 4 kg .. 4 kg + 3); consecutive threads
+  // take consecutive t, so the image stores of Q_G are coalesced 16-byte
+  // pieces.
+  const bool slow = S.slow != 0;
   for (int e = tid; e < kL * kD / 4; e += kThreads) {
     const int t = e & (kL - 1), i0 = 4 * (e >> 5);
     const float4 G4 = *reinterpret_cast<const float4*>(&S.G[t][i0]);
-    const float4 Gm = *reinterpret_cast<const float4*>(&S.G[kRef][i0]);
-    const float4 k4 = *reinterpret_cast<const float4*>(&S.k[t][i0]);
     const float4 q4 = *reinterpret_cast<const float4*>(&S.q[t][i0]);
-    const float d[4] = {G4.x - Gm.x, G4.y - Gm.y, G4.z - Gm.z, G4.w - Gm.w};
-    const float gt[4] = {G4.x, G4.y, G4.z, G4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
-    float ek[4], fk[4], qg[4];
+    const float gt[4] = {G4.x, G4.y, G4.z, G4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+    float qg[4];
+    if (!slow) {
+      const float4 Gm = *reinterpret_cast<const float4*>(&S.G[kRef][i0]);
+      const float4 k4 = *reinterpret_cast<const float4*>(&S.k[t][i0]);
+      const float4 eg4 = *reinterpret_cast<const float4*>(&S.egm[i0]);
+      const float d[4] = {G4.x - Gm.x, G4.y - Gm.y, G4.z - Gm.z, G4.w - Gm.w};
+      const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, egm[4] = {eg4.x, eg4.y, eg4.z, eg4.w};
+      float ek[4], fk[4], eq[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (fabsf(d[c]) > kMaxExponent) S.slow = 1;
-      ek[c] = __expf(d[c]) * kv[c];
-      fk[c] = __expf(-d[c]) * kv[c];
-      qg[c] = __expf(gt[c]) * qv[c];
+      for (int c = 0; c < 4; ++c) {
+        const float ed = expf(d[c]), rd = expf(-d[c]);
+        ek[c] = ed * kv[c];
+        fk[c] = rd * kv[c];
+        eq[c] = ed * qv[c];
+        qg[c] = egm[c] > 0.0f ? egm[c] * eq[c] : expf(gt[c]) * qv[c];
+      }
+      *reinterpret_cast<float4*>(&S.f.ek[t][i0]) = make_float4(ek[0], ek[1], ek[2], ek[3]);
+      *reinterpret_cast<float4*>(&S.f.fk[t][i0]) = make_float4(fk[0], fk[1], fk[2], fk[3]);
+      *reinterpret_cast<float4*>(&S.q[t][i0]) = make_float4(eq[0], eq[1], eq[2], eq[3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) qg[c] = expf(gt[c]) * qv[c];
     }
-    *reinterpret_cast<float4*>(&S.f.ek[t][i0]) = make_float4(ek[0], ek[1], ek[2], ek[3]);
-    *reinterpret_cast<float4*>(&S.f.fk[t][i0]) = make_float4(fk[0], fk[1], fk[2], fk[3]);
     *reinterpret_cast<float4*>(ws + kOffB1 + kpos(t, i0, kNB1)) = make_float4(qg[0], qg[1], qg[2], qg[3]);
   }
   if (tid < kD) ws[kOffC + tid] = expf(S.G[kL - 1][tid]);
@@ -425,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   __syncthreads();
 
   // ---- 5. P (strictly lower, shared memory) and R (lower, image) over the
-  // key channels; R's A operand exp(G - G_m) q^ is formed while loading
-  if (!S.slow) {
+  // key channels
+  if (!slow) {
     // one 16 x 8 output tile y of P (mat 0) or R (mat 1); an R tile runs over
     // all keys, a P tile over the half of them from key block kb and is added
     // into P (cleared above; the two halves add in either order to the same
@@ -441,18 +468,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
       for (int kk = kb; kk < ke; ++kk) {
         const int i0 = 8 * kk + 2 * tq;
         float2 a02, a13;
-        if (mat == 0) {
-          a02 = *reinterpret_cast<const float2*>(&S.f.ek[ta][i0]);
-          a13 = *reinterpret_cast<const float2*>(&S.f.ek[ta + 8][i0]);
-        } else {
-          const float2 q0 = *reinterpret_cast<const float2*>(&S.q[ta][i0]);
-          const float2 q1 = *reinterpret_cast<const float2*>(&S.q[ta + 8][i0]);
-          const float2 g0 = *reinterpret_cast<const float2*>(&S.G[ta][i0]);
-          const float2 g1 = *reinterpret_cast<const float2*>(&S.G[ta + 8][i0]);
-          const float2 gm = *reinterpret_cast<const float2*>(&S.G[kRef][i0]);
-          a02 = make_float2(__expf(g0.x - gm.x) * q0.x, __expf(g0.y - gm.y) * q0.y);
-          a13 = make_float2(__expf(g1.x - gm.x) * q1.x, __expf(g1.y - gm.y) * q1.y);
-        }
+        // A operand: exp(G - G_m) k^ (P) or exp(G - G_m) q^ (R), both formed above
+        const float* arows = mat == 0 ? &S.f.ek[0][0] : &S.q[0][0];
+        a02 = *reinterpret_cast<const float2*>(arows + ta * kSA + i0);
+        a13 = *reinterpret_cast<const float2*>(arows + (ta + 8) * kSA + i0);
         const float2 bb = *reinterpret_cast<const float2*>(&S.f.fk[8 * nn + g8][i0]);
         mma3(acc, make_a(a02.x, a13.x, a02.y, a13.y), bb.x, bb.y);
       }
@@ -495,27 +514,37 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   // ---- 6. triangular solve (thread = one column of [U | W]), left-looking:
   // x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or exp(G) k^ (W),
   // W staged in the (now free) factor buffer; the value-column threads also
-  // write row `tid` of K_E^T = exp(G_{L-1} - G) k^
-  // (the key-column threads spend as many exponentials on exp(G) k^)
+  // write row `tid` of K_E^T = exp(G_{L-1} - G) k^.  Off the element-wise
+  // path both exponential factors come from the split ones:
+  // exp(G_{L-1} - G) k^ = exp(G_{L-1} - G_m) fk, exp(G) k^ = exp(G_m) ek.
   {
     const bool vcol = tid < kD;
     const int i = tid - kD;
     if (vcol) {
-      const float GL = S.G[kL - 1][tid];
+      const float GL = S.G[kL - 1][tid], cl = S.cl[tid];
 #pragma unroll 4
       for (int t = 0; t < kL; t += 4) {
         float4 ke;
-        ke.x = expf(GL - S.G[t][tid]) * S.k[t][tid];
-        ke.y = expf(GL - S.G[t + 1][tid]) * S.k[t + 1][tid];
-        ke.z = expf(GL - S.G[t + 2][tid]) * S.k[t + 2][tid];
-        ke.w = expf(GL - S.G[t + 3][tid]) * S.k[t + 3][tid];
+        if (!slow) {
+          ke.x = cl * S.f.fk[t][tid];
+          ke.y = cl * S.f.fk[t + 1][tid];
+          ke.z = cl * S.f.fk[t + 2][tid];
+          ke.w = cl * S.f.fk[t + 3][tid];
+        } else {
+          ke.x = expf(GL - S.G[t][tid]) * S.k[t][tid];
+          ke.y = expf(GL - S.G[t + 1][tid]) * S.k[t + 1][tid];
+          ke.z = expf(GL - S.G[t + 2][tid]) * S.k[t + 2][tid];
+          ke.w = expf(GL - S.G[t + 3][tid]) * S.k[t + 3][tid];
+        }
         *reinterpret_cast<float4*>(ws + kOffB2 + kpos(tid, t, kNB2)) = ke;
       }
     }
+    const float egm = vcol ? 0.0f : S.egm[i];
+    const bool split_y = !slow && egm > 0.0f;
     float x[kL];
 #pragma unroll
     for (int t = 0; t < kL; ++t) {
-      float a0 = vcol ? S.v[t][tid] : expf(S.G[t][i]) * S.k[t][i];
+      float a0 = vcol ? S.v[t][tid] : split_y ? egm * S.f.ek[t][i] : expf(S.G[t][i]) * S.k[t][i];
       float a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
       for (int s4 = 0; s4 < t / 4 + 1; ++s4) {
