@@ -347,6 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       if (kOutNorm) l2_prefetch(p.gate + n * p.gate_stride + static_cast<int64_t>(h) * kDim, kXSliceBytes);
       for (int c = 0; c < 3; ++c)
         for (int t = 0; t < kWidth; ++t) l2_prefetch(p.conv_w + (c * kWidth + t) * D + static_cast<int64_t>(h) * kDim, kDim * 4);
+      // beta: the 16-byte piece holding it, when that piece lies inside the
+      // tensor (beta needs only 2-byte alignment); the norm weight
+      const uintptr_t b0 = reinterpret_cast<uintptr_t>(p.beta);
+      const uintptr_t b1 = reinterpret_cast<uintptr_t>(p.beta + static_cast<int64_t>(p.N) * p.H);
+      const uintptr_t bp = reinterpret_cast<uintptr_t>(p.beta + static_cast<int64_t>(n) * p.H + h) & ~uintptr_t{15};
+      if (bp >= b0 && bp + 16 <= b1) l2_prefetch(reinterpret_cast<const void*>(bp), 16);
+      if (kOutNorm) l2_prefetch(p.norm_w, kDim * 4);
     };
     // First ring: static units.  With KDA_EARLY_PREFETCH the first unit's
     // state streams in before the previous kernel in the stream has finished
