@@ -50,8 +50,10 @@ constexpr int kD = 128;           // head dim (key = value)
 constexpr int kWidth = 4;         // conv taps
 constexpr int kHist = kWidth - 1; // older taps carried between chunks
 constexpr int kL = KDA_PREFILL_CHUNK;  // 32 tokens per chunk
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;                        // scan kernel
 constexpr int kThreads = kWarps * 32;
+constexpr int kChunkWarps = 12;                  // chunk kernel: one thread per q|k|v channel
+constexpr int kChunkThreads = kChunkWarps * 32;
 constexpr int kCh = 3 * kD;       // q | k | v channels of one head
 constexpr int kSA = 136;          // row stride (floats) of [token][128] operands
 constexpr int kSP = 36;           // row stride (floats) of P (rows read as float4)
@@ -234,7 +236,7 @@ __device__ __forceinline__ void cp16(void* dst, const void* src, int bytes) {
 // the chunk: conv, norms, cumulative decays, P and R, the triangular solve
 // for U and W, and the decayed Q_G and K_E.  Results go to the workspace
 // image of (c, h).
-__global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(const PrefillParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ChunkSmem& S = *reinterpret_cast<ChunkSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, tq = lane & 3;
@@ -267,24 +269,24 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
     // tap r of channel c at c * 3 + r (dim-first) or r * C + c (tap-first)
     const uint16_t* cs = p.conv_state + static_cast<int64_t>(slot) * 3 * D * kHist;
     const int64_t sc = p.conv_sd ? 1 : kHist, sr = p.conv_sd ? 3 * D : 1;
-    for (int ch = tid; ch < kCh; ch += kThreads)
+    for (int ch = tid; ch < kCh; ch += kChunkThreads)
 #pragma unroll
       for (int r = 0; r < kHist; ++r) S.raw[r][ch] = cs[ch_global(ch) * sc + r * sr];
   } else {
-    for (int e = tid; e < kHist * 48; e += kThreads) {
+    for (int e = tid; e < kHist * 48; e += kChunkThreads) {
       const int r = e / 48, q = e - r * 48, seg = q >> 4, u = q & 15;
       cp16(&S.raw[r][seg * kD + 8 * u],
            p.qkv + (t0 - kHist + r) * p.qkv_stride + seg * D + static_cast<int64_t>(h) * kD + 8 * u, 16);
     }
   }
-  for (int e = tid; e < kL * 48; e += kThreads) {
+  for (int e = tid; e < kL * 48; e += kChunkThreads) {
     const int t = e / 48, q = e - t * 48, seg = q >> 4, u = q & 15;
     const int tr = t < L ? t : L - 1;  // rows past L: zero-filled (the source row is only an address)
     cp16(&S.raw[kHist + t][seg * kD + 8 * u],
          p.qkv + (t0 + tr) * p.qkv_stride + seg * D + static_cast<int64_t>(h) * kD + 8 * u, t < L ? 16 : 0);
   }
   if (!p.fused_gate) {
-    for (int e = tid; e < kL * 32; e += kThreads) {
+    for (int e = tid; e < kL * 32; e += kChunkThreads) {
       const int t = e >> 5, u = e & 31, tr = t < L ? t : L - 1;
       cp16(&S.G[t][4 * u], p.g + ((t0 + tr) * p.H + h) * kD + 4 * u, t < L ? 16 : 0);
     }
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
     // standard KDA form): z = raw + dt_bias, g = lb * sigmoid(e^A_log z) for
     // a lower bound lb < 0, else g = -e^A_log softplus(z)
     const float a = expf(__ldg(p.A_log + h));
-    for (int e = tid; e < kL * 32; e += kThreads) {
+    for (int e = tid; e < kL * 32; e += kChunkThreads) {
       const int t = e >> 5, u = e & 31;
       float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
       if (t < L) {
@@ -326,21 +328,17 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   __syncthreads();
 
   // ---- 2. conv + SiLU over the window (outputs past L are zero); thread
-  // tid convolves channel tid (q or k block) over all tokens and v channel
-  // tid % 128 over half of them (threads below 128 the first 16 tokens)
+  // tid convolves channel tid of the head's q | k | v channels over all
+  // tokens
   {
-    float wa[kWidth], wv[kWidth], ba = 0.0f, bv = 0.0f;
+    const int c = tid >> 7, j = tid & (kD - 1);
+    float wa[kWidth], ba = 0.0f;
 #pragma unroll
-    for (int t = 0; t < kWidth; ++t) {
-      wa[t] = __ldg(p.conv_w + ((tid >> 7) * kWidth + t) * D + static_cast<int64_t>(h) * kD + (tid & 127));
-      wv[t] = __ldg(p.conv_w + (2 * kWidth + t) * D + static_cast<int64_t>(h) * kD + (tid & (kD - 1)));
-    }
-    if (p.conv_b) {
-      ba = __ldg(p.conv_b + ch_global(tid));
-      bv = __ldg(p.conv_b + ch_global(2 * kD + (tid & (kD - 1))));
-    }
+    for (int t = 0; t < kWidth; ++t)
+      wa[t] = __ldg(p.conv_w + (c * kWidth + t) * D + static_cast<int64_t>(h) * kD + j);
+    if (p.conv_b) ba = __ldg(p.conv_b + ch_global(tid));
     float x0 = bf16f(S.raw[0][tid]), x1 = bf16f(S.raw[1][tid]), x2 = bf16f(S.raw[2][tid]);
-    float* dst = tid < kD ? &S.q[0][tid] : &S.k[0][tid - kD];
+    float* dst = c == 0 ? &S.q[0][j] : c == 1 ? &S.k[0][j] : &S.v[0][j];
 #pragma unroll
     for (int t = 0; t < kL; ++t) {
       const float x3 = bf16f(S.raw[kHist + t][tid]);
@@ -352,30 +350,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
       dst[t * kSA] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
       x0 = x1; x1 = x2; x2 = x3;
     }
-    {
-      const int jv = tid & (kD - 1), cv = 2 * kD + jv, th = (tid >> 7) * (kL / 2);
-      float z0 = bf16f(S.raw[th][cv]), z1 = bf16f(S.raw[th + 1][cv]), z2 = bf16f(S.raw[th + 2][cv]);
-#pragma unroll
-      for (int tt = 0; tt < kL / 2; ++tt) {
-        const int t = th + tt;
-        const float z3 = bf16f(S.raw[kHist + t][cv]);
-        float y = bv;
-        y = fmaf(wv[0], z0, y);
-        y = fmaf(wv[1], z1, y);
-        y = fmaf(wv[2], z2, y);
-        y = fmaf(wv[3], z3, y);
-        S.v[t][jv] = t < L ? __fdividef(y, 1.0f + __expf(-y)) : 0.0f;
-        z0 = z1; z1 = z2; z2 = z3;
-      }
-    }
   }
   __syncthreads();
 
-  // ---- 3. L2 norms (warp w: tokens 4w..4w+3); cumulative decay
+  // ---- 3. L2 norms (warp w: tokens w, w + 12, w + 24); cumulative decay
   const float qs = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
-#pragma unroll
-  for (int tt = 0; tt < 4; ++tt) {
-    const int t = warp * 4 + tt;
+  for (int t = warp; t < kL; t += kChunkWarps) {
     float4 qv = reinterpret_cast<float4*>(S.q[t])[lane];
     float4 kv = reinterpret_cast<float4*>(S.k[t])[lane];
     const float sq = warp_sum((qv.x * qv.x + qv.y * qv.y) + (qv.z * qv.z + qv.w * qv.w));
@@ -416,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   // take consecutive t, so the image stores of Q_G are coalesced 16-byte
   // pieces.
   const bool slow = S.slow != 0;
-  for (int e = tid; e < kL * kD / 4; e += kThreads) {
+  for (int e = tid; e < kL * kD / 4; e += kChunkThreads) {
     const int t = e & (kL - 1), i0 = 4 * (e >> 5);
     const float4 G4 = *reinterpret_cast<const float4*>(&S.G[t][i0]);
     const float4 q4 = *reinterpret_cast<const float4*>(&S.q[t][i0]);
@@ -447,25 +427,23 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
     *reinterpret_cast<float4*>(ws + kOffB1 + kpos(t, i0, kNB1)) = make_float4(qg[0], qg[1], qg[2], qg[3]);
   }
   if (tid < kD) ws[kOffC + tid] = expf(S.G[kL - 1][tid]);
-  for (int e = tid; e < kL * kL; e += kThreads) ws[kOffB2 + kpos(kD + (e >> 5), e & (kL - 1), kNB2)] = 0.0f;
-  for (int e = tid; e < kL * kSP; e += kThreads) (&S.P[0][0])[e] = 0.0f;
+  for (int e = tid; e < kL * kL; e += kChunkThreads) ws[kOffB2 + kpos(kD + (e >> 5), e & (kL - 1), kNB2)] = 0.0f;
+  for (int e = tid; e < kL * kSP; e += kChunkThreads) (&S.P[0][0])[e] = 0.0f;
   __syncthreads();
 
   // ---- 5. P (strictly lower, shared memory) and R (lower, image) over the
   // key channels
   if (!slow) {
-    // one 16 x 8 output tile y of P (mat 0) or R (mat 1); an R tile runs over
-    // all keys, a P tile over the half of them from key block kb and is added
-    // into P (cleared above; the two halves add in either order to the same
-    // value).  R tiles cost more (their A operand takes exponentials), so
-    // warps 0-5 take one R tile and one P half each, warps 6-7 three P halves
-    auto tile = [&](const int mat, const int y, const int kb) {
+    // one 16 x 8 output tile y of P (mat 0) or R (mat 1) over all keys: the
+    // tiles of the lower triangle, (rows 0-15, columns 0-15) and (rows 16-31,
+    // columns 0-31); warps 0-5 take the six R tiles, warps 6-11 the six P
+    // tiles
+    auto tile = [&](const int mat, const int y) {
       const int mm = y < 2 ? 0 : 1, nn = y < 2 ? y : y - 2;
       const int ta = 16 * mm + g8;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int ke = mat == 0 ? kb + kD / 16 : kD / 8;
 #pragma unroll 4
-      for (int kk = kb; kk < ke; ++kk) {
+      for (int kk = 0; kk < kD / 8; ++kk) {
         const int i0 = 8 * kk + 2 * tq;
         float2 a02, a13;
         // A operand: exp(G - G_m) k^ (P) or exp(G - G_m) q^ (R), both formed above
@@ -480,21 +458,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
       for (int e = 0; e < 4; ++e) {
         const int te = ta + (e >> 1) * 8, se = s + (e & 1);
         if (mat == 0) {
-          if (te > se) atomicAdd(&S.P[te][se], acc[e]);
+          if (te > se) S.P[te][se] = acc[e];
         } else {
           if (te >= se) ws[kOffB2 + kpos(kD + te, se, kNB2)] = acc[e];
         }
       }
     };
-    if (warp < 6) {
-      tile(1, warp, 0);
-      tile(0, warp >> 1, (warp & 1) * (kD / 16));
-    } else {
-      for (int q = warp; q < 12; q += 2) tile(0, q >> 1, (q & 1) * (kD / 16));
-    }
+    if (warp < 6)
+      tile(1, warp);
+    else
+      tile(0, warp - 6);
   } else {
     // element-wise: pairs (t, s), s <= t
-    for (int e = tid; e < kL * (kL + 1) / 2; e += kThreads) {
+    for (int e = tid; e < kL * (kL + 1) / 2; e += kChunkThreads) {
       int t = static_cast<int>((sqrtf(8.0f * e + 1.0f) - 1.0f) * 0.5f);
       while ((t + 1) * (t + 2) / 2 <= e) ++t;
       while (t * (t + 1) / 2 > e) --t;
@@ -511,34 +487,34 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   }
   __syncthreads();
 
-  // ---- 6. triangular solve (thread = one column of [U | W]), left-looking:
-  // x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or exp(G) k^ (W),
-  // W staged in the (now free) factor buffer; the value-column threads also
-  // write row `tid` of K_E^T = exp(G_{L-1} - G) k^.  Off the element-wise
-  // path both exponential factors come from the split ones:
+  // ---- 6. triangular solve (threads 0-255: one column of [U | W] each),
+  // left-looking: x_t = beta_t (y_t - sum_{s<t} P_ts x_s), y = v~ (U) or
+  // exp(G) k^ (W), W staged in the (now free) factor buffer; meanwhile
+  // threads 256-383 write row i of K_E^T = exp(G_{L-1} - G) k^.  Off the
+  // element-wise path both exponential factors come from the split ones:
   // exp(G_{L-1} - G) k^ = exp(G_{L-1} - G_m) fk, exp(G) k^ = exp(G_m) ek.
-  {
+  if (tid >= 2 * kD) {
+    const int i = tid - 2 * kD;
+    const float GL = S.G[kL - 1][i], cl = S.cl[i];
+#pragma unroll 4
+    for (int t = 0; t < kL; t += 4) {
+      float4 ke;
+      if (!slow) {
+        ke.x = cl * S.f.fk[t][i];
+        ke.y = cl * S.f.fk[t + 1][i];
+        ke.z = cl * S.f.fk[t + 2][i];
+        ke.w = cl * S.f.fk[t + 3][i];
+      } else {
+        ke.x = expf(GL - S.G[t][i]) * S.k[t][i];
+        ke.y = expf(GL - S.G[t + 1][i]) * S.k[t + 1][i];
+        ke.z = expf(GL - S.G[t + 2][i]) * S.k[t + 2][i];
+        ke.w = expf(GL - S.G[t + 3][i]) * S.k[t + 3][i];
+      }
+      *reinterpret_cast<float4*>(ws + kOffB2 + kpos(i, t, kNB2)) = ke;
+    }
+  } else {
     const bool vcol = tid < kD;
     const int i = tid - kD;
-    if (vcol) {
-      const float GL = S.G[kL - 1][tid], cl = S.cl[tid];
-#pragma unroll 4
-      for (int t = 0; t < kL; t += 4) {
-        float4 ke;
-        if (!slow) {
-          ke.x = cl * S.f.fk[t][tid];
-          ke.y = cl * S.f.fk[t + 1][tid];
-          ke.z = cl * S.f.fk[t + 2][tid];
-          ke.w = cl * S.f.fk[t + 3][tid];
-        } else {
-          ke.x = expf(GL - S.G[t][tid]) * S.k[t][tid];
-          ke.y = expf(GL - S.G[t + 1][tid]) * S.k[t + 1][tid];
-          ke.z = expf(GL - S.G[t + 2][tid]) * S.k[t + 2][tid];
-          ke.w = expf(GL - S.G[t + 3][tid]) * S.k[t + 3][tid];
-        }
-        *reinterpret_cast<float4*>(ws + kOffB2 + kpos(tid, t, kNB2)) = ke;
-      }
-    }
     const float egm = vcol ? 0.0f : S.egm[i];
     const bool split_y = !slow && egm > 0.0f;
     float x[kL];
@@ -562,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_chunk_kernel(const Pr
   }
   __syncthreads();
   // W to the image as coalesced 16-byte pieces (t, keys 4 kg .. 4 kg + 3)
-  for (int e = tid; e < kL * kD / 4; e += kThreads) {
+  for (int e = tid; e < kL * kD / 4; e += kChunkThreads) {
     const int t = e & (kL - 1), i0 = 4 * (e >> 5);
     *reinterpret_cast<float4*>(ws + kOffB1 + kpos(kL + t, i0, kNB1)) =
         *reinterpret_cast<const float4*>(&S.f.ek[t][i0]);
@@ -1110,7 +1086,7 @@ extern "C" int kda_prefill(const KdaPrefillArgs* a, void* stream) {
   p.seq_order = a->seq_order;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a->num_chunks > 0)
-    kda_prefill_chunk_kernel<<<dim3(static_cast<unsigned>(a->num_chunks), static_cast<unsigned>(a->H)), kThreads,
+    kda_prefill_chunk_kernel<<<dim3(static_cast<unsigned>(a->num_chunks), static_cast<unsigned>(a->H)), kChunkThreads,
                                sizeof(ChunkSmem), s>>>(p);
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(a->B) * a->H));
   if (norm)
