@@ -261,7 +261,7 @@ def single_launch(device, spec, warmup: int, n: int, graph: bool = True) -> dict
     return res
 
 
-def spec_launch(device, spec, warmup: int, n: int) -> dict:
+def spec_launch(device, spec, warmup: int, n: int, reset_timeline_before_last: bool = False) -> dict:
     """One multi-token (speculative) decode launch of ``spec`` (work queue)
     replayed from a CUDA graph, timed per launch over ``n`` replays."""
     import torch
@@ -291,6 +291,15 @@ def spec_launch(device, spec, warmup: int, n: int) -> dict:
             graph.replay()
     torch.cuda.synchronize(device)
     st = replay_stats(graph.replay, stream, n)
+    timeline = None
+    if reset_timeline_before_last:  # one more replay, recorded (timeline build)
+        from linear_attention_decode_04_gb300 import binding
+        binding.timeline_reset()
+        torch.cuda.synchronize(device)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize(device)
+        timeline = binding.timeline_read()
     if int(t["err"].item()):
         raise SystemExit("device error flag raised")
     valid = lambda sl: 0 < sl < spec.num_slots  # noqa: E731
@@ -307,6 +316,8 @@ def spec_launch(device, spec, warmup: int, n: int) -> dict:
            "algorithmic_bytes_per_launch": nbytes,
            "bytes_note": "per (sequence, head): 64 KiB state read once + 64 KiB written per present token, "
                          "plus windows and per-token inputs / outputs"}
+    if timeline is not None:
+        res["_timeline"] = timeline
     del call, graph, t
     torch.cuda.empty_cache()
     return res
@@ -688,6 +699,32 @@ def run_timeline(args) -> dict:
     return res
 
 
+def run_spec_timeline(args) -> dict:
+    """The multi-token batch with the timeline build: per CTA the time
+    waiting for a unit's data, in the state-independent phase, in the token
+    loop (including waits for an output buffer), medians over the CTAs of
+    one launch, per unit and per token; us."""
+    import torch
+
+    from linear_attention_decode_04_gb300 import binding
+    from linear_attention_decode_04_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    spec_res = spec_launch(dev, W.MULTI_BENCH, args.warmup, 3, reset_timeline_before_last=True)
+    rec = spec_res.pop("_timeline").astype(np.float64)
+    units = rec[:, 5]
+    tokens = units * W.MULTI_BENCH.T
+    per_unit = lambda col: float(np.median(rec[:, col] / np.maximum(units, 1))) / 1e3  # noqa: E731
+    res = {"mode": "spec_timeline", "workload": W.MULTI_BENCH.name, "ctas": int(len(rec)),
+           "units_per_cta_median": float(np.median(units)),
+           "launch_us": float((rec[:, 4].max() - rec[:, 2].min()) / 1e3),
+           "per_unit_us": {"waiting_for_data": per_unit(7), "state_independent_phase": per_unit(3),
+                           "token_loop": per_unit(6), "of_which_waiting_for_an_output_buffer": per_unit(1)},
+           "token_loop_per_token_us": float(np.median(rec[:, 6] / np.maximum(tokens, 1))) / 1e3,
+           "note": "timeline build; padding sequences count as units with no tokens"}
+    return res
+
+
 def run_reference(args) -> dict | None:
     """The oracle as it stands, timed on the host cores on a bounded sample
     of the same workload (rank 0 only)."""
@@ -739,13 +776,13 @@ def main(argv=None):
     ap.add_argument("--no-cfg3", action="store_true",
                     help="skip the N=256/H=96 single-launch and the multi-token measurements in the headline line")
     ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill", "spec",
-                                       "configs", "timeline"),
+                                       "configs", "timeline", "spec_timeline"),
                     default="stack69",
                     help="stack69: the headline 69-layer graph step; layer / roofline: one "
                          "launch configuration timed on its own (profiling aid); prefill: the "
                          "chunked varlen prefill")
     args = ap.parse_args(argv)
-    if args.case == "timeline":  # the library with the per-CTA timeline compiled in
+    if args.case in ("timeline", "spec_timeline"):  # the library with the per-CTA timeline compiled in
         os.environ["KDA_DECODE_TIMELINE"] = "1"
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -757,6 +794,8 @@ def main(argv=None):
         res = run_prefill(args)
     elif args.case == "timeline":
         res = run_timeline(args)
+    elif args.case == "spec_timeline":
+        res = run_spec_timeline(args)
     elif args.case == "configs":
         import torch
 

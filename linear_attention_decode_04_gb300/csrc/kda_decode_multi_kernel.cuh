@@ -299,7 +299,39 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
   const float scale = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
   const float nw = (kOutNorm && tid < kDim) ? __ldg(p.norm_w + tid) : 0.0f;
   uint32_t wcnt0 = 0u, wcnt1 = 0u, wcnt2 = 0u;  // states written into each output buffer so far
+  // Conv taps of this thread's channels (q or k channel tid, v channel tid
+  // for tid < 128) and the gate parameters of key channel tid - 128, for the
+  // head in w_head.  When the next unit is already published they are
+  // loaded at the end of the current one, so their latency is off the next
+  // unit's path.
+  const int cq = tid >> 7, jq = tid & (kDim - 1);
+  float wq[kWidth], wv[kWidth], bq = 0.0f, bv = 0.0f, gate_a = 0.0f, gate_bias = 0.0f;
+  int w_head = -1;
+  auto load_head = [&](int hh) {
+    const int64_t wbase = static_cast<int64_t>(hh) * kDim + jq;
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) wq[k] = __ldg(p.conv_w + (cq * kWidth + k) * D + wbase);
+    bq = p.conv_b ? __ldg(p.conv_b + cq * D + wbase) : 0.0f;
+    if (tid < kDim) {
+#pragma unroll
+      for (int k = 0; k < kWidth; ++k) wv[k] = __ldg(p.conv_w + (2 * kWidth + k) * D + wbase);
+      bv = p.conv_b ? __ldg(p.conv_b + 2 * D + wbase) : 0.0f;
+    } else if (p.fused_gate) {
+      gate_a = expf(__ldg(p.A_log + hh));
+      gate_bias = p.dt_bias ? __ldg(p.dt_bias + wbase) : 0.0f;
+    }
+    w_head = hh;
+  };
+#ifdef KDA_DECODE_TIMELINE
+  // timeline build: per CTA the time waiting for a unit's data, in the
+  // state-independent phase, in the token loop, waiting for an output buffer
+  unsigned long long tl_start = 0, tl_in = 0, tl_up = 0, tl_loop = 0, tl_freed = 0, tl_units = 0, tl_t = 0;
+  if (tid == 0) tl_start = global_ns();
+#endif
   for (int it = 0;; ++it) {
+#ifdef KDA_DECODE_TIMELINE
+    if (tid == 0) tl_t = global_ns();
+#endif
     const int st = it % kMStages;
     const uint32_t parity = (it / kMStages) & 1;
     const bool have_info = mbar_wait_bounded(smem_addr(&S.ready[st]), parity, p.wait_limit_ns);
@@ -319,6 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
       }
       break;
     }
+#ifdef KDA_DECODE_TIMELINE
+    if (tid == 0) {
+      const unsigned long long now = global_ns();
+      tl_in += now - tl_t;
+      tl_t = now;
+      if (n >= 0) ++tl_units;
+    }
+#endif
     if (n < 0) break;  // no more units
     const int src = S.info[st][0];
     const bool src_ok = valid(src);
@@ -340,41 +380,36 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     const int* pt = &S.info[st][kMiPt];  // present token indices
 
     // ---- state-independent work of every present token.
-    // Tap i of channel j along the sequence: i < 3 the source window, else
-    // the input of present token i - 3.
-    const int cs_j = p.conv_sd ? 1 : kWidth - 1, cs_t = p.conv_sd ? kDim : 1;
+    // Each thread holds its channels' sequences in registers: taps 0-2 the
+    // source window, tap 3 + m the input of present token m (bf16 bits).
+    if (w_head != h) load_head(h);
     {
-      const int c = tid >> 7, j = tid & (kDim - 1);
-      const int64_t wbase = static_cast<int64_t>(h) * kDim + j;
-      float wq[kWidth], wv[kWidth];
+      const int cs_j = p.conv_sd ? 1 : kWidth - 1, cs_t = p.conv_sd ? kDim : 1;
+      uint16_t sq[kWidth - 1 + kTMax], sv[kWidth - 1 + kTMax];
 #pragma unroll
-      for (int k = 0; k < kWidth; ++k) wq[k] = __ldg(p.conv_w + (c * kWidth + k) * D + wbase);
-      const float bq = p.conv_b ? __ldg(p.conv_b + c * D + wbase) : 0.0f;
-      float bv = 0.0f, gate_a = 0.0f, gate_bias = 0.0f;
-      if (tid < kDim) {
-#pragma unroll
-        for (int k = 0; k < kWidth; ++k) wv[k] = __ldg(p.conv_w + (2 * kWidth + k) * D + wbase);
-        if (p.conv_b) bv = __ldg(p.conv_b + 2 * D + wbase);
-      } else if (p.fused_gate) {
-        gate_a = expf(__ldg(p.A_log + h));
-        if (p.dt_bias) gate_bias = __ldg(p.dt_bias + wbase);
+      for (int i = 0; i < kWidth - 1; ++i) {
+        sq[i] = S.cs[st][cq][cs_j * jq + cs_t * i];
+        sv[i] = tid < kDim ? S.cs[st][2][cs_j * jq + cs_t * i] : uint16_t{0};
       }
-      auto tap = [&](int cc, int i) -> float {
-        return bf16_to_f32(i < kWidth - 1 ? S.cs[st][cc][cs_j * j + cs_t * i] : S.x[st][pt[i - (kWidth - 1)]][cc][j]);
-      };
-      for (int m = 0; m < np; ++m) {
-        const int t = pt[m];
+#pragma unroll
+      for (int m = 0; m < kTMax; ++m) {
+        sq[kWidth - 1 + m] = m < np ? S.x[st][pt[m]][cq][jq] : uint16_t{0};
+        sv[kWidth - 1 + m] = (m < np && tid < kDim) ? S.x[st][pt[m]][2][jq] : uint16_t{0};
+      }
+#pragma unroll
+      for (int m = 0; m < kTMax; ++m) {
+        if (m >= np) break;
         float y = bq;
 #pragma unroll
-        for (int k = 0; k < kWidth; ++k) y = fmaf(wq[k], tap(c, m + k), y);
-        (c == 0 ? S.q[m] : S.k[m])[j] = y / (1.0f + expf(-y));
+        for (int k = 0; k < kWidth; ++k) y = fmaf(wq[k], bf16_to_f32(sq[m + k]), y);
+        (cq == 0 ? S.q[m] : S.k[m])[jq] = y / (1.0f + expf(-y));
         if (tid < kDim) {
           float yv = bv;
 #pragma unroll
-          for (int k = 0; k < kWidth; ++k) yv = fmaf(wv[k], tap(2, m + k), yv);
-          S.v[m][j] = yv / (1.0f + expf(-yv));
+          for (int k = 0; k < kWidth; ++k) yv = fmaf(wv[k], bf16_to_f32(sv[m + k]), yv);
+          S.v[m][jq] = yv / (1.0f + expf(-yv));
         } else {
-          float g = S.g[st][t][j];
+          float g = S.g[st][pt[m]][jq];
           if (p.fused_gate) {
             const float z = g + gate_bias;
             if (p.lower_bound < 0.0f) {
@@ -384,44 +419,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
               g = -gate_a * sp;
             }
           }
-          S.alpha[m][j] = expf(g);
+          S.alpha[m][jq] = expf(g);
+        }
+        // the window after token m (taps m+1 .. m+3, bit patterns) to its slot
+        if (kUpdateConv) {
+          const int64_t dst = S.info[st][kMiDst + pt[m]];
+          const int64_t chq = cq * D + static_cast<int64_t>(h) * kDim + jq, chv = 2 * D + static_cast<int64_t>(h) * kDim + jq;
+#pragma unroll
+          for (int k = 0; k < kWidth - 1; ++k) {
+            if (p.conv_sd) {
+              p.conv_state[(dst * (kWidth - 1) + k) * 3 * D + chq] = sq[m + 1 + k];
+              if (tid < kDim) p.conv_state[(dst * (kWidth - 1) + k) * 3 * D + chv] = sv[m + 1 + k];
+            } else {
+              p.conv_state[(dst * 3 * D + chq) * (kWidth - 1) + k] = sq[m + 1 + k];
+              if (tid < kDim) p.conv_state[(dst * 3 * D + chv) * (kWidth - 1) + k] = sv[m + 1 + k];
+            }
+          }
         }
       }
       if (tid < np) {  // beta of present token tid
-        const float b = bf16_to_f32(__ldg(p.beta + (static_cast<int64_t>(n) * T + pt[tid]) * p.H + h));
-        S.beta[tid] = p.fused_gate ? 1.0f / (1.0f + expf(-b)) : b;
-      }
-    }
-    // The window after each present token (taps m+1 .. m+3 of the sequence,
-    // bit patterns), stored to that token's slot.
-    if (kUpdateConv && tid < 3 * kCsU4) {
-      const int c = tid / kCsU4, e = tid - c * kCsU4;
-      for (int m = 0; m < np; ++m) {
-        const int dst = S.info[st][kMiDst + pt[m]];
-        uint4 wv4;
-        uint4* dstp;
-        if (p.conv_sd) {  // uint4 e: tap row e / 16, channels 8 (e % 16) .. + 7
-          const int k = e >> 4, q = e & 15, i = m + 1 + k;
-          wv4 = (i < kWidth - 1) ? reinterpret_cast<const uint4*>(S.cs[st][c] + i * kDim)[q]
-                                 : reinterpret_cast<const uint4*>(S.x[st][pt[i - (kWidth - 1)]][c])[q];
-          dstp = reinterpret_cast<uint4*>(p.conv_state + (static_cast<int64_t>(dst) * (kWidth - 1) + k) * 3 * D +
-                                          c * D + static_cast<int64_t>(h) * kDim) + q;
-        } else {  // uint4 e: 8 consecutive (channel, tap) elements
-          uint16_t v8[8];
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const int pos = e * 8 + r, j = pos / 3, i = m + 1 + (pos - 3 * j);
-            v8[r] = (i < kWidth - 1) ? S.cs[st][c][3 * j + i] : S.x[st][pt[i - (kWidth - 1)]][c][j];
-          }
-          wv4.x = v8[0] | (static_cast<uint32_t>(v8[1]) << 16);
-          wv4.y = v8[2] | (static_cast<uint32_t>(v8[3]) << 16);
-          wv4.z = v8[4] | (static_cast<uint32_t>(v8[5]) << 16);
-          wv4.w = v8[6] | (static_cast<uint32_t>(v8[7]) << 16);
-          dstp = reinterpret_cast<uint4*>(
-                     p.conv_state +
-                     (static_cast<int64_t>(dst) * 3 * D + c * D + static_cast<int64_t>(h) * kDim) * (kWidth - 1)) + e;
-        }
-        *dstp = wv4;
+        const float bt = bf16_to_f32(__ldg(p.beta + (static_cast<int64_t>(n) * T + pt[tid]) * p.H + h));
+        S.beta[tid] = p.fused_gate ? 1.0f / (1.0f + expf(-bt)) : bt;
       }
     }
     consumer_sync();
@@ -447,6 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     }
     consumer_sync();
 
+#ifdef KDA_DECODE_TIMELINE
+    if (tid == 0) {
+      const unsigned long long now = global_ns();
+      tl_up += now - tl_t;
+      tl_t = now;
+    }
+#endif
     // ---- the recurrence, token by token, state in registers.
     float4 a[kRowsPerWarp];
     {
@@ -530,7 +555,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
       const int bn = out_buf(st, m);
       const uint32_t wc = (bn == 0) ? wcnt0 : (bn == 1) ? wcnt1 : wcnt2;
       bool fok = true;
+#ifdef KDA_DECODE_TIMELINE
+      const unsigned long long tl_f0 = tid == 0 ? global_ns() : 0ull;
+#endif
       if (wc > 0) fok = mbar_wait_bounded(smem_addr(&S.freed[bn]), (wc - 1) & 1u, p.wait_limit_ns);
+#ifdef KDA_DECODE_TIMELINE
+      if (tid == 0) tl_freed += global_ns() - tl_f0;
+#endif
       if (consumer_any(!fok || S.abort)) {
         if (tid == 0) {
           flag_error(p, KDA_DEVERR_TIMEOUT);
@@ -554,7 +585,26 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     if (aborted) break;
     update_and_write(np - 1);
     if (lane == 0) mbar_arrive(smem_addr(&S.done[st]));
+    {  // the next unit's conv taps, if it is published already
+      const int s2 = (it + 1) % kMStages;
+      if (mbar_try_wait(smem_addr(&S.ready[s2]), ((it + 1) / kMStages) & 1)) {
+        const int n2 = S.info[s2][1], h2 = S.info[s2][2];
+        if (n2 >= 0 && h2 != w_head) load_head(h2);
+      }
+    }
+#ifdef KDA_DECODE_TIMELINE
+    if (tid == 0) tl_loop += global_ns() - tl_t;
+#endif
   }
+#ifdef KDA_DECODE_TIMELINE
+  if (tid == 0) {
+    const unsigned int i = atomicAdd(&g_timeline_n, 1u);
+    if (i < kTimelineMax) {
+      g_timeline[i][0] = blockIdx.x; g_timeline[i][1] = tl_freed; g_timeline[i][2] = tl_start; g_timeline[i][3] = tl_up;
+      g_timeline[i][4] = global_ns(); g_timeline[i][5] = tl_units; g_timeline[i][6] = tl_loop; g_timeline[i][7] = tl_in;
+    }
+  }
+#endif
 }
 
 }  // namespace
