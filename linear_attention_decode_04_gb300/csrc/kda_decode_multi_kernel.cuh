@@ -384,6 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     // source window, tap 3 + m the input of present token m (bf16 bits).
     if (w_head != h) load_head(h);
     {
+      // beta of present token tid: loaded here, used after the conv below
+      const uint16_t beta_bits =
+          tid < np ? __ldg(p.beta + (static_cast<int64_t>(n) * T + pt[tid]) * p.H + h) : uint16_t{0};
       const int cs_j = p.conv_sd ? 1 : kWidth - 1, cs_t = p.conv_sd ? kDim : 1;
       uint16_t sq[kWidth - 1 + kTMax], sv[kWidth - 1 + kTMax];
 #pragma unroll
@@ -437,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
           }
         }
       }
-      if (tid < np) {  // beta of present token tid
-        const float bt = bf16_to_f32(__ldg(p.beta + (static_cast<int64_t>(n) * T + pt[tid]) * p.H + h));
+      if (tid < np) {
+        const float bt = bf16_to_f32(beta_bits);
         S.beta[tid] = p.fused_gate ? 1.0f / (1.0f + expf(-bt)) : bt;
       }
     }
