@@ -601,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       y = fmaf(wq[1], bf16_to_f32(cs[1 * cs_t]), y);
       y = fmaf(wq[2], bf16_to_f32(cs[2 * cs_t]), y);
       y = fmaf(wq[3], bf16_to_f32(S.x[stage][c][j]), y);
-      const float act = y / (1.0f + expf(-y));
+      const float act = __fdividef(y, 1.0f + __expf(-y));
       (c == 0 ? S.q : S.k)[j] = act;
       if (tid < kDim) {
         const uint16_t* csv = S.cs[stage][2] + cs_j * j;
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         yv = fmaf(wv[1], bf16_to_f32(csv[1 * cs_t]), yv);
         yv = fmaf(wv[2], bf16_to_f32(csv[2 * cs_t]), yv);
         yv = fmaf(wv[3], bf16_to_f32(S.x[stage][2][j]), yv);
-        S.v[j] = yv / (1.0f + expf(-yv));
+        S.v[j] = __fdividef(yv, 1.0f + __expf(-yv));
       } else {
         float g = S.g[stage][j];
         if (p.fused_gate) {
@@ -659,18 +659,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     }
     reinterpret_cast<float4*>(S.red[0][warp])[lane] = u;
     reinterpret_cast<float4*>(S.red[1][warp])[lane] = w;
-    // The warp's share of |q~|^2, |k~|^2 and q~.k~ over its 16 key rows: lane
-    // l takes row l mod 16, then a 16-lane butterfly.  The three sums run in
-    // the same order, so q~.k~ equals |k~|^2 bit for bit whenever q~ equals k~.
+    // The warp's share of |q~|^2, |k~|^2 and q~.k~ over its 16 key rows, from
+    // the rows every lane already holds.  The three sums run in the same
+    // order, so q~.k~ equals |k~|^2 bit for bit whenever q~ equals k~.
     {
-      const int i = warp * kRowsPerWarp + (lane & (kRowsPerWarp - 1));
-      const float qi = S.q[i], ki = S.k[i];
-      float pqq = qi * qi, pkk = ki * ki, pqk = qi * ki;
+      float pqq = 0.0f, pkk = 0.0f, pqk = 0.0f;
 #pragma unroll
-      for (int off = kRowsPerWarp / 2; off > 0; off >>= 1) {
-        pqq += __shfl_xor_sync(0xffffffffu, pqq, off);
-        pkk += __shfl_xor_sync(0xffffffffu, pkk, off);
-        pqk += __shfl_xor_sync(0xffffffffu, pqk, off);
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        pqq = fmaf(qt_r[r], qt_r[r], pqq);
+        pkk = fmaf(kt_r[r], kt_r[r], pkk);
+        pqk = fmaf(qt_r[r], kt_r[r], pqk);
       }
       if (lane == 0) S.part[warp] = make_float4(pqq, pkk, pqk, 0.0f);
     }
@@ -697,8 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
         sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
       }
-      const float rq = scale / sqrtf(ssq + 1e-6f);
-      const float rk = 1.0f / sqrtf(ssk + 1e-6f);
+      const float rq = scale * rsqrtf(ssq + 1e-6f);
+      const float rk = rsqrtf(ssk + 1e-6f);
       float ut = 0.0f, wt = 0.0f;
 #pragma unroll
       for (int r = 0; r < kConsumerWarps; ++r) {
@@ -723,12 +721,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     const float4 d = reinterpret_cast<const float4*>(S.delta)[lane];
     float4* tile4w = reinterpret_cast<float4*>(S.tile[stage]);
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const int i = warp * kRowsPerWarp + r;
-      const float kt = kt_r[r];
-      a[r].x = fmaf(kt, d.x, a[r].x); a[r].y = fmaf(kt, d.y, a[r].y);
-      a[r].z = fmaf(kt, d.z, a[r].z); a[r].w = fmaf(kt, d.w, a[r].w);
-      tile4w[i * 32 + lane] = a[r];
+    for (int r4 = 0; r4 < kRowsPerWarp / 4; ++r4) {
+      const float4 kt4 = reinterpret_cast<const float4*>(S.k + warp * kRowsPerWarp)[r4];
+      const float kt_4[4] = {kt4.x, kt4.y, kt4.z, kt4.w};
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const int r = 4 * r4 + i4, i = warp * kRowsPerWarp + r;
+        const float kt = kt_4[i4];
+        a[r].x = fmaf(kt, d.x, a[r].x); a[r].y = fmaf(kt, d.y, a[r].y);
+        a[r].z = fmaf(kt, d.z, a[r].z); a[r].w = fmaf(kt, d.w, a[r].w);
+        tile4w[i * 32 + lane] = a[r];
+      }
     }
     fence_proxy_async_smem();  // generic-proxy writes before the async-proxy store
     __syncwarp();
@@ -740,8 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       float y = o;
       if (kOutNorm) {
         const float ss = (S.osum[0] + S.osum[1]) + (S.osum[2] + S.osum[3]);
-        const float rr = 1.0f / sqrtf(ss * (1.0f / kDim) + p.eps);
-        y = o * rr * nw * (1.0f / (1.0f + expf(-gate_j)));
+        const float rr = rsqrtf(ss * (1.0f / kDim) + p.eps);
+        y = o * rr * nw * __fdividef(1.0f, 1.0f + __expf(-gate_j));
       }
       out_row[tid] = f32_to_bf16(y);
     }
