@@ -405,12 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
         float y = bq;
 #pragma unroll
         for (int k = 0; k < kWidth; ++k) y = fmaf(wq[k], bf16_to_f32(sq[m + k]), y);
-        (cq == 0 ? S.q[m] : S.k[m])[jq] = y / (1.0f + expf(-y));
+        (cq == 0 ? S.q[m] : S.k[m])[jq] = __fdividef(y, 1.0f + __expf(-y));
         if (tid < kDim) {
           float yv = bv;
 #pragma unroll
           for (int k = 0; k < kWidth; ++k) yv = fmaf(wv[k], bf16_to_f32(sv[m + k]), yv);
-          S.v[m][jq] = yv / (1.0f + expf(-yv));
+          S.v[m][jq] = __fdividef(yv, 1.0f + __expf(-yv));
         } else {
           float g = S.g[st][pt[m]][jq];
           if (p.fused_gate) {
@@ -461,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
       sqk = warp_sum(sqk);
       if (lane == 0) {
         const float beta = S.beta[m];
-        const float rq = scale / sqrtf(ssq + 1e-6f);
-        const float rk = 1.0f / sqrtf(ssk + 1e-6f);
+        const float rq = scale * rsqrtf(ssq + 1e-6f);
+        const float rk = rsqrtf(ssk + 1e-6f);
         S.coef[m] = make_float4(rq, rk, (fmaf(-beta, sqk, ssk) + 1e-6f) * (rk * rk), beta * sqk * rq * rk);
       }
     }
@@ -579,8 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
         float y = o;
         if (kOutNorm) {
           const float ss = (S.osum[0] + S.osum[1]) + (S.osum[2] + S.osum[3]);
-          const float rr = 1.0f / sqrtf(ss * (1.0f / kDim) + p.eps);
-          y = o * rr * nw * (1.0f / (1.0f + expf(-bf16_to_f32(S.gate[st][t][tid]))));
+          const float rr = rsqrtf(ss * (1.0f / kDim) + p.eps);
+          y = o * rr * nw * __fdividef(1.0f, 1.0f + __expf(-bf16_to_f32(S.gate[st][t][tid])));
         }
         p.out[(static_cast<int64_t>(n) * T + t) * p.out_stride + static_cast<int64_t>(h) * kDim + tid] = f32_to_bf16(y);
       }
