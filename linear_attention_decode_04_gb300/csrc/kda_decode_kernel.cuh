@@ -563,6 +563,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       continue;
     }
 
+    // This warp's 16 rows of the staged tile into registers now: the reads
+    // do not depend on the conv below and overlap it.
+    float4 a[kRowsPerWarp];
+    {
+      const float4* tile4 = reinterpret_cast<const float4*>(S.tile[stage]);
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
+    }
+
     // Conv-state advance: drop the oldest tap, append the new input (a pure
     // move of bf16 bit patterns).
     if (kUpdateConv && tid < 3 * kCsU4 && p.conv_sd) {
@@ -643,10 +652,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       kt_r[4 * r4] = kt4.x; kt_r[4 * r4 + 1] = kt4.y; kt_r[4 * r4 + 2] = kt4.z; kt_r[4 * r4 + 3] = kt4.w;
       qt_r[4 * r4] = qt4.x; qt_r[4 * r4 + 1] = qt4.y; qt_r[4 * r4 + 2] = qt4.z; qt_r[4 * r4 + 3] = qt4.w;
     }
-    const float4* tile4 = reinterpret_cast<const float4*>(S.tile[stage]);
-    float4 a[kRowsPerWarp];
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
     float4 u = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {

@@ -379,6 +379,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     }
     const int* pt = &S.info[st][kMiPt];  // present token indices
 
+    // This warp's 16 rows of the source state into registers now: the reads
+    // overlap the state-independent work below.
+    float4 a[kRowsPerWarp];
+    {
+      const float4* tile4 = reinterpret_cast<const float4*>(S.tile[st]);
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
+    }
     // ---- state-independent work of every present token.
     // Each thread holds its channels' sequences in registers: taps 0-2 the
     // source window, tap 3 + m the input of present token m (bf16 bits).
@@ -476,12 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
     }
 #endif
     // ---- the recurrence, token by token, state in registers.
-    float4 a[kRowsPerWarp];
-    {
-      const float4* tile4 = reinterpret_cast<const float4*>(S.tile[st]);
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) a[r] = tile4[(warp * kRowsPerWarp + r) * 32 + lane];
-    }
     // Token mp's rank-1 update S' = A + k^ delta^T, and its state into its
     // output buffer for the bulk store to its slot.
     auto update_and_write = [&](int mp) {
