@@ -324,6 +324,15 @@ __global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(con
     S.beta[tid] = bt;
   }
   if (tid == 0) S.slow = 0;
+  // this thread's conv taps and bias, loaded while the copies land
+  float wa[kWidth], ba = 0.0f;
+  {
+    const int c = tid >> 7, j = tid & (kD - 1);
+#pragma unroll
+    for (int t = 0; t < kWidth; ++t)
+      wa[t] = __ldg(p.conv_w + (c * kWidth + t) * D + static_cast<int64_t>(h) * kD + j);
+    if (p.conv_b) ba = __ldg(p.conv_b + ch_global(tid));
+  }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 
@@ -332,11 +341,6 @@ __global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(con
   // tokens
   {
     const int c = tid >> 7, j = tid & (kD - 1);
-    float wa[kWidth], ba = 0.0f;
-#pragma unroll
-    for (int t = 0; t < kWidth; ++t)
-      wa[t] = __ldg(p.conv_w + (c * kWidth + t) * D + static_cast<int64_t>(h) * kD + j);
-    if (p.conv_b) ba = __ldg(p.conv_b + ch_global(tid));
     float x0 = bf16f(S.raw[0][tid]), x1 = bf16f(S.raw[1][tid]), x2 = bf16f(S.raw[2][tid]);
     float* dst = c == 0 ? &S.q[0][j] : c == 1 ? &S.k[0][j] : &S.v[0][j];
 #pragma unroll
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(con
     float4 kv = reinterpret_cast<float4*>(S.k[t])[lane];
     const float sq = warp_sum((qv.x * qv.x + qv.y * qv.y) + (qv.z * qv.z + qv.w * qv.w));
     const float sk = warp_sum((kv.x * kv.x + kv.y * kv.y) + (kv.z * kv.z + kv.w * kv.w));
-    const float rq = qs / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
+    const float rq = qs * rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
     qv.x *= rq; qv.y *= rq; qv.z *= rq; qv.w *= rq;
     kv.x *= rk; kv.y *= rk; kv.z *= rk; kv.w *= rk;
     reinterpret_cast<float4*>(S.q[t])[lane] = qv;
@@ -742,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
   static_assert(kTO == kTS + kD, "the accumulators of [K_E^T; R] must be adjacent");
   const uint32_t lo_addr = smem_u32(S.lo);
   bool ok = true;
+  const float4 nw4 = kOutNorm ? __ldg(reinterpret_cast<const float4*>(p.norm_w) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
 
   for (int64_t jj = 0; jj < n_chunks; ++jj) {
     const int64_t t0 = r0 + kL * jj;
@@ -895,10 +900,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
         for (int m = 16; m > 0; m >>= 1)
 #pragma unroll
           for (int tt = 0; tt < 4; ++tt) ss[tt] += __shfl_xor_sync(0xffffffffu, ss[tt], m);
-        const float4 nw4 = __ldg(reinterpret_cast<const float4*>(p.norm_w) + lane);
 #pragma unroll
         for (int tt = 0; tt < 4; ++tt) {
-          const float rr = 1.0f / sqrtf(ss[tt] * (1.0f / kD) + p.eps);
+          const float rr = rsqrtf(ss[tt] * (1.0f / kD) + p.eps);
           const uint2 gb = gate_pf[tt];
           y[tt].x = __fdividef(y[tt].x * rr * nw4.x, 1.0f + __expf(-__uint_as_float(gb.x << 16)));
           y[tt].y = __fdividef(y[tt].y * rr * nw4.y, 1.0f + __expf(-__uint_as_float(gb.x & 0xFFFF0000u)));
