@@ -526,7 +526,7 @@ def run_prefill(args) -> dict:
     from linear_attention_decode_04_gb300 import workloads as W
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    spec = W.PREFILL_BENCH
+    spec = W.PREFILL_PROFILE if args.prefill_workload == "profile" else W.PREFILL_BENCH
     x = W.make_prefill_inputs(spec)
     bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
     t = dict(qkv=bf(x.qkv), conv_weight=torch.from_numpy(x.conv_weight).to(dev), conv_state=bf(x.conv_state),
@@ -565,7 +565,8 @@ def run_prefill(args) -> dict:
            "value": act_tokens * spec.H / (ms / 1e3), "unit": "updates/s", "ms_per_launch": ms,
            "workload": spec.name, "tokens": spec.T, "sequences": spec.B, "H": spec.H,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                        "traffic": recorded_traffic(PREFILL_TRAFFIC_NOTE, PREFILL_SRC),
+                        "traffic": (recorded_traffic(PREFILL_TRAFFIC_NOTE, PREFILL_SRC)
+                                    if spec is W.PREFILL_BENCH else None),
                         "traffic_note": "both kernels; includes the workspace written and read back",
                         "peak_source": f"{kind} hbm_gbs", "algorithmic_bytes_per_launch": nbytes},
            "tensor": {"achieved_tflops": tflops, "peak_tflops": tpeak, "frac": tflops / tpeak,
@@ -773,6 +774,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--ref-layers", type=int, default=2, help="layers per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-workload", choices=("bench", "profile"), default="bench",
+                    help="--case prefill: the measured 16,384-token batch, or a 4,096-token batch for "
+                         "profiler captures")
     ap.add_argument("--no-cfg3", action="store_true",
                     help="skip the N=256/H=96 single-launch and the multi-token measurements in the headline line")
     ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill", "spec",

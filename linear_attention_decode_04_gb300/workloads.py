@@ -345,6 +345,10 @@ PREFILL_BENCH = PrefillSpec("prefill_b16_t16384_h48_pool64",
                             lens=(2900, 1, 1800, 417, 64, 2048, 999, 17, 1500, 700, 2345, 100, 33,
                                   1210, 230, 2020),
                             H=48, num_slots=64, seed=53)
+# A quarter of that for profiler captures: 4 sequences, 4,096 tokens, H = 48
+# (inputs and workspace still larger than L2, under 1 GB on the device).
+PREFILL_PROFILE = PrefillSpec("prefill_b4_t4096_h48_pool16", lens=(1500, 1024, 900, 672), H=48,
+                              num_slots=16, seed=54)
 
 
 @dataclass
