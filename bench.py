@@ -431,6 +431,10 @@ def run_ours(args) -> dict | None:
     spec_decode = None
     if not args.no_cfg3:
         spec_decode = spec_launch(device, W.MULTI_BENCH, args.warmup, max(args.steps, 50))
+    prefill = None
+    if not args.no_cfg3:
+        prefill, _ = prefill_timing(device, W.PREFILL_BENCH, args.warmup, max(args.steps, 50))
+        prefill.pop("mode", None)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -483,6 +487,7 @@ def run_ours(args) -> dict | None:
                   "how": "the same 69 launches issued one C-ABI call at a time from Python, no graph"},
         "cfg3": cfg3,
         "spec_decode": spec_decode,
+        "prefill": prefill,
         "impl": "ours",
     }
 
@@ -522,11 +527,40 @@ def run_prefill(args) -> dict:
     step to step.  ``value`` = (token, head) updates per second."""
     import torch
 
-    from linear_attention_decode_04_gb300 import KdaPrefillCall
     from linear_attention_decode_04_gb300 import workloads as W
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     spec = W.PREFILL_PROFILE if args.prefill_workload == "profile" else W.PREFILL_BENCH
+    res, x = prefill_timing(dev, spec, args.warmup, args.steps)
+    act_tokens = sum(n for b, n in enumerate(spec.lens) if b not in spec.pad_seqs)
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = os.cpu_count() or 1
+        updates = passes = 0
+        t0 = time.perf_counter()
+        while True:  # whole batch, repeated until the time budget is spent
+            oracle.prefill(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state,
+                           g=x.g, beta=x.beta, gate=x.gate, norm_weight=x.norm_weight, slot_idx=x.slot_idx,
+                           cu_seqlens=x.cu_seqlens, H=spec.H, eps=spec.eps, threads=threads, want_f64=False)
+            updates += act_tokens * spec.H
+            passes += 1
+            dt = time.perf_counter() - t0
+            if dt >= args.cpu_budget:
+                break
+        res["cpu_baseline"] = {"value": updates / dt, "unit": "updates/s", "cores": threads, "kind": "oracle",
+                               "sample": f"fp64 C prefill oracle, OpenMP {threads} threads, the whole batch "
+                                         f"x{passes} ({updates} (token, head) updates, {dt:.1f} s)"}
+    return res
+
+
+def prefill_timing(dev, spec, warmup: int, steps: int):
+    """``steps`` kda_prefill launches over one varlen batch timed between
+    CUDA events (after ``warmup`` untimed ones); the result line's fields and
+    the host inputs."""
+    import torch
+
+    from linear_attention_decode_04_gb300 import KdaPrefillCall
+    from linear_attention_decode_04_gb300 import workloads as W
     x = W.make_prefill_inputs(spec)
     bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
     t = dict(qkv=bf(x.qkv), conv_weight=torch.from_numpy(x.conv_weight).to(dev), conv_state=bf(x.conv_state),
@@ -541,19 +575,19 @@ def run_prefill(args) -> dict:
                           norm_weight=t["norm_weight"], eps=spec.eps, out_norm=spec.out_norm,
                           err_flag=t["err_flag"])
     stream = torch.cuda.Stream(dev)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         call(stream)
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clk:
         ev0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             call(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     if int(t["err_flag"].item()):
         raise SystemExit("device error flag raised")
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = ev0.elapsed_time(ev1) / steps
     act_tokens = sum(n for b, n in enumerate(spec.lens) if b not in spec.pad_seqs)
     nbytes = W.prefill_algorithmic_bytes(spec)
     flops = W.prefill_algorithmic_flops(spec)
@@ -573,28 +607,13 @@ def run_prefill(args) -> dict:
                       "peak_source": tkind, "algorithmic_flops_per_launch": flops,
                       "note": "chunk-form contractions counted once; the kernel issues three tf32 "
                               "products per contraction (split operands)"},
-           "clocks": clk.summary(), "steps": args.steps, "warmup": args.warmup,
-           "gpu_launches": 3 * args.steps,
+           "clocks": clk.summary(), "steps": steps, "warmup": warmup,
+           "gpu_launches": 3 * steps,
            "kernels": "per step: chunk metadata, chunk-parallel kernel, scan kernel",
            "scan_order": "longest sequence first" if call.seq_order is not None else "index"}
-    if not args.no_cpu_baseline:
-        import oracle
-        threads = os.cpu_count() or 1
-        updates = passes = 0
-        t0 = time.perf_counter()
-        while True:  # whole batch, repeated until the time budget is spent
-            oracle.prefill(qkv=x.qkv, conv_weight=x.conv_weight, conv_state=x.conv_state, state=x.state,
-                           g=x.g, beta=x.beta, gate=x.gate, norm_weight=x.norm_weight, slot_idx=x.slot_idx,
-                           cu_seqlens=x.cu_seqlens, H=spec.H, eps=spec.eps, threads=threads, want_f64=False)
-            updates += act_tokens * spec.H
-            passes += 1
-            dt = time.perf_counter() - t0
-            if dt >= args.cpu_budget:
-                break
-        res["cpu_baseline"] = {"value": updates / dt, "unit": "updates/s", "cores": threads, "kind": "oracle",
-                               "sample": f"fp64 C prefill oracle, OpenMP {threads} threads, the whole batch "
-                                         f"x{passes} ({updates} (token, head) updates, {dt:.1f} s)"}
-    return res
+    del call, t
+    torch.cuda.empty_cache()
+    return res, x
 
 
 def run_chunk_metadata(args) -> dict:
@@ -778,7 +797,8 @@ def main(argv=None):
                     help="--case prefill: the measured 16,384-token batch, or a 4,096-token batch for "
                          "profiler captures")
     ap.add_argument("--no-cfg3", action="store_true",
-                    help="skip the N=256/H=96 single-launch and the multi-token measurements in the headline line")
+                    help="skip the N=256/H=96 single-launch, multi-token and prefill measurements in the "
+                         "headline line")
     ap.add_argument("--case", choices=("stack69", "layer", "roofline", "chunk_metadata", "prefill", "spec",
                                        "configs", "timeline", "spec_timeline"),
                     default="stack69",
