@@ -714,12 +714,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
 
   // state S^T row j, keys [64 half, 64 half + 64): fp32, high and low words
   float* Sg = p.state + (static_cast<int64_t>(slot) * p.H + h) * (kD * kD);
+  float sx[64];  // all of this thread's loads in flight at once
+#pragma unroll
+  for (int e = 0; e < 64; ++e) sx[e] = Sg[static_cast<int64_t>(64 * half + e) * kD + j];
 #pragma unroll
   for (int cc = 0; cc < 64; cc += 16) {
     uint32_t v[16], hi[16], lo[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const float x = Sg[static_cast<int64_t>(64 * half + cc + e) * kD + j];
+      const float x = sx[cc + e];
       v[e] = __float_as_uint(x);
       hi[e] = tf32_hi(x);
       lo[e] = tf32_lo(x, hi[e]);
@@ -764,11 +767,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     float* img = S.img[buf];
     const uint32_t img_addr = smem_u32(img);
 
-    // split the image's tensor-core operands: high words in place, remainders aside
+    // split the image's tensor-core operands: high words in place, remainders
+    // aside ([Q_G; W] of every chunk after the first was split while the
+    // previous chunk's second product batch ran)
     {
       float4* im = reinterpret_cast<float4*>(img);
       float4* lo4 = reinterpret_cast<float4*>(S.lo);
-      for (int e = tid; e < kSplit / 4; e += kThreads) {
+      for (int e = (jj == 0 ? 0 : kOffB2 / 4) + tid; e < kSplit / 4; e += kThreads) {
         float4 x = im[e], l;
         uint32_t hb;
         hb = tf32_hi(x.x); l.x = __uint_as_float(tf32_lo(x.x, hb)); x.x = __uint_as_float(hb);
@@ -855,7 +860,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
         mma_ts3(tbase + kTS, tbase + kTDH + 8 * ks, tbase + kTDL + 8 * ks, bh + 320 * ks, bl + 320 * ks, kId160, 1);
       mma_commit(smem_u32(&S.bar[1]));
     }
-    ok = bar_wait(smem_u32(&S.bar[1]), par);
+    // While it runs (it reads only [K_E^T; R]'s remainders): the next image's
+    // [Q_G; W], high words in place and remainders aside, once it has landed
+    bool ok_next = true;
+    if (jj + 1 < n_chunks) {
+      ok_next = bar_wait(smem_u32(&S.full[buf ^ 1]), pending_par);
+      if (ok_next) {
+        float4* im = reinterpret_cast<float4*>(S.img[buf ^ 1]);
+        float4* lo4 = reinterpret_cast<float4*>(S.lo);
+        for (int e = kOffB1 / 4 + tid; e < kOffB2 / 4; e += kThreads) {
+          float4 x = im[e], l;
+          uint32_t hb;
+          hb = tf32_hi(x.x); l.x = __uint_as_float(tf32_lo(x.x, hb)); x.x = __uint_as_float(hb);
+          hb = tf32_hi(x.y); l.y = __uint_as_float(tf32_lo(x.y, hb)); x.y = __uint_as_float(hb);
+          hb = tf32_hi(x.z); l.z = __uint_as_float(tf32_lo(x.z, hb)); x.z = __uint_as_float(hb);
+          hb = tf32_hi(x.w); l.w = __uint_as_float(tf32_lo(x.w, hb)); x.w = __uint_as_float(hb);
+          im[e] = x;
+          lo4[e] = l;
+        }
+      }
+    }
+    ok = bar_wait(smem_u32(&S.bar[1]), par) && ok_next;
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
