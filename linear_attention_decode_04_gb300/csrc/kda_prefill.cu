@@ -749,6 +749,24 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
   static_assert(kTO == kTS + kD, "the accumulators of [K_E^T; R] must be adjacent");
   const uint32_t lo_addr = smem_u32(S.lo);
   bool ok = true;
+  // An image's tensor-core operands over float4 pieces [e0, e1): high words
+  // in place, remainders to the same place in `lo`, fenced for the tensor
+  // cores' view.
+  auto split_operands = [&](float* imgp, int e0, int e1) {
+    float4* im = reinterpret_cast<float4*>(imgp);
+    float4* lo4 = reinterpret_cast<float4*>(S.lo);
+    for (int e = e0 + tid; e < e1; e += kThreads) {
+      float4 x = im[e], l;
+      uint32_t hb;
+      hb = tf32_hi(x.x); l.x = __uint_as_float(tf32_lo(x.x, hb)); x.x = __uint_as_float(hb);
+      hb = tf32_hi(x.y); l.y = __uint_as_float(tf32_lo(x.y, hb)); x.y = __uint_as_float(hb);
+      hb = tf32_hi(x.z); l.z = __uint_as_float(tf32_lo(x.z, hb)); x.z = __uint_as_float(hb);
+      hb = tf32_hi(x.w); l.w = __uint_as_float(tf32_lo(x.w, hb)); x.w = __uint_as_float(hb);
+      im[e] = x;
+      lo4[e] = l;
+    }
+    fence_proxy_async();
+  };
   const float4 nw4 = kOutNorm ? __ldg(reinterpret_cast<const float4*>(p.norm_w) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
 
   for (int64_t jj = 0; jj < n_chunks; ++jj) {
@@ -767,26 +785,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     float* img = S.img[buf];
     const uint32_t img_addr = smem_u32(img);
 
-    // split the image's tensor-core operands: high words in place, remainders
-    // aside ([Q_G; W] of every chunk after the first was split while the
-    // previous chunk's second product batch ran)
-    {
-      float4* im = reinterpret_cast<float4*>(img);
-      float4* lo4 = reinterpret_cast<float4*>(S.lo);
-      for (int e = (jj == 0 ? 0 : kOffB2 / 4) + tid; e < kSplit / 4; e += kThreads) {
-        float4 x = im[e], l;
-        uint32_t hb;
-        hb = tf32_hi(x.x); l.x = __uint_as_float(tf32_lo(x.x, hb)); x.x = __uint_as_float(hb);
-        hb = tf32_hi(x.y); l.y = __uint_as_float(tf32_lo(x.y, hb)); x.y = __uint_as_float(hb);
-        hb = tf32_hi(x.z); l.z = __uint_as_float(tf32_lo(x.z, hb)); x.z = __uint_as_float(hb);
-        hb = tf32_hi(x.w); l.w = __uint_as_float(tf32_lo(x.w, hb)); x.w = __uint_as_float(hb);
-        im[e] = x;
-        lo4[e] = l;
-      }
+    // [Q_G; W] of every chunk after the first was split while the previous
+    // chunk's second product batch ran; the first chunk's is split here
+    if (jj == 0) {
+      split_operands(img, kOffB1 / 4, kOffB2 / 4);
+      tc_fence_before();
+      __syncthreads();
     }
-    fence_proxy_async();                   // generic writes -> the tensor cores' view
-    tc_fence_before();
-    __syncthreads();
     tc_fence_after();
 
     // ---- [D_O | D_Delta] = S^T [Q_G; W]^T  (N = 64, one B block; the two
@@ -826,6 +831,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
         gate_pf[tt] = __ldg(reinterpret_cast<const uint2*>(p.gate + (t0 + t) * p.gate_stride +
                                                            static_cast<int64_t>(h) * kD) + lane);
     }
+    // [K_E^T; R] of this image (the first batch reads only [Q_G; W])
+    split_operands(img, kOffB2 / 4, kSplit / 4);
     ok = bar_wait(smem_u32(&S.bar[0]), par);
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
@@ -861,24 +868,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
       mma_commit(smem_u32(&S.bar[1]));
     }
     // While it runs (it reads only [K_E^T; R]'s remainders): the next image's
-    // [Q_G; W], high words in place and remainders aside, once it has landed
+    // [Q_G; W] split, once it has landed
     bool ok_next = true;
     if (jj + 1 < n_chunks) {
       ok_next = bar_wait(smem_u32(&S.full[buf ^ 1]), pending_par);
-      if (ok_next) {
-        float4* im = reinterpret_cast<float4*>(S.img[buf ^ 1]);
-        float4* lo4 = reinterpret_cast<float4*>(S.lo);
-        for (int e = kOffB1 / 4 + tid; e < kOffB2 / 4; e += kThreads) {
-          float4 x = im[e], l;
-          uint32_t hb;
-          hb = tf32_hi(x.x); l.x = __uint_as_float(tf32_lo(x.x, hb)); x.x = __uint_as_float(hb);
-          hb = tf32_hi(x.y); l.y = __uint_as_float(tf32_lo(x.y, hb)); x.y = __uint_as_float(hb);
-          hb = tf32_hi(x.z); l.z = __uint_as_float(tf32_lo(x.z, hb)); x.z = __uint_as_float(hb);
-          hb = tf32_hi(x.w); l.w = __uint_as_float(tf32_lo(x.w, hb)); x.w = __uint_as_float(hb);
-          im[e] = x;
-          lo4[e] = l;
-        }
-      }
+      if (ok_next) split_operands(S.img[buf ^ 1], kOffB1 / 4, kOffB2 / 4);
     }
     ok = bar_wait(smem_u32(&S.bar[1]), par) && ok_next;
     if (__syncthreads_or(!ok)) break;
