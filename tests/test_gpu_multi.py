@@ -72,6 +72,29 @@ def test_multi_token_parity(Tn, out_norm, cuda_device):
     _compare(x, d, _oracle(x))
 
 
+@pytest.mark.parametrize("Tn", [3, 6])
+def test_cancelling_readout(Tn, cuda_device):
+    """Every token in the regime where the readout cancels: q~ = k~ exactly
+    (identical conv weights, taps and inputs for the q and k channels),
+    beta = 1, g = 0, a source state of N(0, 30) and v conv weights scaled by
+    1e-2.  Each token's o is then orders of magnitude below A^T q^; the
+    outputs must still be within one bf16 ulp of the exact value.  T = 3 and
+    6 run the kernel built for up to 4 and up to 8 tokens."""
+    spec = W.MultiSpec(f"spec_n8_t{Tn}_h12_cancel", N=8, T=Tn, H=12, num_slots=8 * (Tn + 1) + 3, seed=340 + Tn)
+    x = W.make_multi_inputs(spec)
+    D = x.H * 128
+    x.conv_weight[1] = x.conv_weight[0]
+    x.conv_weight[2] *= np.float32(1e-2)
+    x.qkv[:, D:2 * D] = x.qkv[:, 0:D]
+    x.conv_state[:, D:2 * D, :] = x.conv_state[:, 0:D, :]
+    x.beta[:] = W.f32_to_bf16_bits(np.ones(1, np.float32))[0]
+    x.g[:] = 0.0
+    x.state *= np.float32(30.0 / 0.02)
+    d = _dev(x, cuda_device)
+    _call(x, d)()
+    _compare(x, d, _oracle(x))
+
+
 def test_t1_with_source_slot(cuda_device):
     """T = 1 with a separate source: decode into a fresh slot (copy on write)."""
     x = W.make_multi_inputs(W.MultiSpec("spec_n16_t1_h12", N=16, T=1, H=12, num_slots=40, seed=320))
