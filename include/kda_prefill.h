@@ -162,7 +162,7 @@ typedef struct KdaPrefillArgs {
 int kda_prefill_longest_first(const int32_t* cu_seqlens, int32_t B, int32_t* order);
 
 /* Workspace bytes a call with `num_chunks` chunks and H heads needs (about
- * 68.5 KiB, 70,144 bytes, per (chunk, head)); -1 for a negative count or H < 1. */
+ * 84.5 KiB, 86,528 bytes, per (chunk, head)); -1 for a negative count or H < 1. */
 int64_t kda_prefill_workspace_bytes(int64_t num_chunks, int32_t H);
 
 /*

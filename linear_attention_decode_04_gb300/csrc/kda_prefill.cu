@@ -19,7 +19,13 @@
 //     O = Q_G S0 + R Delta,                                 R_ts = sum_i q^_ti k^_si exp(G_ti - G_si)  (s <= t)
 //     S_L = Diag(exp G_{L-1}) S0 + K_E^T Delta
 // with K_G = exp(G) . K^, Q_G = exp(G) . Q^ and K_E = exp(G_{L-1} - G) . K^
-// (row-wise).  The triangular system is solved once for both right-hand
+// (row-wise).  The output is evaluated in the decode step's cancellation-safe
+// form instead: o_t = A_t^T q'_t + c_t v~_t, A_t the state before token t's
+// update, q'_t = r_q ((q~_t - k~_t) + m_t k~_t) = q^_t - beta_t (q^_t.k^_t) k^_t
+// and c_t = beta_t (q^_t.k^_t); that is, q^ replaced by q' in Q_G and R, R
+// strictly lower (s < t), and E = Diag(c) V~ added to O.  When q~ = k~ the
+// plain O cancels two terms of the size of the state down to |v~|; q' is then
+// r_q m k~ (tiny) and no such cancellation occurs.  The triangular system is solved once for both right-hand
 // sides, X = [U | W] with (I + Diag(beta) P) X = Diag(beta) [V~ | K_G], so
 // Delta = U - W S0.  P and R are contractions over the key channels once the
 // decay factor is split around a reference token m of the chunk:
@@ -65,7 +71,7 @@ struct PrefillParams {
   const int32_t* chunk_idx;   // [num_chunks][2] (sequence, chunk)
   const int64_t* chunk_off;   // [B + 1]
   int64_t num_chunks;
-  float* ws;                  // per (chunk row, head) one image of kImg floats
+  float* ws;                  // per (chunk row, head) one record of kRec floats
   const uint16_t* qkv;
   int64_t qkv_stride;
   const float* conv_w;
@@ -109,9 +115,11 @@ constexpr int kOffB1 = 0;                     // [Q_G; W]   64 x 128
 constexpr int kOffB2 = kOffB1 + kNB1 * kD;    // [K_E^T; R] 160 x 32 (R zero above its diagonal)
 constexpr int kOffU = kOffB2 + kNB2 * kL;     // U     [32 tokens][128 values], row-major
 constexpr int kOffC = kOffU + kL * kD;        // gamma = exp(G_{L-1}) [128]
-constexpr int kImg = kOffC + kD;              // 17,536 floats = 70,144 bytes
+constexpr int kImg = kOffC + kD;              // 17,536 floats = 70,144 bytes (copied in one piece)
+constexpr int kOffE = kImg;                   // E = Diag(c) V~ [32 tokens][128 values], row-major
+constexpr int kRec = kOffE + kL * kD;         // one workspace record: 21,632 floats = 86,528 bytes
 constexpr int kSplit = kOffU;                 // the operands the scan splits into tf32 words
-static_assert((kImg * 4) % 16 == 0, "image must be a whole number of 16-byte pieces");
+static_assert((kImg * 4) % 16 == 0 && (kRec * 4) % 16 == 0, "records must be whole 16-byte pieces");
 
 // Chunk kernel shared memory (about 107 KB: two CTAs per SM).
 struct __align__(16) ChunkSmem {
@@ -128,6 +136,7 @@ struct __align__(16) ChunkSmem {
   float G[kL][kSA];                 // cumulative log decay
   float P[kL][kSP];                 // P (strictly lower)
   float beta[kL];
+  float c[kL];                      // beta_t (q^_t . k^_t), the weight of v~_t in o_t
   float egm[kD];                    // exp(G_m) per key channel (0 when G_m < -kMaxExponent)
   float cl[kD];                     // exp(G_{L-1} - G_m) per key channel
   int slow;                         // this chunk takes the element-wise P / R path
@@ -140,11 +149,15 @@ struct __align__(16) ChunkSmem {
 struct __align__(128) ScanSmem {
   float img[2][kImg];
   float lo[kSplit];
-  float o[kL][kSA];
+  float o[kL][kD];             // the chunk's output rows: E = Diag(c) V~ (bulk copy), then + D_O
   unsigned long long bar[2];   // the two MMA batches of a chunk
   unsigned long long full[2];  // image buffer 0 / 1 landed
+  unsigned long long efull;    // E landed in o
   uint32_t tmem;
 };
+
+static_assert(sizeof(ScanSmem) <= 227 * 1024, "scan kernel shared memory above the 227 KB a CTA may use");
+static_assert(2 * (sizeof(ChunkSmem) + 1024) <= 228 * 1024, "two chunk-kernel CTAs must fit one SM");
 
 // Tensor-memory columns of the scan kernel (512 allocated; lane = value row):
 // the fp32 state S^T, the chunk's output and S^T W^T accumulators, the
@@ -258,7 +271,7 @@ __global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(con
   const int slot = p.slot_idx[b];
   if (slot <= 0 || slot >= p.num_slots) return;  // the scan kernel zeroes and flags
   const int L = static_cast<int>(r1 - t0 < kL ? r1 - t0 : kL);
-  float* ws = p.ws + (c * p.H + h) * static_cast<int64_t>(kImg);
+  float* ws = p.ws + (c * p.H + h) * static_cast<int64_t>(kRec);
   auto ch_global = [&](int ch) { return static_cast<int64_t>(ch >> 7) * D + static_cast<int64_t>(h) * kD + (ch & 127); };
 
   // ---- 1. inputs: the three older taps (conv state for the first chunk,
@@ -359,16 +372,27 @@ __global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(con
 
   // ---- 3. L2 norms (warp w: tokens w, w + 12, w + 24); cumulative decay
   const float qs = (p.q_scale != 0.0f) ? p.q_scale : 0.088388347648318440550f;  // 1/sqrt(128)
+  // In place of q^_t the chunk carries q'_t = r_q ((q~_t - k~_t) + m_t k~_t),
+  // m_t = (|k~_t|^2 + 1e-6 - beta_t q~_t.k~_t) r_k^2, and c_t = beta_t
+  // (q^_t . k^_t): o_t = A_t^T q'_t + c_t v~_t with A_t the state before token
+  // t's update (the decode step's cancellation-safe readout).  The three
+  // sums run in one order, so q~.k~ equals |k~|^2 bit for bit when q~ equals
+  // k~, and then q' = r_q m k~ is tiny: nothing of the size of the state
+  // cancels in the output.
   for (int t = warp; t < kL; t += kChunkWarps) {
-    float4 qv = reinterpret_cast<float4*>(S.q[t])[lane];
-    float4 kv = reinterpret_cast<float4*>(S.k[t])[lane];
-    const float sq = warp_sum((qv.x * qv.x + qv.y * qv.y) + (qv.z * qv.z + qv.w * qv.w));
-    const float sk = warp_sum((kv.x * kv.x + kv.y * kv.y) + (kv.z * kv.z + kv.w * kv.w));
+    const float4 qv = reinterpret_cast<float4*>(S.q[t])[lane];
+    const float4 kv = reinterpret_cast<float4*>(S.k[t])[lane];
+    const float sq = warp_sum(fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, fmaf(qv.z, qv.z, qv.w * qv.w))));
+    const float sk = warp_sum(fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, fmaf(kv.z, kv.z, kv.w * kv.w))));
+    const float sqk = warp_sum(fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, qv.w * kv.w))));
     const float rq = qs * rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
-    qv.x *= rq; qv.y *= rq; qv.z *= rq; qv.w *= rq;
-    kv.x *= rk; kv.y *= rk; kv.z *= rk; kv.w *= rk;
-    reinterpret_cast<float4*>(S.q[t])[lane] = qv;
-    reinterpret_cast<float4*>(S.k[t])[lane] = kv;
+    const float bt = S.beta[t];
+    const float m = (fmaf(-bt, sqk, sk) + 1e-6f) * (rk * rk);
+    const float4 qp = make_float4(rq * fmaf(m, kv.x, qv.x - kv.x), rq * fmaf(m, kv.y, qv.y - kv.y),
+                                  rq * fmaf(m, kv.z, qv.z - kv.z), rq * fmaf(m, kv.w, qv.w - kv.w));
+    reinterpret_cast<float4*>(S.q[t])[lane] = qp;
+    reinterpret_cast<float4*>(S.k[t])[lane] = make_float4(kv.x * rk, kv.y * rk, kv.z * rk, kv.w * rk);
+    if (lane == 0) S.c[t] = bt * sqk * rq * rk;
   }
   if (tid < kD) {
     float acc = 0.0f;
@@ -400,6 +424,13 @@ __global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(con
   // take consecutive t, so the image stores of Q_G are coalesced 16-byte
   // pieces.
   const bool slow = S.slow != 0;
+  // E = Diag(c) V~ to the record (its own region, row-major)
+  for (int e = tid; e < kL * kD / 4; e += kChunkThreads) {
+    const int t = e >> 5, j4 = e & 31;
+    const float ct = S.c[t];
+    const float4 v4 = reinterpret_cast<const float4*>(S.v[t])[j4];
+    reinterpret_cast<float4*>(ws + kOffE + t * kD)[j4] = make_float4(ct * v4.x, ct * v4.y, ct * v4.z, ct * v4.w);
+  }
   for (int e = tid; e < kL * kD / 4; e += kChunkThreads) {
     const int t = e & (kL - 1), i0 = 4 * (e >> 5);
     const float4 G4 = *reinterpret_cast<const float4*>(&S.G[t][i0]);
@@ -464,7 +495,7 @@ __global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(con
         if (mat == 0) {
           if (te > se) S.P[te][se] = acc[e];
         } else {
-          if (te >= se) ws[kOffB2 + kpos(kD + te, se, kNB2)] = acc[e];
+          if (te > se) ws[kOffB2 + kpos(kD + te, se, kNB2)] = acc[e];
         }
       }
     };
@@ -485,8 +516,10 @@ __global__ void __launch_bounds__(kChunkThreads, 2) kda_prefill_chunk_kernel(con
         pk = fmaf(S.k[t][i], fct, pk);
         pq = fmaf(S.q[t][i], fct, pq);
       }
-      if (t > s) S.P[t][s] = pk;
-      ws[kOffB2 + kpos(kD + t, s, kNB2)] = pq;
+      if (t > s) {
+        S.P[t][s] = pk;
+        ws[kOffB2 + kpos(kD + t, s, kNB2)] = pq;
+      }
     }
   }
   __syncthreads();
@@ -700,6 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.bar[1])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.full[0])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.full[1])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&S.efull)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -737,13 +771,23 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
   auto fetch = [&](int64_t jj, int buf) {
     if (tid == 0) {
       fence_proxy_async();  // earlier generic accesses to the buffer before the async-proxy write
-      bulk_load(smem_u32(S.img[buf]), p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kImg), kImg * 4,
+      bulk_load(smem_u32(S.img[buf]), p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kRec), kImg * 4,
                 smem_u32(&S.full[buf]));
+    }
+  };
+  // chunk jj's E: one bulk copy into the output rows (free once the previous
+  // chunk's epilogue is done), issued by thread 0
+  auto fetch_e = [&](int64_t jj) {
+    if (tid == 0) {
+      fence_proxy_async();  // the previous epilogue's reads before the async-proxy write
+      bulk_load(smem_u32(&S.o[0][0]), p.ws + ((c0 + jj) * p.H + h) * static_cast<int64_t>(kRec) + kOffE,
+                kL * kD * 4, smem_u32(&S.efull));
     }
   };
   fetch(0, 0);
   int pending = 0;           // buffer whose copy is in flight (-1: none)
   uint32_t pending_par = 0;  // and the phase its barrier completes
+  int64_t e_pending = -1;    // chunk whose E copy is in flight (-1: none)
   constexpr uint32_t kId64 = idesc_tf32(kNB1), kId160 = idesc_tf32(kNB2);
   static_assert(kTD == kTO + kL, "the accumulators of [Q_G; W] must be adjacent");
   static_assert(kTO == kTS + kD, "the accumulators of [K_E^T; R] must be adjacent");
@@ -782,6 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
       pending = buf ^ 1;
       pending_par = static_cast<uint32_t>(((jj + 1) >> 1) & 1);
     }
+    fetch_e(jj);
+    e_pending = jj;
     float* img = S.img[buf];
     const uint32_t img_addr = smem_u32(img);
 
@@ -874,16 +920,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
       ok_next = bar_wait(smem_u32(&S.full[buf ^ 1]), pending_par);
       if (ok_next) split_operands(S.img[buf ^ 1], kOffB1 / 4, kOffB2 / 4);
     }
-    ok = bar_wait(smem_u32(&S.bar[1]), par) && ok_next;
+    ok = bar_wait(smem_u32(&S.bar[1]), par) && ok_next && bar_wait(smem_u32(&S.efull), par);
+    if (ok) e_pending = -1;
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // the chunk's output rows to shared memory; the new state's split words
+    // the chunk's output rows (D_O added to E in shared memory); the new state's split words
     {
       uint32_t r[16];
       tm_ld16(tm + kTO + 16 * half, r);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) S.o[16 * half + e][j] = __uint_as_float(r[e]);
+      for (int e = 0; e < 16; ++e) S.o[16 * half + e][j] += __uint_as_float(r[e]);  // E + D_O
 #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
         uint32_t v[32], hi[32];
@@ -942,6 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_scan_kernel(const Pre
     // leaving early: let the copy in flight land before the shared memory goes away
     bar_wait(smem_u32(&S.full[pending]), pending_par);
   }
+  if (!ok && e_pending >= 0) bar_wait(smem_u32(&S.efull), static_cast<uint32_t>(e_pending & 1));
   if (ok) {
     // ---- sequence end: state and conv window back to the slot.  The window
     // [old taps | tokens] ends with its last three inputs; for sequences of
@@ -1006,7 +1054,7 @@ bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 
 extern "C" int64_t kda_prefill_workspace_bytes(int64_t num_chunks, int32_t H) {
   if (num_chunks < 0 || H < 1) return -1;
-  return num_chunks * H * static_cast<int64_t>(kImg) * 4;
+  return num_chunks * H * static_cast<int64_t>(kRec) * 4;
 }
 
 extern "C" int kda_prefill_longest_first(const int32_t* cu_seqlens, int32_t B, int32_t* order) {

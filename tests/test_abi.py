@@ -104,7 +104,7 @@ def test_prefill_host_validation_codes(lib):
     assert call(_pargs(seq_order=0x20002)) == -3        # seq_order needs 4-byte alignment
     L.kda_prefill_workspace_bytes.restype = ctypes.c_int64
     L.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
-    assert L.kda_prefill_workspace_bytes(10, 4) == 10 * 4 * 70144
+    assert L.kda_prefill_workspace_bytes(10, 4) == 10 * 4 * 86528
     assert L.kda_prefill_workspace_bytes(-1, 4) == -1
 
 
