@@ -485,14 +485,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
   UnitInputs cur, nxt;
   bool have_next = false;  // nxt holds the inputs of the coming unit
 #ifdef KDA_DECODE_TIMELINE
-  unsigned long long tl_start = 0, tl_first = 0, tl_wait = 0, tl_comp = 0, tl_units = 0, tl_w0 = 0, tl_r = 0;
-  if (tid == 0) tl_start = global_ns();
+  // thread 0's accumulators, in shared memory so that they take no registers:
+  // start, first unit ready, wait, compute, units, loop top, vote passed
+  __shared__ unsigned long long tl_acc[7];
+  volatile unsigned long long* tl = tl_acc;
+  if (tid == 0) {
+    tl[0] = global_ns();
+    for (int i = 1; i < 7; ++i) tl[i] = 0;
+  }
 #endif
   for (int it = 0;; ++it) {
 #ifdef KDA_DECODE_TIMELINE
     if (tid == 0) {
-      tl_w0 = global_ns();
-      if (it > 0) tl_comp += tl_w0 - tl_r;
+      const unsigned long long now = global_ns();
+      tl[5] = now;
+      if (it > 0) tl[3] += now - tl[6];
     }
 #endif
     const int stage = it % kStages;
@@ -528,10 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     }
 #ifdef KDA_DECODE_TIMELINE
     if (tid == 0) {
-      tl_r = global_ns();
-      tl_wait += tl_r - tl_w0;
-      if (it == 0) tl_first = tl_r;
-      if (n >= 0) ++tl_units;
+      const unsigned long long now = global_ns();
+      tl[6] = now;
+      tl[2] += now - tl[5];
+      if (it == 0) tl[1] = now;
+      if (n >= 0) tl[4] += 1;
     }
 #endif
     if (n < 0) break;  // no more units
@@ -761,8 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     const unsigned int i = atomicAdd(&g_timeline_n, 1u);
     if (i < kTimelineMax) {
-      g_timeline[i][0] = blockIdx.x; g_timeline[i][1] = smid; g_timeline[i][2] = tl_start; g_timeline[i][3] = tl_first;
-      g_timeline[i][4] = te; g_timeline[i][5] = tl_units; g_timeline[i][6] = tl_comp; g_timeline[i][7] = tl_wait;
+      g_timeline[i][0] = blockIdx.x; g_timeline[i][1] = smid; g_timeline[i][2] = tl[0]; g_timeline[i][3] = tl[1];
+      g_timeline[i][4] = te; g_timeline[i][5] = tl[4]; g_timeline[i][6] = tl[3]; g_timeline[i][7] = tl[2];
     }
   }
 #endif

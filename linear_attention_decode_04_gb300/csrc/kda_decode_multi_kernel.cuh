@@ -324,13 +324,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
   };
 #ifdef KDA_DECODE_TIMELINE
   // timeline build: per CTA the time waiting for a unit's data, in the
-  // state-independent phase, in the token loop, waiting for an output buffer
-  unsigned long long tl_start = 0, tl_in = 0, tl_up = 0, tl_loop = 0, tl_freed = 0, tl_units = 0, tl_t = 0;
-  if (tid == 0) tl_start = global_ns();
+  // state-independent phase, in the token loop, waiting for an output
+  // buffer; thread 0's accumulators in shared memory so that they take no
+  // registers: start, in, up, loop, freed, units, last timestamp
+  __shared__ unsigned long long tl_acc[7];
+  volatile unsigned long long* tl = tl_acc;
+  if (tid == 0) {
+    tl[0] = global_ns();
+    for (int i = 1; i < 7; ++i) tl[i] = 0;
+  }
 #endif
   for (int it = 0;; ++it) {
 #ifdef KDA_DECODE_TIMELINE
-    if (tid == 0) tl_t = global_ns();
+    if (tid == 0) tl[6] = global_ns();
 #endif
     const int st = it % kMStages;
     const uint32_t parity = (it / kMStages) & 1;
@@ -354,9 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
 #ifdef KDA_DECODE_TIMELINE
     if (tid == 0) {
       const unsigned long long now = global_ns();
-      tl_in += now - tl_t;
-      tl_t = now;
-      if (n >= 0) ++tl_units;
+      tl[1] += now - tl[6];
+      tl[6] = now;
+      if (n >= 0) tl[5] += 1;
     }
 #endif
     if (n < 0) break;  // no more units
@@ -479,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
 #ifdef KDA_DECODE_TIMELINE
     if (tid == 0) {
       const unsigned long long now = global_ns();
-      tl_up += now - tl_t;
-      tl_t = now;
+      tl[2] += now - tl[6];
+      tl[6] = now;
     }
 #endif
     // ---- the recurrence, token by token, state in registers.
@@ -565,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
 #endif
       if (wc > 0) fok = mbar_wait_bounded(smem_addr(&S.freed[bn]), (wc - 1) & 1u, p.wait_limit_ns);
 #ifdef KDA_DECODE_TIMELINE
-      if (tid == 0) tl_freed += global_ns() - tl_f0;
+      if (tid == 0) tl[4] += global_ns() - tl_f0;
 #endif
       if (consumer_any(!fok || S.abort)) {
         if (tid == 0) {
@@ -598,15 +604,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_multi_kernel(const Par
       }
     }
 #ifdef KDA_DECODE_TIMELINE
-    if (tid == 0) tl_loop += global_ns() - tl_t;
+    if (tid == 0) tl[3] += global_ns() - tl[6];
 #endif
   }
 #ifdef KDA_DECODE_TIMELINE
   if (tid == 0) {
     const unsigned int i = atomicAdd(&g_timeline_n, 1u);
     if (i < kTimelineMax) {
-      g_timeline[i][0] = blockIdx.x; g_timeline[i][1] = tl_freed; g_timeline[i][2] = tl_start; g_timeline[i][3] = tl_up;
-      g_timeline[i][4] = global_ns(); g_timeline[i][5] = tl_units; g_timeline[i][6] = tl_loop; g_timeline[i][7] = tl_in;
+      g_timeline[i][0] = blockIdx.x; g_timeline[i][1] = tl[4]; g_timeline[i][2] = tl[0]; g_timeline[i][3] = tl[2];
+      g_timeline[i][4] = global_ns(); g_timeline[i][5] = tl[5]; g_timeline[i][6] = tl[3]; g_timeline[i][7] = tl[1];
     }
   }
 #endif
