@@ -18,6 +18,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;  // 256 math threads
 constexpr int kThreads = kConsumers + 32;        // + one producer warp
 constexpr int kRowsPerWarp = kDim / kConsumerWarps;  // 16 key rows per consumer warp
+constexpr int kEarlyStages = 2;  // ring stages whose state may stream in before the previous kernel ends
 constexpr uint32_t kTileBytes = kDim * kDim * 4;           // 64 KiB fp32 state tile
 constexpr uint32_t kCsSliceBytes = kDim * (kWidth - 1) * 2;  // 768 B conv state per block
 constexpr uint32_t kXSliceBytes = kDim * 2;                  // 256 B qkv per block
@@ -355,14 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       if (bp >= b0 && bp + 16 <= b1) l2_prefetch(reinterpret_cast<const void*>(bp), 16);
       if (kOutNorm) l2_prefetch(p.norm_w, kDim * 4);
     };
-    // First ring: static units.  With KDA_EARLY_PREFETCH the first unit's
-    // state streams in before the previous kernel in the stream has finished
-    // (the caller guarantees that kernel does not write the slot indices,
-    // the state or the conv state), and its per-token slices and conv taps
-    // are pulled into L2; everything per-token is read only after it.  The
-    // ring then fills one stage at a time (each stage once the one before
-    // it has landed), so that the first tile of every CTA arrives early
-    // instead of all CTAs' three tiles arriving together.
+    // First ring: static units.  With KDA_EARLY_PREFETCH the first two
+    // units' state streams in before the previous kernel in the stream has
+    // finished (the caller guarantees that kernel does not write the slot
+    // indices, the state or the conv state), and the first unit's per-token
+    // slices and conv taps are pulled into L2; everything per-token is read
+    // only after it.  Without it the ring fills one stage at a time (each
+    // stage once the one before it has landed), so that the first tile of
+    // every CTA arrives early instead of all CTAs' three tiles arriving
+    // together; with it the third stage follows the same rule.
     int it = 0;
     for (; it < kStages; ++it) {
       const int u = next_unit();
@@ -371,21 +373,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
       S.info[it][1] = n;
       S.info[it][2] = h;
       S.info[it][3] = (u == p.withhold_unit);
-      if (p.early_prefetch && it == 0) {
+      if (p.early_prefetch && it < kEarlyStages) {
         const int slot = __ldg(p.slot_idx + n);
         S.info[it][0] = slot;
         if (active(slot) && !S.info[it][3]) {
           mbar_arrive_expect_tx(smem_addr(&S.full[it]), in_bytes);
           load_slot_parts(it, h, slot);
-          warm_l2(n, h);
+          if (it == 0) warm_l2(n, h);
         }
       }
     }
     griddep_wait();
     for (int j = 0; j < it; ++j) {
       const int n = S.info[j][1], h = S.info[j][2];
-      if (j > 0 && !S.info[j - 1][3]) mbar_wait_bounded(smem_addr(&S.full[j - 1]), 0, p.wait_limit_ns);
-      if (!p.early_prefetch || j > 0) {
+      const bool early_j = p.early_prefetch && j < kEarlyStages;
+      if (j > 0 && !early_j && !S.info[j - 1][3]) mbar_wait_bounded(smem_addr(&S.full[j - 1]), 0, p.wait_limit_ns);
+      if (!early_j) {
         const int slot = __ldg(p.slot_idx + n);
         S.info[j][0] = slot;
         if (active(slot) && !S.info[j][3]) {
