@@ -359,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
     // First ring: static units.  With KDA_EARLY_PREFETCH the first two
     // units' state streams in before the previous kernel in the stream has
     // finished (the caller guarantees that kernel does not write the slot
-    // indices, the state or the conv state), and the first unit's per-token
-    // slices and conv taps are pulled into L2; everything per-token is read
-    // only after it.  Without it the ring fills one stage at a time (each
+    // indices, the state or the conv state), and their per-token slices and
+    // conv taps are pulled into L2; everything per-token is read only after
+    // it.  Without it the ring fills one stage at a time (each
     // stage once the one before it has landed), so that the first tile of
     // every CTA arrives early instead of all CTAs' three tiles arriving
     // together; with it the third stage follows the same rule.
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_persistent_kernel(cons
         if (active(slot) && !S.info[it][3]) {
           mbar_arrive_expect_tx(smem_addr(&S.full[it]), in_bytes);
           load_slot_parts(it, h, slot);
-          if (it == 0) warm_l2(n, h);
+          warm_l2(n, h);
         }
       }
     }
