@@ -121,7 +121,7 @@ constexpr int kRec = kOffE + kL * kD;         // one workspace record: 21,632 fl
 constexpr int kSplit = kOffU;                 // the operands the scan splits into tf32 words
 static_assert((kImg * 4) % 16 == 0 && (kRec * 4) % 16 == 0, "records must be whole 16-byte pieces");
 
-// Chunk kernel shared memory (about 107 KB: two CTAs per SM).
+// Chunk kernel shared memory (about 108 KB: two CTAs per SM).
 struct __align__(16) ChunkSmem {
   union {
     uint16_t raw[kHist + kL][kCh];  // conv window: 3 older rows, then the chunk's inputs
@@ -142,10 +142,10 @@ struct __align__(16) ChunkSmem {
   int slow;                         // this chunk takes the element-wise P / R path
 };
 
-// Scan kernel shared memory (about 206 KB): two images (double buffer), the
-// tf32 remainders of the image's tensor-core operands, the chunk's output,
-// the MMA-completion and copy-completion barriers and the tensor-memory base
-// address.
+// Scan kernel shared memory (about 205 KB): two images (double buffer), the
+// tf32 remainders of the image's tensor-core operands, the chunk's output
+// rows (E by bulk copy, then D_O added), the MMA-completion and
+// copy-completion barriers and the tensor-memory base address.
 struct __align__(128) ScanSmem {
   float img[2][kImg];
   float lo[kSplit];
